@@ -1,0 +1,144 @@
+"""Seeded synthetic inputs for absorbed MLA decode.
+
+This module only draws random numbers and lays them out; it holds none of the
+method's arithmetic, so both the CUDA path and the CPU oracle may use it.
+
+Recipe (the same for every workload; all draws on a CPU torch.Generator seeded
+with `seed`, in this fixed order):
+  1. seqlens: fixed, or torch.randint(1, max_len + 1, (B,)) for ragged batches;
+  2. block table: a random permutation of a pool of ceil(1.03 * total pages)
+     pages; request b takes the next ceil(seqlen_b / 64) pool pages in order;
+  3. q [B, s_q, H, 576] ~ N(0, 1) in fp32, rounded to bf16 (round-to-nearest-even);
+  4. kv [pool, 64, 576] ~ N(0, 1) in fp32;
+  5. optional outliers: each slot independently with probability p has its
+     whole 576-value row multiplied by a factor (before rounding to bf16);
+  6. optional projection inputs: q_nope [B*s_q, H, 128] and q_pe [B*s_q, H, 64]
+     ~ N(0, 1); W_UK [H, 128, 512] and W_UV [H, 512, 128] ~ N(0, 1/512) (variance).
+Poison: pool pages no request uses, and slots at or beyond seqlen in a
+request's last page, hold NaN; block-table entries past a request's last page
+hold -1.  A correct kernel never reads any of them into its result.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+PAGE = 64
+D_QK = 576
+D_LATENT = 512
+D_NOPE = 128
+D_ROPE = 64
+D_V = 128
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    s_q: int
+    H: int
+    seqlen: int = 0              # fixed length for every request (0: ragged)
+    ragged_max: int = 0          # ragged: seqlens uniform integers in [1, ragged_max]
+    causal: bool = False
+    outlier_p: float = 0.0
+    outlier_scale: float = 1.0
+    with_projections: bool = False
+    fixed_seqlens: tuple = field(default_factory=tuple)
+
+    @property
+    def softmax_scale(self) -> float:
+        # 1/sqrt(qk_nope + qk_rope) = 1/sqrt(192), the per-head q/k width of the
+        # un-absorbed model, which is what the absorbed path must reproduce.
+        return 1.0 / math.sqrt(D_NOPE + D_ROPE)
+
+    @property
+    def rows(self) -> int:
+        return self.s_q * self.H
+
+
+# The five workloads the parity tests and the bench use.
+TINY = Workload("tiny_b2_h16_l256_300", B=2, s_q=1, H=16, fixed_seqlens=(256, 300))
+V3 = Workload("deepseek_v3_b64_h128_l4096", B=64, s_q=1, H=128, seqlen=4096, with_projections=True)
+RAGGED = Workload("ragged_b128_h128_l1_8192", B=128, s_q=1, H=128, ragged_max=8192)
+MTP = Workload("mtp_b64_sq2_causal_h128_l8192", B=64, s_q=2, H=128, seqlen=8192, causal=True)
+LONG = Workload("long_b4_h128_l131072_outliers", B=4, s_q=1, H=128, seqlen=131072,
+                outlier_p=0.01, outlier_scale=8.0)
+ALL = (TINY, V3, RAGGED, MTP, LONG)
+BY_NAME = {w.name: w for w in ALL}
+
+
+def make_seqlens(w: Workload, g: torch.Generator) -> torch.Tensor:
+    if w.fixed_seqlens:
+        return torch.tensor(w.fixed_seqlens, dtype=torch.int32)
+    if w.ragged_max:
+        return torch.randint(1, w.ragged_max + 1, (w.B,), generator=g).to(torch.int32)
+    return torch.full((w.B,), w.seqlen, dtype=torch.int32)
+
+
+def make_inputs(w: Workload, seed: int = 0, seqlens: torch.Tensor | None = None,
+                poison: bool = True, max_blocks: int | None = None) -> dict:
+    """All CPU tensors of one workload.  Keys:
+    q [B,s_q,H,576] bf16, kv_cache [pool,64,576] bf16, block_table [B,max_blocks] int32,
+    seqlens [B] int32, softmax_scale, causal, and with projections also
+    q_nope [B*s_q,H,128], q_pe [B*s_q,H,64], w_uk [H,128,512], w_uv [H,512,128] (bf16).
+    """
+    g = torch.Generator().manual_seed(seed)
+    sl = make_seqlens(w, g) if seqlens is None else seqlens.to(torch.int32).clone()
+    if seqlens is not None and w.ragged_max:
+        torch.randint(1, w.ragged_max + 1, (w.B,), generator=g)  # keep the draw order
+    B = sl.numel()
+    nb = [(int(L) + PAGE - 1) // PAGE if int(L) > 0 else 0 for L in sl]
+    used = sum(nb)
+    pool = max(1, math.ceil(1.03 * used))
+    perm = torch.randperm(pool, generator=g).to(torch.int32)
+    mb = max(max(nb) if nb else 0, 1) if max_blocks is None else max_blocks
+    bt = torch.full((B, mb), -1, dtype=torch.int32)
+    pos = 0
+    for b in range(B):
+        bt[b, :nb[b]] = perm[pos:pos + nb[b]]
+        pos += nb[b]
+    q = torch.randn((B, w.s_q, w.H, D_QK), generator=g).to(torch.bfloat16)
+    kv = torch.randn((pool, PAGE, D_QK), generator=g)
+    if w.outlier_p > 0:
+        hit = torch.rand((pool, PAGE), generator=g) < w.outlier_p
+        kv[hit] *= w.outlier_scale
+    kv = kv.to(torch.bfloat16)
+    if poison:
+        in_use = torch.zeros(pool, dtype=torch.bool)
+        in_use[perm[:used].long()] = True
+        kv[~in_use] = float("nan")
+        for b in range(B):
+            L = int(sl[b])
+            if nb[b] and L % PAGE:
+                kv[int(bt[b, nb[b] - 1]), L % PAGE:] = float("nan")
+    out = dict(q=q, kv_cache=kv, block_table=bt, seqlens=sl,
+               softmax_scale=w.softmax_scale, causal=w.causal)
+    if w.with_projections:
+        n = B * w.s_q
+        out["q_nope"] = torch.randn((n, w.H, D_NOPE), generator=g).to(torch.bfloat16)
+        out["q_pe"] = torch.randn((n, w.H, D_ROPE), generator=g).to(torch.bfloat16)
+        std = 1.0 / math.sqrt(512.0)
+        out["w_uk"] = (torch.randn((w.H, D_NOPE, D_LATENT), generator=g) * std).to(torch.bfloat16)
+        out["w_uv"] = (torch.randn((w.H, D_LATENT, D_V), generator=g) * std).to(torch.bfloat16)
+    return out
+
+
+def small_variant(w: Workload, B: int | None = None, seqlen: int | None = None,
+                  H: int | None = None) -> Workload:
+    """The same workload shape at a size the oracle finishes in seconds."""
+    kw = dict(w.__dict__)
+    kw["name"] = w.name + "_small"
+    if B is not None:
+        kw["B"] = B
+    if H is not None:
+        kw["H"] = H
+    if seqlen is not None:
+        if w.ragged_max:
+            kw["ragged_max"] = seqlen
+        elif w.seqlen:
+            kw["seqlen"] = seqlen
+    if w.fixed_seqlens and B is not None:
+        kw["fixed_seqlens"] = tuple(w.fixed_seqlens[i % len(w.fixed_seqlens)] for i in range(B))
+    return Workload(**kw)

@@ -1,0 +1,281 @@
+"""Plain float64 restatement of weight-absorbed MLA decode (test infrastructure only).
+
+Sources (web pages, cited by title and section):
+
+[MLA-paths]  "MLA 推理：两条计算路径与 FlashMLA" (ai-infra-handbooks, serving/moe/mla),
+             section "两条等价的路径" (the score equation s = q^N·W_UK^T c + q^R·k^R,
+             path 1 = expand, path 2 = absorb), its worked tiny example, and section
+             "decode 注意力变成了计算问题" (split-KV partial results merged at the end).
+[DSV2-MLA]   "DeepSeekV2之MLA", section 4.3 (decode attention is an MQA with one
+             KV head, key width kv_lora_rank + rope = 576, value width 512) and
+             section 4.5 (q_nope @ w_kc into the latent, attention, then @ w_vc).
+[AI-note]    "为什么 MLA + MTP 容易吃亏？从 Arithmetic Intensity 看 Attention",
+             sections 3.1 (K-side absorption), 3.2 (V-side absorption),
+             section 8 (S query positions share one KV read) and appendix A
+             (the 64-dim RoPE key takes part in the score only, it has no value).
+
+Readings taken where the pages are silent:
+* lse is the natural log of the sum of exp of the *scaled* scores.
+* With s_q > 1 and causal masking, seqlens counts the s_q new tokens and new
+  token i (0 = earliest) sees tokens t <= seqlen - s_q + i  ([MLA-paths],
+  FLOP counter: "k includes the new tokens", pairs = q*k - q(q-1)/2).
+* A query row with no visible token has out = 0 and lse = -inf.
+* Token t of request b lives at kv_cache[block_table[b, t // 64], t % 64]; the
+  page size 64 is the one FlashMLA uses ([MLA-paths], FlashMLA paragraph).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+PAGE = 64          # tokens per KV page
+D_LATENT = 512     # latent c (also the value)
+D_ROPE = 64        # shared RoPE key k^R
+D_QK = D_LATENT + D_ROPE  # 576: width of the absorbed key / query
+
+
+def gather_request(kv_cache: np.ndarray, block_row: np.ndarray, n_tokens: int) -> np.ndarray:
+    """Rows 0..n_tokens-1 of one request's latent cache, as float64 [n_tokens, 576].
+
+    kv_cache is [num_blocks, 64, 576]; block_row is that request's row of the
+    block table.  Token t sits in page block_row[t // 64] at slot t % 64.
+    """
+    t = np.arange(n_tokens)
+    pages = np.asarray(block_row)[t // PAGE]
+    return np.asarray(kv_cache[pages, t % PAGE], dtype=np.float64)
+
+
+def visible_tokens(seqlen: int, s_q: int, i: int, causal: bool) -> int:
+    """How many cached tokens query position i (0 = earliest new token) attends to."""
+    if not causal:
+        return int(seqlen)
+    return max(0, min(int(seqlen), int(seqlen) - s_q + i + 1))
+
+
+def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=False):
+    """The absorbed decode definition: an MQA with a 576-wide key and 512-wide value.
+
+    For every request b, query position i and head h, with n = visible tokens:
+        s_t   = softmax_scale * <q[b,i,h,:576], kv_t[:576]>         t < n
+        lse   = ln sum_t exp(s_t)
+        out   = sum_t exp(s_t - lse) * kv_t[:512]
+    ([MLA-paths] path 2; [DSV2-MLA] 4.3; [AI-note] 3.1-3.2 and appendix A.)
+
+    q: [B, s_q, H, 576]; kv_cache: [num_blocks, 64, 576]; block_table: [B, max_blocks];
+    seqlens: [B].  Returns out [B, s_q, H, 512] and lse [B, s_q, H], float64.
+    The softmax is evaluated with its maximum subtracted, which changes only rounding.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, s_q, H, dq = q.shape
+    assert dq == D_QK
+    out = np.zeros((B, s_q, H, D_LATENT))
+    lse = np.full((B, s_q, H), -np.inf)
+    for b in range(B):
+        L = int(seqlens[b])
+        if L <= 0:
+            continue
+        kv = gather_request(kv_cache, block_table[b], L)
+        for i in range(s_q):
+            n = visible_tokens(L, s_q, i, causal)
+            if n == 0:
+                continue
+            s = softmax_scale * (q[b, i] @ kv[:n].T)          # [H, n]
+            m = s.max(axis=1, keepdims=True)
+            e = np.exp(s - m)
+            z = e.sum(axis=1, keepdims=True)
+            lse[b, i] = (m + np.log(z))[:, 0]
+            out[b, i] = (e / z) @ kv[:n, :D_LATENT]
+    return out, lse
+
+
+def absorb_q(q_nope, w_uk):
+    """q_lat[b, h, :] = q_nope[b, h, :] @ W_UK[h]   ([DSV2-MLA] 4.5, "q_nope @ w_kc").
+
+    q_nope: [N, H, 128]; w_uk: [H, 128, 512] -> [N, H, 512] float64.
+    """
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    w_uk = np.asarray(w_uk, dtype=np.float64)
+    return np.einsum("nhd,hdc->nhc", q_nope, w_uk)
+
+
+def unabsorb_o(o_lat, w_uv):
+    """o[b, h, :] = o_lat[b, h, :] @ W_UV[h]   ([DSV2-MLA] 4.5, "attn_output @ w_vc").
+
+    o_lat: [N, H, 512]; w_uv: [H, 512, 128] -> [N, H, 128] float64.
+    """
+    o_lat = np.asarray(o_lat, dtype=np.float64)
+    w_uv = np.asarray(w_uv, dtype=np.float64)
+    return np.einsum("nhc,hcd->nhd", o_lat, w_uv)
+
+
+def decode_expanded(q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, seqlens, softmax_scale,
+                    causal=False, batches=None, head_chunk=16):
+    """The expanded (un-absorbed) definition: per-head K and V built from the latent.
+
+    For head h and cached token t with latent c_t = kv_t[:512] and RoPE key
+    k^R_t = kv_t[512:576]:
+        k_{h,t} = [ W_UK[h] c_t  (128) , k^R_t (64) ]
+        v_{h,t} =   W_UV[h]^T c_t (128)
+        s       = softmax_scale * <[q_nope, q_pe], k_{h,t}>,   o = softmax(s) . v
+    ([MLA-paths] path 1; [AI-note] 3.1-3.2; the orientation of W_UK / W_UV is the
+    bmm one of [DSV2-MLA] 4.5: q_lat = q_nope @ W_UK[h], o = o_lat @ W_UV[h].)
+
+    q_nope: [B, s_q, H, 128], q_pe: [B, s_q, H, 64], w_uk: [H, 128, 512],
+    w_uv: [H, 512, 128].  Returns o [B, s_q, H, 128] (rows of requests not in
+    `batches` stay zero) and lse [B, s_q, H].
+    """
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    q_pe = np.asarray(q_pe, dtype=np.float64)
+    w_uk = np.asarray(w_uk, dtype=np.float64)
+    w_uv = np.asarray(w_uv, dtype=np.float64)
+    B, s_q, H, _ = q_nope.shape
+    dv = w_uv.shape[2]
+    o = np.zeros((B, s_q, H, dv))
+    lse = np.full((B, s_q, H), -np.inf)
+    for b in (range(B) if batches is None else batches):
+        L = int(seqlens[b])
+        if L <= 0:
+            continue
+        kv = gather_request(kv_cache, block_table[b], L)
+        c, k_r = kv[:, :D_LATENT], kv[:, D_LATENT:]
+        for h0 in range(0, H, head_chunk):
+            hs = slice(h0, min(H, h0 + head_chunk))
+            k_n = np.matmul(c[None], np.transpose(w_uk[hs], (0, 2, 1)))   # [h, L, 128]
+            v = np.matmul(c[None], w_uv[hs])                              # [h, L, 128]
+            for i in range(s_q):
+                n = visible_tokens(L, s_q, i, causal)
+                if n == 0:
+                    continue
+                s = np.einsum("hd,hld->hl", q_nope[b, i, hs], k_n[:, :n]) + q_pe[b, i, hs] @ k_r[:n].T
+                s *= softmax_scale
+                m = s.max(axis=1, keepdims=True)
+                e = np.exp(s - m)
+                z = e.sum(axis=1, keepdims=True)
+                lse[b, i, hs] = (m + np.log(z))[:, 0]
+                o[b, i, hs] = np.einsum("hl,hld->hd", e / z, v[:, :n])
+    return o, lse
+
+
+def lse_merge(o_parts, lse_parts):
+    """Merge attention results over disjoint key sets by log-sum-exp.
+
+    ([MLA-paths]: split-KV / flash-decoding computes each KV segment on its own
+    SM and merges the partial results; the chunked-prefix path merges chunks
+    "by LSE", the same way as context parallelism.)
+        lse = ln sum_k exp(lse_k),   o = sum_k exp(lse_k - lse) * o_k
+    o_parts: [K, ..., D]; lse_parts: [K, ...].  Parts with lse = -inf carry no
+    weight; if every part is empty the result is o = 0, lse = -inf.
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    m = lse_parts.max(axis=0)
+    finite = np.isfinite(m)
+    m_safe = np.where(finite, m, 0.0)
+    w = np.where(np.isfinite(lse_parts), np.exp(lse_parts - m_safe), 0.0)
+    z = w.sum(axis=0)
+    lse = np.where(finite, m_safe + np.log(np.where(finite, z, 1.0)), -np.inf)
+    coef = np.where(finite, w / np.where(finite, z, 1.0), 0.0)
+    o = np.einsum("k...,k...d->...d", coef, o_parts)
+    return o, lse
+
+
+def decode_bruteforce(q_row, keys, softmax_scale):
+    """Single query row against a handful of keys, in pure Python loops.
+
+    q_row: 576 numbers; keys: list of 576-number rows.  Returns (out[512], lse).
+    No maximum is subtracted: exp is applied to the raw scaled scores, so this
+    is only for small, moderate inputs (it is the textbook formula, as is).
+    """
+    scores = []
+    for k in keys:
+        acc = 0.0
+        for a, bb in zip(q_row, k):
+            acc += float(a) * float(bb)
+        scores.append(softmax_scale * acc)
+    weights = [math.exp(s) for s in scores]
+    z = sum(weights)
+    out = [0.0] * D_LATENT
+    for w, k in zip(weights, keys):
+        for d in range(D_LATENT):
+            out[d] += (w / z) * float(k[d])
+    return out, math.log(z)
+
+
+def rope_interleaved(x, positions, base=10000.0):
+    """Rotate adjacent pairs (x[2j], x[2j+1]) by angle pos * base^(-2j/R).
+
+    ([MLA-paths] tiny example, its rope helper: angle = pos / 10000^(2j/R), the
+    rotated pairs are written back interleaved.)  x: [..., T, R]; positions: [T].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    R = x.shape[-1]
+    j = np.arange(R // 2, dtype=np.float64)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * base ** (-2.0 * j / R)   # [T, R/2]
+    cos, sin = np.cos(ang), np.sin(ang)
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    y = np.empty_like(x)
+    y[..., 0::2] = x0 * cos - x1 * sin
+    y[..., 1::2] = x0 * sin + x1 * cos
+    return y
+
+
+def tiny_full_mla(seed=0, T=6, D=64, H=4, NOPE=8, ROPE=4, DV=8, DC=16):
+    """The worked tiny full-MLA example with decoupled RoPE, both paths.
+
+    Follows [MLA-paths] section "两条等价的路径": hidden states h [T, D];
+    latent c = h W_dkv (cached); shared RoPE key k^R = rope(h W_kr) (cached);
+    per-head query split into q^N (NOPE) and q^R = rope(.) (ROPE);
+    scale = 1/sqrt(NOPE + ROPE); causal prefill mask (token t sees s <= t).
+      path 1 (expand): k = [c W_uk[h], k^R], v = c W_uv[h]; ordinary MHA.
+      path 2 (absorb): q_lat = W_uk[h] q^N; score = q_lat.c + q^R.k^R;
+                       out = (sum_s p_s c_s) W_uv[h].
+    Both are projected by W_o.  The page's weights come from a seeded torch RNG
+    it does not print; any draw works, since the claim is the equality itself.
+    Returns dict with y_expand, y_absorb [T, D] and the per-token cache counts.
+    """
+    rng = np.random.default_rng(seed)
+    W_q = rng.standard_normal((D, H * (NOPE + ROPE))) / 8
+    W_dkv = rng.standard_normal((D, DC)) / 8
+    W_kr = rng.standard_normal((D, ROPE)) / 8
+    W_uk = rng.standard_normal((H, DC, NOPE)) / 4     # latent -> per-head k^N
+    W_uv = rng.standard_normal((H, DC, DV)) / 4       # latent -> per-head v
+    W_o = rng.standard_normal((H * DV, D)) / 8
+    hid = rng.standard_normal((T, D))
+    pos = np.arange(T)
+    allowed = np.tril(np.ones((T, T), dtype=bool))
+
+    c = hid @ W_dkv                                   # [T, DC]
+    k_r = rope_interleaved(hid @ W_kr, pos)           # [T, ROPE]
+    q = (hid @ W_q).reshape(T, H, NOPE + ROPE).transpose(1, 0, 2)   # [H, T, NOPE+ROPE]
+    q_n = q[..., :NOPE]
+    q_r = rope_interleaved(q[..., NOPE:], pos)
+    scale = 1.0 / math.sqrt(NOPE + ROPE)
+
+    def masked_softmax(s):
+        s = np.where(allowed, s, -np.inf)
+        s = s - s.max(axis=-1, keepdims=True)
+        e = np.exp(s)
+        return e / e.sum(axis=-1, keepdims=True)
+
+    # path 1: expand the latent into per-head keys and values
+    k_n = np.einsum("tc,hcd->htd", c, W_uk)
+    k = np.concatenate([k_n, np.broadcast_to(k_r, (H, T, ROPE))], axis=-1)
+    v = np.einsum("tc,hcd->htd", c, W_uv)
+    qq = np.concatenate([q_n, q_r], axis=-1)
+    out1 = masked_softmax(np.einsum("hid,hjd->hij", qq, k) * scale) @ v        # [H, T, DV]
+
+    # path 2: absorb W_uk into the query, sum in the latent space, then W_uv
+    q_lat = np.einsum("htd,hcd->htc", q_n, W_uk)                               # [H, T, DC]
+    p = masked_softmax((q_lat @ c.T + q_r @ k_r.T) * scale)                    # [H, T, T]
+    lat = p @ c                                                                 # [H, T, DC]
+    out2 = np.einsum("htc,hcd->htd", lat, W_uv)
+
+    y1 = out1.transpose(1, 0, 2).reshape(T, H * DV) @ W_o
+    y2 = out2.transpose(1, 0, 2).reshape(T, H * DV) @ W_o
+    return {
+        "y_expand": y1,
+        "y_absorb": y2,
+        "cache_per_token_mha": H * (NOPE + ROPE) + H * DV,
+        "cache_per_token_mla": DC + ROPE,
+    }
