@@ -1,0 +1,444 @@
+"""Benchmark of one absorbed-MLA decode step on GB300.
+
+A step is one pass of the whole path on one batch: split schedule, W_UK
+absorption (with the q assembly), paged absorbed decode, LSE combine and W_UV
+un-absorption, on the DeepSeek-V3-shaped workload (B=64, H=128, s_q=1, every
+context 4096 tokens, 576/512 dims, page 64, synthetic bf16 data).  The metric
+is algorithmic TFLOP/s of the step; HBM GB/s and the fraction of the roofline
+max(FLOPs / 2.25 PFLOP/s, bytes / 8 TB/s) ride along, and the `roofline` object
+rates the dominant kernel (the mla_decode call) against the measured HBM peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+--impl reference times the CPU oracle (numpy float64) on a bounded sample of
+the same workload per step.  With N > 1 (torchrun) every rank runs its own
+replica of the workload (requests shard across GPUs with no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode TFLOP/s and HBM GB/s, % of GB300 roofline (1 GPU)"
+SPEC_FLOPS = 2.25e15
+SPEC_BW = 8.0e12
+DECODE_KERNEL_SOURCES = ("mla_absorbed_decode_gb300/csrc/mla_decode.cu", "mla_absorbed_decode_gb300/csrc/mla_ptx.cuh")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def _source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in DECODE_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_launch(workload_name):
+    """DRAM bytes per decode launch from a committed ncu summary, if it was taken on
+    the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload_name)
+    if not e or e.get("source_digest") != _source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_sample_step(inp, kv_np, sel, with_proj):
+    """One CPU oracle pass over the sampled requests; returns its algorithmic FLOPs."""
+    import numpy as np
+    import oracle
+    from mla_absorbed_decode_gb300 import accounting as acc
+    B, s_q, H, _ = inp["q"].shape
+    flops = 0
+    if with_proj:
+        qn = inp["q_nope"].float().numpy().reshape(B, s_q, H, 128)[sel].reshape(-1, H, 128)
+        q_lat = oracle.absorb_q(qn, inp["_w_uk_np"])
+        qp = inp["q_pe"].float().numpy().reshape(B, s_q, H, 64)[sel].reshape(-1, H, 64)
+        q = np.concatenate([q_lat, qp], axis=-1).reshape(len(sel), s_q, H, 576)
+        flops += acc.bmm_work(len(sel) * s_q, H, True)[0]
+    else:
+        q = inp["q"][sel].double().numpy()
+    out, _ = oracle.decode_absorbed(q, kv_np, inp["block_table"][sel].numpy(), inp["seqlens"][sel].numpy(),
+                                    inp["softmax_scale"], causal=inp["causal"])
+    flops += acc.decode_work(inp["seqlens"][sel].tolist(), s_q, H, inp["causal"])[0]
+    if with_proj:
+        oracle.unabsorb_o(out.reshape(-1, H, 512), inp["_w_uv_np"])
+        flops += acc.bmm_work(len(sel) * s_q, H, False)[0]
+    return flops
+
+
+def cpu_sample(inp, w, target_s=10.0, max_reqs=None):
+    """Time the oracle on a bounded sample of the workload (about target_s seconds)."""
+    import numpy as np
+    if "_kv_np" not in inp:
+        inp["_kv_np"] = inp["kv_cache"].float().numpy()
+    if w.with_projections and "_w_uk_np" not in inp:
+        inp["_w_uk_np"] = inp["w_uk"].double().numpy()
+        inp["_w_uv_np"] = inp["w_uv"].double().numpy()
+    B = inp["q"].shape[0]
+    t0 = time.perf_counter()
+    flops = oracle_sample_step(inp, inp["_kv_np"], [0], w.with_projections)
+    dt = time.perf_counter() - t0
+    n = max(1, min(B if max_reqs is None else max_reqs, int(target_s / max(dt, 1e-3))))
+    sel = list(range(n))
+    t0 = time.perf_counter()
+    flops = oracle_sample_step(inp, inp["_kv_np"], sel, w.with_projections)
+    dt = time.perf_counter() - t0
+    return flops, dt, sel
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from mla_absorbed_decode_gb300 import workloads as W
+    inp = W.make_inputs(w)
+    inp["_kv_np"] = inp["kv_cache"].float().numpy()
+    if w.with_projections:
+        inp["_w_uk_np"] = inp["w_uk"].double().numpy()
+        inp["_w_uv_np"] = inp["w_uv"].double().numpy()
+    sel = [0]
+    for _ in range(args.warmup):
+        oracle_sample_step(inp, inp["_kv_np"], sel, w.with_projections)
+    times, flops = [], 0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        flops = oracle_sample_step(inp, inp["_kv_np"], sel, w.with_projections)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    value = flops / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "s_q": w.s_q, "H": w.H,
+                   "sample": f"request 0 of {w.B} per step (absorb, decode, un-absorb on the CPU oracle)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"request 0 of {w.B} per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    import mla_absorbed_decode_gb300 as mla
+    from mla_absorbed_decode_gb300 import accounting as acc, build_lib, workloads as W
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build_lib.build()
+    dev = torch.device("cuda", local)
+    inp = W.make_inputs(w, seed=rank)
+    B, s_q, H = w.B, w.s_q, w.H
+    q_nope = inp["q_nope"].to(dev) if w.with_projections else None
+    q_pe = inp["q_pe"].to(dev) if w.with_projections else None
+    w_uk = inp["w_uk"].to(dev) if w.with_projections else None
+    w_uv = inp["w_uv"].to(dev) if w.with_projections else None
+    kv = inp["kv_cache"].to(dev)
+    bt = inp["block_table"].to(dev)
+    sl = inp["seqlens"].to(dev)
+    parts = args.parts or mla.num_sm_parts(s_q, H)
+    step = mla.DecodeStep(B, s_q, H, sl, w.causal, w.softmax_scale, parts=parts, device=dev)
+    q_direct = inp["q"].to(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > 126 MB of L2
+
+    def one_step():
+        step.plan()
+        if w.with_projections:
+            mla.absorb_q(q_nope, w_uk, step.q, q_pe=q_pe)
+            q_in = step.q
+        else:
+            q_in = q_direct
+        ev_d0.record()
+        mla.decode(q_in, kv, bt, sl, w.softmax_scale, w.causal, step.metadata, parts, workspace=step.workspace,
+                   out=step.out, lse=step.lse)
+        ev_d1.record()
+        if w.with_projections:
+            mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
+
+    launches_per_step = 1 + 2 + (2 if w.with_projections else 0)   # schedule, decode+combine, bmms
+    ev_d0, ev_d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        one_step()
+    torch.cuda.synchronize()
+    status = mla.get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            ev_d0, ev_d1 = d0[i], d1[i]
+            starts[i].record()
+            one_step()
+            ends[i].record()
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    status = mla.get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dec_ms = [a.elapsed_time(b) for a, b in zip(d0, d1)]
+    t_step = statistics.mean(step_ms) / 1e3
+    t_dec = statistics.mean(dec_ms) / 1e3
+    if dist:
+        t = torch.tensor([t_step, t_dec], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step, t_dec = t.tolist()
+
+    dflops, dbytes = acc.decode_work(inp["seqlens"].tolist(), s_q, H, w.causal)
+    bflops = bbytes = 0
+    if w.with_projections:
+        for absorb in (True, False):
+            f, b = acc.bmm_work(B * s_q, H, absorb)
+            bflops += f
+            bbytes += b
+    step_flops, step_bytes = dflops + bflops, dbytes + bbytes
+    n = ws
+    value = n * step_flops / t_step / 1e12
+    gbs = n * step_bytes / t_step / 1e9
+    rl_time = acc.roofline_time(step_flops, step_bytes, SPEC_FLOPS, SPEC_BW)
+
+    # end to end through the public API with host buffers: H2D of the step's inputs,
+    # the step, D2H of its result, every step
+    e2e = None
+    if not args.no_e2e:
+        host_in = []
+        if w.with_projections:
+            host_in = [inp["q_nope"].pin_memory(), inp["q_pe"].pin_memory()]
+        else:
+            host_in = [inp["q"].pin_memory()]
+        host_sl = inp["seqlens"].pin_memory()
+        host_bt = inp["block_table"].pin_memory()
+        dev_in = [t.to(dev) for t in host_in]
+        res_dev = step.o if w.with_projections else step.out
+        host_out = torch.empty(res_dev.shape, dtype=res_dev.dtype).pin_memory()
+        host_lse = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in) + host_sl.numel() * 4 + host_bt.numel() * 4
+        d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
+
+        def e2e_step():
+            for src, dst in zip(host_in, dev_in):
+                dst.copy_(src, non_blocking=True)
+            sl.copy_(host_sl, non_blocking=True)
+            bt.copy_(host_bt, non_blocking=True)
+            step.plan()
+            if w.with_projections:
+                mla.absorb_q(dev_in[0], w_uk, step.q, q_pe=dev_in[1])
+                q_in = step.q
+            else:
+                q_in = dev_in[0]
+            mla.decode(q_in, kv, bt, sl, w.softmax_scale, w.causal, step.metadata, parts,
+                       workspace=step.workspace, out=step.out, lse=step.lse)
+            if w.with_projections:
+                mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
+            host_out.copy_(res_dev, non_blocking=True)
+            host_lse.copy_(step.lse, non_blocking=True)
+
+        for _ in range(3):
+            flush.zero_()
+            e2e_step()
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            es[i].record()
+            e2e_step()
+            ee[i].record()
+        torch.cuda.synchronize()
+        t_e2e = statistics.mean(a.elapsed_time(b) for a, b in zip(es, ee)) / 1e3
+        if dist:
+            t = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = t.item()
+        e2e = {"value": n * step_flops / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3}
+
+    peaks = _peaks()
+    dec_achieved = dbytes / t_dec / 1e9
+    roof_bound = "hbm" if dflops / SPEC_FLOPS < dbytes / SPEC_BW else "tensor"
+    if roof_bound == "hbm":
+        roof = {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": dec_achieved / peaks["hbm_gbs"]}
+    else:
+        ach = dflops / t_dec / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"]}
+    roof["peak_source"] = peaks["source"]
+    roof["traffic"] = _traffic_per_launch(w.name)
+    roof["kernel"] = "mla_decode (decode kernel + LSE combine)"
+    roof["algorithmic_per_launch"] = {"bytes": dbytes, "flops": dflops}
+    roof["ms_per_launch"] = t_dec * 1e3
+    roof["frac_of_spec_roofline"] = acc.roofline_time(dflops, dbytes, SPEC_FLOPS, SPEC_BW) / t_dec
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        f, dt, sel = cpu_sample(inp, w, target_s=args.cpu_seconds)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"requests {sel[0]}..{sel[-1]} of {B} ({len(sel)}), one pass of the oracle's "
+                         f"absorb/decode/un-absorb, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": n, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "s_q": s_q, "H": H,
+                       "seqlens": (w.seqlen or f"ragged 1..{w.ragged_max}" if not w.fixed_seqlens
+                                   else list(w.fixed_seqlens)),
+                       "page": 64, "parts": parts, "parallelism": f"replicas x{n}",
+                       "l2": "flushed between timed steps (256 MiB write outside the step events)"},
+            "hbm_gbs": gbs,
+            "pct_of_roofline": 100.0 * rl_time / t_step,
+            "roofline_spec": {"peak_tflops": SPEC_FLOPS / 1e12, "peak_gbs": SPEC_BW / 1e9},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="deepseek_v3_b64_h128_l4096")
+    ap.add_argument("--parts", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    from mla_absorbed_decode_gb300 import workloads as W
+    w = W.BY_NAME[args.workload]
+    if args.batch:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}_b{args.batch}")
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,146 @@
+/*
+ * mla.h -- C ABI of the GB300 (sm_103a) weight-absorbed MLA decode library.
+ *
+ * The operation (web page "MLA 推理：两条计算路径与 FlashMLA", section "两条等价的路径",
+ * path 2; "DeepSeekV2之MLA", sections 4.3 and 4.5): with W_UK absorbed into the
+ * query, decode attention is an MQA in which H query heads share one cached row
+ * of 576 values per token -- the 512-dim latent c followed by the 64-dim shared
+ * RoPE key k^R -- and the first 512 values are also the value vector.  For
+ * request b, query position i (0 = earliest of the s_q new tokens), head h:
+ *
+ *     n     = seqlens[b]                       (no causal masking)
+ *           = seqlens[b] - s_q + i + 1         (causal_s_q != 0)
+ *     s_t   = softmax_scale * <q[b,i,h,0:576], kv_t[0:576]>,  t < n
+ *     lse   = ln sum_t exp(s_t)                          (natural log, scaled scores)
+ *     out   = sum_t exp(s_t - lse) * kv_t[0:512]
+ *
+ * with kv_t = kv_cache[block_table[b, t / 64], t % 64, :] (pages of 64 tokens, the
+ * page size FlashMLA uses; same page, section "decode 注意力变成了计算问题").
+ * A row with n = 0 gets out = 0 and lse = -inf.
+ *
+ * Conventions for every call:
+ *  - Pointers are device pointers unless stated otherwise.  The caller allocates
+ *    and owns every buffer (metadata and workspace included); the library never
+ *    allocates or frees device memory.
+ *  - bf16 = IEEE bfloat16 stored as uint16_t.  All tensors are dense, row-major,
+ *    in the shapes given; q, kv_cache, out, q_nope, w_uk, w_uv, o_lat and o must
+ *    be 16-byte aligned.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream), except
+ *    mla_get_device_status.  Argument errors are found on the host before any
+ *    launch and returned as status codes; nothing aborts or throws.
+ *  - Device-side faults (a block-table entry outside [0, num_blocks), a barrier
+ *    wait that ran out of time) do not trap: the kernels skip the access or end
+ *    their loops and record a code in a device status word that
+ *    mla_get_device_status reads.
+ *  - Supported: 1 <= s_q * H <= 512 (rows are processed in blocks of 128;
+ *    one block per 2-CTA pair, at most 4 pairs per cluster).  Dims are fixed at
+ *    576 (q/k) and 512 (v); page size 64.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int mla_status_t;
+#define MLA_OK                 0
+#define MLA_ERR_INVALID_ARG    1   /* null/misaligned pointer, bad size           */
+#define MLA_ERR_UNSUPPORTED    2   /* shape outside the supported set             */
+#define MLA_ERR_WORKSPACE      3   /* metadata or workspace buffer too small      */
+#define MLA_ERR_CUDA           4   /* a CUDA runtime/driver call failed           */
+#define MLA_ERR_TIMEOUT        5   /* device: a bounded barrier wait ran out      */
+#define MLA_ERR_DEVICE_BOUNDS  6   /* device: block-table entry out of range      */
+
+typedef uint16_t mla_bf16_t;
+typedef struct CUstream_st* mla_stream_t;   /* same handle as cudaStream_t */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mla_status_string(mla_status_t status);
+
+/* Number of split parts (clusters of 2 * ceil(s_q*H/128) CTAs) that fit on the
+ * device at once for this row count; the default num_sm_parts.  Returns <= 0 on
+ * error (no device, unsupported rows). */
+int mla_num_sm_parts(int device, int s_q, int H);
+
+/* Bytes of the tile-schedule metadata for B requests and num_sm_parts parts. */
+size_t mla_metadata_size(int B, int num_sm_parts);
+
+/* Split-KV tile schedule ("get_mla_metadata": computed ahead of the kernel from
+ * the sequence lengths only; page "MLA 推理：两条计算路径与 FlashMLA", FlashMLA
+ * paragraph).  seqlens: [B] int32 device.  Writes metadata (mla_metadata_size
+ * bytes, device): one 8-int record per part then B+1 split offsets.  The rule
+ * (greedy over requests in order, per-segment cost in pages, at most
+ * hbm_parts parts used when the GPU's bandwidth is already saturated) is
+ * restated and checked bit for bit by the tests.  Reuse the result for every
+ * layer of the same batch.  Async on stream. */
+mla_status_t mla_decode_metadata(const int32_t* seqlens, int B, int s_q, int H, int causal_s_q,
+                                 int num_sm_parts, void* metadata, mla_stream_t stream);
+
+/* The schedule's constants, for tests: per-segment cost (pages) and the number
+ * of parts that saturate HBM for one 2-CTA pair per part. */
+void mla_schedule_params(int* fixed_cost_pages, int* hbm_parts);
+
+/* Bytes of the split workspace (fp32 partial outputs and lse of split requests). */
+size_t mla_decode_workspace_size(int B, int s_q, int H, int num_sm_parts);
+
+/* Absorbed MLA decode (see the header comment for the definition).
+ *  q            [B, s_q, H, 576] bf16: [0:512) = q_nope.W_UK, [512:576) = RoPE'd q_pe
+ *  kv_cache     [num_blocks, 64, 576] bf16 latent cache (16-byte aligned rows)
+ *  block_table  [B, max_blocks] int32; only entries < ceil(seqlens[b]/64) are read
+ *  seqlens      [B] int32, each in [0, max_blocks*64]; counts the s_q new tokens
+ *  metadata     from mla_decode_metadata with the same seqlens, B, s_q, H and
+ *               num_sm_parts
+ *  workspace    >= mla_decode_workspace_size bytes, 256-byte aligned
+ *  out          [B, s_q, H, 512] bf16;  lse [B, s_q, H] fp32 (natural log)
+ * Slots at or beyond seqlens[b] in the last page, and unused pages, may hold
+ * anything (NaN included); they never reach the result.  Async on stream. */
+mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t num_blocks,
+                        const int32_t* block_table, int max_blocks, const int32_t* seqlens,
+                        int B, int s_q, int H, float softmax_scale, int causal_s_q,
+                        const void* metadata, int num_sm_parts,
+                        void* workspace, size_t workspace_bytes,
+                        mla_bf16_t* out, float* lse, mla_stream_t stream);
+
+/* W_UK absorption and assembly of the decode query ("DeepSeekV2之MLA" 4.5:
+ * q_nope_out = bmm(q_nope, w_kc) goes into q[..., :kv_lora_rank], the RoPE'd
+ * q_pe into the last 64 values):
+ *   q[n, h, 0:512]   = q_nope[n, h, 0:128] @ w_uk[h]    (fp32 accumulate, bf16 out)
+ *   q[n, h, 512:576] = q_pe[n, h, 0:64]                 (copied; skipped if q_pe is NULL)
+ *  q_nope  [N, H, 128] bf16, q_nope_row_stride elements between consecutive n
+ *          (>= H*128, multiple of 8)
+ *  q_pe    [N, H, 64] bf16 or NULL, q_pe_row_stride elements between consecutive n
+ *          (>= H*64, multiple of 8)
+ *  w_uk    [H, 128, 512] bf16
+ *  q       [N, H, 576] bf16 (the decode q, N = B*s_q)
+ * Async on stream. */
+mla_status_t mla_absorb_q(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                          int64_t q_pe_row_stride, const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H,
+                          mla_stream_t stream);
+
+/* W_UV un-absorption ("DeepSeekV2之MLA" 4.5: bmm(attn_output, w_vc)):
+ *   o[n, h, 0:128] = o_lat[n, h, 0:512] @ w_uv[h]      (fp32 accumulate, bf16 out)
+ *  o_lat [N, H, 512] bf16 (the decode out), w_uv [H, 512, 128] bf16, o [N, H, 128] bf16.
+ * Async on stream. */
+mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* o,
+                            int N, int H, mla_stream_t stream);
+
+/* Synchronizes `stream`, then reads and clears the device status word that the
+ * kernels set (MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_BOUNDS). */
+mla_status_t mla_get_device_status(mla_stream_t stream);
+
+/* Test hook: when nonzero, the next mla_decode launch withholds the first KV
+ * page load of every part, so that each barrier wait on it runs out of time
+ * (about 0.2 s) and the call reports MLA_ERR_TIMEOUT through
+ * mla_get_device_status.  No memory access is made out of bounds and nothing
+ * traps; the flag clears itself after one launch. */
+void mla_debug_withhold_first_load(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

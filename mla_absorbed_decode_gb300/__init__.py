@@ -1,0 +1,200 @@
+"""GB300-native weight-absorbed MLA decode.
+
+Python binding of ``libmla.so``, the C-ABI library declared in ``include/mla.h``.
+The functions here only marshal arguments: every step of the path (schedule,
+W_UK absorption, paged decode, LSE combine, W_UV un-absorption) runs in the
+library's sm_103a kernels.  PyTorch supplies device memory and streams.
+There is no fallback: if the library is not built, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MLAError", "lib", "library_path", "num_sm_parts", "metadata_size", "decode_metadata",
+    "decode_workspace_size", "decode", "absorb_q", "unabsorb_o", "get_device_status",
+    "schedule_params", "debug_withhold_first_load", "DecodeStep", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libmla.so")
+
+MLA_OK = 0
+STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_WORKSPACE",
+                4: "MLA_ERR_CUDA", 5: "MLA_ERR_TIMEOUT", 6: "MLA_ERR_DEVICE_BOUNDS"}
+
+_c_int, _c_size, _c_float, _c_ll, _p = ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_int64, ctypes.c_void_p
+_SIGNATURES = {
+    "mla_status_string": (ctypes.c_char_p, [_c_int]),
+    "mla_num_sm_parts": (_c_int, [_c_int, _c_int, _c_int]),
+    "mla_metadata_size": (_c_size, [_c_int, _c_int]),
+    "mla_decode_metadata": (_c_int, [_p, _c_int, _c_int, _c_int, _c_int, _c_int, _p, _p]),
+    "mla_schedule_params": (None, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
+    "mla_decode_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "mla_decode": (_c_int, [_p, _p, _c_ll, _p, _c_int, _p, _c_int, _c_int, _c_int, _c_float, _c_int,
+                            _p, _c_int, _p, _c_size, _p, _p, _p]),
+    "mla_absorb_q": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _p, _c_int, _c_int, _p]),
+    "mla_unabsorb_o": (_c_int, [_p, _p, _p, _c_int, _c_int, _p]),
+    "mla_get_device_status": (_c_int, [_p]),
+    "mla_debug_withhold_first_load": (None, [_c_int]),
+}
+EXPORTED_SYMBOLS = tuple(_SIGNATURES)
+
+_lib = None
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmla.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"{library_path} is missing: build it with "
+                               "`python -m mla_absorbed_decode_gb300.build_lib`")
+        handle = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != MLA_OK:
+        raise MLAError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return t.data_ptr()
+
+
+def num_sm_parts(s_q: int, H: int, device: int | None = None) -> int:
+    dev = torch.cuda.current_device() if device is None else device
+    n = lib().mla_num_sm_parts(dev, s_q, H)
+    if n <= 0:
+        raise MLAError(-n if n < 0 else 4, "mla_num_sm_parts")
+    return n
+
+
+def metadata_size(B: int, parts: int) -> int:
+    return lib().mla_metadata_size(B, parts)
+
+
+def schedule_params() -> tuple[int, int]:
+    f, h = _c_int(), _c_int()
+    lib().mla_schedule_params(ctypes.byref(f), ctypes.byref(h))
+    return f.value, h.value
+
+
+def decode_metadata(seqlens: torch.Tensor, s_q: int, H: int, causal: bool, parts: int,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Split-KV tile schedule for these sequence lengths (int32 tensor on the device)."""
+    B = seqlens.numel()
+    n_ints = metadata_size(B, parts) // 4
+    if out is None:
+        out = torch.empty(n_ints, dtype=torch.int32, device=seqlens.device)
+    _check(lib().mla_decode_metadata(_ptr(seqlens), B, s_q, H, int(causal), parts, _ptr(out), _stream(stream)),
+           "mla_decode_metadata")
+    return out
+
+
+def decode_workspace_size(B: int, s_q: int, H: int, parts: int) -> int:
+    return lib().mla_decode_workspace_size(B, s_q, H, parts)
+
+
+def decode(q, kv_cache, block_table, seqlens, softmax_scale: float, causal: bool, metadata, parts: int,
+           workspace=None, out=None, lse=None, stream=None):
+    """Absorbed MLA decode: returns (out [B,s_q,H,512] bf16, lse [B,s_q,H] fp32)."""
+    B, s_q, H, _ = q.shape
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, s_q, H, 512), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=dev)
+    need = decode_workspace_size(B, s_q, H, parts)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(lib().mla_decode(_ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(block_table), block_table.shape[1],
+                            _ptr(seqlens), B, s_q, H, float(softmax_scale), int(causal), _ptr(metadata), parts,
+                            _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+                            _stream(stream)), "mla_decode")
+    return out, lse
+
+
+def absorb_q(q_nope: torch.Tensor, w_uk: torch.Tensor, q: torch.Tensor, q_pe: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """q[n, h, 0:512] = q_nope[n, h, :] @ w_uk[h] and q[n, h, 512:576] = q_pe[n, h, :];
+    q is [N, H, 576] (or [B, s_q, H, 576] with N = B*s_q)."""
+    N, H, _ = q_nope.shape
+    pe_ptr, pe_stride = (0, 0) if q_pe is None else (_ptr(q_pe), q_pe.stride(0))
+    _check(lib().mla_absorb_q(_ptr(q_nope), q_nope.stride(0), pe_ptr or None, pe_stride, _ptr(w_uk), _ptr(q), N, H,
+                              _stream(stream)), "mla_absorb_q")
+    return q
+
+
+def unabsorb_o(o_lat: torch.Tensor, w_uv: torch.Tensor, o: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """o[n, h, :] = o_lat[n, h, :] @ w_uv[h]; o_lat is [N, H, 512] -> o [N, H, 128]."""
+    N, H = o_lat.shape[0], o_lat.shape[1]
+    if o is None:
+        o = torch.empty((N, H, 128), dtype=torch.bfloat16, device=o_lat.device)
+    _check(lib().mla_unabsorb_o(_ptr(o_lat), _ptr(w_uv), _ptr(o), N, H, _stream(stream)), "mla_unabsorb_o")
+    return o
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronize the stream; return and clear the kernels' device status word."""
+    return lib().mla_get_device_status(_stream(stream))
+
+
+def debug_withhold_first_load(enable: bool = True):
+    lib().mla_debug_withhold_first_load(int(enable))
+
+
+class DecodeStep:
+    """One decode step of an MLA layer for a fixed batch shape: W_UK absorption,
+    absorbed decode over the paged latent cache, LSE combine, W_UV un-absorption.
+
+    Buffers (q, out, lse, o, metadata, workspace) are allocated once here, with
+    torch, and reused; `run` launches only library kernels.
+    """
+
+    def __init__(self, B: int, s_q: int, H: int, seqlens: torch.Tensor, causal: bool, softmax_scale: float,
+                 parts: int | None = None, device="cuda"):
+        self.B, self.s_q, self.H = B, s_q, H
+        self.causal, self.scale = causal, softmax_scale
+        self.parts = parts if parts is not None else num_sm_parts(s_q, H)
+        dev = torch.device(device)
+        self.q = torch.empty((B, s_q, H, 576), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((B, s_q, H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, s_q, H), dtype=torch.float32, device=dev)
+        self.o = torch.empty((B * s_q, H, 128), dtype=torch.bfloat16, device=dev)
+        self.workspace = torch.empty(decode_workspace_size(B, s_q, H, self.parts), dtype=torch.uint8, device=dev)
+        self.seqlens = seqlens
+        self.metadata = decode_metadata(seqlens, s_q, H, causal, self.parts)
+
+    def plan(self, stream=None):
+        """Recompute the split schedule (after seqlens changed)."""
+        decode_metadata(self.seqlens, self.s_q, self.H, self.causal, self.parts, out=self.metadata, stream=stream)
+
+    def run(self, q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, stream=None):
+        """q_nope [B*s_q,H,128], q_pe [B*s_q,H,64] -> o [B*s_q,H,128] (bf16)."""
+        absorb_q(q_nope, w_uk, self.q, q_pe=q_pe, stream=stream)
+        decode(self.q, kv_cache, block_table, self.seqlens, self.scale, self.causal, self.metadata, self.parts,
+               workspace=self.workspace, out=self.out, lse=self.lse, stream=stream)
+        unabsorb_o(self.out.view(self.B * self.s_q, self.H, 512), w_uv, o=self.o, stream=stream)
+        return self.o

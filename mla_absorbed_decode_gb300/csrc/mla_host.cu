@@ -1,0 +1,282 @@
+// Host side of the C ABI in include/mla.h: argument checks, TMA descriptors,
+// launch configuration.  No device memory is allocated here.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "mla_kernels.h"
+
+namespace mla {
+namespace {
+
+__device__ int g_device_status;   // written by the kernels, read by mla_get_device_status
+
+int g_withhold_first_load = 0;
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  bool ready = false;
+  int* status = nullptr;
+  int sm_count = 0;
+  int parts[kMaxPairsPerCluster + 1] = {0, 0, 0, 0, 0};
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// One-time per-device set-up: kernel attributes, status-word address.
+mla_status_t device_state(int dev, DeviceState** out) {
+  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return MLA_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_device_status) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (decode_set_attributes() != cudaSuccess) return MLA_ERR_CUDA;
+    if (bmm_set_attributes() != cudaSuccess) return MLA_ERR_CUDA;
+    for (int n = 1; n <= kMaxPairsPerCluster; ++n) d.parts[n] = decode_max_clusters(2 * n);
+    d.ready = true;
+  }
+  *out = &d;
+  return MLA_OK;
+}
+
+mla_status_t current_device(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  return device_state(dev, out);
+}
+
+int pairs_for(int s_q, int H) { return (s_q * H + kRowsPerPair - 1) / kRowsPerPair; }
+
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes, uint32_t box_inner,
+               uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
+               uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t max_splits(int B, int num_parts) { return static_cast<size_t>(B) + static_cast<size_t>(num_parts); }
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_string(mla_status_t s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_DEVICE_BOUNDS: return "MLA_ERR_DEVICE_BOUNDS";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+int mla_num_sm_parts(int device, int s_q, int H) {
+  if (s_q < 1 || H < 1) return -MLA_ERR_INVALID_ARG;
+  const int n = pairs_for(s_q, H);
+  if (n > kMaxPairsPerCluster) return -MLA_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  const mla_status_t st = device_state(device, &d);
+  if (st != MLA_OK) return -st;
+  return d->parts[n];
+}
+
+size_t mla_metadata_size(int B, int num_sm_parts) {
+  if (B < 0 || num_sm_parts < 1) return 0;
+  return (static_cast<size_t>(kMetaInts) * num_sm_parts + B + 1) * sizeof(int32_t);
+}
+
+void mla_schedule_params(int* fixed_cost_pages, int* hbm_parts) {
+  if (fixed_cost_pages) *fixed_cost_pages = kSegmentCostPages;
+  if (hbm_parts) *hbm_parts = kHbmParts;
+}
+
+mla_status_t mla_decode_metadata(const int32_t* seqlens, int B, int s_q, int H, int causal_s_q, int num_sm_parts,
+                                 void* metadata, mla_stream_t stream) {
+  (void)causal_s_q;
+  if (!seqlens || !metadata || B < 1 || s_q < 1 || H < 1 || num_sm_parts < 1) return MLA_ERR_INVALID_ARG;
+  if (pairs_for(s_q, H) > kMaxPairsPerCluster) return MLA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(metadata) & 3u) != 0) return MLA_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  mla_status_t st = current_device(&d);
+  if (st != MLA_OK) return st;
+  int32_t* meta = static_cast<int32_t*>(metadata);
+  return launch_schedule(seqlens, B, num_sm_parts, kSegmentCostPages, kHbmParts, meta, meta + kMetaInts * num_sm_parts,
+                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+size_t mla_decode_workspace_size(int B, int s_q, int H, int num_sm_parts) {
+  if (B < 1 || s_q < 1 || H < 1 || num_sm_parts < 1) return 0;
+  const size_t rows = static_cast<size_t>(s_q) * H;
+  const size_t ms = max_splits(B, num_sm_parts);
+  const size_t o_bytes = ms * rows * kDimV * sizeof(float);
+  const size_t l_bytes = ms * rows * sizeof(float);
+  return o_bytes + ((l_bytes + 255) / 256) * 256;
+}
+
+mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t num_blocks, const int32_t* block_table,
+                        int max_blocks, const int32_t* seqlens, int B, int s_q, int H, float softmax_scale,
+                        int causal_s_q, const void* metadata, int num_sm_parts, void* workspace,
+                        size_t workspace_bytes, mla_bf16_t* out, float* lse, mla_stream_t stream) {
+  if (!q || !kv_cache || !block_table || !seqlens || !metadata || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (B < 1 || s_q < 1 || H < 1 || num_blocks < 1 || max_blocks < 1 || num_sm_parts < 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(metadata) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  const int n_rb = pairs_for(s_q, H);
+  if (n_rb > kMaxPairsPerCluster) return MLA_ERR_UNSUPPORTED;
+  if (num_blocks * kPageTokens > (int64_t(1) << 31) - kPageTokens) return MLA_ERR_UNSUPPORTED;
+  const size_t need = mla_decode_workspace_size(B, s_q, H, num_sm_parts);
+  if (workspace_bytes < need || (need > 0 && !workspace)) return MLA_ERR_WORKSPACE;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return MLA_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  mla_status_t st = current_device(&d);
+  if (st != MLA_OK) return st;
+
+  CUtensorMap kv_map;
+  if (!encode_2d(&kv_map, kv_cache, kDimQK, static_cast<uint64_t>(num_blocks) * kPageTokens, kDimQK * 2, 64, 64))
+    return MLA_ERR_CUDA;
+
+  const int rows = s_q * H;
+  const size_t ms = max_splits(B, num_sm_parts);
+  DecodeParams p;
+  p.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  p.kv = reinterpret_cast<const __nv_bfloat16*>(kv_cache);
+  p.num_blocks = num_blocks;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.seqlens = seqlens;
+  p.B = B;
+  p.s_q = s_q;
+  p.H = H;
+  p.rows = rows;
+  p.n_rb = n_rb;
+  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634074);
+  p.causal = causal_s_q ? 1 : 0;
+  p.meta = static_cast<const int32_t*>(metadata);
+  p.num_splits = p.meta + kMetaInts * num_sm_parts;
+  p.num_parts = num_sm_parts;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ms * rows * kDimV * sizeof(float));
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = d->status;
+  p.withhold_first_load = g_withhold_first_load;
+  g_withhold_first_load = 0;
+
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_decode(kv_map, p, 2 * n_rb, cs) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_combine(p.o_part, p.lse_part, p.num_splits, B, rows, p.out, lse, cs) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status_t mla_absorb_q(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                          int64_t q_pe_row_stride, const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H,
+                          mla_stream_t stream) {
+  if (!q_nope || !w_uk || !q || N < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q)) return MLA_ERR_INVALID_ARG;
+  if (q_nope_row_stride < static_cast<int64_t>(H) * 128 || (q_nope_row_stride % 8) != 0) return MLA_ERR_INVALID_ARG;
+  if (q_pe && (!aligned16(q_pe) || q_pe_row_stride < static_cast<int64_t>(H) * 64 || (q_pe_row_stride % 8) != 0))
+    return MLA_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  mla_status_t st = current_device(&d);
+  if (st != MLA_OK) return st;
+  CUtensorMap a_map, w_map;
+  if (!encode_3d(&a_map, q_nope, 128, static_cast<uint64_t>(H), static_cast<uint64_t>(N), 256,
+                 static_cast<uint64_t>(q_nope_row_stride) * 2, 64, 1, 128))
+    return MLA_ERR_CUDA;
+  if (!encode_2d(&w_map, w_uk, 512, static_cast<uint64_t>(H) * 128, 1024, 64, 128)) return MLA_ERR_CUDA;
+  BmmParams p;
+  p.out = reinterpret_cast<__nv_bfloat16*>(q);
+  p.out_row_stride = static_cast<int64_t>(H) * kDimQK;
+  p.out_head_stride = kDimQK;
+  p.N = N;
+  p.H = H;
+  p.status = d->status;
+  p.pe = reinterpret_cast<const __nv_bfloat16*>(q_pe);
+  p.pe_row_stride = q_pe_row_stride;
+  return launch_bmm(true, a_map, w_map, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
+                                                                                               : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* o, int N, int H,
+                            mla_stream_t stream) {
+  if (!o_lat || !w_uv || !o || N < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(o)) return MLA_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  mla_status_t st = current_device(&d);
+  if (st != MLA_OK) return st;
+  CUtensorMap a_map, w_map;
+  if (!encode_3d(&a_map, o_lat, 512, static_cast<uint64_t>(H), static_cast<uint64_t>(N), 1024,
+                 static_cast<uint64_t>(H) * 1024, 64, 1, 128))
+    return MLA_ERR_CUDA;
+  if (!encode_2d(&w_map, w_uv, 128, static_cast<uint64_t>(H) * 512, 256, 64, 256)) return MLA_ERR_CUDA;
+  BmmParams p;
+  p.out = reinterpret_cast<__nv_bfloat16*>(o);
+  p.out_row_stride = static_cast<int64_t>(H) * 128;
+  p.out_head_stride = 128;
+  p.N = N;
+  p.H = H;
+  p.status = d->status;
+  p.pe = nullptr;
+  p.pe_row_stride = 0;
+  return launch_bmm(false, a_map, w_map, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
+                                                                                                : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_get_device_status(mla_stream_t stream) {
+  DeviceState* d = nullptr;
+  mla_status_t st = current_device(&d);
+  if (st != MLA_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
+  return v;
+}
+
+void mla_debug_withhold_first_load(int enable) { g_withhold_first_load = enable ? 1 : 0; }
+
+}  // extern "C"

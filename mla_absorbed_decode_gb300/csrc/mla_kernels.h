@@ -1,0 +1,71 @@
+// Internal interface between the host ABI (mla_host.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kPageTokens = 64;
+constexpr int kDimQK = 576;
+constexpr int kDimV = 512;
+constexpr int kRowsPerPair = 128;
+constexpr int kMaxPairsPerCluster = 4;
+constexpr int kMetaInts = 8;            // ints per part record
+
+// Schedule constants (the CPU restatement in the tests reads them through
+// mla_schedule_params).
+constexpr int kSegmentCostPages = 2;    // one segment's set-up + epilogue, in pages
+constexpr int kHbmParts = 64;           // clusters that already saturate HBM
+
+struct DecodeParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* kv;
+  int64_t num_blocks;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* seqlens;
+  int B, s_q, H, rows, n_rb;
+  float scale_log2;                     // softmax_scale * log2(e)
+  int causal;
+  const int32_t* meta;                  // [num_parts][8]
+  const int32_t* num_splits;            // [B + 1]
+  int num_parts;
+  float* o_part;                        // [max_splits][rows][512]
+  float* lse_part;                      // [max_splits][rows]
+  __nv_bfloat16* out;                   // [B][rows][512]
+  float* lse;                           // [B][rows]
+  int* status;
+  int withhold_first_load;
+};
+
+// Launchers (defined next to their kernels).
+cudaError_t decode_set_attributes();
+int decode_max_clusters(int cluster_ctas);            // occupancy query; 0 on error
+cudaError_t launch_decode(const CUtensorMap& kv_map, const DecodeParams& p, int cluster_ctas, cudaStream_t stream);
+
+cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
+                            int32_t* meta, int32_t* num_splits, cudaStream_t stream);
+cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* num_splits, int B, int rows,
+                           __nv_bfloat16* out, float* lse, cudaStream_t stream);
+
+struct BmmParams {
+  __nv_bfloat16* out;
+  int64_t out_row_stride;   // elements between tokens n
+  int64_t out_head_stride;  // elements between heads h
+  int N;                    // tokens
+  int H;
+  int* status;
+  const __nv_bfloat16* pe;  // optional: copied into out[n, h, 512:576] by the first column tile
+  int64_t pe_row_stride;
+};
+cudaError_t bmm_set_attributes();
+// absorb: K = 128 -> 512 columns; unabsorb: K = 512 -> 128 columns
+cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap& w_map, const BmmParams& p,
+                       cudaStream_t stream);
+
+}  // namespace mla

@@ -53,7 +53,7 @@ def visible_tokens(seqlen: int, s_q: int, i: int, causal: bool) -> int:
     return max(0, min(int(seqlen), int(seqlen) - s_q + i + 1))
 
 
-def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=False):
+def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=False, with_abs=False):
     """The absorbed decode definition: an MQA with a 576-wide key and 512-wide value.
 
     For every request b, query position i and head h, with n = visible tokens:
@@ -65,11 +65,15 @@ def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=Fal
     q: [B, s_q, H, 576]; kv_cache: [num_blocks, 64, 576]; block_table: [B, max_blocks];
     seqlens: [B].  Returns out [B, s_q, H, 512] and lse [B, s_q, H], float64.
     The softmax is evaluated with its maximum subtracted, which changes only rounding.
+    With with_abs=True it also returns out_abs = sum_t p_t |kv_t[:512]|, the
+    attention-weighted magnitude of the values, which sizes the rounding error of
+    a kernel that rounds p_t to bf16 (test tolerance, not part of the method).
     """
     q = np.asarray(q, dtype=np.float64)
     B, s_q, H, dq = q.shape
     assert dq == D_QK
     out = np.zeros((B, s_q, H, D_LATENT))
+    out_abs = np.zeros((B, s_q, H, D_LATENT)) if with_abs else None
     lse = np.full((B, s_q, H), -np.inf)
     for b in range(B):
         L = int(seqlens[b])
@@ -86,6 +90,10 @@ def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=Fal
             z = e.sum(axis=1, keepdims=True)
             lse[b, i] = (m + np.log(z))[:, 0]
             out[b, i] = (e / z) @ kv[:n, :D_LATENT]
+            if with_abs:
+                out_abs[b, i] = (e / z) @ np.abs(kv[:n, :D_LATENT])
+    if with_abs:
+        return out, lse, out_abs
     return out, lse
 
 

@@ -1,0 +1,91 @@
+"""Shared helpers of the parity tests: run the library, run the oracle, compare.
+
+Tolerances (written here, used by every parity test):
+* out: max |delta| <= 2e-2 absolute on bf16 outputs of unit-scale inputs.
+  Inputs with x8 outlier rows are not unit-scale: the kernel feeds P to the
+  tensor cores in bf16, whose rounding (at most 2^-9 relative per p_t) moves
+  an output element by at most 2^-9 * A, A = sum_t p_t |v_t| (the attention-
+  weighted magnitude of the values, from the oracle), and the bf16 output
+  rounding adds at most 2^-9 |out| <= 2^-9 A.  There the bound is elementwise
+  max(2e-2, 2^-7 * A), twice that arithmetic;
+* out, relative: ||delta||_2 / ||ref||_2 <= 1e-2 (typical is ~3e-3: bf16
+  rounding of P and of the output), which guards against the absolute bound
+  being loose when |out| is small;
+* lse: |delta| <= 1e-3 * max(1, |ref|);
+* integer schedule and indexing: bit-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from mla_absorbed_decode_gb300 import workloads as W
+
+OUT_ABS = 2e-2
+OUT_REL_ULP = 2.0 ** -7
+OUT_REL_L2 = 1e-2
+LSE_REL = 1e-3
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def run_library(inp: dict, parts: int | None = None, device="cuda"):
+    """Metadata + decode through the library; returns (out, lse, metadata) as CPU tensors."""
+    import mla_absorbed_decode_gb300 as mla
+    q = inp["q"].to(device)
+    kv = inp["kv_cache"].to(device)
+    bt = inp["block_table"].to(device)
+    sl = inp["seqlens"].to(device)
+    B, s_q, H, _ = q.shape
+    P = parts if parts is not None else mla.num_sm_parts(s_q, H)
+    meta = mla.decode_metadata(sl, s_q, H, inp["causal"], P)
+    out, lse = mla.decode(q, kv, bt, sl, inp["softmax_scale"], inp["causal"], meta, P)
+    st = mla.get_device_status()
+    assert st == 0, f"device status {st}"
+    return out.cpu(), lse.cpu(), meta.cpu(), P
+
+
+def oracle_decode(inp: dict, batches=None):
+    """Oracle on all requests (or a subset); returns float64 arrays for those requests."""
+    sel = list(range(inp["q"].shape[0])) if batches is None else list(batches)
+    kv = inp.get("_kv_np")
+    if kv is None:
+        kv = inp["kv_cache"].float().numpy()
+        inp["_kv_np"] = kv
+    q = to_np(inp["q"][sel])
+    bt = inp["block_table"][sel].numpy()
+    sl = inp["seqlens"][sel].numpy()
+    out, lse, out_abs = oracle.decode_absorbed(q, kv, bt, sl, inp["softmax_scale"], causal=inp["causal"],
+                                               with_abs=True)
+    return out, lse, out_abs
+
+
+def compare(out_gpu: torch.Tensor, lse_gpu: torch.Tensor, ref_out: np.ndarray, ref_lse: np.ndarray,
+            ref_abs: np.ndarray | None = None, what: str = ""):
+    """ref_abs given (inputs with outliers): elementwise bound max(2e-2, 2^-7 * ref_abs)."""
+    o = to_np(out_gpu)
+    lo = to_np(lse_gpu)
+    assert o.shape == ref_out.shape, (o.shape, ref_out.shape)
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    d = np.abs(o - ref_out)
+    bound = np.maximum(OUT_ABS, OUT_REL_ULP * ref_abs) if ref_abs is not None else OUT_ABS
+    worst = np.unravel_index(np.argmax(d - bound), d.shape)
+    assert np.all(d <= bound), f"{what}: max|dout|={d.max():.4g} at {worst} (ref {ref_out[worst]:.4g})"
+    nrm = np.linalg.norm(ref_out)
+    if nrm > 0:
+        rel = np.linalg.norm(o - ref_out) / nrm
+        assert rel <= OUT_REL_L2, f"{what}: relative L2 error {rel:.3g}"
+    both_inf = np.isneginf(lo) & np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lo), np.isneginf(ref_lse)), f"{what}: -inf lse mismatch"
+    with np.errstate(invalid="ignore"):
+        dl = np.where(both_inf, 0.0, np.abs(lo - ref_lse))
+    lb = LSE_REL * np.maximum(1.0, np.abs(np.where(both_inf, 0.0, ref_lse)))
+    assert np.all(dl <= lb), f"{what}: max|dlse|={dl.max():.4g}"
+    return float(d.max()), float(np.linalg.norm(o - ref_out) / max(nrm, 1e-30))
+
+
+def make(w: W.Workload, seed=0, **kw):
+    return W.make_inputs(w, seed=seed, **kw)

@@ -1,0 +1,77 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mla():
+    from mla_absorbed_decode_gb300 import build_lib
+    build_lib.build()
+    import mla_absorbed_decode_gb300 as m
+    m.lib()
+    return m
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "mla.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(mla):
+    names = _declared()
+    assert len(names) >= 11
+    handle = ctypes.CDLL(mla.library_path)
+    for n in names:
+        assert hasattr(handle, n), n
+    assert set(names) == set(mla.EXPORTED_SYMBOLS)
+
+
+def test_status_strings(mla):
+    L = mla.lib()
+    assert L.mla_status_string(0) == b"MLA_OK"
+    assert L.mla_status_string(5) == b"MLA_ERR_TIMEOUT"
+    assert L.mla_status_string(99) == b"MLA_ERR_UNKNOWN"
+
+
+def test_sizes(mla):
+    assert mla.metadata_size(64, 76) == (8 * 76 + 65) * 4
+    assert mla.metadata_size(0, 0) == 0
+    rows = 2 * 128
+    ws = mla.decode_workspace_size(64, 2, 128, 38)
+    assert ws >= (64 + 38) * rows * 513 * 4 and ws % 256 == 0
+    assert mla.decode_workspace_size(0, 1, 1, 1) == 0
+    fixed, hbm = mla.schedule_params()
+    assert fixed >= 0 and hbm >= 1
+
+
+def test_host_argument_checks(mla):
+    L = mla.lib()
+    A = 0x10000  # a 16-byte aligned address that is never dereferenced on these paths
+    ws = mla.decode_workspace_size(2, 1, 16, 4)
+    # a valid-looking argument list; every case below breaks one argument, so the
+    # call returns before touching the device (these addresses are never used)
+    args = [A, A, 10, A, 8, A, 2, 1, 16, 0.1, 0, A, 4, A, ws, A, A, None]
+    bad_null = list(args); bad_null[0] = None
+    assert L.mla_decode(*bad_null) == 1                     # MLA_ERR_INVALID_ARG
+    bad_align = list(args); bad_align[1] = A + 2
+    assert L.mla_decode(*bad_align) == 1
+    bad_shape = list(args); bad_shape[7] = 5; bad_shape[8] = 128   # s_q * H = 640 > 512
+    assert L.mla_decode(*bad_shape) == 2                    # MLA_ERR_UNSUPPORTED
+    small_ws = list(args); small_ws[14] = ws - 1
+    assert L.mla_decode(*small_ws) == 3                     # MLA_ERR_WORKSPACE
+    nan_scale = list(args); nan_scale[9] = float("nan")
+    assert L.mla_decode(*nan_scale) == 1
+    assert L.mla_decode_metadata(None, 2, 1, 16, 0, 4, A, None) == 1
+    assert L.mla_decode_metadata(A, 2, 8, 128, 0, 4, A, None) == 2
+    assert L.mla_absorb_q(A, 100, None, 0, A, A, 4, 1, None) == 1      # stride below H*128
+    assert L.mla_absorb_q(A, 128, A, 8, A, A, 4, 1, None) == 1         # q_pe stride below H*64
+    assert L.mla_unabsorb_o(A + 8, A, A, 4, 1, None) == 1
+    assert L.mla_num_sm_parts(0, 5, 128) < 0

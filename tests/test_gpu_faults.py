@@ -1,0 +1,64 @@
+"""Failure detection on the GPU without a GPU fault.
+
+* A bounded barrier wait that runs out: the test hook withholds the first KV
+  page load of every part; every wait on it gives up after its time limit, the
+  kernel records MLA_ERR_TIMEOUT and exits cleanly, and the context stays
+  usable (the next call is correct).
+* A block-table entry outside [0, num_blocks): the kernel does not read out of
+  bounds (the TMA fills the page with zeros), finishes, and records
+  MLA_ERR_DEVICE_BOUNDS.
+"""
+import pytest
+import torch
+
+from mla_absorbed_decode_gb300 import workloads as W
+
+from _harness import compare, make, oracle_decode, run_library
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_absorbed_decode_gb300 import build_lib
+    build_lib.build()
+    yield
+
+
+def _inputs():
+    w = W.Workload("fault", B=2, s_q=1, H=128, fixed_seqlens=(300, 200))
+    return make(w, seed=2)
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    import mla_absorbed_decode_gb300 as mla
+    inp = _inputs()
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    P = 2
+    meta = mla.decode_metadata(dev["seqlens"], 1, 128, False, P)
+    mla.debug_withhold_first_load(True)
+    mla.decode(dev["q"], dev["kv_cache"], dev["block_table"], dev["seqlens"], inp["softmax_scale"], False, meta, P)
+    assert mla.get_device_status() == 5          # MLA_ERR_TIMEOUT
+    assert mla.get_device_status() == 0          # read-and-clear
+    out, lse, _, _ = run_library(inp, parts=P)   # the next call is correct
+    ref_out, ref_lse, ref_abs = oracle_decode(inp)
+    compare(out, lse, ref_out, ref_lse, what="after timeout")
+
+
+def test_block_table_out_of_range_is_reported():
+    import mla_absorbed_decode_gb300 as mla
+    inp = _inputs()
+    bt = inp["block_table"].clone()
+    bt[1, 1] = inp["kv_cache"].shape[0] + 5      # inside the request's used pages
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    dev["block_table"] = bt.cuda()
+    P = 2
+    meta = mla.decode_metadata(dev["seqlens"], 1, 128, False, P)
+    out, lse = mla.decode(dev["q"], dev["kv_cache"], dev["block_table"], dev["seqlens"], inp["softmax_scale"],
+                          False, meta, P)
+    assert mla.get_device_status() == 6          # MLA_ERR_DEVICE_BOUNDS
+    # request 0 does not use the bad entry and is still exact
+    ref_out, ref_lse, ref_abs = oracle_decode(inp, [0])
+    compare(out[:1].cpu(), lse[:1].cpu(), ref_out, ref_lse, what="request 0 beside a bad entry")

@@ -1,0 +1,96 @@
+"""GPU parity of the W_UK / W_UV projections and of the whole chain
+(absorb -> decode -> un-absorb) against the expanded, un-absorbed definition."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_absorbed_decode_gb300 import workloads as W
+
+from _harness import OUT_ABS, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_absorbed_decode_gb300 import build_lib
+    build_lib.build()
+    yield
+
+
+def _bf(x):
+    return x.to(torch.bfloat16)
+
+
+def _bmm_bound(ref):
+    # one bf16 rounding of an fp32 result: half an ulp is 2^-9 |x|; allow 2^-8 |x| + 1e-3
+    return 2.0 ** -8 * np.abs(ref) + 1e-3
+
+
+@pytest.mark.parametrize("N,H", [(1, 1), (5, 16), (64, 128), (130, 8)])
+def test_absorb_q(N, H):
+    import mla_absorbed_decode_gb300 as mla
+    g = torch.Generator().manual_seed(N * 131 + H)
+    q_nope = _bf(torch.randn((N, H, 128), generator=g))
+    q_pe = _bf(torch.randn((N, H, 64), generator=g))
+    w_uk = _bf(torch.randn((H, 128, 512), generator=g) / math.sqrt(512))
+    q = torch.full((N, H, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mla.absorb_q(q_nope.cuda(), w_uk.cuda(), q, q_pe=q_pe.cuda())
+    assert mla.get_device_status() == 0
+    ref = oracle.absorb_q(to_np(q_nope), to_np(w_uk))
+    got = to_np(q.cpu())
+    assert np.all(np.abs(got[..., :512] - ref) <= _bmm_bound(ref))
+    assert torch.equal(q[..., 512:].cpu(), q_pe)
+
+
+@pytest.mark.parametrize("N,H", [(1, 1), (5, 16), (64, 128), (130, 8)])
+def test_unabsorb_o(N, H):
+    import mla_absorbed_decode_gb300 as mla
+    g = torch.Generator().manual_seed(N * 17 + H)
+    o_lat = _bf(torch.randn((N, H, 512), generator=g) * 0.1)
+    w_uv = _bf(torch.randn((H, 512, 128), generator=g) / math.sqrt(512))
+    o = mla.unabsorb_o(o_lat.cuda(), w_uv.cuda())
+    assert mla.get_device_status() == 0
+    ref = oracle.unabsorb_o(to_np(o_lat), to_np(w_uv))
+    got = to_np(o.cpu())
+    assert np.all(np.abs(got - ref) <= _bmm_bound(ref))
+
+
+def _chain(inp, batches=None):
+    import mla_absorbed_decode_gb300 as mla
+    B, s_q, H = inp["q"].shape[:3]
+    step = mla.DecodeStep(B, s_q, H, inp["seqlens"].cuda(), inp["causal"], inp["softmax_scale"])
+    o = step.run(inp["q_nope"].cuda(), inp["q_pe"].cuda(), inp["w_uk"].cuda(), inp["w_uv"].cuda(),
+                 inp["kv_cache"].cuda(), inp["block_table"].cuda())
+    assert mla.get_device_status() == 0
+    o = o.view(B, s_q, H, 128).cpu()
+    sel = list(range(B)) if batches is None else batches
+    kv = inp["kv_cache"].float().numpy()
+    qn = to_np(inp["q_nope"]).reshape(B, s_q, H, 128)
+    qp = to_np(inp["q_pe"]).reshape(B, s_q, H, 64)
+    ref, ref_lse = oracle.decode_expanded(qn[sel], qp[sel], to_np(inp["w_uk"]), to_np(inp["w_uv"]), kv,
+                                          inp["block_table"][sel].numpy(), inp["seqlens"][sel].numpy(),
+                                          inp["softmax_scale"], causal=inp["causal"])
+    return to_np(o[sel]), ref, step
+
+
+def test_chain_small_vs_expanded_definition():
+    w = W.small_variant(W.V3, B=3, seqlen=700)
+    inp = W.make_inputs(w)
+    got, ref, _ = _chain(inp)
+    d = np.abs(got - ref)
+    assert d.max() <= OUT_ABS, d.max()
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2e-2
+
+
+def test_chain_full_v3_sampled_vs_expanded_definition():
+    inp = W.make_inputs(W.V3)
+    got, ref, _ = _chain(inp, batches=[0, 17, 63])
+    d = np.abs(got - ref)
+    assert d.max() <= OUT_ABS, d.max()
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2e-2

@@ -112,6 +112,18 @@ def test_against_sdpa_fp64(causal, s_q):
         assert np.max(np.abs(ref_lse - lse[b])) < 1e-12
 
 
+def test_weighted_magnitude_output():
+    rng = np.random.default_rng(9)
+    q, kv, bt, lens, scale = _rand_case(rng, B=2, H=3, lens=(70, 129))
+    out, lse, out_abs = oracle.decode_absorbed(q, kv, bt, lens, scale, with_abs=True)
+    assert np.all(np.abs(out) <= out_abs + 1e-12)                  # triangle inequality
+    o2, l2 = oracle.decode_absorbed(q, np.abs(kv), bt, lens, scale)  # with |v| as values
+    # same scores only where the key part is unchanged: compare on a case with non-negative cache
+    kvp = np.abs(kv)
+    out_p, _, abs_p = oracle.decode_absorbed(q, kvp, bt, lens, scale, with_abs=True)
+    assert np.max(np.abs(out_p - abs_p)) < 1e-12                    # non-negative values: equal
+
+
 def test_causal_alignment_matches_shorter_context():
     rng = np.random.default_rng(4)
     q, kv, bt, lens, scale = _rand_case(rng, B=1, s_q=2, H=3, lens=(100,))
