@@ -128,13 +128,39 @@ mla_status_t mla_absorb_q(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, c
 mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* o,
                             int N, int H, mla_stream_t stream);
 
+/* mla_decode without caller-provided scratch.  The paper has no counterpart:
+ * this entry point exists for callers that cannot allocate device memory or pass
+ * a workspace -- code inside an inference engine or plugin whose memory pool
+ * hands out no scratch, or a decode loop that must never enter the allocator
+ * (cudaMalloc can synchronize the device and fail under fragmentation).
+ * It computes the split schedule and runs the same kernels as
+ * mla_decode_metadata + mla_decode, with the schedule metadata and the fp32
+ * split partials placed in one fixed 64 MiB array of device memory that the
+ * library defines and that every GPU loading the library holds until exit.
+ * Limits: mla_metadata_size(B, num_sm_parts) <= 256 KiB and
+ * mla_decode_workspace_size(B, s_q, H, num_sm_parts) <= 64 MiB - 256 KiB, else
+ * MLA_ERR_WORKSPACE and no launch (for H = 128, s_q = 1 that is
+ * B + num_sm_parts <= 254).  It allocates nothing and calls no allocating routine.
+ * The first call on a device resolves the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the array and it keeps the last call's contents (nothing in it needs to
+ * start at zero): calls whose kernels overlap on the GPU -- for example calls
+ * on two streams of one process -- race on it and must be serialized by the
+ * caller.  Arguments are those of mla_decode minus
+ * metadata and workspace; the result is identical to mla_decode's for the same
+ * num_sm_parts.  Async on stream. */
+mla_status_t mla_decode_noalloc(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t num_blocks,
+                                const int32_t* block_table, int max_blocks, const int32_t* seqlens,
+                                int B, int s_q, int H, float softmax_scale, int causal_s_q, int num_sm_parts,
+                                mla_bf16_t* out, float* lse, mla_stream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the device status word that the
  * kernels set (MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_BOUNDS). */
 mla_status_t mla_get_device_status(mla_stream_t stream);
 
 /* Test hook: when nonzero, the next mla_decode launch withholds the first KV
  * page load of every part, so that each barrier wait on it runs out of time
- * (about 0.2 s) and the call reports MLA_ERR_TIMEOUT through
+ * (0.5 s) and the call reports MLA_ERR_TIMEOUT through
  * mla_get_device_status.  No memory access is made out of bounds and nothing
  * traps; the flag clears itself after one launch. */
 void mla_debug_withhold_first_load(int enable);

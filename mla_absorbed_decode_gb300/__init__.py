@@ -38,6 +38,8 @@ _SIGNATURES = {
                             _p, _c_int, _p, _c_size, _p, _p, _p]),
     "mla_absorb_q": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _p, _c_int, _c_int, _p]),
     "mla_unabsorb_o": (_c_int, [_p, _p, _p, _c_int, _c_int, _p]),
+    "mla_decode_noalloc": (_c_int, [_p, _p, _c_ll, _p, _c_int, _p, _c_int, _c_int, _c_int, _c_float, _c_int,
+                                    _c_int, _p, _p, _p]),
     "mla_get_device_status": (_c_int, [_p]),
     "mla_debug_withhold_first_load": (None, [_c_int]),
 }

@@ -89,6 +89,13 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uin
 size_t max_splits(int B, int num_parts) { return static_cast<size_t>(B) + static_cast<size_t>(num_parts); }
 
 }  // namespace
+
+int* device_status_word() {
+  DeviceState* d = nullptr;
+  if (current_device(&d) != MLA_OK) return nullptr;
+  return d->status;
+}
+
 }  // namespace mla
 
 using namespace mla;

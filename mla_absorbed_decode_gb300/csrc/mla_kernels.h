@@ -43,6 +43,10 @@ struct DecodeParams {
   int withhold_first_load;
 };
 
+// Device address of the kernels' status word on the current device (set-up on
+// first use); nullptr on error.
+int* device_status_word();
+
 // Launchers (defined next to their kernels).
 cudaError_t decode_set_attributes();
 int decode_max_clusters(int cluster_ctas);            // occupancy query; 0 on error
