@@ -12,24 +12,28 @@
 // Design on GB300.  A 128-row tile of queries against a 64-token page needs an
 // fp32 output accumulator of 128 x 512 -- all 512 TMEM columns of one SM -- so
 // the work of one row block is split over a CTA pair in one cluster:
-//   * the S-CTA (even cluster rank) keeps Q in TMEM (288 columns, A operand),
-//     computes S = Q K^T for each page with tcgen05 (A from TMEM, B = the page in
-//     shared memory), runs the online softmax in fp32, and ships P (bf16, in the
-//     MMA operand layout) plus the per-row rescale factors to its partner with a
-//     shared-to-shared bulk copy;
+//   * the S-CTA (even cluster rank) keeps Q in TMEM (288 columns, the MMA's A
+//     operand), computes S = Q K^T for each page with tcgen05 (B = the page in
+//     shared memory, two pages in flight), and runs the online softmax in fp32
+//     with two warpgroups that split the page's 64 columns.  It stages P (bf16,
+//     already in the MMA operand layout) and the per-row rescale factors in its
+//     shared memory and ships them to its partner with one shared-to-shared bulk
+//     copy per page (many small remote stores are several times slower);
 //   * the O-CTA (odd rank) keeps O (128 x 512 fp32) in TMEM, loads the value
-//     part of each page, runs O += P V with tcgen05, rescales O only when a row
-//     maximum grew by more than 2^8 (exact: the final normalisation uses the same
-//     reference maximum), and writes the normalised output (bf16) or, for a
-//     split request, an fp32 partial that the combine kernel merges.
+//     part of each page (three in flight), runs O += P V with tcgen05, rescales O
+//     only when a row maximum grew by more than 2^8 (exact: the final
+//     normalisation uses the same reference maximum), and writes the normalised
+//     output (bf16) or, for a split request, an fp32 partial that the combine
+//     kernel merges.
 // Rows beyond 128 (s_q * H > 128) go to further pairs of the same cluster, which
 // walk the same pages at the same time so that a page is fetched from HBM once.
 // A cluster is one "part" of the split schedule and walks the segments the
 // metadata assigns to it.
 //
-// Roles inside a CTA (256 threads): warp 0 = TMA producer, warp 1 = MMA issuer,
-// warp 2 = credit forwarder (O-CTA), warps 4..7 = softmax (S-CTA) or
-// rescale/epilogue (O-CTA) warpgroup, one query row per thread.
+// Roles (384 threads): warp 0 = TMA producer, warp 1 = MMA issuer (warp-uniform,
+// one elected lane issues), warp 2 = credit forwarder (O-CTA), warps 4..7 and
+// 8..11 = two softmax (S-CTA) or rescale/epilogue (O-CTA) warpgroups; a thread
+// of a warpgroup owns one query row (its TMEM lane).
 // Every barrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT,
 // raises an abort flag in every CTA of its cluster, drains what it has in
 // flight and exits.
@@ -47,58 +51,64 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr uint32_t kKStageBytes = 9 * 8192;          // 64 tokens x 576 dims, 9 swizzled chunks
-constexpr uint32_t kVStageBytes = 8 * 8192;          // 64 tokens x 512 dims
-constexpr uint32_t kPBytes = 128 * 128;              // P: 128 rows x 64 tokens bf16
-constexpr uint32_t kPktAlpha = kPBytes;              // float[128]
-constexpr uint32_t kPktInvL = kPBytes + 512;         // float[128]
-constexpr uint32_t kPktFlags = kPBytes + 1024;       // uint32[4]
-constexpr uint32_t kPktBytes = kPBytes + 1024 + 16;  // bytes moved per page
-constexpr uint32_t kPktStride = 18 * 1024;
+constexpr int kThreads = 384;
+constexpr int kKStages = 2;                           // S-CTA: pages in flight
+constexpr int kVStages = 2;                           // O-CTA: pages in flight (its loads hit L2)
+constexpr int kStages = 2;                            // barrier slots (the larger of the two)
+constexpr int kSlots = 4;                             // O-CTA packet receive slots: a slot's credit
+                                                      // round trip over DSMEM is hidden 4 pages deep
+constexpr uint32_t kKStageBytes = 9 * 8192;           // S-CTA: 64 tokens x 576 dims, 9 swizzled chunks
+constexpr uint32_t kVStageBytes = 8 * 8192;           // O-CTA: 64 tokens x 512 dims
+constexpr uint32_t kPBytes = 128 * 128;               // P: 128 rows x 64 tokens bf16 (MMA A layout)
+constexpr uint32_t kPktAlpha = kPBytes;               // float[128] rescale factor per row
+constexpr uint32_t kPktInvL = kPBytes + 512;          // float[128] 1/l per row (last page of a segment)
+constexpr uint32_t kPktStride = kPBytes + 1024;       // 17 KiB, a multiple of 1024; all of it is copied
 // dynamic shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t kOffStage = 0;                    // 2 K stages (S-CTA) or 2 V stages (O-CTA)
-constexpr uint32_t kOffRecv = 2 * kVStageBytes;      // O-CTA: 2 packet receive slots
-constexpr uint32_t kOffSend = 2 * kKStageBytes;      // S-CTA: 2 packet staging slots
-constexpr uint32_t kSmemBytes = kOffSend + 2 * kPktStride;
-constexpr uint32_t kQCol = 0, kSCol0 = 320;          // S-CTA TMEM columns: Q [0,288), S buffers 320, 384
-constexpr float kRescaleLog2 = 8.0f;                 // rebase the row max when it grows by more than 2^8
-constexpr int kPrefetchAhead = 4;                    // pages prefetched into L2 ahead of the loads
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kOffRecv = kVStages * kVStageBytes;            // O-CTA: kSlots packet receive slots
+constexpr uint32_t kOffSend = kKStages * kKStageBytes;            // S-CTA: 2 packet staging slots
+constexpr uint32_t kOffPm = kOffSend + 2 * kPktStride;            // S-CTA: row-max exchange [2][128]
+constexpr uint32_t kOffLpart = kOffPm + 1024;                     // S-CTA: partial row sums [128]
+constexpr uint32_t kOffInvL = kOffRecv + kSlots * kPktStride;     // O-CTA: 1/l of the segment [128]
+constexpr uint32_t kOffSharedO = kOffInvL + 512;
+constexpr uint32_t kOffShared = kOffSharedO > kOffLpart + 512 ? kOffSharedO : kOffLpart + 512;  // both roles
+constexpr uint32_t kSmemBytes = kOffShared + 640;
+static_assert(kOffLpart + 512 <= kOffShared, "S-CTA layout");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+constexpr uint32_t kQCol = 0, kSCol0 = 320;           // S-CTA TMEM columns: Q [0,288), S buffers 320, 384
+constexpr float kRescaleLog2 = 8.0f;                  // rebase the row max when it grows by more than 2^8
 constexpr uint64_t kTimeoutNs = 500ull * 1000 * 1000;
 constexpr float kLn2 = 0.69314718055994530942f;
-
-static_assert(kOffRecv + 2 * kPktStride <= kSmemBytes, "O-CTA layout");
-static_assert(kPktBytes % 16 == 0 && kPktStride % 1024 == 0, "packet alignment");
+constexpr uint32_t kSoftThreads = 256;                // two warpgroups
 
 struct Bars {
-  uint64_t full[2];       // page landed (S: K, O: V)
-  uint64_t empty[2];      // stage free again
-  uint64_t s_full[2];     // S-CTA: S = QK^T ready in TMEM
-  uint64_t s_empty[2];    // S-CTA: S read by the softmax warps
-  uint64_t q_full;        // S-CTA: Q of the segment stored in TMEM
-  uint64_t credit[2];     // S-CTA: the partner's receive slot is free (remote arrivals)
-  uint64_t p_full[2];     // O-CTA: packet received (bulk-copy bytes)
-  uint64_t p_free[2];     // O-CTA: PV MMAs that read a packet slot are done
-  uint64_t o_full;        // O-CTA: the segment's last PV MMAs are done
-  uint64_t o_free;        // O-CTA: epilogue finished reading O
-  uint64_t o_sync;        // O-CTA: all PV MMAs issued so far are done (before a rescale)
-  uint64_t corr_go;       // O-CTA: command for the rescale/epilogue warpgroup
-  uint64_t corr_done;     // O-CTA: rescale finished
-  uint64_t drain;         // both: final MMA completion
+  uint64_t full[kStages];   // page landed (S: K, O: V)
+  uint64_t empty[kStages];  // stage free again
+  uint64_t s_full[2];       // S-CTA: S = QK^T ready in TMEM
+  uint64_t s_empty[2];      // S-CTA: S read by the softmax warps (8 arrivals)
+  uint64_t q_full;          // S-CTA: Q of the segment stored in TMEM (8 arrivals)
+  uint64_t credit[kSlots];  // S-CTA: the partner's receive slot is free (remote arrival)
+  uint64_t p_full[kSlots];  // O-CTA: packet bytes arrived (bulk copy from the partner)
+  uint64_t p_free[kSlots];  // O-CTA: PV MMAs that read a packet slot are done
+  uint64_t o_full;          // O-CTA: the segment's last PV MMAs are done
+  uint64_t o_free;          // O-CTA: epilogue finished reading O (8 arrivals)
+  uint64_t o_sync;          // O-CTA: all PV MMAs issued so far are done (before a rescale)
+  uint64_t corr_go;         // O-CTA: command for the rescale/epilogue warpgroups
+  uint64_t corr_done;       // O-CTA: rescale finished (8 arrivals)
+  uint64_t drain;           // both: final MMA completion
 };
 
-struct __align__(16) Shared {
+struct Shared {
   Bars bar;
   uint32_t tmem_base;
   volatile int abort;
-  int cmd;                // O-CTA command: 1 = rescale (slot in cmd_arg), 2 = epilogue, 3 = exit
+  int cmd;                  // O-CTA command: 1 = rescale (slot in cmd_arg), 2 = epilogue, 3 = exit
   int cmd_arg;
-  __align__(16) float inv_l[128];   // O-CTA: 1/l of the segment's rows (16-byte vector copies)
 };
-static_assert(offsetof(Shared, inv_l) % 16 == 0, "inv_l is copied with 16-byte shared stores");
+static_assert(sizeof(Shared) <= 640, "control block");
 
 struct Segment {
-  int b, kb, ke, split;   // request, page range, split index within the request
+  int b, kb, ke, split;     // request, page range, split index within the request
 };
 
 // Walks the segments of one part in order (same walk in every role).
@@ -146,10 +156,8 @@ __device__ __forceinline__ void raise_abort(Shared& sh, int* status, int code, u
   sh.abort = 1;
 }
 
-// Bounded wait.  Returns false on abort or timeout (after raising the abort).
-__device__ __noinline__ bool wait_bar(Shared& sh, uint32_t bar, uint32_t parity, int* status,
-                                      uint32_t cluster_ctas, bool cluster_scope = false) {
-  if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+__device__ __noinline__ bool wait_bar_slow(Shared& sh, uint32_t bar, uint32_t parity, int* status,
+                                           uint32_t cluster_ctas, bool cluster_scope) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
@@ -159,6 +167,12 @@ __device__ __noinline__ bool wait_bar(Shared& sh, uint32_t bar, uint32_t parity,
       return false;
     }
   }
+}
+// Bounded wait.  Returns false on abort or timeout (after raising the abort).
+__device__ __forceinline__ bool wait_bar(Shared& sh, uint32_t bar, uint32_t parity, int* status,
+                                         uint32_t cluster_ctas, bool cluster_scope = false) {
+  if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+  return wait_bar_slow(sh, bar, parity, status, cluster_ctas, cluster_scope);
 }
 // All 32 lanes wait; the result is made uniform across the warp.
 __device__ __forceinline__ bool warp_wait(Shared& sh, uint32_t bar, uint32_t parity, int* status, uint32_t cluster_ctas,
@@ -189,46 +203,42 @@ __device__ __forceinline__ int request_block(const DecodeParams& p, int b, int k
   return blk;
 }
 
-// ------------------------------------------------------------------ S-CTA --
-__device__ void s_cta_producer(const DecodeParams& p, const CUtensorMap* kv_map, Shared& sh, uint32_t smem,
-                               int part, uint32_t cl, bool prefetcher) {
+// Lane 0 of warp 0: stream every page of every segment through the page stages.
+// S-CTA: all 576 dims (9 swizzled 64 x 64 chunks, 72 KiB); O-CTA: the 512 value
+// dims (8 chunks, 64 KiB).
+template <int NST, int NCHUNK>
+__device__ void producer(const DecodeParams& p, const CUtensorMap* kv_map, Shared& sh, uint32_t smem, int part,
+                         uint32_t cl, bool withhold) {
+  constexpr uint32_t kBytes = NCHUNK * 8192;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
   uint32_t T = 0;
-  uint32_t issued_mask_phase[2] = {0, 0};
-  int issued[2] = {0, 0};
+  int issued[NST];
+  uint32_t issued_phase[NST];
+  for (int i = 0; i < NST; ++i) issued[i] = 0, issued_phase[i] = 0;
   const uint64_t policy = l2_policy_evict_first();
   bool ok = true;
   while (ok && w.next(s)) {
-    if (prefetcher) {
-      for (int k = s.kb; k < s.ke && k < s.kb + kPrefetchAhead && k < p.max_blocks; ++k) {
-        const int blk = __ldg(p.block_table + static_cast<int64_t>(s.b) * p.max_blocks + k);
-        if (blk >= 0 && blk < p.num_blocks) prefetch_l2(p.kv + static_cast<int64_t>(blk) * 64 * 576, kKStageBytes);
-      }
-    }
     for (int k = s.kb; k < s.ke; ++k, ++T) {
-      const uint32_t st = T & 1, ph = (T >> 1) & 1;
+      const uint32_t st = T % NST, ph = (T / NST) & 1;
       if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      if (prefetcher && k + kPrefetchAhead < s.ke && k + kPrefetchAhead < p.max_blocks) {
-        const int blk = __ldg(p.block_table + static_cast<int64_t>(s.b) * p.max_blocks + k + kPrefetchAhead);
-        if (blk >= 0 && blk < p.num_blocks) prefetch_l2(p.kv + static_cast<int64_t>(blk) * 64 * 576, kKStageBytes);
-      }
-      if (p.withhold_first_load && T == 0) continue;   // test hook: this page never arrives
+      if (withhold && T == 0) continue;   // test hook: this page never arrives
       const int blk = request_block(p, s.b, k);
       const uint32_t full = smem_u32(&sh.bar.full[st]);
-      mbar_arrive_expect_tx(full, kKStageBytes);
-      const uint32_t dst = smem + kOffStage + st * kKStageBytes;
-      for (int c = 0; c < 9; ++c) tma_load_2d_hint(dst + c * 8192, kv_map, full, c * 64, blk * 64, policy);
+      mbar_arrive_expect_tx(full, kBytes);
+      const uint32_t dst = smem + kOffStage + st * kBytes;
+      for (int c = 0; c < NCHUNK; ++c) tma_load_2d_hint(dst + c * 8192, kv_map, full, c * 64, blk * 64, policy);
       issued[st] = 1;
-      issued_mask_phase[st] = ph;
+      issued_phase[st] = ph;
     }
   }
   // drain: loads still in flight land before the CTA may exit
-  for (int st = 0; st < 2; ++st)
-    if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_mask_phase[st]);
+  for (int st = 0; st < NST; ++st)
+    if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
 }
 
+// ------------------------------------------------------------------ S-CTA --
 // Warp 1 of the S-CTA; all 32 lanes run the loop, one elected lane issues.
 __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl) {
   SegmentWalker w;
@@ -241,19 +251,20 @@ __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
   while (ok && w.next(s)) {
     if (!warp_wait(sh, smem_u32(&sh.bar.q_full), seg & 1, p.status, cl)) break;
     for (int k = s.kb; k < s.ke; ++k, ++T) {
-      const uint32_t st = T & 1, ph = (T >> 1) & 1;
+      const uint32_t st = T % kKStages, ph = (T / kKStages) & 1;
+      const uint32_t sb = T & 1, sph = (T >> 1) & 1;
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
-      if (!warp_wait(sh, smem_u32(&sh.bar.s_empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      if (!warp_wait(sh, smem_u32(&sh.bar.s_empty[sb]), sph ^ 1, p.status, cl)) { ok = false; break; }
       tc_fence_after();
       const uint32_t kstage = smem + kOffStage + st * kKStageBytes;
-      const uint32_t d = tmem + kSCol0 + st * 64;
+      const uint32_t d = tmem + kSCol0 + sb * 64;
 #pragma unroll
       for (int kk = 0; kk < 36; ++kk) {
         const uint64_t bdesc = smem_desc_sw128(kstage + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
         mma_bf16_ts_warp(d, tmem + kQCol + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
       }
       mma_commit_warp(smem_u32(&sh.bar.empty[st]));
-      mma_commit_warp(smem_u32(&sh.bar.s_full[st]));
+      mma_commit_warp(smem_u32(&sh.bar.s_full[sb]));
       any = true;
     }
     ++seg;
@@ -265,17 +276,36 @@ __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
   __syncwarp();
 }
 
+__device__ __forceinline__ float max32(const float (&x)[32]) {
+  float m[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m[i] = fmaxf(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return m[0];
+}
+
+// Warps 4..11 of the S-CTA.  Warpgroup wg (0 or 1) handles columns [32*wg, 32*wg+32)
+// of every page for its 128 rows; the two exchange row maxima and partial sums
+// through shared memory and use named barrier 1 (256 threads).
 __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb,
                               uint32_t peer) {
-  const int r = threadIdx.x - 128;          // row within the block == TMEM lane
+  const int t = threadIdx.x - 128;
+  const int wg = t >> 7;
+  const int r = t & 127;                    // row within the block == TMEM lane
   const int wq = r >> 5, lane = r & 31;
+  const int c0 = wg * 32;
   const int g = rb * 128 + r;               // row within the request: i * H + h
   const bool row_valid = g < p.rows;
   const int pos_i = row_valid ? g / p.H : 0;
   const uint32_t tmem_lane = sh.tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
   const uint32_t peer_recv = map_to_rank(smem + kOffRecv, peer);
   const uint32_t peer_pfull0 = map_to_rank(smem_u32(&sh.bar.p_full[0]), peer);
-  const uint32_t peer_pfull1 = map_to_rank(smem_u32(&sh.bar.p_full[1]), peer);
+  const uint32_t pm_mine = smem + kOffPm + (wg * 128 + r) * 4;
+  const uint32_t pm_other = smem + kOffPm + ((1 - wg) * 128 + r) * 4;
+  const uint32_t lpart = smem + kOffLpart + r * 4;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
@@ -285,19 +315,27 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
     const int L = __ldg(p.seqlens + s.b);
     int vis = L;
     if (p.causal && row_valid) vis = L - p.s_q + pos_i + 1;
-    // Q of this request into TMEM columns [0, 288): one row per thread.
+    // Q of this request into TMEM columns [0, 288): warpgroup wg stores words
+    // [144 wg, 144 wg + 144).  The 36 loads per thread go out in two batches so
+    // that the row costs two memory round trips, not nine.
     {
       const int gq = row_valid ? g : 0;
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(s.b) * p.rows + gq) * 576);
-#pragma unroll 1
-      for (int c = 0; c < 9; ++c) {
-        uint32_t v[32];
+      const uint4* src =
+          reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(s.b) * p.rows + gq) * 576) + wg * 36;
+      {
+        uint4 x[20];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4 x = row_valid ? __ldg(src + c * 8 + j) : make_uint4(0, 0, 0, 0);
-          v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
-        }
-        tmem_st32(tmem_lane + kQCol + c * 32, v);
+        for (int j = 0; j < 20; ++j) x[j] = row_valid ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < 5; ++c) tmem_st16(tmem_lane + kQCol + wg * 144 + c * 16, reinterpret_cast<uint32_t*>(&x[4 * c]));
+      }
+      {
+        uint4 x[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[j] = row_valid ? __ldg(src + 20 + j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_st16(tmem_lane + kQCol + wg * 144 + (5 + c) * 16, reinterpret_cast<uint32_t*>(&x[4 * c]));
       }
       tmem_wait_st();
       tc_fence_before();
@@ -308,27 +346,24 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
     for (int k = s.kb; k < s.ke; ++k, ++T) {
       const uint32_t sb = T & 1, ph = (T >> 1) & 1;
       const bool got = wait_bar(sh, smem_u32(&sh.bar.s_full[sb]), ph, p.status, cl);
-      if (named_bar_or(1, 128, !got)) { ok = false; break; }   // same decision in all 128 threads
+      if (named_bar_or(1, kSoftThreads, !got)) { ok = false; break; }   // same decision in all 256 threads
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(tmem_lane + kSCol0 + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tmem_lane + kSCol0 + sb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      uint32_t sr[32];
+      tmem_ld32(tmem_lane + kSCol0 + sb * 64 + c0, sr);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.bar.s_empty[sb]));
 
       // scaled, masked scores (log2 units); slots at or past `vis` become -inf
-      const int t0 = k * 64;
-      const int nvalid = vis - t0;              // columns c < nvalid are visible
-      float x[64];
-      float mt = -INFINITY;
+      const int nvalid = vis - (k * 64 + c0);   // columns c < nvalid are visible
+      float x[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        x[c] = (c < nvalid) ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[c]);
-      }
-      const float m_new = fmaxf(m_ref, mt);
+      for (int c = 0; c < 32; ++c) x[c] = (c < nvalid) ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
+      const float my_max = max32(x);
+      asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine), "f"(my_max) : "memory");
+      named_bar_sync(1, kSoftThreads);
+      const float m_new = fmaxf(m_ref, fmaxf(my_max, ld_shared_f32(pm_other)));
       float alpha = 1.f;
       const bool rebase = m_new > m_ref + kRescaleLog2;
       if (rebase) {
@@ -336,49 +371,52 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
         m_ref = m_new;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      uint32_t pk[32];
-      float psum = 0.f;
+      uint32_t pk[16];
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {   // l sums the fp32 probabilities; P goes to the MMA in bf16
+      for (int c = 0; c < 16; ++c) {   // l sums the fp32 probabilities; P goes to the MMA in bf16
         const float e0 = fast_exp2(x[2 * c] - m_use), e1 = fast_exp2(x[2 * c + 1] - m_use);
         pk[c] = pack_bf16x2(e0, e1);
-        psum += e0 + e1;
+        ps[c & 3] += e0 + e1;
       }
-      l = l * alpha + psum;
+      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       const bool last = (k == s.ke - 1);
-      const bool first = (k == s.kb);
-      const uint32_t need = __ballot_sync(0xffffffffu, rebase && !first);
+      if (last && wg == 1) asm volatile("st.shared.f32 [%0], %1;" :: "r"(lpart), "f"(l) : "memory");
 
-      // packet into the staging slot, then one bulk copy to the partner
+      // Staging slot sb is free once the bulk copy that used it two pages ago has
+      // read it, and the partner's receive slot rs once its PV of the page that used
+      // it (kSlots pages ago) is done.
+      const uint32_t rs = T % kSlots, rph = (T / kSlots) & 1;
+      bool ready = true;
+      if (t == 0) {
+        bulk_wait_group_read<1>();
+        ready = wait_bar(sh, smem_u32(&sh.bar.credit[rs]), rph ^ 1, p.status, cl, true);
+      }
+      if (named_bar_or(1, kSoftThreads, !ready)) { ok = false; break; }
       const uint32_t slot = smem + kOffSend + sb * kPktStride;
-      if (r == 0) bulk_wait_group_read<1>();     // the copy that used this slot two pages ago has read it
-      named_bar_sync(1, 128);
-      {
-        const uint32_t row = slot + r * 128;
+      const uint32_t row = slot + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t a = row + ((c ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       :: "r"(a), "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3]) : "memory");
-        }
+      for (int j = 0; j < 4; ++j) {
+        const int cc = wg * 4 + j;              // 16-byte chunk: tokens 8cc .. 8cc+7
+        st_shared_v4(row + ((cc ^ (r & 7)) << 4), make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
+      }
+      if (wg == 0) {
         asm volatile("st.shared.f32 [%0], %1;" :: "r"(slot + kPktAlpha + r * 4), "f"(alpha) : "memory");
         if (last) {
-          const float inv_l = l > 0.f ? 1.f / l : 0.f;
-          asm volatile("st.shared.f32 [%0], %1;" :: "r"(slot + kPktInvL + r * 4), "f"(inv_l) : "memory");
+          l += ld_shared_f32(lpart);          // total over both warpgroups
+          asm volatile("st.shared.f32 [%0], %1;" :: "r"(slot + kPktInvL + r * 4), "f"(l > 0.f ? 1.f / l : 0.f)
+                       : "memory");
         }
-        if (lane == 0) asm volatile("st.shared.u32 [%0], %1;" :: "r"(slot + kPktFlags + wq * 4), "r"(need) : "memory");
       }
       fence_proxy_async_smem();
-      bool credit_ok = true;
-      if (r == 0) credit_ok = wait_bar(sh, smem_u32(&sh.bar.credit[sb]), ph ^ 1, p.status, cl, true);
-      if (named_bar_or(1, 128, !credit_ok)) { ok = false; break; }
-      if (r == 0) {
-        bulk_copy_to_cluster(peer_recv + sb * kPktStride, slot, kPktBytes, sb ? peer_pfull1 : peer_pfull0);
+      named_bar_sync(1, kSoftThreads);
+      if (t == 0) {
+        bulk_copy_to_cluster(peer_recv + rs * kPktStride, slot, kPktStride, peer_pfull0 + rs * 8);
         bulk_commit_group();
       }
     }
     if (!ok) break;
-    if (row_valid) {
+    if (row_valid && wg == 0) {
       const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
       const int ns0 = __ldg(p.num_splits + s.b);
       const int nsplit = __ldg(p.num_splits + s.b + 1) - ns0;
@@ -388,44 +426,17 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
         p.lse_part[static_cast<int64_t>(ns0 + s.split) * p.rows + g] = lse;
     }
   }
-  if (r == 0) bulk_wait_group<0>();
+  if (t == 0) bulk_wait_group<0>();   // copies land before the CTA may exit
 }
 
 // ------------------------------------------------------------------ O-CTA --
-__device__ void o_cta_producer(const DecodeParams& p, const CUtensorMap* kv_map, Shared& sh, uint32_t smem,
-                               int part, uint32_t cl) {
-  SegmentWalker w;
-  w.init(p, part);
-  Segment s;
-  uint32_t T = 0;
-  int issued[2] = {0, 0};
-  uint32_t issued_phase[2] = {0, 0};
-  const uint64_t policy = l2_policy_evict_first();
-  bool ok = true;
-  while (ok && w.next(s)) {
-    for (int k = s.kb; k < s.ke; ++k, ++T) {
-      const uint32_t st = T & 1, ph = (T >> 1) & 1;
-      if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      const int blk = request_block(p, s.b, k);
-      const uint32_t full = smem_u32(&sh.bar.full[st]);
-      mbar_arrive_expect_tx(full, kVStageBytes);
-      const uint32_t dst = smem + kOffStage + st * kVStageBytes;
-      for (int c = 0; c < 8; ++c) tma_load_2d_hint(dst + c * 8192, kv_map, full, c * 64, blk * 64, policy);
-      issued[st] = 1;
-      issued_phase[st] = ph;
-    }
-  }
-  for (int st = 0; st < 2; ++st)
-    if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
-}
-
-// Warp 1 of the O-CTA (all 32 lanes enter; lane 0 issues).
+// Warp 1 of the O-CTA (all 32 lanes; one elected lane issues the MMAs).
 __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl) {
   const int lane = threadIdx.x & 31;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
-  uint32_t T = 0, seg = 0, ncmd = 0, nresc = 0;
+  uint32_t T = 0, seg = 0, nresc = 0;
   const uint32_t tmem = sh.tmem_base;
   constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
   bool ok = true, any = false;
@@ -433,13 +444,14 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
     if (seg > 0 && !warp_wait(sh, smem_u32(&sh.bar.o_free), (seg - 1) & 1, p.status, cl)) break;
     const int L = __ldg(p.seqlens + s.b);
     for (int k = s.kb; k < s.ke; ++k, ++T) {
-      const uint32_t st = T & 1, ph = (T >> 1) & 1;
+      const uint32_t st = T % kVStages, ph = (T / kVStages) & 1;
+      const uint32_t ps = T % kSlots, pph = (T / kSlots) & 1;
       const uint32_t vstage = smem + kOffStage + st * kVStageBytes;
-      const uint32_t pkt = smem + kOffRecv + st * kPktStride;
-      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.bar.p_full[st]), kPktBytes);
+      const uint32_t pkt = smem + kOffRecv + ps * kPktStride;
+      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.bar.p_full[ps]), kPktStride);
       __syncwarp();
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
-      if (!warp_wait(sh, smem_u32(&sh.bar.p_full[st]), ph, p.status, cl, true)) { ok = false; break; }
+      if (!warp_wait(sh, smem_u32(&sh.bar.p_full[ps]), pph, p.status, cl, true)) { ok = false; break; }
       // tail page: zero the value rows past the sequence end up to the next 16-row
       // boundary, so that P = 0 never meets a non-finite value in the MMA
       const int nvalid = min(64, L - k * 64);
@@ -448,29 +460,28 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
         const int nz = krows - nvalid;                 // rows to clear, < 16
         for (int i = lane; i < nz * 8 * 8; i += 32) {  // rows x chunks x 16-byte units
           const int row = nvalid + i / 64, chunk = (i / 8) % 8, u = i % 8;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
-                       :: "r"(vstage + chunk * 8192 + row * 128 + u * 16), "r"(0u) : "memory");
+          st_shared_v4(vstage + chunk * 8192 + row * 128 + u * 16, make_uint4(0, 0, 0, 0));
         }
         fence_proxy_async_smem();
       }
       const bool last = (k == s.ke - 1);
       if (last)     // keep 1/l of the segment's rows before the slot can be reused
-        st_shared_v4(smem_u32(&sh.inv_l[lane * 4]), ld_shared_v4(pkt + kPktInvL + lane * 16));
-      __syncwarp();
-      uint32_t need = 0;
-      if (k != s.kb) {
-        const uint4 f = ld_shared_v4(pkt + kPktFlags);
-        need = f.x | f.y | f.z | f.w;
+        st_shared_v4(smem + kOffInvL + lane * 16, ld_shared_v4(pkt + kPktInvL + lane * 16));
+      bool need = false;
+      if (k != s.kb) {   // did any row rebase its maximum on this page?
+        const uint4 a = ld_shared_v4(pkt + kPktAlpha + lane * 16);
+        need = __any_sync(0xffffffffu, a.x != 0x3f800000u || a.y != 0x3f800000u || a.z != 0x3f800000u ||
+                                           a.w != 0x3f800000u);
       }
-      if (need) {   // a row maximum was rebased: scale O by alpha before adding this page
+      __syncwarp();
+      if (need) {   // scale O by alpha before adding this page
         mma_commit_warp(smem_u32(&sh.bar.o_sync));
         if (!warp_wait(sh, smem_u32(&sh.bar.o_sync), nresc & 1, p.status, cl)) { ok = false; break; }
         if (lane == 0) {
           sh.cmd = 1;
-          sh.cmd_arg = static_cast<int>(st);
+          sh.cmd_arg = static_cast<int>(ps);
           mbar_arrive(smem_u32(&sh.bar.corr_go));
         }
-        ++ncmd;
         __syncwarp();
         if (!warp_wait(sh, smem_u32(&sh.bar.corr_done), nresc & 1, p.status, cl)) { ok = false; break; }
         ++nresc;
@@ -487,19 +498,17 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
           }
         }
         mma_commit_warp(smem_u32(&sh.bar.empty[st]));
-        mma_commit_warp(smem_u32(&sh.bar.p_free[st]));
+        mma_commit_warp(smem_u32(&sh.bar.p_free[ps]));
         if (last) mma_commit_warp(smem_u32(&sh.bar.o_full));
       }
       any = true;
       __syncwarp();
-      if (last) {
-        if (lane == 0) {
-          sh.cmd = 2;
-          sh.cmd_arg = static_cast<int>(seg);
-          mbar_arrive(smem_u32(&sh.bar.corr_go));
-        }
-        ++ncmd;
+      if (last && lane == 0) {
+        sh.cmd = 2;
+        sh.cmd_arg = static_cast<int>(seg);
+        mbar_arrive(smem_u32(&sh.bar.corr_go));
       }
+      __syncwarp();
     }
     ++seg;
   }
@@ -515,7 +524,6 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
     mbar_arrive(smem_u32(&sh.bar.corr_go));
   }
   __syncwarp();
-  (void)ncmd;
 }
 
 // Warp 2 of the O-CTA: returns each packet slot to the S-CTA once the MMAs reading it are done.
@@ -525,24 +533,26 @@ __device__ void o_cta_forwarder(const DecodeParams& p, Shared& sh, int part, uin
   Segment s;
   uint32_t T = 0;
   const uint32_t credit0 = map_to_rank(smem_u32(&sh.bar.credit[0]), peer);
-  const uint32_t credit1 = map_to_rank(smem_u32(&sh.bar.credit[1]), peer);
   bool ok = true;
   while (ok && w.next(s)) {
     for (int k = s.kb; k < s.ke; ++k, ++T) {
-      const uint32_t st = T & 1, ph = (T >> 1) & 1;
-      if (!wait_bar(sh, smem_u32(&sh.bar.p_free[st]), ph, p.status, cl)) { ok = false; break; }
-      mbar_arrive_remote(st ? credit1 : credit0);
+      const uint32_t ps = T % kSlots, pph = (T / kSlots) & 1;
+      if (!wait_bar(sh, smem_u32(&sh.bar.p_free[ps]), pph, p.status, cl)) { ok = false; break; }
+      mbar_arrive_remote(credit0 + ps * 8);
     }
   }
 }
 
-// Warps 4..7 of the O-CTA: rescale O rows, or normalise and store a finished segment.
+// Warps 4..11 of the O-CTA: rescale O rows, or normalise and store a finished
+// segment.  Warpgroup wg owns O columns [256 wg, 256 wg + 256).
 __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb) {
-  const int r = threadIdx.x - 128;
+  const int t = threadIdx.x - 128;
+  const int wg = t >> 7;
+  const int r = t & 127;
   const int wq = r >> 5, lane = r & 31;
   const int g = rb * 128 + r;
   const bool row_valid = g < p.rows;
-  const uint32_t tmem_lane = sh.tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
+  const uint32_t tmem_lane = sh.tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + wg * 256;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
@@ -554,12 +564,11 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
     const int cmd = sh.cmd, arg = sh.cmd_arg;
     if (cmd == 3) break;
     if (cmd == 1) {
-      const uint32_t pkt = smem + kOffRecv + arg * kPktStride;
-      const float alpha = ld_shared_f32(pkt + kPktAlpha + r * 4);
+      const float alpha = ld_shared_f32(smem + kOffRecv + arg * kPktStride + kPktAlpha + r * 4);
       tc_fence_after();
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c = 0; c < 512; c += 32) {
+        for (int c = 0; c < 256; c += 32) {
           uint32_t v[32];
           tmem_ld32(tmem_lane + c, v);
           tmem_wait_ld();
@@ -578,18 +587,18 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
     if (!have_seg) break;
     if (!warp_wait(sh, smem_u32(&sh.bar.o_full), seg & 1, p.status, cl)) break;
     tc_fence_after();
-    const float inv_l = sh.inv_l[r];
+    const float inv_l = ld_shared_f32(smem + kOffInvL + r * 4);
     const int ns0 = __ldg(p.num_splits + s.b);
     const int nsplit = __ldg(p.num_splits + s.b + 1) - ns0;
     const bool final_out = (nsplit == 1);
-    __nv_bfloat16* orow = p.out + (static_cast<int64_t>(s.b) * p.rows + g) * 512;
-    float* prow = p.o_part + (static_cast<int64_t>(ns0 + s.split) * p.rows + g) * 512;
+    __nv_bfloat16* orow = p.out + (static_cast<int64_t>(s.b) * p.rows + g) * 512 + wg * 256;
+    float* prow = p.o_part + (static_cast<int64_t>(ns0 + s.split) * p.rows + g) * 512 + wg * 256;
 #pragma unroll 1
-    for (int c = 0; c < 512; c += 32) {
+    for (int c = 0; c < 256; c += 32) {
       uint32_t v[32];
       tmem_ld32(tmem_lane + c, v);
       tmem_wait_ld();
-      if (c == 480) {   // everything read: O may be overwritten by the next segment
+      if (c == 224) {   // everything read: O may be overwritten by the next segment
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.bar.o_free));
@@ -624,8 +633,13 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
 __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
-  __shared__ Shared sh;
-  const uint32_t smem = (smem_u32(dyn_smem) + 1023u) & ~1023u;
+  const uint32_t base = smem_u32(dyn_smem);
+  if (base & 1023u) {   // the layout needs a 1024-byte aligned base (no static shared memory is declared)
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, MLA_ERR_UNSUPPORTED);
+    return;             // every CTA of the grid takes this branch alike
+  }
+  const uint32_t smem = base;
+  Shared& sh = *reinterpret_cast<Shared*>(dyn_smem + kOffShared);
   const int warp = threadIdx.x >> 5;
   const uint32_t rank = cluster_ctarank();
   const uint32_t cl = 2u * static_cast<uint32_t>(p.n_rb);   // CTAs per cluster
@@ -637,26 +651,25 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams
   if (threadIdx.x == 0) {
     sh.abort = 0;
     sh.cmd = 0;
-    mbar_init(smem_u32(&sh.bar.full[0]), 1);
-    mbar_init(smem_u32(&sh.bar.full[1]), 1);
-    mbar_init(smem_u32(&sh.bar.empty[0]), 1);
-    mbar_init(smem_u32(&sh.bar.empty[1]), 1);
-    mbar_init(smem_u32(&sh.bar.s_full[0]), 1);
-    mbar_init(smem_u32(&sh.bar.s_full[1]), 1);
-    mbar_init(smem_u32(&sh.bar.s_empty[0]), 4);
-    mbar_init(smem_u32(&sh.bar.s_empty[1]), 4);
-    mbar_init(smem_u32(&sh.bar.q_full), 4);
-    mbar_init(smem_u32(&sh.bar.credit[0]), 1);
-    mbar_init(smem_u32(&sh.bar.credit[1]), 1);
-    mbar_init(smem_u32(&sh.bar.p_full[0]), 1);
-    mbar_init(smem_u32(&sh.bar.p_full[1]), 1);
-    mbar_init(smem_u32(&sh.bar.p_free[0]), 1);
-    mbar_init(smem_u32(&sh.bar.p_free[1]), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&sh.bar.full[i]), 1);
+      mbar_init(smem_u32(&sh.bar.empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh.bar.s_full[i]), 1);
+      mbar_init(smem_u32(&sh.bar.s_empty[i]), 8);
+    }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_u32(&sh.bar.credit[i]), 1);
+      mbar_init(smem_u32(&sh.bar.p_full[i]), 1);
+      mbar_init(smem_u32(&sh.bar.p_free[i]), 1);
+    }
+    mbar_init(smem_u32(&sh.bar.q_full), 8);
     mbar_init(smem_u32(&sh.bar.o_full), 1);
-    mbar_init(smem_u32(&sh.bar.o_free), 4);
+    mbar_init(smem_u32(&sh.bar.o_free), 8);
     mbar_init(smem_u32(&sh.bar.o_sync), 1);
     mbar_init(smem_u32(&sh.bar.corr_go), 1);
-    mbar_init(smem_u32(&sh.bar.corr_done), 4);
+    mbar_init(smem_u32(&sh.bar.corr_done), 8);
     mbar_init(smem_u32(&sh.bar.drain), 1);
     fence_mbar_init();
   }
@@ -669,7 +682,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams
 
   if (is_s) {
     if (warp == 0) {
-      if ((threadIdx.x & 31) == 0) s_cta_producer(p, &kv_map, sh, smem, part, cl, rb == 0);
+      if ((threadIdx.x & 31) == 0)
+        producer<kKStages, 9>(p, &kv_map, sh, smem, part, cl, p.withhold_first_load != 0);
     } else if (warp == 1) {
       s_cta_mma(p, sh, smem, part, cl);
     } else if (warp >= 4) {
@@ -677,7 +691,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams
     }
   } else {
     if (warp == 0) {
-      if ((threadIdx.x & 31) == 0) o_cta_producer(p, &kv_map, sh, smem, part, cl);
+      if ((threadIdx.x & 31) == 0) producer<kVStages, 8>(p, &kv_map, sh, smem, part, cl, false);
     } else if (warp == 1) {
       o_cta_mma(p, sh, smem, part, cl);
     } else if (warp == 2) {
@@ -700,7 +714,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams
 
 cudaError_t decode_set_attributes() {
   return cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemBytes + 1024));
+                              static_cast<int>(kSmemBytes));
 }
 
 static cudaLaunchConfig_t decode_config(int grid_ctas, int cluster_ctas, cudaStream_t stream,
@@ -712,7 +726,7 @@ static cudaLaunchConfig_t decode_config(int grid_ctas, int cluster_ctas, cudaStr
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes + 1024;
+  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
