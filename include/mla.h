@@ -92,6 +92,7 @@ size_t mla_decode_workspace_size(int B, int s_q, int H, int num_sm_parts);
  *  kv_cache     [num_blocks, 64, 576] bf16 latent cache (16-byte aligned rows)
  *  block_table  [B, max_blocks] int32; only entries < ceil(seqlens[b]/64) are read
  *  seqlens      [B] int32, each in [0, max_blocks*64]; counts the s_q new tokens
+ *  softmax_scale  finite and > 0 (else MLA_ERR_INVALID_ARG)
  *  metadata     from mla_decode_metadata with the same seqlens, B, s_q, H and
  *               num_sm_parts
  *  workspace    >= mla_decode_workspace_size bytes, 256-byte aligned

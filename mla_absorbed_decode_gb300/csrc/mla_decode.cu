@@ -188,6 +188,18 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   }
 }
 
+// L2 prefetch of what a segment of request b starts with: its q rows (rows x 576
+// bf16, contiguous) and its block-table row.  Cold, these are many small loads
+// that otherwise queue behind each other at every segment start.
+__device__ __forceinline__ void prefetch_request(const DecodeParams& p, int b) {
+  const uintptr_t q0 = reinterpret_cast<uintptr_t>(p.q + static_cast<int64_t>(b) * p.rows * 576);
+  prefetch_l2(reinterpret_cast<const void*>(q0), static_cast<uint32_t>(p.rows) * 576 * 2);   // 16-byte multiple
+  const uintptr_t t0 = reinterpret_cast<uintptr_t>(p.block_table + static_cast<int64_t>(b) * p.max_blocks);
+  const uintptr_t t1 = t0 + static_cast<uintptr_t>(p.max_blocks) * 4;
+  const uintptr_t a0 = t0 & ~uintptr_t(15), a1 = (t1 + 15) & ~uintptr_t(15);
+  prefetch_l2(reinterpret_cast<const void*>(a0), static_cast<uint32_t>(a1 - a0));
+}
+
 // Page id of page k of request b, or -1 (and a recorded bounds error) if the
 // table entry is outside [0, num_blocks) or k is past the table's width.
 __device__ __forceinline__ int request_block(const DecodeParams& p, int b, int k) {
@@ -207,7 +219,7 @@ __device__ __forceinline__ int request_block(const DecodeParams& p, int b, int k
 // S-CTA: all 576 dims (9 swizzled 64 x 64 chunks, 72 KiB); O-CTA: the 512 value
 // dims (8 chunks, 64 KiB).
 template <int NST, int NCHUNK>
-__device__ void producer(const DecodeParams& p, const CUtensorMap* kv_map, Shared& sh, uint32_t smem, int part,
+__device__ void producer(const DecodeParams& p, const CUtensorMap* page_map, Shared& sh, uint32_t smem, int part,
                          uint32_t cl, bool withhold) {
   constexpr uint32_t kBytes = NCHUNK * 8192;
   SegmentWalker w;
@@ -228,7 +240,7 @@ __device__ void producer(const DecodeParams& p, const CUtensorMap* kv_map, Share
       const uint32_t full = smem_u32(&sh.bar.full[st]);
       mbar_arrive_expect_tx(full, kBytes);
       const uint32_t dst = smem + kOffStage + st * kBytes;
-      for (int c = 0; c < NCHUNK; ++c) tma_load_2d_hint(dst + c * 8192, kv_map, full, c * 64, blk * 64, policy);
+      tma_load_3d_hint(dst, page_map, full, 0, blk * 64, 0, policy);   // the whole page, one box
       issued[st] = 1;
       issued_phase[st] = ph;
     }
@@ -341,58 +353,67 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.bar.q_full));
+      if (t == 0) {   // the next segment's q rows and block-table row, into L2 now
+        SegmentWalker nx = w;
+        Segment ns;
+        if (nx.next(ns)) prefetch_request(p, ns.b);
+      }
     }
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f;   // reference maximum (log2 units) and running sum of the rows
     for (int k = s.kb; k < s.ke; ++k, ++T) {
       const uint32_t sb = T & 1, ph = (T >> 1) & 1;
-      const bool got = wait_bar(sh, smem_u32(&sh.bar.s_full[sb]), ph, p.status, cl);
-      if (named_bar_or(1, kSoftThreads, !got)) { ok = false; break; }   // same decision in all 256 threads
+      const uint32_t rs = T % kSlots, rph = (T / kSlots) & 1;
+      // S of this page; thread 0 also makes sure that staging slot sb is free (the bulk
+      // copy that used it two pages ago has read it) and that the partner's receive
+      // slot rs is free (its PV of the page that used it, kSlots pages ago, is done).
+      bool ok_t = wait_bar(sh, smem_u32(&sh.bar.s_full[sb]), ph, p.status, cl);
+      if (t == 0 && ok_t) {
+        bulk_wait_group_read<1>();
+        ok_t = wait_bar(sh, smem_u32(&sh.bar.credit[rs]), rph ^ 1, p.status, cl, true);
+      }
       tc_fence_after();
-      uint32_t sr[32];
-      tmem_ld32(tmem_lane + kSCol0 + sb * 64 + c0, sr);
+      float sv[32];
+      tmem_ld32(tmem_lane + kSCol0 + sb * 64 + c0, *reinterpret_cast<uint32_t(*)[32]>(sv));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.bar.s_empty[sb]));
 
-      // scaled, masked scores (log2 units); slots at or past `vis` become -inf
+      // raw scores; slots at or past `vis` are masked to -inf (only on the last pages)
       const int nvalid = vis - (k * 64 + c0);   // columns c < nvalid are visible
-      float x[32];
+      if (nvalid < 32) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) x[c] = (c < nvalid) ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-      const float my_max = max32(x);
+        for (int c = 0; c < 32; ++c) sv[c] = (c < nvalid) ? sv[c] : -INFINITY;
+      }
+      const float my_max = max32(sv);
       asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine), "f"(my_max) : "memory");
-      named_bar_sync(1, kSoftThreads);
-      const float m_new = fmaxf(m_ref, fmaxf(my_max, ld_shared_f32(pm_other)));
+      // one barrier both exchanges the row maxima and makes the abort decision uniform
+      if (named_bar_or(1, kSoftThreads, !ok_t)) { ok = false; break; }
+      // softmax_scale > 0, so the scaled maximum is the scaled raw maximum
+      const float m_new = fmaxf(m_ref, fmaxf(my_max, ld_shared_f32(pm_other)) * p.scale_log2);
       float alpha = 1.f;
       const bool rebase = m_new > m_ref + kRescaleLog2;
       if (rebase) {
         alpha = fast_exp2(m_ref - m_new);       // 0 when m_ref = -inf
         m_ref = m_new;
       }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
       uint32_t pk[16];
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 16; ++c) {   // l sums the fp32 probabilities; P goes to the MMA in bf16
-        const float e0 = fast_exp2(x[2 * c] - m_use), e1 = fast_exp2(x[2 * c + 1] - m_use);
+        const float e0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, neg_m));
+        const float e1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, neg_m));
         pk[c] = pack_bf16x2(e0, e1);
         ps[c & 3] += e0 + e1;
       }
       l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       const bool last = (k == s.ke - 1);
-      if (last && wg == 1) asm volatile("st.shared.f32 [%0], %1;" :: "r"(lpart), "f"(l) : "memory");
-
-      // Staging slot sb is free once the bulk copy that used it two pages ago has
-      // read it, and the partner's receive slot rs once its PV of the page that used
-      // it (kSlots pages ago) is done.
-      const uint32_t rs = T % kSlots, rph = (T / kSlots) & 1;
-      bool ready = true;
-      if (t == 0) {
-        bulk_wait_group_read<1>();
-        ready = wait_bar(sh, smem_u32(&sh.bar.credit[rs]), rph ^ 1, p.status, cl, true);
+      if (last) {   // the row sum over both warpgroups is needed for 1/l
+        if (wg == 1) asm volatile("st.shared.f32 [%0], %1;" :: "r"(lpart), "f"(l) : "memory");
+        named_bar_sync(1, kSoftThreads);
+        if (wg == 0) l += ld_shared_f32(lpart);
       }
-      if (named_bar_or(1, kSoftThreads, !ready)) { ok = false; break; }
       const uint32_t slot = smem + kOffSend + sb * kPktStride;
       const uint32_t row = slot + r * 128;
 #pragma unroll
@@ -402,11 +423,9 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       }
       if (wg == 0) {
         asm volatile("st.shared.f32 [%0], %1;" :: "r"(slot + kPktAlpha + r * 4), "f"(alpha) : "memory");
-        if (last) {
-          l += ld_shared_f32(lpart);          // total over both warpgroups
+        if (last)
           asm volatile("st.shared.f32 [%0], %1;" :: "r"(slot + kPktInvL + r * 4), "f"(l > 0.f ? 1.f / l : 0.f)
                        : "memory");
-        }
       }
       fence_proxy_async_smem();
       named_bar_sync(1, kSoftThreads);
@@ -631,7 +650,7 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
-mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
+mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   const uint32_t base = smem_u32(dyn_smem);
   if (base & 1023u) {   // the layout needs a 1024-byte aligned base (no static shared memory is declared)
@@ -649,6 +668,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams
   const uint32_t peer = rank ^ 1u;
 
   if (threadIdx.x == 0) {
+    prefetch_tensormap(is_s ? &maps.k : &maps.v);
+    if (is_s && rb == 0) {   // first request's q rows and block-table row, before anything else queues
+      const int b0 = __ldg(p.meta + part * 8);
+      if (b0 >= 0) prefetch_request(p, b0);
+    }
     sh.abort = 0;
     sh.cmd = 0;
     for (int i = 0; i < kStages; ++i) {
@@ -683,7 +707,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams
   if (is_s) {
     if (warp == 0) {
       if ((threadIdx.x & 31) == 0)
-        producer<kKStages, 9>(p, &kv_map, sh, smem, part, cl, p.withhold_first_load != 0);
+        producer<kKStages, 9>(p, &maps.k, sh, smem, part, cl, p.withhold_first_load != 0);
     } else if (warp == 1) {
       s_cta_mma(p, sh, smem, part, cl);
     } else if (warp >= 4) {
@@ -691,7 +715,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams
     }
   } else {
     if (warp == 0) {
-      if ((threadIdx.x & 31) == 0) producer<kVStages, 8>(p, &kv_map, sh, smem, part, cl, false);
+      if ((threadIdx.x & 31) == 0) producer<kVStages, 8>(p, &maps.v, sh, smem, part, cl, false);
     } else if (warp == 1) {
       o_cta_mma(p, sh, smem, part, cl);
     } else if (warp == 2) {
@@ -744,10 +768,10 @@ int decode_max_clusters(int cluster_ctas) {
   return clusters;
 }
 
-cudaError_t launch_decode(const CUtensorMap& kv_map, const DecodeParams& p, int cluster_ctas, cudaStream_t stream) {
+cudaError_t launch_decode(const KvMaps& maps, const DecodeParams& p, int cluster_ctas, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = decode_config(p.num_parts * cluster_ctas, cluster_ctas, stream, attr);
-  return cudaLaunchKernelEx(&cfg, mla_decode_kernel, kv_map, p);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel, maps, p);
 }
 
 }  // namespace mla

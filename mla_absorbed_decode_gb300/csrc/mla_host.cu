@@ -86,6 +86,25 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uin
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache, int64_t num_blocks) {
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_blocks) * kPageTokens, kDimQK / 64};
+  const cuuint64_t strides[2] = {kDimQK * 2, 128};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const cuuint32_t kbox[3] = {64, kPageTokens, kDimQK / 64};
+  const cuuint32_t vbox[3] = {64, kPageTokens, kDimV / 64};
+  void* base = const_cast<void*>(kv_cache);
+  return encode(&maps->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, kbox, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+         encode(&maps->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, vbox, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
 size_t max_splits(int B, int num_parts) { return static_cast<size_t>(B) + static_cast<size_t>(num_parts); }
 
 }  // namespace
@@ -170,7 +189,7 @@ mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t
       (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u) ||
       (reinterpret_cast<uintptr_t>(metadata) & 3u))
     return MLA_ERR_INVALID_ARG;
-  if (!std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   const int n_rb = pairs_for(s_q, H);
   if (n_rb > kMaxPairsPerCluster) return MLA_ERR_UNSUPPORTED;
   if (num_blocks * kPageTokens > (int64_t(1) << 31) - kPageTokens) return MLA_ERR_UNSUPPORTED;
@@ -181,9 +200,8 @@ mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t
   mla_status_t st = current_device(&d);
   if (st != MLA_OK) return st;
 
-  CUtensorMap kv_map;
-  if (!encode_2d(&kv_map, kv_cache, kDimQK, static_cast<uint64_t>(num_blocks) * kPageTokens, kDimQK * 2, 64, 64))
-    return MLA_ERR_CUDA;
+  KvMaps kv_maps;
+  if (!encode_kv_maps(g_encode, &kv_maps, kv_cache, num_blocks)) return MLA_ERR_CUDA;
 
   const int rows = s_q * H;
   const size_t ms = max_splits(B, num_sm_parts);
@@ -213,7 +231,7 @@ mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t
   g_withhold_first_load = 0;
 
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_decode(kv_map, p, 2 * n_rb, cs) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_decode(kv_maps, p, 2 * n_rb, cs) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_combine(p.o_part, p.lse_part, p.num_splits, B, rows, p.out, lse, cs) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }

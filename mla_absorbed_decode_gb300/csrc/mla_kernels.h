@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "mla.h"
@@ -43,6 +44,18 @@ struct DecodeParams {
   int withhold_first_load;
 };
 
+// Tensor maps of the paged latent cache, viewed as [chunk 0..8][token row][64 dims]:
+// dim 0 = 64 dims of a chunk (128 B, contiguous), dim 1 = token rows (stride 1152 B),
+// dim 2 = chunk (stride 128 B).  One box is a whole page in the swizzled, chunk-major
+// shared-memory layout the MMAs read: `k` takes all 9 chunks (576 dims, 72 KiB),
+// `v` the 8 value chunks (512 dims, 64 KiB).
+struct KvMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
+// Encodes both maps for a cache of num_blocks pages; false on failure.
+bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache, int64_t num_blocks);
+
 // Device address of the kernels' status word on the current device (set-up on
 // first use); nullptr on error.
 int* device_status_word();
@@ -50,7 +63,7 @@ int* device_status_word();
 // Launchers (defined next to their kernels).
 cudaError_t decode_set_attributes();
 int decode_max_clusters(int cluster_ctas);            // occupancy query; 0 on error
-cudaError_t launch_decode(const CUtensorMap& kv_map, const DecodeParams& p, int cluster_ctas, cudaStream_t stream);
+cudaError_t launch_decode(const KvMaps& maps, const DecodeParams& p, int cluster_ctas, cudaStream_t stream);
 
 cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
                             int32_t* meta, int32_t* num_splits, cudaStream_t stream);

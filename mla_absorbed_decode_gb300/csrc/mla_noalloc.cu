@@ -80,7 +80,7 @@ extern "C" mla_status_t mla_decode_noalloc(const mla_bf16_t* q, const mla_bf16_t
   if (misaligned(q, 16) || misaligned(kv_cache, 16) || misaligned(out, 16) || misaligned(lse, 4) ||
       misaligned(block_table, 4) || misaligned(seqlens, 4))
     return MLA_ERR_INVALID_ARG;
-  if (!std::isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   const int n_rb = (s_q * H + kRowsPerPair - 1) / kRowsPerPair;
   if (n_rb > kMaxPairsPerCluster) return MLA_ERR_UNSUPPORTED;
   if (num_blocks * kPageTokens > (int64_t(1) << 31) - kPageTokens) return MLA_ERR_UNSUPPORTED;
@@ -95,17 +95,8 @@ extern "C" mla_status_t mla_decode_noalloc(const mla_bf16_t* q, const mla_bf16_t
   int* status = device_status_word();
   if (!status) return MLA_ERR_CUDA;
 
-  CUtensorMap kv_map;
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDimQK), static_cast<cuuint64_t>(num_blocks) * kPageTokens};
-    cuuint64_t strides[1] = {kDimQK * 2};
-    cuuint32_t box[2] = {64, 64};
-    cuuint32_t es[2] = {1, 1};
-    if (g_na_encode(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<mla_bf16_t*>(kv_cache), dims, strides,
-                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MLA_ERR_CUDA;
-  }
+  KvMaps kv_maps;
+  if (!encode_kv_maps(g_na_encode, &kv_maps, kv_cache, num_blocks)) return MLA_ERR_CUDA;
   // Nothing in the scratch has to start at zero: the schedule kernel writes every
   // metadata entry, and the decode kernel writes each partial slot before the
   // combine kernel of the same call reads it.
@@ -141,7 +132,7 @@ extern "C" mla_status_t mla_decode_noalloc(const mla_bf16_t* q, const mla_bf16_t
   p.lse = lse;
   p.status = status;
   p.withhold_first_load = 0;
-  if (launch_decode(kv_map, p, 2 * n_rb, cs) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_decode(kv_maps, p, 2 * n_rb, cs) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_combine(p.o_part, p.lse_part, p.num_splits, B, rows, p.out, lse, cs) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -69,6 +69,9 @@ def test_host_argument_checks(mla):
     assert L.mla_decode(*small_ws) == 3                     # MLA_ERR_WORKSPACE
     nan_scale = list(args); nan_scale[9] = float("nan")
     assert L.mla_decode(*nan_scale) == 1
+    for bad in (0.0, -0.5):   # the kernel takes the row maximum on unscaled scores
+        neg_scale = list(args); neg_scale[9] = bad
+        assert L.mla_decode(*neg_scale) == 1
     assert L.mla_decode_metadata(None, 2, 1, 16, 0, 4, A, None) == 1
     assert L.mla_decode_metadata(A, 2, 8, 128, 0, 4, A, None) == 2
     assert L.mla_absorb_q(A, 100, None, 0, A, A, 4, 1, None) == 1      # stride below H*128
