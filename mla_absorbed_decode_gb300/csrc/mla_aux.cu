@@ -17,65 +17,120 @@ namespace mla {
 // processes.  Greedy over the requests in order with a per-segment cost of
 // `fixed_cost` pages; at most `hbm_parts` parts are used, since that many
 // already keep HBM busy.  One thread: the walk is sequential and short.
-__global__ void mla_schedule_kernel(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
-                                    int32_t* meta, int32_t* num_splits) {
-  if (blockIdx.x != 0 || threadIdx.x != 0) return;
-  int64_t pages = 0;
-  int nonempty = 0;
-  for (int b = 0; b < B; ++b) {
-    const int L = seqlens[b];
-    const int nb = L > 0 ? (L + kPageTokens - 1) / kPageTokens : 0;
-    pages += nb;
-    nonempty += nb > 0;
-    num_splits[b + 1] = 0;   // per-request segment counts for now
+constexpr int kScheduleThreads = 256;
+constexpr int kScheduleSmemMaxB = 12 * 1024;   // page counts and segment counts of up to this many requests in smem
+
+// One CTA.  The page count of every request is read once, in parallel, into shared
+// memory (or, for batches too large for it, re-read from global memory); thread 0
+// then walks the parts; the segment counts are prefix-summed by all threads.
+__global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const int32_t* seqlens, int B, int num_parts,
+                                                                        int fixed_cost, int hbm_parts, int32_t* meta,
+                                                                        int32_t* num_splits) {
+  extern __shared__ int32_t sched_smem[];
+  __shared__ unsigned long long s_pages;
+  __shared__ int s_nonempty;
+  __shared__ int32_t s_chunk[kScheduleThreads];
+  const int tid = threadIdx.x;
+  const bool in_smem = B <= kScheduleSmemMaxB;
+  int32_t* nb_s = sched_smem;          // [B] pages per request (in_smem only)
+  int32_t* seg_s = sched_smem + (in_smem ? B : 0);   // [B] segments per request (in_smem only)
+  if (tid == 0) {
+    s_pages = 0;
+    s_nonempty = 0;
   }
-  const int p_eff = max(1, min(num_parts, hbm_parts));
-  const int64_t cost = pages + static_cast<int64_t>(fixed_cost) * (nonempty + p_eff - 1);
-  const int64_t target = (cost + p_eff - 1) / p_eff;
-  int b = 0, k = 0;
-  for (int part = 0; part < num_parts; ++part) {
-    int32_t* m = meta + part * kMetaInts;
+  __syncthreads();
+  unsigned long long my_pages = 0;
+  int my_nonempty = 0;
+  for (int i = tid; i < B; i += kScheduleThreads) {
+    const int L = seqlens[i];
+    const int nb = L > 0 ? (L + kPageTokens - 1) / kPageTokens : 0;
+    my_pages += static_cast<unsigned long long>(nb);
+    my_nonempty += nb > 0;
+    if (in_smem) {
+      nb_s[i] = nb;
+      seg_s[i] = 0;
+    } else {
+      num_splits[i + 1] = 0;
+    }
+  }
+  atomicAdd(&s_pages, my_pages);
+  atomicAdd(&s_nonempty, my_nonempty);
+  __syncthreads();
+  if (tid == 0) {
     auto pages_of = [&](int i) {
+      if (in_smem) return nb_s[i];
       const int L = seqlens[i];
       return L > 0 ? (L + kPageTokens - 1) / kPageTokens : 0;
     };
-    while (b < B && pages_of(b) == 0) ++b;
-    for (int j = 0; j < kMetaInts; ++j) m[j] = 0;
-    if (b >= B) {
-      m[0] = -1;
-      continue;
-    }
-    m[0] = b;
-    m[1] = k;
-    m[4] = num_splits[b + 1];   // segments of request b made so far
-    int last_b = b, last_end = k;
-    int64_t budget = target;
-    while (b < B) {
-      const int nb = pages_of(b);
-      if (nb == 0) { ++b; continue; }
-      const int left = nb - k;
-      if (part == num_parts - 1 || left + fixed_cost <= budget) {
-        budget -= left + fixed_cost;
-        num_splits[b + 1] += 1;
-        last_b = b;
-        last_end = nb;
-        ++b;
-        k = 0;
+    auto segs = [&](int i) -> int32_t& { return in_smem ? seg_s[i] : num_splits[i + 1]; };
+    const int p_eff = max(1, min(num_parts, hbm_parts));
+    const int64_t cost = static_cast<int64_t>(s_pages) + static_cast<int64_t>(fixed_cost) * (s_nonempty + p_eff - 1);
+    const int64_t target = (cost + p_eff - 1) / p_eff;
+    int b = 0, k = 0;
+    for (int part = 0; part < num_parts; ++part) {
+      int32_t m[kMetaInts] = {0, 0, 0, 0, 0, 0, 0, 0};
+      while (b < B && pages_of(b) == 0) ++b;
+      if (b >= B) {
+        m[0] = -1;
       } else {
-        const int64_t take = budget - fixed_cost;
-        if (take < 1) break;
-        k += static_cast<int>(take);
-        num_splits[b + 1] += 1;
-        last_b = b;
-        last_end = k;
-        break;
+        m[0] = b;
+        m[1] = k;
+        m[4] = segs(b);   // segments of request b made so far
+        int last_b = b, last_end = k;
+        int64_t budget = target;
+        while (b < B) {
+          const int nb = pages_of(b);
+          if (nb == 0) { ++b; continue; }
+          const int left = nb - k;
+          if (part == num_parts - 1 || left + fixed_cost <= budget) {
+            budget -= left + fixed_cost;
+            segs(b) += 1;
+            last_b = b;
+            last_end = nb;
+            ++b;
+            k = 0;
+          } else {
+            const int64_t take = budget - fixed_cost;
+            if (take < 1) break;
+            k += static_cast<int>(take);
+            segs(b) += 1;
+            last_b = b;
+            last_end = k;
+            break;
+          }
+        }
+        m[2] = last_b;
+        m[3] = last_end;
       }
+      int32_t* dst = meta + part * kMetaInts;   // 4-byte aligned (all the ABI asks for)
+#pragma unroll
+      for (int j = 0; j < kMetaInts; ++j) dst[j] = m[j];
     }
-    m[2] = last_b;
-    m[3] = last_end;
   }
-  num_splits[0] = 0;
-  for (int i = 0; i < B; ++i) num_splits[i + 1] += num_splits[i];
+  __syncthreads();
+  // num_splits = exclusive prefix sums of the segment counts: each thread scans a
+  // contiguous chunk, thread 0 scans the chunk totals.
+  const int chunk = (B + kScheduleThreads - 1) / kScheduleThreads;
+  const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
+  int32_t sum = 0;
+  for (int i = lo; i < hi; ++i) sum += in_smem ? seg_s[i] : num_splits[i + 1];
+  s_chunk[tid] = sum;
+  __syncthreads();
+  if (tid == 0) {
+    int32_t run = 0;
+    for (int j = 0; j < kScheduleThreads; ++j) {
+      const int32_t v = s_chunk[j];
+      s_chunk[j] = run;
+      run += v;
+    }
+    num_splits[0] = 0;
+  }
+  __syncthreads();
+  int32_t run = s_chunk[tid];
+  for (int i = lo; i < hi; ++i) {
+    run += in_smem ? seg_s[i] : num_splits[i + 1];
+    num_splits[i + 1] = run;
+  }
 }
 
 // ---------------------------------------------------------------- combine --
@@ -280,7 +335,14 @@ cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap&
 
 cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
                             int32_t* meta, int32_t* num_splits, cudaStream_t stream) {
-  mla_schedule_kernel<<<1, 32, 0, stream>>>(seqlens, B, num_parts, fixed_cost, hbm_parts, meta, num_splits);
+  const size_t smem = B <= kScheduleSmemMaxB ? 2 * sizeof(int32_t) * static_cast<size_t>(B) : 0;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(mla_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  mla_schedule_kernel<<<1, kScheduleThreads, smem, stream>>>(seqlens, B, num_parts, fixed_cost, hbm_parts, meta,
+                                                              num_splits);
   return cudaGetLastError();
 }
 

@@ -13,7 +13,9 @@
 // fp32 output accumulator of 128 x 512 -- all 512 TMEM columns of one SM -- so
 // the work of one row block is split over a CTA pair in one cluster:
 //   * the S-CTA (even cluster rank) keeps Q in TMEM (288 columns, the MMA's A
-//     operand), computes S = Q K^T for each page with tcgen05 (B = the page in
+//     operand; a segment's q rows arrive by TMA through the same two stages as the
+//     pages, 64 rows per stage, and the softmax warps copy them into TMEM),
+//     computes S = Q K^T for each page with tcgen05 (B = the page in
 //     shared memory, two pages in flight), and runs the online softmax in fp32
 //     with two warpgroups that split the page's 64 columns.  It stages P (bf16,
 //     already in the MMA operand layout) and the per-row rescale factors in its
@@ -86,7 +88,7 @@ struct Bars {
   uint64_t empty[kStages];  // stage free again
   uint64_t s_full[2];       // S-CTA: S = QK^T ready in TMEM
   uint64_t s_empty[2];      // S-CTA: S read by the softmax warps (8 arrivals)
-  uint64_t q_full;          // S-CTA: Q of the segment stored in TMEM (8 arrivals)
+  uint64_t q_full;          // S-CTA: Q of the segment stored in TMEM
   uint64_t credit[kSlots];  // S-CTA: the partner's receive slot is free (remote arrival)
   uint64_t p_full[kSlots];  // O-CTA: packet bytes arrived (bulk copy from the partner)
   uint64_t p_free[kSlots];  // O-CTA: PV MMAs that read a packet slot are done
@@ -251,19 +253,60 @@ __device__ void producer(const DecodeParams& p, const CUtensorMap* page_map, Sha
 }
 
 // ------------------------------------------------------------------ S-CTA --
+// The S-CTA ring walks, per segment, two q blocks (rows 0..63 and 64..127 of the
+// pair's row block) and then the segment's pages; ring item i uses stage i % 2.
+
+// Lane 0 of warp 0: every ring item (a q block or a page, 72 KiB, one TMA box).
+__device__ void s_producer(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
+                           uint32_t cl, int rb, bool withhold) {
+  SegmentWalker w;
+  w.init(p, part);
+  Segment s;
+  uint32_t i = 0;
+  int issued[kKStages];
+  uint32_t issued_phase[kKStages];
+  for (int j = 0; j < kKStages; ++j) issued[j] = 0, issued_phase[j] = 0;
+  const uint64_t policy = l2_policy_evict_first();
+  bool ok = true;
+  while (ok && w.next(s)) {
+    const int qrow0 = s.b * p.rows + rb * 128;
+    for (int j = 0; j < 2 && ok; ++j, ++i) {
+      const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
+      if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      if (withhold && i == 0) continue;   // test hook: this block never arrives
+      const uint32_t full = smem_u32(&sh.bar.full[st]);
+      mbar_arrive_expect_tx(full, kKStageBytes);
+      tma_load_3d(smem + kOffStage + st * kKStageBytes, &maps->q, full, 0, qrow0 + 64 * j, 0);
+      issued[st] = 1, issued_phase[st] = ph;
+    }
+    for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
+      const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
+      if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      const int blk = request_block(p, s.b, k);
+      const uint32_t full = smem_u32(&sh.bar.full[st]);
+      mbar_arrive_expect_tx(full, kKStageBytes);
+      tma_load_3d_hint(smem + kOffStage + st * kKStageBytes, &maps->k, full, 0, blk * 64, 0, policy);
+      issued[st] = 1, issued_phase[st] = ph;
+    }
+  }
+  for (int st = 0; st < kKStages; ++st)   // loads still in flight land before the CTA may exit
+    if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
+}
+
 // Warp 1 of the S-CTA; all 32 lanes run the loop, one elected lane issues.
 __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl) {
   SegmentWalker w;
   w.init(p, part);
   Segment s;
-  uint32_t T = 0, seg = 0;
+  uint32_t i = 0, T = 0, seg = 0;
   const uint32_t tmem = sh.tmem_base;
   constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
   bool ok = true, any = false;
   while (ok && w.next(s)) {
+    i += 2;   // the q blocks are consumed by the softmax warps
     if (!warp_wait(sh, smem_u32(&sh.bar.q_full), seg & 1, p.status, cl)) break;
-    for (int k = s.kb; k < s.ke; ++k, ++T) {
-      const uint32_t st = T % kKStages, ph = (T / kKStages) & 1;
+    for (int k = s.kb; k < s.ke; ++k, ++T, ++i) {
+      const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
       const uint32_t sb = T & 1, sph = (T >> 1) & 1;
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.s_empty[sb]), sph ^ 1, p.status, cl)) { ok = false; break; }
@@ -299,6 +342,25 @@ __device__ __forceinline__ float max32(const float (&x)[32]) {
   return m[0];
 }
 
+// Q rows of the segment from the two q-block stages into TMEM columns [0, 288):
+// thread (wg, r) moves dims [288 wg, 288 wg + 288) of row r (36 16-byte units).
+__device__ __forceinline__ void copy_q_to_tmem(uint32_t smem, uint32_t tmem_lane, uint32_t qstage0, uint32_t qstage1,
+                                               int wg, int r) {
+  const int rl = r & 63;
+  const uint32_t base = smem + kOffStage + ((r < 64) ? qstage0 : qstage1) * kKStageBytes + rl * 128;
+#pragma unroll
+  for (int c = 0; c < 9; ++c) {          // 9 groups of 4 units = 16 TMEM columns
+    uint32_t v[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int u = wg * 36 + c * 4 + j;   // unit over the 576 dims: chunk u / 8, unit u % 8
+      const uint4 x = ld_shared_v4(base + (u >> 3) * 8192 + (((u & 7) ^ (rl & 7)) << 4));
+      v[4 * j] = x.x, v[4 * j + 1] = x.y, v[4 * j + 2] = x.z, v[4 * j + 3] = x.w;
+    }
+    tmem_st16(tmem_lane + kQCol + wg * 144 + c * 16, v);
+  }
+}
+
 // Warps 4..11 of the S-CTA.  Warpgroup wg (0 or 1) handles columns [32*wg, 32*wg+32)
 // of every page for its 128 rows; the two exchange row maxima and partial sums
 // through shared memory and use named barrier 1 (256 threads).
@@ -321,43 +383,32 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
   SegmentWalker w;
   w.init(p, part);
   Segment s;
-  uint32_t T = 0;
+  uint32_t i = 0, T = 0;   // ring item (q blocks and pages) and page counters
   bool ok = true;
   while (ok && w.next(s)) {
     const int L = __ldg(p.seqlens + s.b);
     int vis = L;
     if (p.causal && row_valid) vis = L - p.s_q + pos_i + 1;
-    // Q of this request into TMEM columns [0, 288): warpgroup wg stores words
-    // [144 wg, 144 wg + 144).  The 36 loads per thread go out in two batches so
-    // that the row costs two memory round trips, not nine.
-    {
-      const int gq = row_valid ? g : 0;
-      const uint4* src =
-          reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(s.b) * p.rows + gq) * 576) + wg * 36;
-      {
-        uint4 x[20];
-#pragma unroll
-        for (int j = 0; j < 20; ++j) x[j] = row_valid ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c = 0; c < 5; ++c) tmem_st16(tmem_lane + kQCol + wg * 144 + c * 16, reinterpret_cast<uint32_t*>(&x[4 * c]));
-      }
-      {
-        uint4 x[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) x[j] = row_valid ? __ldg(src + 20 + j) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_st16(tmem_lane + kQCol + wg * 144 + (5 + c) * 16, reinterpret_cast<uint32_t*>(&x[4 * c]));
-      }
+    {   // Q of this request into TMEM (every QK^T of the previous segment is complete:
+        // its last S was waited for below)
+      const uint32_t q0 = i % kKStages, q1 = (i + 1) % kKStages;
+      const uint32_t mine = (r < 64) ? q0 : q1;
+      const uint32_t mph = ((i + ((r < 64) ? 0u : 1u)) / kKStages) & 1;
+      const bool got = wait_bar(sh, smem_u32(&sh.bar.full[mine]), mph, p.status, cl);
+      if (named_bar_or(1, kSoftThreads, !got)) break;
+      copy_q_to_tmem(smem, tmem_lane, q0, q1, wg, r);
       tmem_wait_st();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.bar.q_full));
-      if (t == 0) {   // the next segment's q rows and block-table row, into L2 now
-        SegmentWalker nx = w;
+      named_bar_sync(1, kSoftThreads);
+      if (t == 0) {
+        mbar_arrive(smem_u32(&sh.bar.q_full));
+        mbar_arrive(smem_u32(&sh.bar.empty[q0]));
+        mbar_arrive(smem_u32(&sh.bar.empty[q1]));
+        SegmentWalker nx = w;   // the next segment's q rows and block-table row, into L2 now
         Segment ns;
         if (nx.next(ns)) prefetch_request(p, ns.b);
       }
+      i += 2 + static_cast<uint32_t>(s.ke - s.kb);   // ring items of this segment
     }
     float m_ref = -INFINITY, l = 0.f;   // reference maximum (log2 units) and running sum of the rows
     for (int k = s.kb; k < s.ke; ++k, ++T) {
@@ -668,7 +719,12 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
   const uint32_t peer = rank ^ 1u;
 
   if (threadIdx.x == 0) {
-    prefetch_tensormap(is_s ? &maps.k : &maps.v);
+    if (is_s) {
+      prefetch_tensormap(&maps.q);
+      prefetch_tensormap(&maps.k);
+    } else {
+      prefetch_tensormap(&maps.v);
+    }
     if (is_s && rb == 0) {   // first request's q rows and block-table row, before anything else queues
       const int b0 = __ldg(p.meta + part * 8);
       if (b0 >= 0) prefetch_request(p, b0);
@@ -688,7 +744,7 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
       mbar_init(smem_u32(&sh.bar.p_full[i]), 1);
       mbar_init(smem_u32(&sh.bar.p_free[i]), 1);
     }
-    mbar_init(smem_u32(&sh.bar.q_full), 8);
+    mbar_init(smem_u32(&sh.bar.q_full), 1);
     mbar_init(smem_u32(&sh.bar.o_full), 1);
     mbar_init(smem_u32(&sh.bar.o_free), 8);
     mbar_init(smem_u32(&sh.bar.o_sync), 1);
@@ -706,8 +762,7 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
 
   if (is_s) {
     if (warp == 0) {
-      if ((threadIdx.x & 31) == 0)
-        producer<kKStages, 9>(p, &maps.k, sh, smem, part, cl, p.withhold_first_load != 0);
+      if ((threadIdx.x & 31) == 0) s_producer(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
     } else if (warp == 1) {
       s_cta_mma(p, sh, smem, part, cl);
     } else if (warp >= 4) {

@@ -88,19 +88,20 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uin
 
 }  // namespace
 
-bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache, int64_t num_blocks) {
-  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_blocks) * kPageTokens, kDimQK / 64};
+bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache, int64_t num_blocks,
+                    const void* q, int64_t q_rows) {
   const cuuint64_t strides[2] = {kDimQK * 2, 128};
   const cuuint32_t es[3] = {1, 1, 1};
-  const cuuint32_t kbox[3] = {64, kPageTokens, kDimQK / 64};
-  const cuuint32_t vbox[3] = {64, kPageTokens, kDimV / 64};
-  void* base = const_cast<void*>(kv_cache);
-  return encode(&maps->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, kbox, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
-         encode(&maps->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, vbox, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  auto enc = [&](CUtensorMap* m, const void* base, int64_t rows, uint32_t chunk0_count) {
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), kDimQK / 64};
+    const cuuint32_t box[3] = {64, 64, chunk0_count};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  const int64_t cache_rows = num_blocks * kPageTokens;
+  return enc(&maps->k, kv_cache, cache_rows, kDimQK / 64) && enc(&maps->v, kv_cache, cache_rows, kDimV / 64) &&
+         enc(&maps->q, q, q_rows, kDimQK / 64);
 }
 
 namespace {
@@ -201,7 +202,8 @@ mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t
   if (st != MLA_OK) return st;
 
   KvMaps kv_maps;
-  if (!encode_kv_maps(g_encode, &kv_maps, kv_cache, num_blocks)) return MLA_ERR_CUDA;
+  if (!encode_kv_maps(g_encode, &kv_maps, kv_cache, num_blocks, q, static_cast<int64_t>(B) * s_q * H))
+    return MLA_ERR_CUDA;
 
   const int rows = s_q * H;
   const size_t ms = max_splits(B, num_sm_parts);

@@ -44,17 +44,21 @@ struct DecodeParams {
   int withhold_first_load;
 };
 
-// Tensor maps of the paged latent cache, viewed as [chunk 0..8][token row][64 dims]:
-// dim 0 = 64 dims of a chunk (128 B, contiguous), dim 1 = token rows (stride 1152 B),
-// dim 2 = chunk (stride 128 B).  One box is a whole page in the swizzled, chunk-major
-// shared-memory layout the MMAs read: `k` takes all 9 chunks (576 dims, 72 KiB),
-// `v` the 8 value chunks (512 dims, 64 KiB).
+// Tensor maps of the decode kernel.  The paged latent cache and q are both viewed
+// as [chunk 0..8][row][64 dims]: dim 0 = 64 dims of a chunk (128 B, contiguous),
+// dim 1 = rows (stride 1152 B: cache tokens, or q rows b * s_q * H + i * H + h),
+// dim 2 = chunk (stride 128 B).  A box lands in the swizzled, chunk-major shared-
+// memory layout the MMAs read: k = a whole page (9 chunks, 72 KiB), v = the 8 value
+// chunks of a page (64 KiB), q = 64 q rows (72 KiB).
 struct KvMaps {
   CUtensorMap k;
   CUtensorMap v;
+  CUtensorMap q;
 };
-// Encodes both maps for a cache of num_blocks pages; false on failure.
-bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache, int64_t num_blocks);
+// Encodes the three maps for a cache of num_blocks pages and q_rows rows of q;
+// false on failure.
+bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache, int64_t num_blocks,
+                    const void* q, int64_t q_rows);
 
 // Device address of the kernels' status word on the current device (set-up on
 // first use); nullptr on error.

@@ -96,7 +96,8 @@ extern "C" mla_status_t mla_decode_noalloc(const mla_bf16_t* q, const mla_bf16_t
   if (!status) return MLA_ERR_CUDA;
 
   KvMaps kv_maps;
-  if (!encode_kv_maps(g_na_encode, &kv_maps, kv_cache, num_blocks)) return MLA_ERR_CUDA;
+  if (!encode_kv_maps(g_na_encode, &kv_maps, kv_cache, num_blocks, q, static_cast<int64_t>(B) * s_q * H))
+    return MLA_ERR_CUDA;
   // Nothing in the scratch has to start at zero: the schedule kernel writes every
   // metadata entry, and the decode kernel writes each partial slot before the
   // combine kernel of the same call reads it.
