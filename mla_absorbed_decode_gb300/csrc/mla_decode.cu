@@ -60,6 +60,8 @@ constexpr int kStages = 2;                            // barrier slots (the larg
 constexpr int kSlots = 4;                             // O-CTA packet receive slots: a slot's credit
                                                       // round trip over DSMEM is hidden 4 pages deep
 constexpr uint32_t kKStageBytes = 9 * 8192;           // S-CTA: 64 tokens x 576 dims, 9 swizzled chunks
+constexpr uint32_t kKPartA = 5;                       // chunks 0..4 of a page stage are released and
+                                                      // refilled as soon as QK^T is done with them
 constexpr uint32_t kVStageBytes = 8 * 8192;           // O-CTA: 64 tokens x 512 dims
 constexpr uint32_t kPBytes = 128 * 128;               // P: 128 rows x 64 tokens bf16 (MMA A layout)
 constexpr uint32_t kPktAlpha = kPBytes;               // float[128] rescale factor per row
@@ -84,8 +86,10 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint32_t kSoftThreads = 256;                // two warpgroups
 
 struct Bars {
-  uint64_t full[kStages];   // page landed (S: K, O: V)
-  uint64_t empty[kStages];  // stage free again
+  uint64_t full[kStages];   // O: chunks 0..3 of V landed; S: chunks 0..4 of K, or a whole q block
+  uint64_t empty[kStages];  // O: chunks 0..3 free again; S: chunks 0..4 free again
+  uint64_t full_b[kStages];   // S: chunks 5..8 of K landed (plain arrival for a q block); O: chunks 4..7 of V
+  uint64_t empty_b[kStages];  // S: chunks 5..8 free again; O: chunks 4..7 free again
   uint64_t s_full[2];       // S-CTA: S = QK^T ready in TMEM
   uint64_t s_empty[2];      // S-CTA: S read by the softmax warps (8 arrivals)
   uint64_t q_full;          // S-CTA: Q of the segment stored in TMEM
@@ -217,39 +221,41 @@ __device__ __forceinline__ int request_block(const DecodeParams& p, int b, int k
   return blk;
 }
 
-// Lane 0 of warp 0: stream every page of every segment through the page stages.
-// S-CTA: all 576 dims (9 swizzled 64 x 64 chunks, 72 KiB); O-CTA: the 512 value
-// dims (8 chunks, 64 KiB).
-template <int NST, int NCHUNK>
-__device__ void producer(const DecodeParams& p, const CUtensorMap* page_map, Shared& sh, uint32_t smem, int part,
-                         uint32_t cl, bool withhold) {
-  constexpr uint32_t kBytes = NCHUNK * 8192;
+// Lane 0 of warp 0 of the O-CTA: the 512 value dims of every page, as two 32 KiB
+// halves (chunks 0..3 and 4..7); each half is refilled as soon as the PV MMAs that
+// read it are done.
+__device__ void o_producer(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
+                           uint32_t cl) {
   SegmentWalker w;
   w.init(p, part);
   Segment s;
   uint32_t T = 0;
-  int issued[NST];
-  uint32_t issued_phase[NST];
-  for (int i = 0; i < NST; ++i) issued[i] = 0, issued_phase[i] = 0;
+  int issued[kVStages], issued_b[kVStages];
+  uint32_t issued_phase[kVStages], issued_phase_b[kVStages];
+  for (int j = 0; j < kVStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
   const uint64_t policy = l2_policy_evict_first();
   bool ok = true;
   while (ok && w.next(s)) {
-    for (int k = s.kb; k < s.ke; ++k, ++T) {
-      const uint32_t st = T % NST, ph = (T / NST) & 1;
+    for (int k = s.kb; k < s.ke && ok; ++k, ++T) {
+      const uint32_t st = T % kVStages, ph = (T / kVStages) & 1;
+      const uint32_t stage = smem + kOffStage + st * kVStageBytes;
       if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      if (withhold && T == 0) continue;   // test hook: this page never arrives
       const int blk = request_block(p, s.b, k);
       const uint32_t full = smem_u32(&sh.bar.full[st]);
-      mbar_arrive_expect_tx(full, kBytes);
-      const uint32_t dst = smem + kOffStage + st * kBytes;
-      tma_load_3d_hint(dst, page_map, full, 0, blk * 64, 0, policy);   // the whole page, one box
-      issued[st] = 1;
-      issued_phase[st] = ph;
+      mbar_arrive_expect_tx(full, kVStageBytes / 2);
+      tma_load_3d_hint(stage, &maps->c4, full, 0, blk * 64, 0, policy);
+      issued[st] = 1, issued_phase[st] = ph;
+      if (!wait_bar(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      const uint32_t full_b = smem_u32(&sh.bar.full_b[st]);
+      mbar_arrive_expect_tx(full_b, kVStageBytes / 2);
+      tma_load_3d_hint(stage + kVStageBytes / 2, &maps->c4, full_b, 0, blk * 64, 4, policy);
+      issued_b[st] = 1, issued_phase_b[st] = ph;
     }
   }
-  // drain: loads still in flight land before the CTA may exit
-  for (int st = 0; st < NST; ++st)
+  for (int st = 0; st < kVStages; ++st) {   // loads still in flight land before the CTA may exit
     if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
+    if (issued_b[st]) drain_bar(smem_u32(&sh.bar.full_b[st]), issued_phase_b[st]);
+  }
 }
 
 // ------------------------------------------------------------------ S-CTA --
@@ -263,16 +269,22 @@ __device__ void s_producer(const DecodeParams& p, const KvMaps* maps, Shared& sh
   w.init(p, part);
   Segment s;
   uint32_t i = 0;
-  int issued[kKStages];
-  uint32_t issued_phase[kKStages];
-  for (int j = 0; j < kKStages; ++j) issued[j] = 0, issued_phase[j] = 0;
+  int issued[kKStages], issued_b[kKStages];
+  uint32_t issued_phase[kKStages], issued_phase_b[kKStages];
+  for (int j = 0; j < kKStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
   const uint64_t policy = l2_policy_evict_first();
   bool ok = true;
   while (ok && w.next(s)) {
     const int qrow0 = s.b * p.rows + rb * 128;
     for (int j = 0; j < 2 && ok; ++j, ++i) {
       const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
-      if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl) ||
+          !wait_bar(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive(smem_u32(&sh.bar.full_b[st]));   // a q block lands whole; its second half needs no bytes
+      issued_b[st] = 1, issued_phase_b[st] = ph;
       if (withhold && i == 0) continue;   // test hook: this block never arrives
       const uint32_t full = smem_u32(&sh.bar.full[st]);
       mbar_arrive_expect_tx(full, kKStageBytes);
@@ -281,16 +293,24 @@ __device__ void s_producer(const DecodeParams& p, const KvMaps* maps, Shared& sh
     }
     for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
       const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
+      const uint32_t stage = smem + kOffStage + st * kKStageBytes;
       if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
       const int blk = request_block(p, s.b, k);
       const uint32_t full = smem_u32(&sh.bar.full[st]);
-      mbar_arrive_expect_tx(full, kKStageBytes);
-      tma_load_3d_hint(smem + kOffStage + st * kKStageBytes, &maps->k, full, 0, blk * 64, 0, policy);
+      mbar_arrive_expect_tx(full, kKPartA * 8192);
+      tma_load_3d_hint(stage, &maps->k_a, full, 0, blk * 64, 0, policy);
       issued[st] = 1, issued_phase[st] = ph;
+      if (!wait_bar(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      const uint32_t full_b = smem_u32(&sh.bar.full_b[st]);
+      mbar_arrive_expect_tx(full_b, kKStageBytes - kKPartA * 8192);
+      tma_load_3d_hint(stage + kKPartA * 8192, &maps->c4, full_b, 0, blk * 64, kKPartA, policy);
+      issued_b[st] = 1, issued_phase_b[st] = ph;
     }
   }
-  for (int st = 0; st < kKStages; ++st)   // loads still in flight land before the CTA may exit
+  for (int st = 0; st < kKStages; ++st) {   // loads still in flight land before the CTA may exit
     if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
+    if (issued_b[st]) drain_bar(smem_u32(&sh.bar.full_b[st]), issued_phase_b[st]);
+  }
 }
 
 // Warp 1 of the S-CTA; all 32 lanes run the loop, one elected lane issues.
@@ -314,11 +334,19 @@ __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       const uint32_t kstage = smem + kOffStage + st * kKStageBytes;
       const uint32_t d = tmem + kSCol0 + sb * 64;
 #pragma unroll
-      for (int kk = 0; kk < 36; ++kk) {
+      for (int kk = 0; kk < 4 * kKPartA; ++kk) {
         const uint64_t bdesc = smem_desc_sw128(kstage + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
         mma_bf16_ts_warp(d, tmem + kQCol + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
       }
-      mma_commit_warp(smem_u32(&sh.bar.empty[st]));
+      mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // chunks 0..4 may be refilled
+      if (!warp_wait(sh, smem_u32(&sh.bar.full_b[st]), ph, p.status, cl)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 4 * kKPartA; kk < 36; ++kk) {
+        const uint64_t bdesc = smem_desc_sw128(kstage + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+        mma_bf16_ts_warp(d, tmem + kQCol + kk * 8, bdesc, idesc, 1u);
+      }
+      mma_commit_warp(smem_u32(&sh.bar.empty_b[st]));
       mma_commit_warp(smem_u32(&sh.bar.s_full[sb]));
       any = true;
     }
@@ -403,7 +431,9 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       if (t == 0) {
         mbar_arrive(smem_u32(&sh.bar.q_full));
         mbar_arrive(smem_u32(&sh.bar.empty[q0]));
+        mbar_arrive(smem_u32(&sh.bar.empty_b[q0]));
         mbar_arrive(smem_u32(&sh.bar.empty[q1]));
+        mbar_arrive(smem_u32(&sh.bar.empty_b[q1]));
         SegmentWalker nx = w;   // the next segment's q rows and block-table row, into L2 now
         Segment ns;
         if (nx.next(ns)) prefetch_request(p, ns.b);
@@ -523,17 +553,20 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.p_full[ps]), pph, p.status, cl, true)) { ok = false; break; }
       // tail page: zero the value rows past the sequence end up to the next 16-row
-      // boundary, so that P = 0 never meets a non-finite value in the MMA
+      // boundary, so that P = 0 never meets a non-finite value in the MMA (per half)
       const int nvalid = min(64, L - k * 64);
       const int krows = (nvalid + 15) & ~15;
-      if (nvalid < krows) {
-        const int nz = krows - nvalid;                 // rows to clear, < 16
-        for (int i = lane; i < nz * 8 * 8; i += 32) {  // rows x chunks x 16-byte units
-          const int row = nvalid + i / 64, chunk = (i / 8) % 8, u = i % 8;
-          st_shared_v4(vstage + chunk * 8192 + row * 128 + u * 16, make_uint4(0, 0, 0, 0));
+      auto zero_tail = [&](uint32_t half) {
+        if (nvalid < krows) {
+          const int nz = krows - nvalid;                 // rows to clear, < 16
+          for (int i = lane; i < nz * 4 * 8; i += 32) {  // rows x chunks x 16-byte units
+            const int row = nvalid + i / 32, chunk = (i / 8) % 4, u = i % 8;
+            st_shared_v4(half + chunk * 8192 + row * 128 + u * 16, make_uint4(0, 0, 0, 0));
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
-      }
+      };
+      zero_tail(vstage);
       const bool last = (k == s.ke - 1);
       if (last)     // keep 1/l of the segment's rows before the slot can be reused
         st_shared_v4(smem + kOffInvL + lane * 16, ld_shared_v4(pkt + kPktInvL + lane * 16));
@@ -556,18 +589,26 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
         if (!warp_wait(sh, smem_u32(&sh.bar.corr_done), nresc & 1, p.status, cl)) { ok = false; break; }
         ++nresc;
       }
+      __syncwarp();
       tc_fence_after();
       {
         const int ksteps = krows / 16;
-        for (int js = 0; js < ksteps; ++js) {
+        for (int js = 0; js < ksteps; ++js) {   // output columns 0..255 from value chunks 0..3
           const uint64_t adesc = smem_desc_sw128(pkt + js * 32, 16, 1024);
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const uint64_t bdesc = smem_desc_sw128(vstage + h2 * 4 * 8192 + js * 2048, 8192, 1024);
-            mma_bf16_ss_warp(tmem + h2 * 256, adesc, bdesc, idesc, (k == s.kb && js == 0) ? 0u : 1u);
-          }
+          const uint64_t bdesc = smem_desc_sw128(vstage + js * 2048, 8192, 1024);
+          mma_bf16_ss_warp(tmem, adesc, bdesc, idesc, (k == s.kb && js == 0) ? 0u : 1u);
         }
-        mma_commit_warp(smem_u32(&sh.bar.empty[st]));
+        mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // chunks 0..3 may be refilled
+        if (!warp_wait(sh, smem_u32(&sh.bar.full_b[st]), ph, p.status, cl)) { ok = false; break; }
+        zero_tail(vstage + kVStageBytes / 2);
+        __syncwarp();
+        tc_fence_after();
+        for (int js = 0; js < ksteps; ++js) {   // output columns 256..511 from value chunks 4..7
+          const uint64_t adesc = smem_desc_sw128(pkt + js * 32, 16, 1024);
+          const uint64_t bdesc = smem_desc_sw128(vstage + kVStageBytes / 2 + js * 2048, 8192, 1024);
+          mma_bf16_ss_warp(tmem + 256, adesc, bdesc, idesc, (k == s.kb && js == 0) ? 0u : 1u);
+        }
+        mma_commit_warp(smem_u32(&sh.bar.empty_b[st]));
         mma_commit_warp(smem_u32(&sh.bar.p_free[ps]));
         if (last) mma_commit_warp(smem_u32(&sh.bar.o_full));
       }
@@ -721,10 +762,9 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
   if (threadIdx.x == 0) {
     if (is_s) {
       prefetch_tensormap(&maps.q);
-      prefetch_tensormap(&maps.k);
-    } else {
-      prefetch_tensormap(&maps.v);
+      prefetch_tensormap(&maps.k_a);
     }
+    prefetch_tensormap(&maps.c4);
     if (is_s && rb == 0) {   // first request's q rows and block-table row, before anything else queues
       const int b0 = __ldg(p.meta + part * 8);
       if (b0 >= 0) prefetch_request(p, b0);
@@ -734,6 +774,8 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&sh.bar.full[i]), 1);
       mbar_init(smem_u32(&sh.bar.empty[i]), 1);
+      mbar_init(smem_u32(&sh.bar.full_b[i]), 1);
+      mbar_init(smem_u32(&sh.bar.empty_b[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.bar.s_full[i]), 1);
@@ -770,7 +812,7 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     }
   } else {
     if (warp == 0) {
-      if ((threadIdx.x & 31) == 0) producer<kVStages, 8>(p, &maps.v, sh, smem, part, cl, false);
+      if ((threadIdx.x & 31) == 0) o_producer(p, &maps, sh, smem, part, cl);
     } else if (warp == 1) {
       o_cta_mma(p, sh, smem, part, cl);
     } else if (warp == 2) {

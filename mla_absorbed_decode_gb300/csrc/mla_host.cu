@@ -100,7 +100,7 @@ bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, cons
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
   const int64_t cache_rows = num_blocks * kPageTokens;
-  return enc(&maps->k, kv_cache, cache_rows, kDimQK / 64) && enc(&maps->v, kv_cache, cache_rows, kDimV / 64) &&
+  return enc(&maps->k_a, kv_cache, cache_rows, 5) && enc(&maps->c4, kv_cache, cache_rows, 4) &&
          enc(&maps->q, q, q_rows, kDimQK / 64);
 }
 

@@ -48,11 +48,12 @@ struct DecodeParams {
 // as [chunk 0..8][row][64 dims]: dim 0 = 64 dims of a chunk (128 B, contiguous),
 // dim 1 = rows (stride 1152 B: cache tokens, or q rows b * s_q * H + i * H + h),
 // dim 2 = chunk (stride 128 B).  A box lands in the swizzled, chunk-major shared-
-// memory layout the MMAs read: k = a whole page (9 chunks, 72 KiB), v = the 8 value
-// chunks of a page (64 KiB), q = 64 q rows (72 KiB).
+// memory layout the MMAs read: k_a = chunks 0..4 of a page (40 KiB), c4 = four
+// chunks of a page (32 KiB: K chunks 5..8, V chunks 0..3 or 4..7), q = 64 q rows
+// (72 KiB).
 struct KvMaps {
-  CUtensorMap k;
-  CUtensorMap v;
+  CUtensorMap k_a;
+  CUtensorMap c4;
   CUtensorMap q;
 };
 // Encodes the three maps for a cache of num_blocks pages and q_rows rows of q;
