@@ -33,8 +33,8 @@
  *    their loops and record a code in a device status word that
  *    mla_get_device_status reads.
  *  - Supported: 1 <= s_q * H <= 512 (rows are processed in blocks of 128;
- *    one block per 2-CTA pair, at most 4 pairs per cluster).  Dims are fixed at
- *    576 (q/k) and 512 (v); page size 64.
+ *    one block per 2-CTA pair, at most 4 pairs per cluster); 1 <= B <= 16384.
+ *    Dims are fixed at 576 (q/k) and 512 (v); page size 64.
  */
 #ifndef MLA_H_
 #define MLA_H_
@@ -73,10 +73,11 @@ size_t mla_metadata_size(int B, int num_sm_parts);
  * the sequence lengths only; page "MLA 推理：两条计算路径与 FlashMLA", FlashMLA
  * paragraph).  seqlens: [B] int32 device.  Writes metadata (mla_metadata_size
  * bytes, device): one 8-int record per part then B+1 split offsets.  The rule
- * (greedy over requests in order, per-segment cost in pages, at most
- * hbm_parts parts used when the GPU's bandwidth is already saturated) is
- * restated and checked bit for bit by the tests.  Reuse the result for every
- * layer of the same batch.  Async on stream. */
+ * (requests laid out in order on a line of cost positions -- a fixed set-up
+ * cost per request, then one position per page -- cut into equal pieces, one
+ * per part; at most hbm_parts parts are used when they already saturate the
+ * GPU's bandwidth) is restated and checked bit for bit by the tests.  Reuse the
+ * result for every layer of the same batch.  Async on stream. */
 mla_status_t mla_decode_metadata(const int32_t* seqlens, int B, int s_q, int H, int causal_s_q,
                                  int num_sm_parts, void* metadata, mla_stream_t stream);
 

@@ -17,120 +17,129 @@ namespace mla {
 // processes.  Greedy over the requests in order with a per-segment cost of
 // `fixed_cost` pages; at most `hbm_parts` parts are used, since that many
 // already keep HBM busy.  One thread: the walk is sequential and short.
-constexpr int kScheduleThreads = 256;
-constexpr int kScheduleSmemMaxB = 12 * 1024;   // page counts and segment counts of up to this many requests in smem
-
-// One CTA.  The page count of every request is read once, in parallel, into shared
-// memory (or, for batches too large for it, re-read from global memory); thread 0
-// then walks the parts; the segment counts are prefix-summed by all threads.
+// One CTA.  Every request is laid out on a line of cost positions: F set-up
+// positions, then one position per page; request b occupies [C[b], C[b+1]).  The
+// line is cut into P_eff equal pieces of T = ceil(C[B] / P_eff) positions, part p
+// taking the pages whose positions lie in [p T, (p + 1) T).  The costs are
+// prefix-summed by all threads; each part then finds its first and last page with
+// two binary searches, independently of the other parts.
 __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const int32_t* seqlens, int B, int num_parts,
                                                                         int fixed_cost, int hbm_parts, int32_t* meta,
                                                                         int32_t* num_splits) {
-  extern __shared__ int32_t sched_smem[];
-  __shared__ unsigned long long s_pages;
-  __shared__ int s_nonempty;
-  __shared__ int32_t s_chunk[kScheduleThreads];
+  extern __shared__ int64_t sched_c[];                                      // C[0..B]
+  int32_t* sched_nb = reinterpret_cast<int32_t*>(sched_c + B + 1);         // nb[0..B)
+  __shared__ int64_t s_part[kScheduleThreads];
   const int tid = threadIdx.x;
-  const bool in_smem = B <= kScheduleSmemMaxB;
-  int32_t* nb_s = sched_smem;          // [B] pages per request (in_smem only)
-  int32_t* seg_s = sched_smem + (in_smem ? B : 0);   // [B] segments per request (in_smem only)
-  if (tid == 0) {
-    s_pages = 0;
-    s_nonempty = 0;
-  }
-  __syncthreads();
-  unsigned long long my_pages = 0;
-  int my_nonempty = 0;
-  for (int i = tid; i < B; i += kScheduleThreads) {
-    const int L = seqlens[i];
-    const int nb = L > 0 ? (L + kPageTokens - 1) / kPageTokens : 0;
-    my_pages += static_cast<unsigned long long>(nb);
-    my_nonempty += nb > 0;
-    if (in_smem) {
-      nb_s[i] = nb;
-      seg_s[i] = 0;
-    } else {
-      num_splits[i + 1] = 0;
-    }
-  }
-  atomicAdd(&s_pages, my_pages);
-  atomicAdd(&s_nonempty, my_nonempty);
-  __syncthreads();
-  if (tid == 0) {
-    auto pages_of = [&](int i) {
-      if (in_smem) return nb_s[i];
-      const int L = seqlens[i];
-      return L > 0 ? (L + kPageTokens - 1) / kPageTokens : 0;
-    };
-    auto segs = [&](int i) -> int32_t& { return in_smem ? seg_s[i] : num_splits[i + 1]; };
-    const int p_eff = max(1, min(num_parts, hbm_parts));
-    const int64_t cost = static_cast<int64_t>(s_pages) + static_cast<int64_t>(fixed_cost) * (s_nonempty + p_eff - 1);
-    const int64_t target = (cost + p_eff - 1) / p_eff;
-    int b = 0, k = 0;
-    for (int part = 0; part < num_parts; ++part) {
-      int32_t m[kMetaInts] = {0, 0, 0, 0, 0, 0, 0, 0};
-      while (b < B && pages_of(b) == 0) ++b;
-      if (b >= B) {
-        m[0] = -1;
-      } else {
-        m[0] = b;
-        m[1] = k;
-        m[4] = segs(b);   // segments of request b made so far
-        int last_b = b, last_end = k;
-        int64_t budget = target;
-        while (b < B) {
-          const int nb = pages_of(b);
-          if (nb == 0) { ++b; continue; }
-          const int left = nb - k;
-          if (part == num_parts - 1 || left + fixed_cost <= budget) {
-            budget -= left + fixed_cost;
-            segs(b) += 1;
-            last_b = b;
-            last_end = nb;
-            ++b;
-            k = 0;
-          } else {
-            const int64_t take = budget - fixed_cost;
-            if (take < 1) break;
-            k += static_cast<int>(take);
-            segs(b) += 1;
-            last_b = b;
-            last_end = k;
-            break;
-          }
-        }
-        m[2] = last_b;
-        m[3] = last_end;
-      }
-      int32_t* dst = meta + part * kMetaInts;   // 4-byte aligned (all the ABI asks for)
-#pragma unroll
-      for (int j = 0; j < kMetaInts; ++j) dst[j] = m[j];
-    }
-  }
-  __syncthreads();
-  // num_splits = exclusive prefix sums of the segment counts: each thread scans a
-  // contiguous chunk, thread 0 scans the chunk totals.
+  const int64_t F = fixed_cost;
   const int chunk = (B + kScheduleThreads - 1) / kScheduleThreads;
   const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
-  int32_t sum = 0;
-  for (int i = lo; i < hi; ++i) sum += in_smem ? seg_s[i] : num_splits[i + 1];
-  s_chunk[tid] = sum;
+  // 1. page counts, per-thread sums of the costs, block-wide exclusive scan, C
+  int64_t sum = 0;
+  for (int i = lo; i < hi; ++i) {
+    const int L = seqlens[i];
+    const int nb = L > 0 ? (L + kPageTokens - 1) / kPageTokens : 0;
+    sched_nb[i] = nb;
+    sum += nb > 0 ? nb + F : 0;
+  }
+  s_part[tid] = sum;
   __syncthreads();
   if (tid == 0) {
-    int32_t run = 0;
+    int64_t run = 0;
     for (int j = 0; j < kScheduleThreads; ++j) {
-      const int32_t v = s_chunk[j];
-      s_chunk[j] = run;
+      const int64_t v = s_part[j];
+      s_part[j] = run;
       run += v;
+    }
+    sched_c[0] = 0;
+  }
+  __syncthreads();
+  int64_t run = s_part[tid];
+  for (int i = lo; i < hi; ++i) {
+    run += sched_nb[i] > 0 ? sched_nb[i] + F : 0;
+    sched_c[i + 1] = run;
+  }
+  __syncthreads();
+  const int64_t total = sched_c[B];
+  const int p_eff = max(1, min(num_parts, hbm_parts));
+  const int64_t T = (total + p_eff - 1) / p_eff;
+  // first index b in [0, B) with C[b + 1] > x (C[1..B] is non-decreasing); B if none
+  auto first_above = [&](int64_t x) {
+    int l = 0, h = B;
+    while (l < h) {
+      const int m = (l + h) >> 1;
+      if (sched_c[m + 1] > x) h = m; else l = m + 1;
+    }
+    return l;
+  };
+  // 2. one metadata record per part
+  for (int p = tid; p < num_parts; p += kScheduleThreads) {
+    int32_t m[kMetaInts] = {-1, 0, 0, 0, 0, 0, 0, 0};
+    const int64_t plo = static_cast<int64_t>(p) * T, phi = plo + T;
+    if (total > 0 && p < p_eff && plo < total) {
+      const int bf = first_above(plo);
+      const int64_t kf0 = plo - sched_c[bf] - F;
+      const int64_t kf = kf0 > 0 ? kf0 : 0;
+      if (sched_c[bf] + F + kf < phi) {
+        // the last non-empty request whose first page lies before phi: x = the number of
+        // requests b with C[b] + F < phi; the last page before C[x] belongs to it
+        int l = 0, h = B;
+        while (l < h) {
+          const int mid = (l + h) >> 1;
+          if (sched_c[mid] + F >= phi) h = mid; else l = mid + 1;
+        }
+        const int bl = first_above(sched_c[l] - 1);
+        const int64_t ke0 = phi - sched_c[bl] - F;
+        const int64_t ke = ke0 < sched_nb[bl] ? ke0 : static_cast<int64_t>(sched_nb[bl]);
+        m[0] = bf;
+        m[1] = static_cast<int32_t>(kf);
+        m[2] = bl;
+        m[3] = static_cast<int32_t>(ke);
+        m[4] = static_cast<int32_t>(p - (sched_c[bf] + F) / T);
+      }
+    }
+    int32_t* dst = meta + p * kMetaInts;   // 4-byte aligned (all the ABI asks for)
+#pragma unroll
+    for (int j = 0; j < kMetaInts; ++j) dst[j] = (j == 0 || m[0] >= 0) ? m[j] : 0;
+  }
+  // 3. segments per request, prefix-summed into num_splits
+  int32_t segs = 0;
+  for (int i = lo; i < hi; ++i) {
+    const int nb = sched_nb[i];
+    if (nb > 0) segs += static_cast<int32_t>((sched_c[i] + F + nb - 1) / T - (sched_c[i] + F) / T + 1);
+  }
+  __syncthreads();
+  s_part[tid] = segs;
+  __syncthreads();
+  if (tid == 0) {
+    int64_t r = 0;
+    for (int j = 0; j < kScheduleThreads; ++j) {
+      const int64_t v = s_part[j];
+      s_part[j] = r;
+      r += v;
     }
     num_splits[0] = 0;
   }
   __syncthreads();
-  int32_t run = s_chunk[tid];
+  int32_t r = static_cast<int32_t>(s_part[tid]);
   for (int i = lo; i < hi; ++i) {
-    run += in_smem ? seg_s[i] : num_splits[i + 1];
-    num_splits[i + 1] = run;
+    const int nb = sched_nb[i];
+    if (nb > 0) r += static_cast<int32_t>((sched_c[i] + F + nb - 1) / T - (sched_c[i] + F) / T + 1);
+    num_splits[i + 1] = r;
   }
+}
+
+cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
+                            int32_t* meta, int32_t* num_splits, cudaStream_t stream) {
+  if (B < 1 || B > kScheduleMaxB) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(int64_t) * (static_cast<size_t>(B) + 1) + sizeof(int32_t) * static_cast<size_t>(B);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(mla_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  mla_schedule_kernel<<<1, kScheduleThreads, smem, stream>>>(seqlens, B, num_parts, fixed_cost, hbm_parts, meta,
+                                                              num_splits);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- combine --
@@ -333,18 +342,6 @@ cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap&
   return cudaGetLastError();
 }
 
-cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
-                            int32_t* meta, int32_t* num_splits, cudaStream_t stream) {
-  const size_t smem = B <= kScheduleSmemMaxB ? 2 * sizeof(int32_t) * static_cast<size_t>(B) : 0;
-  if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(mla_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  mla_schedule_kernel<<<1, kScheduleThreads, smem, stream>>>(seqlens, B, num_parts, fixed_cost, hbm_parts, meta,
-                                                              num_splits);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* num_splits, int B, int rows,
                            __nv_bfloat16* out, float* lse, cudaStream_t stream) {

@@ -159,7 +159,7 @@ mla_status_t mla_decode_metadata(const int32_t* seqlens, int B, int s_q, int H, 
                                  void* metadata, mla_stream_t stream) {
   (void)causal_s_q;
   if (!seqlens || !metadata || B < 1 || s_q < 1 || H < 1 || num_sm_parts < 1) return MLA_ERR_INVALID_ARG;
-  if (pairs_for(s_q, H) > kMaxPairsPerCluster) return MLA_ERR_UNSUPPORTED;
+  if (pairs_for(s_q, H) > kMaxPairsPerCluster || B > kScheduleMaxB) return MLA_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(metadata) & 3u) != 0) return MLA_ERR_INVALID_ARG;
   DeviceState* d = nullptr;
   mla_status_t st = current_device(&d);

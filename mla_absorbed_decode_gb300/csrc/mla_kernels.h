@@ -22,6 +22,8 @@ constexpr int kMetaInts = 8;            // ints per part record
 // mla_schedule_params).
 constexpr int kSegmentCostPages = 2;    // one segment's set-up + epilogue, in pages
 constexpr int kHbmParts = 64;           // clusters that already saturate HBM
+constexpr int kScheduleThreads = 512;
+constexpr int kScheduleMaxB = 16384;    // requests per batch (the schedule keeps its prefix sums in shared memory)
 
 struct DecodeParams {
   const __nv_bfloat16* q;

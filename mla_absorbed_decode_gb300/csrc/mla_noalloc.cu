@@ -82,7 +82,7 @@ extern "C" mla_status_t mla_decode_noalloc(const mla_bf16_t* q, const mla_bf16_t
     return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   const int n_rb = (s_q * H + kRowsPerPair - 1) / kRowsPerPair;
-  if (n_rb > kMaxPairsPerCluster) return MLA_ERR_UNSUPPORTED;
+  if (n_rb > kMaxPairsPerCluster || B > kScheduleMaxB) return MLA_ERR_UNSUPPORTED;
   if (num_blocks * kPageTokens > (int64_t(1) << 31) - kPageTokens) return MLA_ERR_UNSUPPORTED;
   // the sizes must fit the fixed scratch; larger problems are refused, not truncated
   const size_t meta_bytes = mla_metadata_size(B, num_sm_parts);

@@ -9,19 +9,21 @@ axis across SMs with the partial results merged afterwards ("MLA 推理：两条
 路径与 FlashMLA", section "decode 注意力变成了计算问题").  Which rule balances
 the work is left open, so any schedule is correct that covers every page of
 every request exactly once; ``check_schedule`` tests exactly that.  The library
-uses one particular greedy rule, restated in ``schedule_reference`` so that its
-integer output can be compared bit for bit:
+uses one particular rule, restated in ``schedule_reference`` so that its
+integer output can be compared bit for bit.  Every request is laid out on one
+line of "cost" positions, F positions of segment set-up cost followed by one
+position per page, and the line is cut into equal pieces, one per part:
 
-  nb[b]   = ceil(seqlen[b] / 64)          (0 for an empty request)
-  P_eff   = min(P, hbm_parts)             parts that already saturate HBM
-  cost    = sum_b nb[b] + F * (#{b : nb[b] > 0} + P_eff - 1)
-            (F = cost of one segment in pages; a schedule over P_eff parts has
-            at most one segment per request plus one per part boundary)
-  target  = ceil(cost / P_eff)
-  Parts p = 0..P-1 walk the requests in order.  A part takes whole requests
-  while (pages left in it + F) fits in its budget; otherwise it takes
-  (budget - F) pages of the current request (at least one) and stops.  The
-  last part takes everything still left.  Parts that get nothing are empty.
+  nb[b]   = ceil(seqlen[b] / 64)           (0 for an empty request)
+  cost[b] = nb[b] + F if nb[b] > 0 else 0  (F = set-up cost of a segment, in pages)
+  C[b]    = cost[0] + ... + cost[b-1]      (request b occupies positions [C[b], C[b+1]))
+  page k of request b sits at position C[b] + F + k
+  P_eff   = min(P, hbm_parts)              parts that already saturate HBM
+  T       = ceil(C[B] / P_eff)             positions per part
+  part p takes the pages whose position lies in [p T, (p + 1) T)
+
+Each part's pages are contiguous in (request, page) order, so a part is found
+by two binary searches on C, independently of the other parts.
 
 Metadata row of part p (all int32): [b_first, k_first, b_last, k_end, split_first]
   - empty part: b_first = -1 (the rest 0);
@@ -41,47 +43,40 @@ def pages_of(seqlen: int) -> int:
 
 
 def schedule_reference(seqlens, num_parts: int, fixed_cost: int, hbm_parts: int):
-    """The greedy rule above.  Returns (meta: list of 5-tuples, num_splits: list)."""
+    """The rule above.  Returns (meta: list of 5-tuples, num_splits: list)."""
     B = len(seqlens)
+    F = fixed_cost
     nb = [pages_of(L) for L in seqlens]
-    nonempty = sum(1 for n in nb if n > 0)
+    cost = [n + F if n > 0 else 0 for n in nb]
+    C = [0] * (B + 1)
+    for b in range(B):
+        C[b + 1] = C[b] + cost[b]
+    total = C[B]
     p_eff = max(1, min(num_parts, hbm_parts))
-    cost = sum(nb) + fixed_cost * (nonempty + p_eff - 1)
-    target = (cost + p_eff - 1) // p_eff
-    segs = [0] * B
+    T = (total + p_eff - 1) // p_eff
     meta = []
-    b, k = 0, 0
     for p in range(num_parts):
-        while b < B and nb[b] == 0:
-            b += 1
-        if b >= B:
+        lo, hi = p * T, (p + 1) * T
+        if total == 0 or p >= p_eff or lo >= total:
             meta.append((-1, 0, 0, 0, 0))
             continue
-        first = (b, k, segs[b])
-        last_b, last_end = b, k
-        budget = target
-        while b < B:
-            if nb[b] == 0:
-                b += 1
-                continue
-            left = nb[b] - k
-            if p == num_parts - 1 or left + fixed_cost <= budget:
-                budget -= left + fixed_cost
-                segs[b] += 1
-                last_b, last_end = b, nb[b]
-                b, k = b + 1, 0
-            else:
-                take = budget - fixed_cost
-                if take < 1:
-                    break
-                k += take
-                segs[b] += 1
-                last_b, last_end = b, k
-                break
-        meta.append((first[0], first[1], last_b, last_end, first[2]))
+        # first page: request b_first is the first b with C[b + 1] > lo (never empty)
+        b_first = next(b for b in range(B) if C[b + 1] > lo)
+        k_first = max(0, lo - C[b_first] - F)
+        if C[b_first] + F + k_first >= hi:
+            meta.append((-1, 0, 0, 0, 0))      # the piece holds set-up positions only
+            continue
+        # last page: request b_last is the last non-empty b whose first page lies before hi
+        b_last = max(b for b in range(B) if nb[b] > 0 and C[b] + F < hi)
+        k_end = min(nb[b_last], hi - C[b_last] - F)
+        split_first = p - (C[b_first] + F) // T
+        meta.append((b_first, k_first, b_last, k_end, split_first))
     num_splits = [0] * (B + 1)
-    for i in range(B):
-        num_splits[i + 1] = num_splits[i] + segs[i]
+    for b in range(B):
+        n = 0
+        if nb[b] > 0:
+            n = (C[b] + F + nb[b] - 1) // T - (C[b] + F) // T + 1
+        num_splits[b + 1] = num_splits[b] + n
     return meta, num_splits
 
 

@@ -74,6 +74,7 @@ def test_host_argument_checks(mla):
         assert L.mla_decode(*neg_scale) == 1
     assert L.mla_decode_metadata(None, 2, 1, 16, 0, 4, A, None) == 1
     assert L.mla_decode_metadata(A, 2, 8, 128, 0, 4, A, None) == 2
+    assert L.mla_decode_metadata(A, 16385, 1, 128, 0, 4, A, None) == 2   # more requests than supported
     assert L.mla_absorb_q(A, 100, None, 0, A, A, 4, 1, None) == 1      # stride below H*128
     assert L.mla_absorb_q(A, 128, A, 8, A, A, 4, 1, None) == 1         # q_pe stride below H*64
     assert L.mla_unabsorb_o(A + 8, A, A, 4, 1, None) == 1

@@ -10,7 +10,8 @@ def test_hand_worked_example():
     # pages per request: 3, 5, 0, 2; two parts, per-segment cost 1
     seqlens = [3 * 64, 4 * 64 + 1, 0, 2 * 64]
     meta, ns = schedule_reference(seqlens, num_parts=2, fixed_cost=1, hbm_parts=100)
-    # cost = 10 + 1 * (3 + 2 - 1) = 14, target = ceil(14 / 2) = 7
+    # costs 4, 6, 0, 3 -> C = 0, 4, 10, 10, 13; T = ceil(13 / 2) = 7; pages sit at
+    # positions 1-3 (request 0), 5-9 (request 1), 11-12 (request 3)
     assert meta == [(0, 0, 1, 2, 0), (1, 2, 3, 2, 1)]
     assert ns == [0, 1, 3, 3, 4]
     check_schedule(meta, ns, seqlens)
@@ -39,7 +40,8 @@ def test_single_long_request_is_split_evenly():
     segs = expand_segments(meta, seqlens)
     sizes = [ke - kb for _, _, kb, ke, _ in segs]
     assert len(segs) == 16 and ns == [0, 16]
-    assert sizes == [128] * 16      # cost 2048 + 2 * 16 = 2080 -> 130 per part, 128 pages
+    # cost 2048 + 2 = 2050 -> T = 129 positions per part; part 0 also holds the set-up
+    assert sizes == [127] + [129] * 14 + [115]
     check_schedule(meta, ns, seqlens)
 
 
