@@ -75,15 +75,18 @@ size_t mla_metadata_size(int B, int num_sm_parts);
  * bytes, device): one 8-int record per part then B+1 split offsets.  The rule
  * (requests laid out in order on a line of cost positions -- a fixed set-up
  * cost per request, then one position per page -- cut into equal pieces, one
- * per part; at most hbm_parts parts are used when they already saturate the
- * GPU's bandwidth) is restated and checked bit for bit by the tests.  Reuse the
+ * per part; hbm_parts parts are used when they already saturate the GPU's
+ * bandwidth, all parts when that is estimated to pay for the extra splits) is
+ * restated and checked bit for bit by the tests.  Reuse the
  * result for every layer of the same batch.  Async on stream. */
 mla_status_t mla_decode_metadata(const int32_t* seqlens, int B, int s_q, int H, int causal_s_q,
                                  int num_sm_parts, void* metadata, mla_stream_t stream);
 
-/* The schedule's constants, for tests: per-segment cost (pages) and the number
- * of parts that saturate HBM for one 2-CTA pair per part. */
-void mla_schedule_params(int* fixed_cost_pages, int* hbm_parts);
+/* The schedule's constants, for tests: per-segment set-up cost (pages), the
+ * number of parts that saturate HBM for one 2-CTA pair per part, and the cost of
+ * an extra segment (pages) used to choose between that many parts and all of them.
+ * Any pointer may be NULL. */
+void mla_schedule_params(int* fixed_cost_pages, int* hbm_parts, int* split_cost_pages);
 
 /* Bytes of the split workspace (fp32 partial outputs and lse of split requests). */
 size_t mla_decode_workspace_size(int B, int s_q, int H, int num_sm_parts);

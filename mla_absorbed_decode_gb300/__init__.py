@@ -32,7 +32,7 @@ _SIGNATURES = {
     "mla_num_sm_parts": (_c_int, [_c_int, _c_int, _c_int]),
     "mla_metadata_size": (_c_size, [_c_int, _c_int]),
     "mla_decode_metadata": (_c_int, [_p, _c_int, _c_int, _c_int, _c_int, _c_int, _p, _p]),
-    "mla_schedule_params": (None, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
+    "mla_schedule_params": (None, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
     "mla_decode_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "mla_decode": (_c_int, [_p, _p, _c_ll, _p, _c_int, _p, _c_int, _c_int, _c_int, _c_float, _c_int,
                             _p, _c_int, _p, _c_size, _p, _p, _p]),
@@ -97,10 +97,11 @@ def metadata_size(B: int, parts: int) -> int:
     return lib().mla_metadata_size(B, parts)
 
 
-def schedule_params() -> tuple[int, int]:
-    f, h = _c_int(), _c_int()
-    lib().mla_schedule_params(ctypes.byref(f), ctypes.byref(h))
-    return f.value, h.value
+def schedule_params() -> tuple[int, int, int]:
+    """(set-up cost per segment, parts that saturate HBM, cost of an extra segment), in pages."""
+    f, h, c = _c_int(), _c_int(), _c_int()
+    lib().mla_schedule_params(ctypes.byref(f), ctypes.byref(h), ctypes.byref(c))
+    return f.value, h.value, c.value
 
 
 def decode_metadata(seqlens: torch.Tensor, s_q: int, H: int, causal: bool, parts: int,

@@ -14,18 +14,17 @@ namespace mla {
 // --------------------------------------------------------------- schedule --
 // get_mla_metadata's role ("MLA 推理：两条计算路径与 FlashMLA", FlashMLA paragraph):
 // from the sequence lengths alone, decide which KV pages each part (cluster)
-// processes.  Greedy over the requests in order with a per-segment cost of
-// `fixed_cost` pages; at most `hbm_parts` parts are used, since that many
-// already keep HBM busy.  One thread: the walk is sequential and short.
-// One CTA.  Every request is laid out on a line of cost positions: F set-up
+// processes; at most `hbm_parts` parts are used, since that many already keep HBM
+// busy, unless using all parts is estimated to be faster even with the splits it
+// causes (`split_cost` pages per extra segment).  One CTA.  Every request is laid out on a line of cost positions: F set-up
 // positions, then one position per page; request b occupies [C[b], C[b+1]).  The
 // line is cut into P_eff equal pieces of T = ceil(C[B] / P_eff) positions, part p
 // taking the pages whose positions lie in [p T, (p + 1) T).  The costs are
 // prefix-summed by all threads; each part then finds its first and last page with
 // two binary searches, independently of the other parts.
 __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const int32_t* seqlens, int B, int num_parts,
-                                                                        int fixed_cost, int hbm_parts, int32_t* meta,
-                                                                        int32_t* num_splits) {
+                                                                        int fixed_cost, int hbm_parts, int split_cost,
+                                                                        int32_t* meta, int32_t* num_splits) {
   extern __shared__ int64_t sched_c[];                                      // C[0..B]
   int32_t* sched_nb = reinterpret_cast<int32_t*>(sched_c + B + 1);         // nb[0..B)
   __shared__ int64_t s_part[kScheduleThreads];
@@ -60,7 +59,35 @@ __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const in
   }
   __syncthreads();
   const int64_t total = sched_c[B];
-  const int p_eff = max(1, min(num_parts, hbm_parts));
+  int p_eff = max(1, min(num_parts, hbm_parts));
+  // segments of request i when parts hold T positions each
+  auto segments = [&](int i, int64_t T) -> int64_t {
+    const int nb = sched_nb[i];
+    return nb > 0 ? (sched_c[i] + F + nb - 1) / T - (sched_c[i] + F) / T + 1 : 0;
+  };
+  if (split_cost > 0 && total > 0 && num_parts > p_eff) {
+    int64_t best_est = -1;
+    int best_p = p_eff;
+    const int cand[2] = {p_eff, num_parts};
+    for (int c = 0; c < 2; ++c) {
+      const int pe = cand[c];
+      const int64_t Tc = (total + pe - 1) / pe;
+      int64_t extra = 0;
+      for (int i = lo; i < hi; ++i) extra += sched_nb[i] > 0 ? segments(i, Tc) - 1 : 0;
+      __syncthreads();
+      s_part[tid] = extra;
+      __syncthreads();
+      if (tid == 0) {
+        int64_t e = 0;
+        for (int j = 0; j < kScheduleThreads; ++j) e += s_part[j];
+        s_part[0] = e;
+      }
+      __syncthreads();
+      const int64_t est = Tc + static_cast<int64_t>(split_cost) * ((s_part[0] + pe - 1) / pe);
+      if (best_est < 0 || est < best_est) best_est = est, best_p = pe;
+    }
+    p_eff = best_p;
+  }
   const int64_t T = (total + p_eff - 1) / p_eff;
   // first index b in [0, B) with C[b + 1] > x (C[1..B] is non-decreasing); B if none
   auto first_above = [&](int64_t x) {
@@ -103,10 +130,8 @@ __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const in
   }
   // 3. segments per request, prefix-summed into num_splits
   int32_t segs = 0;
-  for (int i = lo; i < hi; ++i) {
-    const int nb = sched_nb[i];
-    if (nb > 0) segs += static_cast<int32_t>((sched_c[i] + F + nb - 1) / T - (sched_c[i] + F) / T + 1);
-  }
+  if (total > 0)
+    for (int i = lo; i < hi; ++i) segs += static_cast<int32_t>(segments(i, T));
   __syncthreads();
   s_part[tid] = segs;
   __syncthreads();
@@ -122,14 +147,13 @@ __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const in
   __syncthreads();
   int32_t r = static_cast<int32_t>(s_part[tid]);
   for (int i = lo; i < hi; ++i) {
-    const int nb = sched_nb[i];
-    if (nb > 0) r += static_cast<int32_t>((sched_c[i] + F + nb - 1) / T - (sched_c[i] + F) / T + 1);
+    if (total > 0) r += static_cast<int32_t>(segments(i, T));
     num_splits[i + 1] = r;
   }
 }
 
 cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
-                            int32_t* meta, int32_t* num_splits, cudaStream_t stream) {
+                            int split_cost, int32_t* meta, int32_t* num_splits, cudaStream_t stream) {
   if (B < 1 || B > kScheduleMaxB) return cudaErrorInvalidValue;
   const size_t smem = sizeof(int64_t) * (static_cast<size_t>(B) + 1) + sizeof(int32_t) * static_cast<size_t>(B);
   if (smem > 48 * 1024) {
@@ -137,8 +161,8 @@ cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fi
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  mla_schedule_kernel<<<1, kScheduleThreads, smem, stream>>>(seqlens, B, num_parts, fixed_cost, hbm_parts, meta,
-                                                              num_splits);
+  mla_schedule_kernel<<<1, kScheduleThreads, smem, stream>>>(seqlens, B, num_parts, fixed_cost, hbm_parts,
+                                                              split_cost, meta, num_splits);
   return cudaGetLastError();
 }
 

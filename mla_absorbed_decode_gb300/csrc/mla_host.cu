@@ -150,9 +150,10 @@ size_t mla_metadata_size(int B, int num_sm_parts) {
   return (static_cast<size_t>(kMetaInts) * num_sm_parts + B + 1) * sizeof(int32_t);
 }
 
-void mla_schedule_params(int* fixed_cost_pages, int* hbm_parts) {
+void mla_schedule_params(int* fixed_cost_pages, int* hbm_parts, int* split_cost_pages) {
   if (fixed_cost_pages) *fixed_cost_pages = kSegmentCostPages;
   if (hbm_parts) *hbm_parts = kHbmParts;
+  if (split_cost_pages) *split_cost_pages = kSplitCostPages;
 }
 
 mla_status_t mla_decode_metadata(const int32_t* seqlens, int B, int s_q, int H, int causal_s_q, int num_sm_parts,
@@ -165,7 +166,7 @@ mla_status_t mla_decode_metadata(const int32_t* seqlens, int B, int s_q, int H, 
   mla_status_t st = current_device(&d);
   if (st != MLA_OK) return st;
   int32_t* meta = static_cast<int32_t*>(metadata);
-  return launch_schedule(seqlens, B, num_sm_parts, kSegmentCostPages, kHbmParts, meta, meta + kMetaInts * num_sm_parts,
+  return launch_schedule(seqlens, B, num_sm_parts, kSegmentCostPages, kHbmParts, kSplitCostPages, meta, meta + kMetaInts * num_sm_parts,
                          reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;

@@ -22,6 +22,7 @@ constexpr int kMetaInts = 8;            // ints per part record
 // mla_schedule_params).
 constexpr int kSegmentCostPages = 2;    // one segment's set-up + epilogue, in pages
 constexpr int kHbmParts = 64;           // clusters that already saturate HBM
+constexpr int kSplitCostPages = 12;     // estimated cost of an extra segment (q reload, partials, combine)
 constexpr int kScheduleThreads = 512;
 constexpr int kScheduleMaxB = 16384;    // requests per batch (the schedule keeps its prefix sums in shared memory)
 
@@ -73,7 +74,7 @@ int decode_max_clusters(int cluster_ctas);            // occupancy query; 0 on e
 cudaError_t launch_decode(const KvMaps& maps, const DecodeParams& p, int cluster_ctas, cudaStream_t stream);
 
 cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
-                            int32_t* meta, int32_t* num_splits, cudaStream_t stream);
+                            int split_cost, int32_t* meta, int32_t* num_splits, cudaStream_t stream);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* num_splits, int B, int rows,
                            __nv_bfloat16* out, float* lse, cudaStream_t stream);
 

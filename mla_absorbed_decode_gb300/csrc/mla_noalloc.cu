@@ -104,7 +104,7 @@ extern "C" mla_status_t mla_decode_noalloc(const mla_bf16_t* q, const mla_bf16_t
   int32_t* meta = reinterpret_cast<int32_t*>(d->scratch);
   uint8_t* ws = d->scratch + kMetaBytes;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_schedule(seqlens, B, num_sm_parts, kSegmentCostPages, kHbmParts, meta, meta + kMetaInts * num_sm_parts,
+  if (launch_schedule(seqlens, B, num_sm_parts, kSegmentCostPages, kHbmParts, kSplitCostPages, meta, meta + kMetaInts * num_sm_parts,
                       cs) != cudaSuccess)
     return MLA_ERR_CUDA;
 

@@ -18,7 +18,10 @@ position per page, and the line is cut into equal pieces, one per part:
   cost[b] = nb[b] + F if nb[b] > 0 else 0  (F = set-up cost of a segment, in pages)
   C[b]    = cost[0] + ... + cost[b-1]      (request b occupies positions [C[b], C[b+1]))
   page k of request b sits at position C[b] + F + k
-  P_eff   = min(P, hbm_parts)              parts that already saturate HBM
+  P_eff   = min(P, hbm_parts)              parts that already saturate HBM; with a split
+            cost S > 0 (in pages), P_eff is instead whichever of min(P, hbm_parts)
+            and P has the smaller estimate T + S * ceil(extra / P_eff), where
+            extra counts the segments beyond one per request (ties: the smaller)
   T       = ceil(C[B] / P_eff)             positions per part
   part p takes the pages whose position lies in [p T, (p + 1) T)
 
@@ -42,7 +45,14 @@ def pages_of(seqlen: int) -> int:
     return (int(seqlen) + PAGE - 1) // PAGE if seqlen > 0 else 0
 
 
-def schedule_reference(seqlens, num_parts: int, fixed_cost: int, hbm_parts: int):
+def _segments(C, nb, F, T, b):
+    """Segments of request b when parts hold T positions each."""
+    if nb[b] == 0:
+        return 0
+    return (C[b] + F + nb[b] - 1) // T - (C[b] + F) // T + 1
+
+
+def schedule_reference(seqlens, num_parts: int, fixed_cost: int, hbm_parts: int, split_cost: int = 0):
     """The rule above.  Returns (meta: list of 5-tuples, num_splits: list)."""
     B = len(seqlens)
     F = fixed_cost
@@ -53,6 +63,15 @@ def schedule_reference(seqlens, num_parts: int, fixed_cost: int, hbm_parts: int)
         C[b + 1] = C[b] + cost[b]
     total = C[B]
     p_eff = max(1, min(num_parts, hbm_parts))
+    if split_cost > 0 and total > 0 and num_parts > p_eff:
+        best = None
+        for pe in (p_eff, num_parts):
+            T = (total + pe - 1) // pe
+            extra = sum(_segments(C, nb, F, T, b) - 1 for b in range(B) if nb[b] > 0)
+            est = T + split_cost * ((extra + pe - 1) // pe)
+            if best is None or est < best[0]:
+                best = (est, pe)
+        p_eff = best[1]
     T = (total + p_eff - 1) // p_eff
     meta = []
     for p in range(num_parts):
@@ -73,10 +92,7 @@ def schedule_reference(seqlens, num_parts: int, fixed_cost: int, hbm_parts: int)
         meta.append((b_first, k_first, b_last, k_end, split_first))
     num_splits = [0] * (B + 1)
     for b in range(B):
-        n = 0
-        if nb[b] > 0:
-            n = (C[b] + F + nb[b] - 1) // T - (C[b] + F) // T + 1
-        num_splits[b + 1] = num_splits[b] + n
+        num_splits[b + 1] = num_splits[b] + (_segments(C, nb, F, T, b) if total > 0 else 0)
     return meta, num_splits
 
 

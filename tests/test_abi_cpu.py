@@ -48,8 +48,8 @@ def test_sizes(mla):
     ws = mla.decode_workspace_size(64, 2, 128, 38)
     assert ws >= (64 + 38) * rows * 513 * 4 and ws % 256 == 0
     assert mla.decode_workspace_size(0, 1, 1, 1) == 0
-    fixed, hbm = mla.schedule_params()
-    assert fixed >= 0 and hbm >= 1
+    fixed, hbm, split_cost = mla.schedule_params()
+    assert fixed >= 0 and hbm >= 1 and split_cost >= 0
 
 
 def test_host_argument_checks(mla):

@@ -45,7 +45,7 @@ def test_tiny_workload():
 
 def test_schedule_bit_exact():
     import mla_absorbed_decode_gb300 as mla
-    fixed, hbm = mla.schedule_params()
+    fixed, hbm, split_cost = mla.schedule_params()
     rng = np.random.default_rng(0)
     cases = [[4096] * 64, [131072] * 4, [256, 300], [0, 5, 0, 700, 64, 65, 0]]
     for _ in range(12):
@@ -55,7 +55,7 @@ def test_schedule_bit_exact():
         for P in (1, 3, 17, 38, 64, 74, 76, 148):
             sl = torch.tensor(seqlens, dtype=torch.int32, device="cuda")
             meta = mla.decode_metadata(sl, 1, 128, False, P).cpu().numpy()
-            ref_meta, ref_ns = schedule_reference(seqlens, P, fixed, hbm)
+            ref_meta, ref_ns = schedule_reference(seqlens, P, fixed, hbm, split_cost)
             got = [tuple(int(v) for v in meta[8 * p: 8 * p + 5]) for p in range(P)]
             assert got == ref_meta, (seqlens[:8], P)
             assert list(meta[8 * P:]) == ref_ns

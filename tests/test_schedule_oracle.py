@@ -77,3 +77,26 @@ def test_checker_rejects_broken_schedules():
     bad_ns[-1] += 1
     with pytest.raises(AssertionError):
         check_schedule(meta, bad_ns, seqlens)
+
+
+def test_split_cost_picks_the_part_count():
+    # 64 equal requests: 64 parts take one request each; 76 parts would split them all
+    seqlens = [4096] * 64
+    meta, ns = schedule_reference(seqlens, num_parts=76, fixed_cost=2, hbm_parts=64, split_cost=12)
+    assert ns == list(range(65)) and all(m[0] == -1 for m in meta[64:])
+    # 4 long requests are split anyway: all 76 parts are used
+    seqlens = [131072] * 4
+    meta, ns = schedule_reference(seqlens, num_parts=76, fixed_cost=2, hbm_parts=64, split_cost=12)
+    assert sum(1 for m in meta if m[0] >= 0) == 76
+    check_schedule(meta, ns, seqlens)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_random_schedules_with_split_cost_are_valid(seed):
+    rng = random.Random(100 + seed)
+    B = rng.randint(1, 200)
+    seqlens = [rng.choice([0, rng.randint(1, 64), rng.randint(1, 20000)]) for _ in range(B)]
+    P = rng.randint(1, 160)
+    meta, ns = schedule_reference(seqlens, P, fixed_cost=rng.randint(0, 6), hbm_parts=rng.randint(1, 200),
+                                  split_cost=rng.randint(1, 20))
+    check_schedule(meta, ns, seqlens)
