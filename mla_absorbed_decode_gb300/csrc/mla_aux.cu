@@ -22,13 +22,47 @@ namespace mla {
 // taking the pages whose positions lie in [p T, (p + 1) T).  The costs are
 // prefix-summed by all threads; each part then finds its first and last page with
 // two binary searches, independently of the other parts.
+// Exclusive prefix sum of one value per thread over the block (kScheduleThreads
+// threads): warp shuffles, then one warp over the warp totals.  `scratch` holds
+// kScheduleThreads / 32 + 1 entries; the block total is returned in *total.
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* scratch, int64_t* total) {
+  constexpr int kWarps = kScheduleThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t x = v;   // inclusive scan within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();   // scratch may still be read by a previous scan
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < kWarps ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kWarps) scratch[lane] = w;          // inclusive warp prefix
+    if (lane == kWarps - 1) scratch[kWarps] = w;   // block total
+  }
+  __syncthreads();
+  const int64_t before = warp > 0 ? scratch[warp - 1] : 0;
+  *total = scratch[kWarps];
+  return before + x - v;
+}
+
 __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const int32_t* seqlens, int B, int num_parts,
                                                                         int fixed_cost, int hbm_parts, int split_cost,
                                                                         int32_t* meta, int32_t* num_splits) {
   extern __shared__ int64_t sched_c[];                                      // C[0..B]
   int32_t* sched_nb = reinterpret_cast<int32_t*>(sched_c + B + 1);         // nb[0..B)
-  __shared__ int64_t s_part[kScheduleThreads];
+  static_assert(kScheduleThreads % 32 == 0 && kScheduleThreads / 32 <= 32, "scan shape");
+  __shared__ int64_t s_scan[kScheduleThreads / 32 + 1];
   const int tid = threadIdx.x;
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t F = fixed_cost;
   const int chunk = (B + kScheduleThreads - 1) / kScheduleThreads;
   const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
@@ -40,19 +74,9 @@ __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const in
     sched_nb[i] = nb;
     sum += nb > 0 ? nb + F : 0;
   }
-  s_part[tid] = sum;
-  __syncthreads();
-  if (tid == 0) {
-    int64_t run = 0;
-    for (int j = 0; j < kScheduleThreads; ++j) {
-      const int64_t v = s_part[j];
-      s_part[j] = run;
-      run += v;
-    }
-    sched_c[0] = 0;
-  }
-  __syncthreads();
-  int64_t run = s_part[tid];
+  int64_t block_total;
+  int64_t run = block_exclusive_scan(sum, s_scan, &block_total);
+  if (tid == 0) sched_c[0] = 0;
   for (int i = lo; i < hi; ++i) {
     run += sched_nb[i] > 0 ? sched_nb[i] + F : 0;
     sched_c[i + 1] = run;
@@ -74,16 +98,9 @@ __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const in
       const int64_t Tc = (total + pe - 1) / pe;
       int64_t extra = 0;
       for (int i = lo; i < hi; ++i) extra += sched_nb[i] > 0 ? segments(i, Tc) - 1 : 0;
-      __syncthreads();
-      s_part[tid] = extra;
-      __syncthreads();
-      if (tid == 0) {
-        int64_t e = 0;
-        for (int j = 0; j < kScheduleThreads; ++j) e += s_part[j];
-        s_part[0] = e;
-      }
-      __syncthreads();
-      const int64_t est = Tc + static_cast<int64_t>(split_cost) * ((s_part[0] + pe - 1) / pe);
+      int64_t all_extra;
+      block_exclusive_scan(extra, s_scan, &all_extra);
+      const int64_t est = Tc + static_cast<int64_t>(split_cost) * ((all_extra + pe - 1) / pe);
       if (best_est < 0 || est < best_est) best_est = est, best_p = pe;
     }
     p_eff = best_p;
@@ -129,23 +146,12 @@ __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const in
     for (int j = 0; j < kMetaInts; ++j) dst[j] = (j == 0 || m[0] >= 0) ? m[j] : 0;
   }
   // 3. segments per request, prefix-summed into num_splits
-  int32_t segs = 0;
+  int64_t segs = 0;
   if (total > 0)
-    for (int i = lo; i < hi; ++i) segs += static_cast<int32_t>(segments(i, T));
-  __syncthreads();
-  s_part[tid] = segs;
-  __syncthreads();
-  if (tid == 0) {
-    int64_t r = 0;
-    for (int j = 0; j < kScheduleThreads; ++j) {
-      const int64_t v = s_part[j];
-      s_part[j] = r;
-      r += v;
-    }
-    num_splits[0] = 0;
-  }
-  __syncthreads();
-  int32_t r = static_cast<int32_t>(s_part[tid]);
+    for (int i = lo; i < hi; ++i) segs += segments(i, T);
+  int64_t all_segs;
+  int32_t r = static_cast<int32_t>(block_exclusive_scan(segs, s_scan, &all_segs));
+  if (tid == 0) num_splits[0] = 0;
   for (int i = lo; i < hi; ++i) {
     if (total > 0) r += static_cast<int32_t>(segments(i, T));
     num_splits[i + 1] = r;
@@ -161,9 +167,10 @@ cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fi
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  mla_schedule_kernel<<<1, kScheduleThreads, smem, stream>>>(seqlens, B, num_parts, fixed_cost, hbm_parts,
-                                                              split_cost, meta, num_splits);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(1), dim3(kScheduleThreads), smem, stream, attr);
+  return cudaLaunchKernelEx(&cfg, mla_schedule_kernel, seqlens, B, num_parts, fixed_cost, hbm_parts, split_cost, meta,
+                            num_splits);
 }
 
 // ---------------------------------------------------------------- combine --
@@ -175,6 +182,8 @@ cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fi
 __global__ void __launch_bounds__(128)
 mla_combine_kernel(const float* o_part, const float* lse_part, const int32_t* num_splits, int B, int rows,
                    __nv_bfloat16* out, float* lse) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int b = blockIdx.x;
   const int g = blockIdx.y * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -199,20 +208,43 @@ mla_combine_kernel(const float* o_part, const float* lse_part, const int32_t* nu
   for (int j = 0; j < 16; ++j) acc[j] = 0.f;
   float z = 0.f;
   if (m != -INFINITY) {
-    for (int k = 0; k < n; ++k) {
-      const float lk = lse_part[static_cast<int64_t>(s0 + k) * rows + g];
-      const float wk = (lk == -INFINITY) ? 0.f : expf(lk - m);
-      z += wk;
-      if (wk == 0.f) continue;
-      const float4* src = reinterpret_cast<const float4*>(o_part + (static_cast<int64_t>(s0 + k) * rows + g) * kDimV +
-                                                          lane * 16);
+    // two partials per pass, their loads issued together (a long merge is latency-
+    // bound otherwise); a partial with weight 0 is never multiplied in
+    for (int k0 = 0; k0 < n; k0 += 2) {
+      const bool two = k0 + 1 < n;
+      const int64_t r0 = static_cast<int64_t>(s0 + k0) * rows + g;
+      const int64_t r1 = two ? r0 + rows : r0;
+      const float l0 = lse_part[r0], l1 = lse_part[r1];
+      const float w0 = (l0 == -INFINITY) ? 0.f : expf(l0 - m);
+      const float w1 = (!two || l1 == -INFINITY) ? 0.f : expf(l1 - m);
+      const float4* p0 = reinterpret_cast<const float4*>(o_part + r0 * kDimV + lane * 16);
+      const float4* p1 = reinterpret_cast<const float4*>(o_part + r1 * kDimV + lane * 16);
+      float4 v0[4], v1[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 v = src[j];
-        acc[4 * j + 0] += wk * v.x;
-        acc[4 * j + 1] += wk * v.y;
-        acc[4 * j + 2] += wk * v.z;
-        acc[4 * j + 3] += wk * v.w;
+      for (int j = 0; j < 4; ++j) v0[j] = p0[j];
+      if (two) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v1[j] = p1[j];
+      }
+      z += w0;
+      if (w0 != 0.f) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[4 * j + 0] += w0 * v0[j].x;
+          acc[4 * j + 1] += w0 * v0[j].y;
+          acc[4 * j + 2] += w0 * v0[j].z;
+          acc[4 * j + 3] += w0 * v0[j].w;
+        }
+      }
+      z += w1;
+      if (w1 != 0.f) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[4 * j + 0] += w1 * v1[j].x;
+          acc[4 * j + 1] += w1 * v1[j].y;
+          acc[4 * j + 2] += w1 * v1[j].z;
+          acc[4 * j + 3] += w1 * v1[j].w;
+        }
       }
     }
   }
@@ -230,114 +262,154 @@ mla_combine_kernel(const float* o_part, const float* lse_part, const int32_t* nu
 // out[n, h, n0 : n0+NT] = A[n, h, 0:K] @ W[h][0:K, n0 : n0+NT]  for a tile of
 // 128 tokens n, one head h and one NT-wide column tile.  Used for the W_UK
 // absorption (K = 128, NT = 256 of 512) and the W_UV un-absorption (K = 512,
-// NT = 64 of 128): "DeepSeekV2之MLA" 4.5, the bmm calls with w_kc and w_vc.
-// A (K-major) arrives by a 3-D TMA [K, H, N] in 64-wide swizzled boxes; W[h]
-// (N contiguous, so an MN-major B operand) by a 2-D TMA over [H*K, N_total].
-// The accumulator is in TMEM; one thread issues TMA and MMA, 128 threads run
-// the epilogue (one token row each).
-template <int K, int NT>
+// NT = 128): "DeepSeekV2之MLA" 4.5, the bmm calls with w_kc and w_vc.
+// K is walked in chunks of 64 through a ring of STAGES shared-memory stages; a
+// stage holds the A chunk (128 tokens x 64, K-major, one 3-D TMA box over
+// [K, H, N]) and the W chunk (64 rows of W[h] x NT columns, N contiguous, so an
+// MN-major B operand: NT / 64 2-D boxes over [H*K, N_total]).  The accumulator is
+// in TMEM; one thread issues TMA, one warp the MMAs, and all 128 threads run the
+// epilogue (one token row each), with the TMEM load of the next 32 columns in
+// flight while the previous ones are stored.
+template <int K, int NT, int STAGES>
+__host__ __device__ constexpr uint32_t bmm_stage_bytes() {
+  return 16384u + static_cast<uint32_t>(NT) * 128u;
+}
+template <int K, int NT, int STAGES>
 uint32_t bmm_smem_bytes() {
-  return 128 * K * 2 + K * NT * 2 + 1024;
+  return STAGES * bmm_stage_bytes<K, NT, STAGES>() + 1024;
 }
 
-template <int K, int NT>
+__device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > 500000000ull) return false;
+  }
+  return true;
+}
+
+// 32 fp32 accumulator columns of one row -> 32 bf16 at dst (64 bytes, 16-byte aligned)
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 u;
+    u.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+    u.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+    u.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+    u.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+    d4[j] = u;
+  }
+}
+
+template <int K, int NT, int STAGES>
 __global__ void __launch_bounds__(128, 1)
 mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap w_map,
                const BmmParams p) {
-  static_assert(K % 64 == 0 && NT % 64 == 0 && NT <= 256, "tile shape");
-  constexpr uint32_t kABytes = 128 * K * 2;         // K/64 boxes of [128 rows x 128 B]
-  constexpr uint32_t kWChunk = K * 128;             // one 64-column chunk of W[h]: K rows x 128 B
-  constexpr int kWBoxRows = K > 256 ? 256 : K;
-  constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
+  static_assert(K % 64 == 0 && NT % 64 == 0 && NT >= 64 && NT <= 256 && STAGES >= 1, "tile shape");
+  constexpr int KC = K / 64;
+  constexpr uint32_t kSB = bmm_stage_bytes<K, NT, STAGES>();
+  constexpr uint32_t kTmemCols = NT;
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
-  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint64_t full[STAGES], empty[STAGES], acc_full;
   __shared__ uint32_t tmem_base_s;
+  __shared__ int fail_s;
   const uint32_t smem = (smem_u32(dyn_smem) + 1023u) & ~1023u;
-  const uint32_t sA = smem, sW = smem + kABytes;
   const int n0 = blockIdx.x * NT, h = blockIdx.y, m0 = blockIdx.z * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bar_tma), 1);
-    mbar_init(smem_u32(&bar_mma), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(&acc_full), 1);
+    fail_s = 0;
     fence_mbar_init();
+    prefetch_tensormap(&a_map);
+    prefetch_tensormap(&w_map);
   }
   if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  griddep_wait();
+  griddep_launch_dependents();
 
-  __shared__ int ok_s;
-  if (threadIdx.x == 0) {
-    ok_s = 0;
-    mbar_arrive_expect_tx(smem_u32(&bar_tma), kABytes + (NT / 64) * kWChunk);
-#pragma unroll 1
-    for (int c = 0; c < K / 64; ++c) tma_load_3d(sA + c * 16384, &a_map, smem_u32(&bar_tma), c * 64, h, m0);
-#pragma unroll 1
-    for (int j = 0; j < NT / 64; ++j)
-#pragma unroll 1
-      for (int r0 = 0; r0 < K; r0 += kWBoxRows)
-        tma_load_2d(sW + j * kWChunk + r0 * 128, &w_map, smem_u32(&bar_tma), n0 + j * 64, h * K + r0);
-  }
-  if (warp == 0) {   // the whole warp waits; one elected lane issues the MMAs
-    const uint64_t t0 = global_timer_ns();
-    bool got = true;
-    while (!mbar_test(smem_u32(&bar_tma), 0)) {
-      if (global_timer_ns() - t0 > 500000000ull) { got = false; break; }
-    }
-    got = __all_sync(0xffffffffu, got);
-    if (got) {
-      tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16_f32(128, NT, 0, 1);
+  if (warp == 0) {
+    if (lane == 0) {   // producer: K chunks through the ring
+      int last_phase[STAGES];
+      for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
+      for (int c = 0; c < KC; ++c) {
+        const int s = c % STAGES;
+        if (c >= STAGES && !bmm_wait(smem_u32(&empty[s]), ((c / STAGES) - 1) & 1)) {
+          fail_s = 1;
+          break;
+        }
+        const uint32_t st = smem + s * kSB;
+        const uint32_t bar = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(bar, kSB);
+        tma_load_3d(st, &a_map, bar, c * 64, h, m0);
 #pragma unroll
-      for (int kk = 0; kk < K / 16; ++kk) {
-        const uint64_t a = smem_desc_sw128(sA + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-        const uint64_t w = smem_desc_sw128(sW + kk * 2048, kWChunk, 1024);
-        mma_bf16_ss_warp(tmem, a, w, idesc, kk > 0 ? 1u : 0u);
+        for (int j = 0; j < NT / 64; ++j) tma_load_2d(st + 16384 + j * 8192, &w_map, bar, n0 + j * 64, h * K + c * 64);
+        last_phase[s] = (c / STAGES) & 1;
       }
-      mma_commit_warp(smem_u32(&bar_mma));
-      if (lane == 0) ok_s = 1;
-    } else if (lane == 0) {
-      atomicCAS(p.status, 0, MLA_ERR_TIMEOUT);
-      mbar_arrive(smem_u32(&bar_mma));   // release the epilogue without MMAs in flight
+      for (int s = 0; s < STAGES; ++s)   // loads in flight land before the CTA may exit
+        if (last_phase[s] >= 0) bmm_wait(smem_u32(&full[s]), static_cast<uint32_t>(last_phase[s]));
     }
-  }
-  {
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_test(smem_u32(&bar_mma), 0)) {
-      if (global_timer_ns() - t0 > 500000000ull) break;
+  } else if (warp == 1) {   // MMA issue: the whole warp waits, one elected lane issues
+    constexpr uint32_t idesc = idesc_bf16_f32(128, NT, 0, 1);
+    bool ok = true;
+    for (int c = 0; c < KC; ++c) {
+      const int s = c % STAGES;
+      ok = __all_sync(0xffffffffu, bmm_wait(smem_u32(&full[s]), (c / STAGES) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t st = smem + s * kSB;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t a = smem_desc_sw128(st + kk * 32, 16, 1024);
+        const uint64_t w = smem_desc_sw128(st + 16384 + kk * 2048, 8192, 1024);
+        mma_bf16_ss_warp(tmem, a, w, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit_warp(smem_u32(&empty[s]));
     }
+    if (!ok && lane == 0) fail_s = 1;
+    mma_commit_warp(smem_u32(&acc_full));   // arrives once every MMA issued so far is done
   }
-  tc_fence_after();
-  __syncthreads();
   const int n = m0 + threadIdx.x;
-  const bool store = ok_s && n < p.N;
+  // the RoPE part of the decode query is copied by the first column tile; its load
+  // is issued now so that it does not trail the epilogue
+  const bool copy_pe = blockIdx.x == 0 && p.pe != nullptr && n < p.N;
+  uint4 pe[8];
+  if (copy_pe) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.pe + static_cast<int64_t>(n) * p.pe_row_stride + h * 64);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) pe[j] = __ldg(src + j);
+  }
+  __syncthreads();
+  const bool got = bmm_wait(smem_u32(&acc_full), 0);
+  tc_fence_after();
+  if ((!got || fail_s) && threadIdx.x == 0) atomicCAS(p.status, 0, MLA_ERR_TIMEOUT);
+  const bool store = got && !fail_s && n < p.N;
   __nv_bfloat16* dst = p.out + static_cast<int64_t>(n) * p.out_row_stride + static_cast<int64_t>(h) * p.out_head_stride + n0;
   const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  uint32_t va[32], vb[32];
+  tmem_ld32(tl, va);
 #pragma unroll 1
-  for (int c = 0; c < NT; c += 32) {
-    uint32_t v[32];
-    tmem_ld32(tl + c, v);
+  for (int c = 0; c < NT; c += 64) {
     tmem_wait_ld();
-    if (store) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 u;
-        u.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-        u.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-        u.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-        u.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-        d4[j] = u;
-      }
-    }
+    tmem_ld32(tl + c + 32, vb);
+    if (store) store_bf16x32(dst + c, va);
+    tmem_wait_ld();
+    if (c + 64 < NT) tmem_ld32(tl + c + 64, va);
+    if (store) store_bf16x32(dst + c + 32, vb);
   }
-  if (store && blockIdx.x == 0 && p.pe != nullptr) {   // RoPE part of the decode query
-    const uint4* src = reinterpret_cast<const uint4*>(p.pe + static_cast<int64_t>(n) * p.pe_row_stride + h * 64);
+  tmem_wait_ld();
+  if (store && copy_pe) {
     uint4* d4 = reinterpret_cast<uint4*>(dst + 512);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) d4[j] = __ldg(src + j);
+    for (int j = 0; j < 8; ++j) d4[j] = pe[j];
   }
   tc_fence_before();
   __syncthreads();
@@ -347,28 +419,37 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
   }
 }
 
+// absorb: K = 128 -> two 256-column tiles of 512; un-absorb: K = 512 -> one 128-column tile
+#define MLA_BMM_ABSORB 128, 256, 2
+#define MLA_BMM_UNABSORB 512, 128, 3
+
 cudaError_t bmm_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(mla_bmm_kernel<128, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bmm_smem_bytes<128, 256>()));
+  cudaError_t e = cudaFuncSetAttribute(mla_bmm_kernel<MLA_BMM_ABSORB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bmm_smem_bytes<MLA_BMM_ABSORB>()));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mla_bmm_kernel<512, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(bmm_smem_bytes<512, 64>()));
+  return cudaFuncSetAttribute(mla_bmm_kernel<MLA_BMM_UNABSORB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(bmm_smem_bytes<MLA_BMM_UNABSORB>()));
 }
 
 cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap& w_map, const BmmParams& p,
                        cudaStream_t stream) {
   const unsigned mt = static_cast<unsigned>((p.N + 127) / 128);
+  cudaLaunchAttribute attr[1];
   if (absorb) {
-    mla_bmm_kernel<128, 256><<<dim3(2, p.H, mt), 128, bmm_smem_bytes<128, 256>(), stream>>>(a_map, w_map, p);
-  } else {
-    mla_bmm_kernel<512, 64><<<dim3(2, p.H, mt), 128, bmm_smem_bytes<512, 64>(), stream>>>(a_map, w_map, p);
+    const cudaLaunchConfig_t cfg =
+        pdl_config(dim3(512 / 256, p.H, mt), dim3(128), bmm_smem_bytes<MLA_BMM_ABSORB>(), stream, attr);
+    return cudaLaunchKernelEx(&cfg, mla_bmm_kernel<MLA_BMM_ABSORB>, a_map, w_map, p);
   }
-  return cudaGetLastError();
+  const cudaLaunchConfig_t cfg =
+      pdl_config(dim3(128 / 128, p.H, mt), dim3(128), bmm_smem_bytes<MLA_BMM_UNABSORB>(), stream, attr);
+  return cudaLaunchKernelEx(&cfg, mla_bmm_kernel<MLA_BMM_UNABSORB>, a_map, w_map, p);
 }
 
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* num_splits, int B, int rows,
                            __nv_bfloat16* out, float* lse, cudaStream_t stream) {
+  // An ordinary launch: started early, its CTAs would pile onto the few SMs that the
+  // decode kernel frees first and the merge of long requests would run on those alone.
   dim3 grid(static_cast<unsigned>(B), static_cast<unsigned>((rows + 3) / 4), 1);
   mla_combine_kernel<<<grid, 128, 0, stream>>>(o_part, lse_part, num_splits, B, rows, out, lse);
   return cudaGetLastError();

@@ -22,11 +22,15 @@
 //     shared memory and ships them to its partner with one shared-to-shared bulk
 //     copy per page (many small remote stores are several times slower);
 //   * the O-CTA (odd rank) keeps O (128 x 512 fp32) in TMEM, loads the value
-//     part of each page (three in flight), runs O += P V with tcgen05, rescales O
+//     part of each page (two in flight), runs O += P V with tcgen05, rescales O
 //     only when a row maximum grew by more than 2^8 (exact: the final
 //     normalisation uses the same reference maximum), and writes the normalised
 //     output (bf16) or, for a split request, an fp32 partial that the combine
 //     kernel merges.
+// Both CTAs load a page stage in two parts and release each part as soon as the
+// MMAs that read it are done (S-CTA: chunks 0..4 and 5..8 of the 576 dims; O-CTA:
+// value chunks 0..3 and 4..7), so the refill of the first part overlaps the MMAs
+// on the second.
 // Rows beyond 128 (s_q * H > 128) go to further pairs of the same cluster, which
 // walk the same pages at the same time so that a page is fetched from HBM once.
 // A cluster is one "part" of the split schedule and walks the segments the
@@ -765,10 +769,6 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
       prefetch_tensormap(&maps.k_a);
     }
     prefetch_tensormap(&maps.c4);
-    if (is_s && rb == 0) {   // first request's q rows and block-table row, before anything else queues
-      const int b0 = __ldg(p.meta + part * 8);
-      if (b0 >= 0) prefetch_request(p, b0);
-    }
     sh.abort = 0;
     sh.cmd = 0;
     for (int i = 0; i < kStages; ++i) {
@@ -801,6 +801,11 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
   __syncthreads();
   cluster_sync();        // every barrier of the cluster is initialised before any remote use
   tc_fence_after();
+  griddep_wait();        // the metadata, q and the cache are complete from here on
+  if (threadIdx.x == 0 && is_s && rb == 0) {   // first request's q rows and block-table row
+    const int b0 = p.meta[part * 8];
+    if (b0 >= 0) prefetch_request(p, b0);
+  }
 
   if (is_s) {
     if (warp == 0) {
@@ -838,25 +843,23 @@ cudaError_t decode_set_attributes() {
                               static_cast<int>(kSmemBytes));
 }
 
+// attr[0] = the cluster shape; with pdl, attr[1] = programmatic stream serialisation
 static cudaLaunchConfig_t decode_config(int grid_ctas, int cluster_ctas, cudaStream_t stream,
-                                        cudaLaunchAttribute* attr) {
-  cudaLaunchConfig_t cfg = {};
+                                        cudaLaunchAttribute* attr, bool pdl) {
+  cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(grid_ctas), 1, 1), dim3(kThreads, 1, 1), kSmemBytes,
+                                      stream, attr + 1);
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_ctas);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cfg;
 }
 
 int decode_max_clusters(int cluster_ctas) {
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = decode_config(cluster_ctas, cluster_ctas, nullptr, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = decode_config(cluster_ctas, cluster_ctas, nullptr, attr, false);
   int clusters = 0;
   if (cudaOccupancyMaxActiveClusters(&clusters, mla_decode_kernel, &cfg) != cudaSuccess) {
     cudaGetLastError();
@@ -866,8 +869,8 @@ int decode_max_clusters(int cluster_ctas) {
 }
 
 cudaError_t launch_decode(const KvMaps& maps, const DecodeParams& p, int cluster_ctas, cudaStream_t stream) {
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = decode_config(p.num_parts * cluster_ctas, cluster_ctas, stream, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = decode_config(p.num_parts * cluster_ctas, cluster_ctas, stream, attr, true);
   return cudaLaunchKernelEx(&cfg, mla_decode_kernel, maps, p);
 }
 

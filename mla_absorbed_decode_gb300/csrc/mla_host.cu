@@ -254,7 +254,7 @@ mla_status_t mla_absorb_q(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, c
   if (!encode_3d(&a_map, q_nope, 128, static_cast<uint64_t>(H), static_cast<uint64_t>(N), 256,
                  static_cast<uint64_t>(q_nope_row_stride) * 2, 64, 1, 128))
     return MLA_ERR_CUDA;
-  if (!encode_2d(&w_map, w_uk, 512, static_cast<uint64_t>(H) * 128, 1024, 64, 128)) return MLA_ERR_CUDA;
+  if (!encode_2d(&w_map, w_uk, 512, static_cast<uint64_t>(H) * 128, 1024, 64, 64)) return MLA_ERR_CUDA;
   BmmParams p;
   p.out = reinterpret_cast<__nv_bfloat16*>(q);
   p.out_row_stride = static_cast<int64_t>(H) * kDimQK;
@@ -279,7 +279,7 @@ mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla
   if (!encode_3d(&a_map, o_lat, 512, static_cast<uint64_t>(H), static_cast<uint64_t>(N), 1024,
                  static_cast<uint64_t>(H) * 1024, 64, 1, 128))
     return MLA_ERR_CUDA;
-  if (!encode_2d(&w_map, w_uv, 128, static_cast<uint64_t>(H) * 512, 256, 64, 256)) return MLA_ERR_CUDA;
+  if (!encode_2d(&w_map, w_uv, 128, static_cast<uint64_t>(H) * 512, 256, 64, 64)) return MLA_ERR_CUDA;
   BmmParams p;
   p.out = reinterpret_cast<__nv_bfloat16*>(o);
   p.out_row_stride = static_cast<int64_t>(H) * 128;

@@ -68,6 +68,23 @@ bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, cons
 // first use); nullptr on error.
 int* device_status_word();
 
+// Launch configuration shared by every kernel of the library: programmatic stream
+// serialisation, so that a kernel's set-up overlaps the tail of the kernel before it
+// on the stream (each kernel waits on griddepcontrol before its first global access).
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                     cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 // Launchers (defined next to their kernels).
 cudaError_t decode_set_attributes();
 int decode_max_clusters(int cluster_ctas);            // occupancy query; 0 on error

@@ -160,6 +160,14 @@ __device__ __forceinline__ void prefetch_tensormap(const void* map) {
 __device__ __forceinline__ void prefetch_l2(const void* gptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(gptr), "r"(bytes) : "memory");
 }
+// Programmatic dependent launch.  Every kernel of the library is launched so that
+// it may start while the previous kernel of the stream is still running; before
+// its first global access it waits here until that kernel has completed and its
+// memory is visible.  launch_dependents lets the next kernel be scheduled early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 // Bulk copy of `bytes` from this CTA's shared memory to another CTA's shared
 // memory; completion is signalled on the destination CTA's barrier.
 __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,

@@ -51,8 +51,11 @@ def test_schedule_bit_exact():
     for _ in range(12):
         B = int(rng.integers(1, 200))
         cases.append([int(x) for x in rng.choice([0, int(rng.integers(1, 64)), int(rng.integers(1, 9000))], size=B)])
+    # more requests than the schedule kernel has threads: several requests per thread
+    for B in (513, 3000, 16384):
+        cases.append([int(x) for x in rng.integers(0, 9000, size=B)])
     for seqlens in cases:
-        for P in (1, 3, 17, 38, 64, 74, 76, 148):
+        for P in ((1, 3, 17, 38, 64, 74, 76, 148) if len(seqlens) < 512 else (5, 76, 148)):
             sl = torch.tensor(seqlens, dtype=torch.int32, device="cuda")
             meta = mla.decode_metadata(sl, 1, 128, False, P).cpu().numpy()
             ref_meta, ref_ns = schedule_reference(seqlens, P, fixed, hbm, split_cost)
