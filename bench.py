@@ -218,6 +218,20 @@ def run_reference(args, w):
     return 0
 
 
+def _graphed(torch, fn, dev):
+    """Record fn's stream work once in a CUDA graph (after one uncaptured run on a side
+    stream); returns a callable that replays it on the current stream."""
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g.replay
+
+
 def run_ours(args, w):
     import torch
     import mla_absorbed_decode_gb300 as mla
@@ -280,6 +294,9 @@ def run_ours(args, w):
     status = mla.get_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} during warm-up")
+    # the step's library calls recorded once in a CUDA graph and replayed (one host call
+    # per step); --eager issues them one by one
+    step_fn = one_step if args.eager else _graphed(torch, one_step, dev)
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -292,7 +309,7 @@ def run_ours(args, w):
         for i in range(args.steps):
             flush.zero_()
             starts[i].record()
-            one_step()
+            step_fn()
             ends[i].record()
         # the decode call (decode kernel + combine) on its own, with the step's metadata
         # and q, L2 flushed before each launch: events between the kernels of a step
@@ -370,12 +387,13 @@ def run_ours(args, w):
             flush.zero_()
             e2e_step()
         torch.cuda.synchronize()
+        e2e_fn = e2e_step if args.eager else _graphed(torch, e2e_step, dev)
         es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         for i in range(args.steps):
             flush.zero_()
             es[i].record()
-            e2e_step()
+            e2e_fn()
             ee[i].record()
         torch.cuda.synchronize()
         t_e2e = statistics.mean(a.elapsed_time(b) for a, b in zip(es, ee)) / 1e3
@@ -420,7 +438,8 @@ def run_ours(args, w):
                                    else list(w.fixed_seqlens)),
                        "page": 64, "parts": parts, "parallelism": f"replicas x{n}",
                        "l2": "flushed between timed steps (256 MiB write, then 256 MiB read; outside the step events)",
-                       "decode_timing": "K further decode calls inside the timed region, L2 flushed before each"},
+                       "decode_timing": "K further decode calls inside the timed region, L2 flushed before each",
+                       "launch": "eager" if args.eager else "CUDA graph of the step's library calls"},
             "hbm_gbs": gbs,
             "pct_of_roofline": 100.0 * rl_time / t_step,
             "roofline_spec": {"peak_tflops": SPEC_FLOPS / 1e12, "peak_gbs": SPEC_BW / 1e9},
@@ -446,6 +465,7 @@ def main():
     ap.add_argument("--parts", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override B (smaller cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch the step's calls one by one instead of a CUDA graph")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()

@@ -201,3 +201,35 @@ class DecodeStep:
                workspace=self.workspace, out=self.out, lse=self.lse, stream=stream)
         unabsorb_o(self.out.view(self.B * self.s_q, self.H, 512), w_uv, o=self.o, stream=stream)
         return self.o
+
+    def capture(self, q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, plan=True, before=None, after=None):
+        """Record the step (plan() if `plan`, then run()) into a CUDA graph; `replay()` relaunches it
+        with one host call.  `before` / `after` are optional callables whose stream work (for example
+        copies of the step's inputs from pinned host buffers, or of its result back) is recorded in
+        the same graph.  The graph holds the addresses of every buffer: refill them in place between
+        replays.  The step runs once, uncaptured, first (one-time library set-up happens there)."""
+        def body():
+            if before is not None:
+                before()
+            if plan:
+                self.plan()
+            self.run(q_nope, q_pe, w_uk, w_uv, kv_cache, block_table)
+            if after is not None:
+                after()
+        side = torch.cuda.Stream(device=self.q.device)
+        side.wait_stream(torch.cuda.current_stream(self.q.device))
+        with torch.cuda.stream(side):
+            body()
+        torch.cuda.current_stream(self.q.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            body()
+        self._graph = graph
+        return graph
+
+    def replay(self):
+        """Relaunch the captured step on the current stream (see `capture`); returns o."""
+        if getattr(self, "_graph", None) is None:
+            raise RuntimeError("DecodeStep.replay() before capture()")
+        self._graph.replay()
+        return self.o
