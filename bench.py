@@ -218,6 +218,18 @@ def run_reference(args, w):
     return 0
 
 
+def max_over_ranks(values, dist, device):
+    """Each value's maximum over all ranks (every rank gets the result); the values
+    unchanged without a process group.  Timings are reduced this way: the job's step
+    time is that of its slowest replica."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def _graphed(torch, fn, dev):
     """Record fn's stream work once in a CUDA graph (after one uncaptured run on a side
     stream); returns a callable that replays it on the current stream."""
@@ -329,10 +341,7 @@ def run_ours(args, w):
     dec_ms = [a.elapsed_time(b) for a, b in zip(d0, d1)]
     t_step = statistics.mean(step_ms) / 1e3
     t_dec = statistics.mean(dec_ms) / 1e3
-    if dist:
-        t = torch.tensor([t_step, t_dec], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step, t_dec = t.tolist()
+    t_step, t_dec = max_over_ranks([t_step, t_dec], dist, dev)
 
     dflops, dbytes = acc.decode_work(inp["seqlens"].tolist(), s_q, H, w.causal)
     bflops = bbytes = 0
@@ -397,10 +406,7 @@ def run_ours(args, w):
             ee[i].record()
         torch.cuda.synchronize()
         t_e2e = statistics.mean(a.elapsed_time(b) for a, b in zip(es, ee)) / 1e3
-        if dist:
-            t = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = t.item()
+        t_e2e, = max_over_ranks([t_e2e], dist, dev)
         e2e = {"value": n * step_flops / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3}
 
