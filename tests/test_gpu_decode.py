@@ -85,6 +85,35 @@ def test_mtp_causal_two_queries(H):
         compare(out, lse, ref_out, ref_lse, what=f"s_q=2 H={H} parts={P}")
 
 
+@pytest.mark.parametrize("s_q,H", [(3, 128), (4, 128), (2, 80), (3, 40)])
+def test_more_query_rows_than_one_pair(s_q, H):
+    # s_q * H rows beyond 128 go to further CTA pairs of the same cluster (up to four,
+    # a cluster of eight CTAs); the last pair may be partly filled
+    seqlens = [5, 200, 1100]
+    inp = _case(len(seqlens), s_q, H, seqlens, causal=True, seed=s_q * 1000 + H)
+    ref_out, ref_lse, ref_abs = oracle_decode(inp)
+    for parts in (None, 4):
+        out, lse, _, P = run_library(inp, parts=parts)
+        compare(out, lse, ref_out, ref_lse, what=f"s_q={s_q} H={H} parts={P}")
+
+
+def test_largest_batch():
+    # the schedule's maximum batch (16384 requests), short contexts, sampled against the oracle
+    B = 16384
+    seqlens = np.random.default_rng(4).integers(1, 200, size=B).tolist()
+    inp = _case(B, 1, 16, seqlens, seed=4)
+    out, lse, _, _ = run_library(inp)
+    sel = [0, 1, 777, 8191, B - 2, B - 1]
+    # the oracle on the sampled requests only: their pages gathered into a small cache
+    bt = inp["block_table"][sel]
+    pages = sorted({int(x) for x in bt.flatten().tolist() if x >= 0})
+    remap = {pg: i for i, pg in enumerate(pages)}
+    sub = dict(inp, q=inp["q"][sel], seqlens=inp["seqlens"][sel], kv_cache=inp["kv_cache"][pages],
+               block_table=bt.clone().apply_(lambda x: remap.get(x, -1)))
+    ref_out, ref_lse, ref_abs = oracle_decode(sub)
+    compare(out[sel], lse[sel], ref_out, ref_lse, what="B=16384")
+
+
 def test_empty_and_degenerate_requests():
     # an empty request, one token, and s_q > seqlen under causal masking
     inp = _case(3, 2, 16, [0, 1, 3], causal=True, seed=3)
