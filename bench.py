@@ -337,6 +337,29 @@ def run_ours(args, w):
     status = mla.get_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
+
+    # per-call breakdown of a step, outside the timed region: eager calls with events
+    # between them (so without launch overlap), L2 flushed before each step
+    comp = {"schedule": [], "absorb": [], "decode_and_combine": [], "unabsorb": []}
+    for i in range(args.steps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev[0].record()
+        step.plan()
+        ev[1].record()
+        if w.with_projections:
+            mla.absorb_q(q_nope, w_uk, step.q, q_pe=q_pe)
+        ev[2].record()
+        decode_only()
+        ev[3].record()
+        if w.with_projections:
+            mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
+        ev[4].record()
+        torch.cuda.synchronize()
+        for j, k in enumerate(comp):
+            comp[k].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+    components = {k: round(statistics.mean(v), 2) for k, v in comp.items()
+                  if w.with_projections or k not in ("absorb", "unabsorb")}
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     dec_ms = [a.elapsed_time(b) for a, b in zip(d0, d1)]
     t_step = statistics.mean(step_ms) / 1e3
@@ -452,6 +475,7 @@ def run_ours(args, w):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "components_us": components,
             "gpu_launches": launches_per_step * args.steps + 2 * args.steps,
             "clocks": clocks.summary(),
         }

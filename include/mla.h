@@ -29,11 +29,11 @@
  *    mla_get_device_status.  Argument errors are found on the host before any
  *    launch and returned as status codes; nothing aborts or throws.
  *  - Stream order holds as usual: every kernel sees the complete results of
- *    all work queued before it on the stream.  The kernels (the LSE combine
- *    excepted) are launched with programmatic stream serialisation, so their
- *    launch and on-chip set-up may overlap the tail of the kernel queued just
- *    before them; they wait for that kernel to complete before their first
- *    global-memory access.  The calls may be recorded in CUDA graphs.
+ *    all work queued before it on the stream.  The kernels are launched with
+ *    programmatic stream serialisation, so their launch and on-chip set-up may
+ *    overlap the tail of the kernel queued just before them; they wait for that
+ *    kernel to complete before their first global-memory access.  The calls
+ *    may be recorded in CUDA graphs.
  *  - Device-side faults (a block-table entry outside [0, num_blocks), a barrier
  *    wait that ran out of time) do not trap: the kernels skip the access or end
  *    their loops and record a code in a device status word that

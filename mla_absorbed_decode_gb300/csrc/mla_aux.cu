@@ -448,11 +448,15 @@ cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap&
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* num_splits, int B, int rows,
                            __nv_bfloat16* out, float* lse, cudaStream_t stream) {
-  // An ordinary launch: started early, its CTAs would pile onto the few SMs that the
-  // decode kernel frees first and the merge of long requests would run on those alone.
-  dim3 grid(static_cast<unsigned>(B), static_cast<unsigned>((rows + 3) / 4), 1);
-  mla_combine_kernel<<<grid, 128, 0, stream>>>(o_part, lse_part, num_splits, B, rows, out, lse);
-  return cudaGetLastError();
+  // The decode kernel never signals its dependents early, so the combine's CTAs are
+  // placed only once the whole decode grid is done (spread over every SM) and the
+  // programmatic launch just hides the launch latency.  An early signal would let them
+  // pile onto the few SMs that the decode frees first, where the merge of long
+  // requests then runs alone.
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      pdl_config(dim3(static_cast<unsigned>(B), static_cast<unsigned>((rows + 3) / 4), 1), dim3(128), 0, stream, attr);
+  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, o_part, lse_part, num_splits, B, rows, out, lse);
 }
 
 }  // namespace mla
