@@ -1,7 +1,8 @@
 """Benchmark of one absorbed-MLA decode step on GB300.
 
 A step is one pass of the whole path on one batch: split schedule, W_UK
-absorption (with the q assembly), paged absorbed decode, LSE combine and W_UV
+absorption (with the q assembly: RoPE of q_pe at each new token's position),
+paged absorbed decode, LSE combine and W_UV
 un-absorption, on the DeepSeek-V3-shaped workload (B=64, H=128, s_q=1, every
 context 4096 tokens, 576/512 dims, page 64, synthetic bf16 data).  The metric
 is algorithmic TFLOP/s of the step; HBM GB/s and the fraction of the roofline
@@ -149,9 +150,10 @@ def oracle_sample_step(inp, kv_np, sel, with_proj):
     flops = 0
     if with_proj:
         qn = inp["q_nope"].float().numpy().reshape(B, s_q, H, 128)[sel].reshape(-1, H, 128)
-        q_lat = oracle.absorb_q(qn, inp["_w_uk_np"])
         qp = inp["q_pe"].float().numpy().reshape(B, s_q, H, 64)[sel].reshape(-1, H, 64)
-        q = np.concatenate([q_lat, qp], axis=-1).reshape(len(sel), s_q, H, 576)
+        sl = inp["seqlens"][sel].numpy()
+        pos = (np.repeat(sl, s_q) - s_q + np.tile(np.arange(s_q), len(sel))).clip(min=0)
+        q = oracle.assemble_q(qn, qp, inp["_w_uk_np"], positions=pos).reshape(len(sel), s_q, H, 576)
         flops += acc.bmm_work(len(sel) * s_q, H, True)[0]
     else:
         q = inp["q"][sel].double().numpy()
@@ -259,6 +261,10 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     inp = W.make_inputs(w, seed=rank)
     B, s_q, H = w.B, w.s_q, w.H
+    # RoPE positions of the new tokens (row b * s_q + i sits at position seqlens[b] - s_q + i)
+    pos_host = (inp["seqlens"].repeat_interleave(s_q) - s_q
+                + torch.arange(s_q, dtype=torch.int32).repeat(B)).clamp_min(0).to(torch.int32)
+    positions = pos_host.to(dev)
     q_nope = inp["q_nope"].to(dev) if w.with_projections else None
     q_pe = inp["q_pe"].to(dev) if w.with_projections else None
     w_uk = inp["w_uk"].to(dev) if w.with_projections else None
@@ -293,7 +299,7 @@ def run_ours(args, w):
     def one_step():
         step.plan()
         if w.with_projections:
-            mla.absorb_q(q_nope, w_uk, step.q, q_pe=q_pe)
+            mla.absorb_q(q_nope, w_uk, step.q, q_pe=q_pe, positions=positions)
         decode_only()
         if w.with_projections:
             mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
@@ -348,7 +354,7 @@ def run_ours(args, w):
         step.plan()
         ev[1].record()
         if w.with_projections:
-            mla.absorb_q(q_nope, w_uk, step.q, q_pe=q_pe)
+            mla.absorb_q(q_nope, w_uk, step.q, q_pe=q_pe, positions=positions)
         ev[2].record()
         decode_only()
         ev[3].record()
@@ -385,7 +391,7 @@ def run_ours(args, w):
     if not args.no_e2e:
         host_in = []
         if w.with_projections:
-            host_in = [inp["q_nope"].pin_memory(), inp["q_pe"].pin_memory()]
+            host_in = [inp["q_nope"].pin_memory(), inp["q_pe"].pin_memory(), pos_host.pin_memory()]
         else:
             host_in = [inp["q"].pin_memory()]
         host_sl = inp["seqlens"].pin_memory()
@@ -404,7 +410,7 @@ def run_ours(args, w):
             bt.copy_(host_bt, non_blocking=True)
             step.plan()
             if w.with_projections:
-                mla.absorb_q(dev_in[0], w_uk, step.q, q_pe=dev_in[1])
+                mla.absorb_q(dev_in[0], w_uk, step.q, q_pe=dev_in[1], positions=dev_in[2])
                 q_in = step.q
             else:
                 q_in = dev_in[0]

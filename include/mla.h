@@ -132,6 +132,20 @@ mla_status_t mla_absorb_q(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, c
                           int64_t q_pe_row_stride, const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H,
                           mla_stream_t stream);
 
+/* mla_absorb_q with the RoPE of q_pe fused in (the query side of the decoupled
+ * RoPE, page "MLA 推理：两条计算路径与 FlashMLA", section "两条等价的路径", its tiny
+ * example: adjacent pairs rotated, written back interleaved):
+ *   q[n, h, 512 + 2j]     = x0 cos(a) - x1 sin(a)
+ *   q[n, h, 512 + 2j + 1] = x0 sin(a) + x1 cos(a),   x0, x1 = q_pe[n, h, 2j], q_pe[n, h, 2j+1]
+ *   a = positions[n] * rope_theta^(-2j/64),  j = 0..31
+ * (fp32 arithmetic on an angle reduced to within ~1e-7 rad, bf16 out).
+ *  positions  [N] int32 device, each in [0, 2^24); 4-byte aligned
+ *  rope_theta finite and > 1 (DeepSeek: 10000)
+ * q_pe may not be NULL.  Other arguments as for mla_absorb_q.  Async on stream. */
+mla_status_t mla_absorb_q_rope(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                               int64_t q_pe_row_stride, const int32_t* positions, float rope_theta,
+                               const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H, mla_stream_t stream);
+
 /* W_UV un-absorption ("DeepSeekV2之MLA" 4.5: bmm(attn_output, w_vc)):
  *   o[n, h, 0:128] = o_lat[n, h, 0:512] @ w_uv[h]      (fp32 accumulate, bf16 out)
  *  o_lat [N, H, 512] bf16 (the decode out), w_uv [H, 512, 128] bf16, o [N, H, 128] bf16.

@@ -37,6 +37,7 @@ _SIGNATURES = {
     "mla_decode": (_c_int, [_p, _p, _c_ll, _p, _c_int, _p, _c_int, _c_int, _c_int, _c_float, _c_int,
                             _p, _c_int, _p, _c_size, _p, _p, _p]),
     "mla_absorb_q": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _p, _c_int, _c_int, _p]),
+    "mla_absorb_q_rope": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _p, _c_int, _c_int, _p]),
     "mla_unabsorb_o": (_c_int, [_p, _p, _p, _c_int, _c_int, _p]),
     "mla_decode_noalloc": (_c_int, [_p, _p, _c_ll, _p, _c_int, _p, _c_int, _c_int, _c_int, _c_float, _c_int,
                                     _c_int, _p, _p, _p]),
@@ -140,13 +141,18 @@ def decode(q, kv_cache, block_table, seqlens, softmax_scale: float, causal: bool
 
 
 def absorb_q(q_nope: torch.Tensor, w_uk: torch.Tensor, q: torch.Tensor, q_pe: torch.Tensor | None = None,
-             stream=None) -> torch.Tensor:
-    """q[n, h, 0:512] = q_nope[n, h, :] @ w_uk[h] and q[n, h, 512:576] = q_pe[n, h, :];
-    q is [N, H, 576] (or [B, s_q, H, 576] with N = B*s_q)."""
+             stream=None, positions: torch.Tensor | None = None, rope_theta: float = 10000.0) -> torch.Tensor:
+    """q[n, h, 0:512] = q_nope[n, h, :] @ w_uk[h] and q[n, h, 512:576] = q_pe[n, h, :], RoPE-rotated
+    by positions[n] (int32 [N]) when positions is given; q is [N, H, 576] (or [B, s_q, H, 576])."""
     N, H, _ = q_nope.shape
     pe_ptr, pe_stride = (0, 0) if q_pe is None else (_ptr(q_pe), q_pe.stride(0))
-    _check(lib().mla_absorb_q(_ptr(q_nope), q_nope.stride(0), pe_ptr or None, pe_stride, _ptr(w_uk), _ptr(q), N, H,
-                              _stream(stream)), "mla_absorb_q")
+    if positions is None:
+        _check(lib().mla_absorb_q(_ptr(q_nope), q_nope.stride(0), pe_ptr or None, pe_stride, _ptr(w_uk), _ptr(q), N,
+                                  H, _stream(stream)), "mla_absorb_q")
+    else:
+        _check(lib().mla_absorb_q_rope(_ptr(q_nope), q_nope.stride(0), pe_ptr or None, pe_stride, _ptr(positions),
+                                       float(rope_theta), _ptr(w_uk), _ptr(q), N, H, _stream(stream)),
+               "mla_absorb_q_rope")
     return q
 
 
@@ -194,15 +200,18 @@ class DecodeStep:
         """Recompute the split schedule (after seqlens changed)."""
         decode_metadata(self.seqlens, self.s_q, self.H, self.causal, self.parts, out=self.metadata, stream=stream)
 
-    def run(self, q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, stream=None):
-        """q_nope [B*s_q,H,128], q_pe [B*s_q,H,64] -> o [B*s_q,H,128] (bf16)."""
-        absorb_q(q_nope, w_uk, self.q, q_pe=q_pe, stream=stream)
+    def run(self, q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, stream=None, positions=None,
+            rope_theta: float = 10000.0):
+        """q_nope [B*s_q,H,128], q_pe [B*s_q,H,64] -> o [B*s_q,H,128] (bf16); with positions
+        (int32 [B*s_q]) q_pe is RoPE-rotated inside the absorption."""
+        absorb_q(q_nope, w_uk, self.q, q_pe=q_pe, stream=stream, positions=positions, rope_theta=rope_theta)
         decode(self.q, kv_cache, block_table, self.seqlens, self.scale, self.causal, self.metadata, self.parts,
                workspace=self.workspace, out=self.out, lse=self.lse, stream=stream)
         unabsorb_o(self.out.view(self.B * self.s_q, self.H, 512), w_uv, o=self.o, stream=stream)
         return self.o
 
-    def capture(self, q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, plan=True, before=None, after=None):
+    def capture(self, q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, plan=True, before=None, after=None,
+                positions=None, rope_theta: float = 10000.0):
         """Record the step (plan() if `plan`, then run()) into a CUDA graph; `replay()` relaunches it
         with one host call.  `before` / `after` are optional callables whose stream work (for example
         copies of the step's inputs from pinned host buffers, or of its result back) is recorded in
@@ -213,7 +222,7 @@ class DecodeStep:
                 before()
             if plan:
                 self.plan()
-            self.run(q_nope, q_pe, w_uk, w_uv, kv_cache, block_table)
+            self.run(q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, positions=positions, rope_theta=rope_theta)
             if after is not None:
                 after()
         side = torch.cuda.Stream(device=self.q.device)

@@ -301,6 +301,30 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t
   }
 }
 
+// RoPE of one q_pe row in place (64 bf16 values as 32 interleaved pairs; the page's tiny
+// example and "DeepSeekV2之MLA" 4.2: the pair (x[2j], x[2j+1]) turns by the angle
+// pos * theta^(-2j/64)).  The angle is carried as a float pair: pos is exact in fp32, the
+// product with the inverse frequency (itself a float pair) keeps its rounding error via
+// fma, and the reduction by 2*pi subtracts k * 2*pi in two parts (Cody and Waite's
+// method), so that the argument of the sine and cosine stays within ~1e-7 rad of the
+// exact angle for positions up to 2^24.
+__device__ __forceinline__ void rope_row(uint4 (&pe)[8], int pos, const BmmParams& p) {
+  const float fp = static_cast<float>(pos);
+  const float inv_two_pi = 1.0f / p.two_pi_hi;
+  uint32_t* w = reinterpret_cast<uint32_t*>(pe);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float a_hi = fp * p.rope_hi[j];
+    const float a_lo = fmaf(fp, p.rope_lo[j], fmaf(fp, p.rope_hi[j], -a_hi));
+    const float k = rintf(a_hi * inv_two_pi);
+    const float r = fmaf(-k, p.two_pi_lo, fmaf(-k, p.two_pi_hi, a_hi)) + a_lo;
+    float sn, cs;
+    __sincosf(r, &sn, &cs);   // |r| <= pi + 1e-6: the hardware sine/cosine, absolute error < 2^-21
+    const float x0 = bf16_lo(w[j]), x1 = bf16_hi(w[j]);
+    w[j] = pack_bf16x2(fmaf(x0, cs, -x1 * sn), fmaf(x0, sn, x1 * cs));
+  }
+}
+
 template <int K, int NT, int STAGES>
 __global__ void __launch_bounds__(128, 1)
 mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap w_map,
@@ -336,26 +360,45 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
   griddep_wait();
   griddep_launch_dependents();
 
+  // producer (warp 0, lane 0): K chunks through the ring; the chunks that fit the
+  // ring at once are issued first, before anything else of the CTA
+  int last_phase[STAGES];
+  for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
+  auto issue = [&](int c) {
+    const int s = c % STAGES;
+    const uint32_t st = smem + s * kSB;
+    const uint32_t bar = smem_u32(&full[s]);
+    mbar_arrive_expect_tx(bar, kSB);
+    tma_load_3d(st, &a_map, bar, c * 64, h, m0);
+#pragma unroll
+    for (int j = 0; j < NT / 64; ++j) tma_load_2d(st + 16384 + j * 8192, &w_map, bar, n0 + j * 64, h * K + c * 64);
+    last_phase[s] = (c / STAGES) & 1;
+  };
+  constexpr int kFirst = KC < STAGES ? KC : STAGES;
+  if (warp == 0 && lane == 0)
+    for (int c = 0; c < kFirst; ++c) issue(c);
+
+  const int n = m0 + threadIdx.x;
+  // the RoPE part of the decode query is copied by the first column tile; it is
+  // loaded (and rotated) while the tiles are in flight
+  const bool copy_pe = blockIdx.x == 0 && p.pe != nullptr && n < p.N;
+  uint4 pe[8];
+  if (copy_pe) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.pe + static_cast<int64_t>(n) * p.pe_row_stride + h * 64);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) pe[j] = __ldg(src + j);
+    if (p.positions != nullptr) rope_row(pe, __ldg(p.positions + n), p);
+  }
+
   if (warp == 0) {
-    if (lane == 0) {   // producer: K chunks through the ring
-      int last_phase[STAGES];
-      for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
-      for (int c = 0; c < KC; ++c) {
-        const int s = c % STAGES;
-        if (c >= STAGES && !bmm_wait(smem_u32(&empty[s]), ((c / STAGES) - 1) & 1)) {
+    if (lane == 0) {   // the rest of K, each chunk once the MMAs have freed its stage
+      for (int c = kFirst; c < KC; ++c) {
+        if (!bmm_wait(smem_u32(&empty[c % STAGES]), ((c / STAGES) - 1) & 1)) {
           fail_s = 1;
           break;
         }
-        const uint32_t st = smem + s * kSB;
-        const uint32_t bar = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(bar, kSB);
-        tma_load_3d(st, &a_map, bar, c * 64, h, m0);
-#pragma unroll
-        for (int j = 0; j < NT / 64; ++j) tma_load_2d(st + 16384 + j * 8192, &w_map, bar, n0 + j * 64, h * K + c * 64);
-        last_phase[s] = (c / STAGES) & 1;
+        issue(c);
       }
-      for (int s = 0; s < STAGES; ++s)   // loads in flight land before the CTA may exit
-        if (last_phase[s] >= 0) bmm_wait(smem_u32(&full[s]), static_cast<uint32_t>(last_phase[s]));
     }
   } else if (warp == 1) {   // MMA issue: the whole warp waits, one elected lane issues
     constexpr uint32_t idesc = idesc_bf16_f32(128, NT, 0, 1);
@@ -376,16 +419,6 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
     }
     if (!ok && lane == 0) fail_s = 1;
     mma_commit_warp(smem_u32(&acc_full));   // arrives once every MMA issued so far is done
-  }
-  const int n = m0 + threadIdx.x;
-  // the RoPE part of the decode query is copied by the first column tile; its load
-  // is issued now so that it does not trail the epilogue
-  const bool copy_pe = blockIdx.x == 0 && p.pe != nullptr && n < p.N;
-  uint4 pe[8];
-  if (copy_pe) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.pe + static_cast<int64_t>(n) * p.pe_row_stride + h * 64);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) pe[j] = __ldg(src + j);
   }
   __syncthreads();
   const bool got = bmm_wait(smem_u32(&acc_full), 0);
@@ -411,6 +444,9 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
 #pragma unroll
     for (int j = 0; j < 8; ++j) d4[j] = pe[j];
   }
+  if (warp == 0 && lane == 0)   // loads in flight land before the CTA may exit
+    for (int s = 0; s < STAGES; ++s)
+      if (last_phase[s] >= 0) bmm_wait(smem_u32(&full[s]), static_cast<uint32_t>(last_phase[s]));
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

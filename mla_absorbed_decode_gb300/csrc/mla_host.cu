@@ -239,9 +239,14 @@ mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t
   return MLA_OK;
 }
 
-mla_status_t mla_absorb_q(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
-                          int64_t q_pe_row_stride, const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H,
-                          mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of mla_absorb_q and mla_absorb_q_rope (positions == nullptr: plain copy of q_pe).
+mla_status_t absorb_impl(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                         int64_t q_pe_row_stride, const int32_t* positions, double rope_theta, const mla_bf16_t* w_uk,
+                         mla_bf16_t* q, int N, int H, mla_stream_t stream) {
   if (!q_nope || !w_uk || !q || N < 1 || H < 1) return MLA_ERR_INVALID_ARG;
   if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q)) return MLA_ERR_INVALID_ARG;
   if (q_nope_row_stride < static_cast<int64_t>(H) * 128 || (q_nope_row_stride % 8) != 0) return MLA_ERR_INVALID_ARG;
@@ -255,7 +260,7 @@ mla_status_t mla_absorb_q(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, c
                  static_cast<uint64_t>(q_nope_row_stride) * 2, 64, 1, 128))
     return MLA_ERR_CUDA;
   if (!encode_2d(&w_map, w_uk, 512, static_cast<uint64_t>(H) * 128, 1024, 64, 64)) return MLA_ERR_CUDA;
-  BmmParams p;
+  BmmParams p = {};
   p.out = reinterpret_cast<__nv_bfloat16*>(q);
   p.out_row_stride = static_cast<int64_t>(H) * kDimQK;
   p.out_head_stride = kDimQK;
@@ -264,8 +269,38 @@ mla_status_t mla_absorb_q(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, c
   p.status = d->status;
   p.pe = reinterpret_cast<const __nv_bfloat16*>(q_pe);
   p.pe_row_stride = q_pe_row_stride;
+  p.positions = positions;
+  if (positions) {   // inverse frequencies theta^(-2j/64) and 2*pi, each as a float pair (hi + lo)
+    for (int j = 0; j < 32; ++j) {
+      const double inv = std::pow(rope_theta, -2.0 * j / 64.0);
+      p.rope_hi[j] = static_cast<float>(inv);
+      p.rope_lo[j] = static_cast<float>(inv - static_cast<double>(p.rope_hi[j]));
+    }
+    const double two_pi = 6.283185307179586476925286766559;
+    p.two_pi_hi = static_cast<float>(two_pi);
+    p.two_pi_lo = static_cast<float>(two_pi - static_cast<double>(p.two_pi_hi));
+  }
   return launch_bmm(true, a_map, w_map, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
                                                                                                : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_absorb_q(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                          int64_t q_pe_row_stride, const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H,
+                          mla_stream_t stream) {
+  return absorb_impl(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, nullptr, 0.0, w_uk, q, N, H, stream);
+}
+
+mla_status_t mla_absorb_q_rope(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                               int64_t q_pe_row_stride, const int32_t* positions, float rope_theta,
+                               const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H, mla_stream_t stream) {
+  if (!q_pe || !positions || (reinterpret_cast<uintptr_t>(positions) & 3u)) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(rope_theta) || !(rope_theta > 1.f)) return MLA_ERR_INVALID_ARG;
+  return absorb_impl(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, positions, static_cast<double>(rope_theta),
+                     w_uk, q, N, H, stream);
 }
 
 mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* o, int N, int H,

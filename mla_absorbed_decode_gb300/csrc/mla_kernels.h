@@ -104,6 +104,12 @@ struct BmmParams {
   int* status;
   const __nv_bfloat16* pe;  // optional: copied into out[n, h, 512:576] by the first column tile
   int64_t pe_row_stride;
+  // optional RoPE of the copied q_pe: positions [N] and, per pair j of the 64 values,
+  // the inverse frequency theta^(-2j/64) as a float pair (hi + lo); 2*pi as a float
+  // pair for the reduction of the angle
+  const int32_t* positions;
+  float rope_hi[32], rope_lo[32];
+  float two_pi_hi, two_pi_lo;
 };
 cudaError_t bmm_set_attributes();
 // absorb: K = 128 -> 512 columns; unabsorb: K = 512 -> 128 columns

@@ -21,7 +21,7 @@ Parity status: every function is pinned by a ``-m "not gpu"`` test in
 from .mla import (  # noqa: F401
     PAGE, D_LATENT, D_ROPE, D_QK,
     gather_request, visible_tokens,
-    decode_absorbed, decode_expanded, absorb_q, unabsorb_o,
+    decode_absorbed, decode_expanded, absorb_q, assemble_q, unabsorb_o,
     lse_merge, decode_bruteforce, tiny_full_mla, rope_interleaved,
 )
 from .schedule import schedule_reference, check_schedule  # noqa: F401

@@ -107,6 +107,22 @@ def absorb_q(q_nope, w_uk):
     return np.einsum("nhd,hdc->nhc", q_nope, w_uk)
 
 
+def assemble_q(q_nope, q_pe, w_uk, positions=None, base=10000.0):
+    """The decode query of the absorbed path: q[n, h, 0:512] = q_nope[n, h] @ W_UK[h] and
+    q[n, h, 512:576] = q_pe[n, h], rotated by RoPE at positions[n] when positions is given.
+
+    ([DSV2-MLA] 4.5: the absorbed q_nope goes into the first kv_lora_rank values, the
+    RoPE'd q_pe into the last 64; the rotation is the decoupled RoPE of the [MLA-paths]
+    tiny example, rope_interleaved below.)  q_nope [N, H, 128], q_pe [N, H, 64],
+    w_uk [H, 128, 512], positions [N] -> [N, H, 576] float64.
+    """
+    q_lat = absorb_q(q_nope, w_uk)
+    pe = np.asarray(q_pe, dtype=np.float64)
+    if positions is not None:
+        pe = np.swapaxes(rope_interleaved(np.swapaxes(pe, 0, 1), positions, base), 0, 1)   # rows = tokens
+    return np.concatenate([q_lat, pe], axis=-1)
+
+
 def unabsorb_o(o_lat, w_uv):
     """o[b, h, :] = o_lat[b, h, :] @ W_UV[h]   ([DSV2-MLA] 4.5, "attn_output @ w_vc").
 

@@ -49,6 +49,44 @@ def test_absorb_q(N, H):
 
 
 @pytest.mark.parametrize("N,H", [(1, 1), (5, 16), (64, 128), (130, 8)])
+def test_absorb_q_with_rope(N, H):
+    import mla_absorbed_decode_gb300 as mla
+    g = torch.Generator().manual_seed(N * 7 + H)
+    q_nope = _bf(torch.randn((N, H, 128), generator=g))
+    q_pe = _bf(torch.randn((N, H, 64), generator=g))
+    w_uk = _bf(torch.randn((H, 128, 512), generator=g) / math.sqrt(512))
+    pos = torch.randint(0, 1 << 17, (N,), generator=g, dtype=torch.int32)
+    pos[0] = 0
+    if N > 2:
+        pos[1], pos[2] = 131071, (1 << 24) - 1    # the largest supported position
+    q = torch.full((N, H, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mla.absorb_q(q_nope.cuda(), w_uk.cuda(), q, q_pe=q_pe.cuda(), positions=pos.cuda(), rope_theta=10000.0)
+    assert mla.get_device_status() == 0
+    ref = oracle.assemble_q(to_np(q_nope), to_np(q_pe), to_np(w_uk), positions=pos.numpy(), base=10000.0)
+    got = to_np(q.cpu())
+    assert np.all(np.abs(got[..., :512] - ref[..., :512]) <= _bmm_bound(ref[..., :512]))
+    # the rotation in fp32 on an angle accurate to ~1e-7 rad, then one bf16 rounding
+    d = np.abs(got[..., 512:] - ref[..., 512:])
+    assert np.all(d <= _bmm_bound(ref[..., 512:])), d.max()
+    assert torch.equal(q[0, :, 512:].cpu(), q_pe[0])   # position 0 is the identity, bit for bit
+
+
+def test_absorb_q_rope_rejects_bad_arguments():
+    import mla_absorbed_decode_gb300 as mla
+    N, H = 4, 2
+    q_nope = torch.zeros((N, H, 128), dtype=torch.bfloat16, device="cuda")
+    q_pe = torch.zeros((N, H, 64), dtype=torch.bfloat16, device="cuda")
+    w_uk = torch.zeros((H, 128, 512), dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((N, H, 576), dtype=torch.bfloat16, device="cuda")
+    pos = torch.zeros(N, dtype=torch.int32, device="cuda")
+    for theta in (1.0, 0.5, float("nan"), float("inf")):
+        with pytest.raises(mla.MLAError):
+            mla.absorb_q(q_nope, w_uk, q, q_pe=q_pe, positions=pos, rope_theta=theta)
+    with pytest.raises(mla.MLAError):   # RoPE needs q_pe
+        mla.absorb_q(q_nope, w_uk, q, q_pe=None, positions=pos)
+
+
+@pytest.mark.parametrize("N,H", [(1, 1), (5, 16), (64, 128), (130, 8)])
 def test_unabsorb_o(N, H):
     import mla_absorbed_decode_gb300 as mla
     g = torch.Generator().manual_seed(N * 17 + H)

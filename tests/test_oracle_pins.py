@@ -222,6 +222,34 @@ def test_rope_properties():
     assert abs(r[2, 0] - math.cos(2.0)) < 1e-15 and abs(r[2, 1] - math.sin(2.0)) < 1e-15
 
 
+def test_assemble_q_layout_and_rope_per_token():
+    rng = np.random.default_rng(12)
+    N, H = 5, 3
+    q_nope = rng.standard_normal((N, H, 128))
+    w_uk = rng.standard_normal((H, 128, 512)) / math.sqrt(512)
+    q_pe = rng.standard_normal((N, H, 64))
+    plain = om.assemble_q(q_nope, q_pe, w_uk)
+    assert plain.shape == (N, H, 576)
+    assert np.array_equal(plain[..., 512:], q_pe)
+    assert np.allclose(plain[..., :512], np.einsum("nhd,hdc->nhc", q_nope, w_uk), rtol=0, atol=1e-12)
+    assert np.array_equal(om.assemble_q(q_nope, q_pe, w_uk, positions=np.zeros(N)), plain)   # pos 0: identity
+    # every token turns by its own position: a unit vector in dim 0 ends at (cos p, sin p);
+    # in the last pair (j = 31) the angle is p * base^(-62/64)
+    pos = np.array([0, 1, 7, 4096, 131071])
+    e0 = np.zeros((N, H, 64)); e0[..., 0] = 1.0
+    e62 = np.zeros((N, H, 64)); e62[..., 62] = 1.0
+    r0 = om.assemble_q(q_nope, e0, w_uk, positions=pos)[..., 512:]
+    r62 = om.assemble_q(q_nope, e62, w_uk, positions=pos)[..., 512:]
+    for n, p in enumerate(pos):
+        assert np.allclose(r0[n, :, 0], math.cos(p), atol=1e-12) and np.allclose(r0[n, :, 1], math.sin(p), atol=1e-12)
+        a = p * 10000.0 ** (-62.0 / 64.0)
+        assert np.allclose(r62[n, :, 62], math.cos(a), atol=1e-12)
+        assert np.allclose(r62[n, :, 63], math.sin(a), atol=1e-12)
+    rot = om.assemble_q(q_nope, q_pe, w_uk, positions=pos)[..., 512:]
+    assert np.allclose(rot[..., 0::2] ** 2 + rot[..., 1::2] ** 2, q_pe[..., 0::2] ** 2 + q_pe[..., 1::2] ** 2,
+                       atol=1e-12)
+
+
 # ---- planted mistakes: each must make at least one pin fail -----------------------------
 
 def _pins_pass():
