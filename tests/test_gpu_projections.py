@@ -99,18 +99,22 @@ def test_unabsorb_o(N, H):
     assert np.all(np.abs(got - ref) <= _bmm_bound(ref))
 
 
-def _chain(inp, batches=None):
+def _chain(inp, batches=None, positions=None):
     import mla_absorbed_decode_gb300 as mla
     B, s_q, H = inp["q"].shape[:3]
     step = mla.DecodeStep(B, s_q, H, inp["seqlens"].cuda(), inp["causal"], inp["softmax_scale"])
     o = step.run(inp["q_nope"].cuda(), inp["q_pe"].cuda(), inp["w_uk"].cuda(), inp["w_uv"].cuda(),
-                 inp["kv_cache"].cuda(), inp["block_table"].cuda())
+                 inp["kv_cache"].cuda(), inp["block_table"].cuda(),
+                 positions=None if positions is None else positions.cuda())
     assert mla.get_device_status() == 0
     o = o.view(B, s_q, H, 128).cpu()
     sel = list(range(B)) if batches is None else batches
     kv = inp["kv_cache"].float().numpy()
     qn = to_np(inp["q_nope"]).reshape(B, s_q, H, 128)
-    qp = to_np(inp["q_pe"]).reshape(B, s_q, H, 64)
+    qp = to_np(inp["q_pe"])
+    if positions is not None:   # the expanded definition sees the rotated q^R
+        qp = np.swapaxes(oracle.rope_interleaved(np.swapaxes(qp, 0, 1), positions.numpy()), 0, 1)
+    qp = qp.reshape(B, s_q, H, 64)
     ref, ref_lse = oracle.decode_expanded(qn[sel], qp[sel], to_np(inp["w_uk"]), to_np(inp["w_uv"]), kv,
                                           inp["block_table"][sel].numpy(), inp["seqlens"][sel].numpy(),
                                           inp["softmax_scale"], causal=inp["causal"])
@@ -126,9 +130,21 @@ def test_chain_small_vs_expanded_definition():
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2e-2
 
 
-def test_chain_full_v3_sampled_vs_expanded_definition():
+def test_chain_with_rope_vs_expanded_definition():
+    w = W.small_variant(W.V3, B=3, seqlen=700)
+    inp = W.make_inputs(w)
+    positions = inp["seqlens"] - 1   # the new token's position
+    got, ref, _ = _chain(inp, positions=positions.to(torch.int32))
+    d = np.abs(got - ref)
+    assert d.max() <= OUT_ABS, d.max()
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2e-2
+
+
+def test_chain_full_v3_vs_expanded_definition():
+    # every request of the full DeepSeek-V3-shaped workload through absorb -> decode ->
+    # un-absorb, against the expanded (un-absorbed) definition (~4.4e12 fp64 FLOPs on the host)
     inp = W.make_inputs(W.V3)
-    got, ref, _ = _chain(inp, batches=[0, 17, 63])
+    got, ref, _ = _chain(inp)
     d = np.abs(got - ref)
     assert d.max() <= OUT_ABS, d.max()
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2e-2
