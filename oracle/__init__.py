@@ -9,9 +9,10 @@ input generator, which holds none of the method's arithmetic.
 Everything here is plain numpy in float64 (or pure Python for the brute-force
 checks), written for a reader to check against the pages by eye:
 
-* ``mla.py``      -- the absorbed decode definition, the expanded (un-absorbed)
-                    chain, the LSE merge, a pure-Python brute force and the
-                    tiny full-MLA example with decoupled RoPE.
+* ``mla.py``      -- the absorbed decode definition (dense, and over a selected
+                    top-k token list), the expanded (un-absorbed) chain, the
+                    LSE merge, a pure-Python brute force and the tiny full-MLA
+                    example with decoupled RoPE.
 * ``schedule.py`` -- a restatement of the split-KV schedule rule and the
                     invariants any valid schedule must satisfy.
 
@@ -21,7 +22,7 @@ Parity status: every function is pinned by a ``-m "not gpu"`` test in
 from .mla import (  # noqa: F401
     PAGE, D_LATENT, D_ROPE, D_QK,
     gather_request, visible_tokens,
-    decode_absorbed, decode_expanded, absorb_q, assemble_q, unabsorb_o,
+    decode_absorbed, decode_sparse, decode_expanded, absorb_q, assemble_q, unabsorb_o,
     lse_merge, decode_bruteforce, tiny_full_mla, rope_interleaved,
 )
 from .schedule import schedule_reference, check_schedule  # noqa: F401

@@ -97,6 +97,50 @@ def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=Fal
     return out, lse
 
 
+def decode_sparse(q, kv_cache, block_table, seqlens, indices, topk_lens, softmax_scale, causal=False,
+                  with_abs=False):
+    """Sparse (top-k) absorbed decode: the same attention, over a selected list of tokens.
+
+    [AI-note] section 6 ("Sparse attention 把方向反过来"): a selector picks k of the L
+    cached latents (DeepSeek-V3.2's DSA, index_topk = 2048); they are gathered by
+    index and the scores and the weighted sum run over those k only.  For request b
+    the list is indices[b, 0:topk_lens[b]] (token positions, each in [0, seqlens[b]),
+    looked up through the block table as in the dense case); with causal masking query
+    position i keeps only listed tokens t <= seqlens[b] - s_q + i:
+        s_t = softmax_scale * <q[b,i,h,:576], kv_t[:576]>,  t listed and visible
+        lse = ln sum_t exp(s_t),   out = sum_t exp(s_t - lse) * kv_t[:512]
+    A listed token counts once per listing.  Returns out [B, s_q, H, 512], lse [B, s_q, H].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, s_q, H, dq = q.shape
+    assert dq == D_QK
+    out = np.zeros((B, s_q, H, D_LATENT))
+    out_abs = np.zeros((B, s_q, H, D_LATENT)) if with_abs else None
+    lse = np.full((B, s_q, H), -np.inf)
+    for b in range(B):
+        sel = np.asarray(indices[b][: int(topk_lens[b])], dtype=np.int64)
+        L = int(seqlens[b])
+        if sel.size == 0:
+            continue
+        assert sel.min() >= 0 and sel.max() < L
+        kv = np.asarray(kv_cache[np.asarray(block_table[b])[sel // PAGE], sel % PAGE], dtype=np.float64)
+        for i in range(s_q):
+            keep = sel < visible_tokens(L, s_q, i, causal)
+            if not keep.any():
+                continue
+            s = softmax_scale * (q[b, i] @ kv[keep].T)          # [H, kept]
+            m = s.max(axis=1, keepdims=True)
+            e = np.exp(s - m)
+            z = e.sum(axis=1, keepdims=True)
+            lse[b, i] = (m + np.log(z))[:, 0]
+            out[b, i] = (e / z) @ kv[keep, :D_LATENT]
+            if with_abs:
+                out_abs[b, i] = (e / z) @ np.abs(kv[keep, :D_LATENT])
+    if with_abs:
+        return out, lse, out_abs
+    return out, lse
+
+
 def absorb_q(q_nope, w_uk):
     """q_lat[b, h, :] = q_nope[b, h, :] @ W_UK[h]   ([DSV2-MLA] 4.5, "q_nope @ w_kc").
 
