@@ -116,6 +116,30 @@ mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t
                         void* workspace, size_t workspace_bytes,
                         mla_bf16_t* out, float* lse, mla_stream_t stream);
 
+/* Sparse (top-k) absorbed decode (web page "为什么 MLA + MTP 容易吃亏？从 Arithmetic
+ * Intensity 看 Attention", section 6: a selector picks k of the cached latents --
+ * DeepSeek-V3.2 keeps index_topk = 2048 -- and attention runs over those only, so
+ * its cost follows k instead of the context length).  For request b, the list is
+ * indices[b * index_stride + e], e < topk_lens[b]: token positions in [0, seqlens[b]),
+ * looked up through the block table as in mla_decode.  Every query position and
+ * head of the request attends to the listed tokens (with causal_s_q, query position
+ * i drops listed tokens t > seqlens[b] - s_q + i):
+ *     s_e = softmax_scale * <q[b,i,h,0:576], kv_t[0:576]>,  t = indices[b][e]
+ *     lse = ln sum_e exp(s_e),   out = sum_e exp(s_e - lse) * kv_t[0:512]
+ * A token listed twice counts twice.  An empty list gives out = 0, lse = -inf.
+ *  indices      int32 device, 4-byte aligned; index_stride >= max topk_lens
+ *  topk_lens    [B] int32 device, each in [0, index_stride]
+ *  metadata     from mla_decode_metadata called with topk_lens in place of seqlens
+ * Entries outside [0, seqlens[b]) are reported as MLA_ERR_DEVICE_BOUNDS (their rows
+ * are skipped, the result is then undefined).  Other arguments as for mla_decode.
+ * Async on stream. */
+mla_status_t mla_decode_sparse(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t num_blocks,
+                               const int32_t* block_table, int max_blocks, const int32_t* seqlens,
+                               const int32_t* indices, int64_t index_stride, const int32_t* topk_lens, int B, int s_q,
+                               int H, float softmax_scale, int causal_s_q, const void* metadata, int num_sm_parts,
+                               void* workspace, size_t workspace_bytes, mla_bf16_t* out, float* lse,
+                               mla_stream_t stream);
+
 /* W_UK absorption and assembly of the decode query ("DeepSeekV2之MLA" 4.5:
  * q_nope_out = bmm(q_nope, w_kc) goes into q[..., :kv_lora_rank], the RoPE'd
  * q_pe into the last 64 values):

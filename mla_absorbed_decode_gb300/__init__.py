@@ -15,7 +15,7 @@ import torch
 
 __all__ = [
     "MLAError", "lib", "library_path", "num_sm_parts", "metadata_size", "decode_metadata",
-    "decode_workspace_size", "decode", "absorb_q", "unabsorb_o", "get_device_status",
+    "decode_workspace_size", "decode", "decode_sparse", "absorb_q", "unabsorb_o", "get_device_status",
     "schedule_params", "debug_withhold_first_load", "DecodeStep", "EXPORTED_SYMBOLS",
 ]
 
@@ -36,6 +36,8 @@ _SIGNATURES = {
     "mla_decode_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "mla_decode": (_c_int, [_p, _p, _c_ll, _p, _c_int, _p, _c_int, _c_int, _c_int, _c_float, _c_int,
                             _p, _c_int, _p, _c_size, _p, _p, _p]),
+    "mla_decode_sparse": (_c_int, [_p, _p, _c_ll, _p, _c_int, _p, _p, _c_ll, _p, _c_int, _c_int, _c_int, _c_float,
+                                   _c_int, _p, _c_int, _p, _c_size, _p, _p, _p]),
     "mla_absorb_q": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _p, _c_int, _c_int, _p]),
     "mla_absorb_q_rope": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _p, _c_int, _c_int, _p]),
     "mla_unabsorb_o": (_c_int, [_p, _p, _p, _c_int, _c_int, _p]),
@@ -137,6 +139,26 @@ def decode(q, kv_cache, block_table, seqlens, softmax_scale: float, causal: bool
                             _ptr(seqlens), B, s_q, H, float(softmax_scale), int(causal), _ptr(metadata), parts,
                             _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
                             _stream(stream)), "mla_decode")
+    return out, lse
+
+
+def decode_sparse(q, kv_cache, block_table, seqlens, indices, topk_lens, softmax_scale: float, causal: bool, metadata,
+                  parts: int, workspace=None, out=None, lse=None, stream=None):
+    """Sparse (top-k) absorbed decode over indices[b, :topk_lens[b]] (int32 token positions);
+    metadata from decode_metadata(topk_lens, ...).  Returns (out [B,s_q,H,512] bf16, lse [B,s_q,H] fp32)."""
+    B, s_q, H, _ = q.shape
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, s_q, H, 512), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_size(B, s_q, H, parts), dtype=torch.uint8, device=dev)
+    _check(lib().mla_decode_sparse(_ptr(q), _ptr(kv_cache), kv_cache.shape[0], _ptr(block_table), block_table.shape[1],
+                                   _ptr(seqlens), _ptr(indices), indices.stride(0), _ptr(topk_lens), B, s_q, H,
+                                   float(softmax_scale), int(causal), _ptr(metadata), parts, _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+                                   _stream(stream)), "mla_decode_sparse")
     return out, lse
 
 

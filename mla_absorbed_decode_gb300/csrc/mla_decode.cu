@@ -141,7 +141,7 @@ struct SegmentWalker {
   __device__ bool next(Segment& s) {
     while (!done) {
       if (b > b_last) { done = true; break; }
-      const int nb = pages_of(__ldg(p->seqlens + b));
+      const int nb = pages_of(__ldg(p->lens + b));
       const int k0 = first ? kb : 0;
       const int k1 = (b == b_last) ? k_end : nb;
       const int sp = first ? split0 : 0;
@@ -223,6 +223,127 @@ __device__ __forceinline__ int request_block(const DecodeParams& p, int b, int k
     blk = -1;   // the TMA then reads out-of-range rows, which it fills with zeros
   }
   return blk;
+}
+
+// ---------------------------------------------------------- sparse gather --
+// Sparse decode ("为什么 MLA + MTP 容易吃亏？" section 6: the selected latents are
+// gathered by index): page k of request b is entries [64k, 64k + 64) of its list, and
+// entry e is the token at position t = indices[b][e], read through the block table
+// like a dense token.  A whole warp gathers a page with 16-byte cp.async copies into
+// the same swizzled layout a TMA box would produce; the stage's barrier expects one
+// arrival per lane (cp.async.mbarrier.arrive.noinc when the lane's copies land).
+
+// Address of list entry e's cached row, or nullptr (and a recorded bounds error) if
+// the entry is not a position of the request or its page is out of range.
+__device__ __forceinline__ const __nv_bfloat16* sparse_row(const DecodeParams& p, int b, int e) {
+  const int t = __ldg(p.indices + static_cast<int64_t>(b) * p.idx_stride + e);
+  if (t < 0 || t >= __ldg(p.seqlens + b)) {
+    atomicCAS(p.status, 0, MLA_ERR_DEVICE_BOUNDS);
+    return nullptr;
+  }
+  const int blk = request_block(p, b, t / kPageTokens);
+  if (blk < 0) return nullptr;
+  return p.kv + (static_cast<int64_t>(blk) * kPageTokens + t % kPageTokens) * kDimQK;
+}
+
+// The warp copies 16-byte units [u0, u1) (unit u = dims 8u..8u+7, chunk u / 8) of the
+// page's rows into `stage` (chunk c at c * 8192, row r at r * 128, 128-byte swizzle):
+// one row at a time, the lanes taking consecutive units of it.  rows_lo / rows_hi are
+// this lane's row addresses for rows lane and lane + 32 (nullptr: not gathered).
+__device__ __forceinline__ void gather_units(uint32_t stage, const __nv_bfloat16* rows_lo, const __nv_bfloat16* rows_hi,
+                                             int u0, int u1, int lane) {
+#pragma unroll 1
+  for (int r = 0; r < 64; ++r) {
+    const uint64_t mine = reinterpret_cast<uint64_t>(r < 32 ? rows_lo : rows_hi);
+    const __nv_bfloat16* row = reinterpret_cast<const __nv_bfloat16*>(__shfl_sync(0xffffffffu, mine, r & 31));
+    if (row == nullptr) continue;
+    for (int u = u0 + lane; u < u1; u += 32) {
+      const int c = u >> 3, v = u & 7;
+      cp_async16(stage + c * 8192 + r * 128 + ((v ^ (r & 7)) << 4), row + u * 8);
+    }
+  }
+}
+
+// Warp 0 of the S-CTA, sparse decode: the q blocks by TMA (lane 0) and the pages by
+// warp-wide gathers, both through the same two stages as the dense producer.
+__device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
+                                  uint32_t cl, int rb, bool withhold) {
+  const int lane = threadIdx.x & 31;
+  SegmentWalker w;
+  w.init(p, part);
+  Segment s;
+  uint32_t i = 0;
+  int issued[kKStages];
+  uint32_t issued_phase[kKStages];
+  for (int j = 0; j < kKStages; ++j) issued[j] = 0, issued_phase[j] = 0;
+  bool ok = true;
+  while (ok && w.next(s)) {
+    const int qrow0 = s.b * p.rows + rb * 128;
+    for (int j = 0; j < 2 && ok; ++j, ++i) {
+      const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
+      if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl) ||
+          !warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive(smem_u32(&sh.bar.full_b[st]));   // a q block lands whole; its second half needs no bytes
+      const uint32_t full = smem_u32(&sh.bar.full[st]);
+      if (lane != 0) {
+        mbar_arrive(full);
+      } else if (!(withhold && i == 0)) {   // test hook: this block never arrives
+        mbar_arrive_expect_tx(full, kKStageBytes);
+        tma_load_3d(smem + kOffStage + st * kKStageBytes, &maps->q, full, 0, qrow0 + 64 * j, 0);
+        issued[st] = 1, issued_phase[st] = ph;
+      }
+    }
+    const int n = __ldg(p.lens + s.b);
+    for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
+      const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
+      const uint32_t stage = smem + kOffStage + st * kKStageBytes;
+      if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      const int e0 = k * 64 + lane;
+      const __nv_bfloat16* lo = e0 < n ? sparse_row(p, s.b, e0) : nullptr;
+      const __nv_bfloat16* hi = e0 + 32 < n ? sparse_row(p, s.b, e0 + 32) : nullptr;
+      gather_units(stage, lo, hi, 0, kKPartA * 8, lane);
+      cp_async_arrive_noinc(smem_u32(&sh.bar.full[st]));
+      if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      gather_units(stage, lo, hi, kKPartA * 8, 72, lane);
+      cp_async_arrive_noinc(smem_u32(&sh.bar.full_b[st]));
+    }
+  }
+  cp_async_wait_all();   // this lane's copies land before the CTA may exit
+  if (lane == 0)
+    for (int st = 0; st < kKStages; ++st)
+      if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
+  __syncwarp();
+}
+
+// Warp 0 of the O-CTA, sparse decode: the 512 value dims of every gathered page.
+__device__ void o_producer_sparse(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl) {
+  const int lane = threadIdx.x & 31;
+  SegmentWalker w;
+  w.init(p, part);
+  Segment s;
+  uint32_t T = 0;
+  bool ok = true;
+  while (ok && w.next(s)) {
+    const int n = __ldg(p.lens + s.b);
+    for (int k = s.kb; k < s.ke && ok; ++k, ++T) {
+      const uint32_t st = T % kVStages, ph = (T / kVStages) & 1;
+      const uint32_t stage = smem + kOffStage + st * kVStageBytes;
+      if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      const int e0 = k * 64 + lane;
+      const __nv_bfloat16* lo = e0 < n ? sparse_row(p, s.b, e0) : nullptr;
+      const __nv_bfloat16* hi = e0 + 32 < n ? sparse_row(p, s.b, e0 + 32) : nullptr;
+      gather_units(stage, lo, hi, 0, 32, lane);
+      cp_async_arrive_noinc(smem_u32(&sh.bar.full[st]));
+      if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      gather_units(stage, lo, hi, 32, 64, lane);
+      cp_async_arrive_noinc(smem_u32(&sh.bar.full_b[st]));
+    }
+  }
+  cp_async_wait_all();
+  __syncwarp();
 }
 
 // Lane 0 of warp 0 of the O-CTA: the 512 value dims of every page, as two 32 KiB
@@ -318,6 +439,7 @@ __device__ void s_producer(const DecodeParams& p, const KvMaps* maps, Shared& sh
 }
 
 // Warp 1 of the S-CTA; all 32 lanes run the loop, one elected lane issues.
+template <bool sparse>
 __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl) {
   SegmentWalker w;
   w.init(p, part);
@@ -334,6 +456,7 @@ __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       const uint32_t sb = T & 1, sph = (T >> 1) & 1;
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.s_empty[sb]), sph ^ 1, p.status, cl)) { ok = false; break; }
+      if constexpr (sparse) fence_proxy_async_smem();   // gathered by cp.async: generic-proxy writes
       tc_fence_after();
       const uint32_t kstage = smem + kOffStage + st * kKStageBytes;
       const uint32_t d = tmem + kSCol0 + sb * 64;
@@ -344,6 +467,7 @@ __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       }
       mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // chunks 0..4 may be refilled
       if (!warp_wait(sh, smem_u32(&sh.bar.full_b[st]), ph, p.status, cl)) { ok = false; break; }
+      if constexpr (sparse) fence_proxy_async_smem();
       tc_fence_after();
 #pragma unroll
       for (int kk = 4 * kKPartA; kk < 36; ++kk) {
@@ -396,6 +520,7 @@ __device__ __forceinline__ void copy_q_to_tmem(uint32_t smem, uint32_t tmem_lane
 // Warps 4..11 of the S-CTA.  Warpgroup wg (0 or 1) handles columns [32*wg, 32*wg+32)
 // of every page for its 128 rows; the two exchange row maxima and partial sums
 // through shared memory and use named barrier 1 (256 threads).
+template <bool sparse>
 __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb,
                               uint32_t peer) {
   const int t = threadIdx.x - 128;
@@ -418,9 +543,11 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
   uint32_t i = 0, T = 0;   // ring item (q blocks and pages) and page counters
   bool ok = true;
   while (ok && w.next(s)) {
-    const int L = __ldg(p.seqlens + s.b);
+    const int L = __ldg(p.lens + s.b);   // the request's list: its tokens, or its top-k entries
     int vis = L;
-    if (p.causal && row_valid) vis = L - p.s_q + pos_i + 1;
+    if (p.causal && row_valid && !sparse) vis = L - p.s_q + pos_i + 1;
+    // sparse with causal masking: an entry is visible if its token position is below
+    const int vis_pos = (sparse && p.causal) ? __ldg(p.seqlens + s.b) - p.s_q + (row_valid ? pos_i : 0) + 1 : 0;
     {   // Q of this request into TMEM (every QK^T of the previous segment is complete:
         // its last S was waited for below)
       const uint32_t q0 = i % kKStages, q1 = (i + 1) % kKStages;
@@ -469,6 +596,12 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       if (nvalid < 32) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[c] = (c < nvalid) ? sv[c] : -INFINITY;
+      }
+      if (sparse && p.causal) {   // token positions of this thread's 32 columns (sparse only)
+        const int32_t* ix = p.indices + static_cast<int64_t>(s.b) * p.idx_stride + k * 64 + c0;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c < nvalid && __ldg(ix + c) >= vis_pos) sv[c] = -INFINITY;
       }
       const float my_max = max32(sv);
       asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine), "f"(my_max) : "memory");
@@ -535,6 +668,7 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
 
 // ------------------------------------------------------------------ O-CTA --
 // Warp 1 of the O-CTA (all 32 lanes; one elected lane issues the MMAs).
+template <bool sparse>
 __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl) {
   const int lane = threadIdx.x & 31;
   SegmentWalker w;
@@ -546,7 +680,7 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
   bool ok = true, any = false;
   while (ok && w.next(s)) {
     if (seg > 0 && !warp_wait(sh, smem_u32(&sh.bar.o_free), (seg - 1) & 1, p.status, cl)) break;
-    const int L = __ldg(p.seqlens + s.b);
+    const int L = __ldg(p.lens + s.b);
     for (int k = s.kb; k < s.ke; ++k, ++T) {
       const uint32_t st = T % kVStages, ph = (T / kVStages) & 1;
       const uint32_t ps = T % kSlots, pph = (T / kSlots) & 1;
@@ -556,6 +690,7 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       __syncwarp();
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.p_full[ps]), pph, p.status, cl, true)) { ok = false; break; }
+      if constexpr (sparse) fence_proxy_async_smem();
       // tail page: zero the value rows past the sequence end up to the next 16-row
       // boundary, so that P = 0 never meets a non-finite value in the MMA (per half)
       const int nvalid = min(64, L - k * 64);
@@ -604,6 +739,7 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
         }
         mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // chunks 0..3 may be refilled
         if (!warp_wait(sh, smem_u32(&sh.bar.full_b[st]), ph, p.status, cl)) { ok = false; break; }
+        if constexpr (sparse) fence_proxy_async_smem();
         zero_tail(vstage + kVStageBytes / 2);
         __syncwarp();
         tc_fence_after();
@@ -745,6 +881,8 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
 
 }  // namespace
 
+// kSparse: the pages are gathered from the top-k lists (p.indices) instead of read whole.
+template <bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
@@ -771,10 +909,11 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     prefetch_tensormap(&maps.c4);
     sh.abort = 0;
     sh.cmd = 0;
+    constexpr uint32_t fills = kSparse ? 32u : 1u;   // sparse: one arrival per gathering lane
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(smem_u32(&sh.bar.full[i]), 1);
+      mbar_init(smem_u32(&sh.bar.full[i]), fills);
       mbar_init(smem_u32(&sh.bar.empty[i]), 1);
-      mbar_init(smem_u32(&sh.bar.full_b[i]), 1);
+      mbar_init(smem_u32(&sh.bar.full_b[i]), fills);
       mbar_init(smem_u32(&sh.bar.empty_b[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -809,17 +948,23 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
 
   if (is_s) {
     if (warp == 0) {
-      if ((threadIdx.x & 31) == 0) s_producer(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
+      if constexpr (kSparse)
+        s_producer_sparse(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
+      else if ((threadIdx.x & 31) == 0)
+        s_producer(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
     } else if (warp == 1) {
-      s_cta_mma(p, sh, smem, part, cl);
+      s_cta_mma<kSparse>(p, sh, smem, part, cl);
     } else if (warp >= 4) {
-      s_cta_softmax(p, sh, smem, part, cl, rb, peer);
+      s_cta_softmax<kSparse>(p, sh, smem, part, cl, rb, peer);
     }
   } else {
     if (warp == 0) {
-      if ((threadIdx.x & 31) == 0) o_producer(p, &maps, sh, smem, part, cl);
+      if constexpr (kSparse)
+        o_producer_sparse(p, sh, smem, part, cl);
+      else if ((threadIdx.x & 31) == 0)
+        o_producer(p, &maps, sh, smem, part, cl);
     } else if (warp == 1) {
-      o_cta_mma(p, sh, smem, part, cl);
+      o_cta_mma<kSparse>(p, sh, smem, part, cl);
     } else if (warp == 2) {
       if ((threadIdx.x & 31) == 0) o_cta_forwarder(p, sh, part, cl, peer);
     } else if (warp >= 4) {
@@ -839,7 +984,10 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
 }
 
 cudaError_t decode_set_attributes() {
-  return cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(kSmemBytes));
 }
 
@@ -861,7 +1009,7 @@ int decode_max_clusters(int cluster_ctas) {
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = decode_config(cluster_ctas, cluster_ctas, nullptr, attr, false);
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, mla_decode_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, mla_decode_kernel<false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -871,7 +1019,8 @@ int decode_max_clusters(int cluster_ctas) {
 cudaError_t launch_decode(const KvMaps& maps, const DecodeParams& p, int cluster_ctas, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = decode_config(p.num_parts * cluster_ctas, cluster_ctas, stream, attr, true);
-  return cudaLaunchKernelEx(&cfg, mla_decode_kernel, maps, p);
+  if (p.indices) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, maps, p);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, maps, p);
 }
 
 }  // namespace mla

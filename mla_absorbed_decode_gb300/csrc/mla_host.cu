@@ -181,15 +181,24 @@ size_t mla_decode_workspace_size(int B, int s_q, int H, int num_sm_parts) {
   return o_bytes + ((l_bytes + 255) / 256) * 256;
 }
 
-mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t num_blocks, const int32_t* block_table,
-                        int max_blocks, const int32_t* seqlens, int B, int s_q, int H, float softmax_scale,
-                        int causal_s_q, const void* metadata, int num_sm_parts, void* workspace,
-                        size_t workspace_bytes, mla_bf16_t* out, float* lse, mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of mla_decode (indices == nullptr) and mla_decode_sparse.
+mla_status_t decode_impl(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t num_blocks,
+                         const int32_t* block_table, int max_blocks, const int32_t* seqlens, const int32_t* indices,
+                         int64_t idx_stride, const int32_t* topk_lens, int B, int s_q, int H, float softmax_scale,
+                         int causal_s_q, const void* metadata, int num_sm_parts, void* workspace,
+                         size_t workspace_bytes, mla_bf16_t* out, float* lse, mla_stream_t stream) {
   if (!q || !kv_cache || !block_table || !seqlens || !metadata || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (B < 1 || s_q < 1 || H < 1 || num_blocks < 1 || max_blocks < 1 || num_sm_parts < 1) return MLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
       (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u) ||
       (reinterpret_cast<uintptr_t>(metadata) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  if (indices && (!topk_lens || idx_stride < 1 || (reinterpret_cast<uintptr_t>(indices) & 3u) ||
+                  (reinterpret_cast<uintptr_t>(topk_lens) & 3u)))
     return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
   const int n_rb = pairs_for(s_q, H);
@@ -215,6 +224,9 @@ mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t
   p.block_table = block_table;
   p.max_blocks = max_blocks;
   p.seqlens = seqlens;
+  p.lens = indices ? topk_lens : seqlens;
+  p.indices = indices;
+  p.idx_stride = indices ? idx_stride : 0;
   p.B = B;
   p.s_q = s_q;
   p.H = H;
@@ -237,6 +249,30 @@ mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t
   if (launch_decode(kv_maps, p, 2 * n_rb, cs) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_combine(p.o_part, p.lse_part, p.num_splits, B, rows, p.out, lse, cs) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t num_blocks, const int32_t* block_table,
+                        int max_blocks, const int32_t* seqlens, int B, int s_q, int H, float softmax_scale,
+                        int causal_s_q, const void* metadata, int num_sm_parts, void* workspace,
+                        size_t workspace_bytes, mla_bf16_t* out, float* lse, mla_stream_t stream) {
+  return decode_impl(q, kv_cache, num_blocks, block_table, max_blocks, seqlens, nullptr, 0, nullptr, B, s_q, H,
+                     softmax_scale, causal_s_q, metadata, num_sm_parts, workspace, workspace_bytes, out, lse, stream);
+}
+
+mla_status_t mla_decode_sparse(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t num_blocks,
+                               const int32_t* block_table, int max_blocks, const int32_t* seqlens,
+                               const int32_t* indices, int64_t index_stride, const int32_t* topk_lens, int B, int s_q,
+                               int H, float softmax_scale, int causal_s_q, const void* metadata, int num_sm_parts,
+                               void* workspace, size_t workspace_bytes, mla_bf16_t* out, float* lse,
+                               mla_stream_t stream) {
+  if (!indices) return MLA_ERR_INVALID_ARG;
+  return decode_impl(q, kv_cache, num_blocks, block_table, max_blocks, seqlens, indices, index_stride, topk_lens, B,
+                     s_q, H, softmax_scale, causal_s_q, metadata, num_sm_parts, workspace, workspace_bytes, out, lse,
+                     stream);
 }
 
 }  // extern "C"

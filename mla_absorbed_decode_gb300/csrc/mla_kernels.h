@@ -33,6 +33,12 @@ struct DecodeParams {
   const int32_t* block_table;
   int max_blocks;
   const int32_t* seqlens;
+  // The per-request list the kernel walks in pages of 64 entries: seqlens itself
+  // (dense), or the top-k list lengths (sparse: entry e of request b is the token at
+  // position indices[b * idx_stride + e]; indices == nullptr for the dense decode).
+  const int32_t* lens;
+  const int32_t* indices;
+  int64_t idx_stride;
   int B, s_q, H, rows, n_rb;
   float scale_log2;                     // softmax_scale * log2(e)
   int causal;

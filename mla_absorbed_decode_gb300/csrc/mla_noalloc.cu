@@ -117,6 +117,9 @@ extern "C" mla_status_t mla_decode_noalloc(const mla_bf16_t* q, const mla_bf16_t
   p.block_table = block_table;
   p.max_blocks = max_blocks;
   p.seqlens = seqlens;
+  p.lens = seqlens;
+  p.indices = nullptr;
+  p.idx_stride = 0;
   p.B = B;
   p.s_q = s_q;
   p.H = H;

@@ -160,6 +160,17 @@ __device__ __forceinline__ void prefetch_tensormap(const void* map) {
 __device__ __forceinline__ void prefetch_l2(const void* gptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(gptr), "r"(bytes) : "memory");
 }
+// Per-thread asynchronous copy of 16 bytes global -> shared (L2 only); an mbarrier
+// tracks a thread's copies issued so far with cp_async_arrive_noinc (the barrier's
+// expected count includes one arrival per tracking thread).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Programmatic dependent launch.  Every kernel of the library is launched so that
 // it may start while the previous kernel of the stream is still running; before
 // its first global access it waits here until that kernel has completed and its
