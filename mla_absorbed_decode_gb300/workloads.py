@@ -13,7 +13,9 @@ with `seed`, in this fixed order):
   5. optional outliers: each slot independently with probability p has its
      whole 576-value row multiplied by a factor (before rounding to bf16);
   6. optional projection inputs: q_nope [B*s_q, H, 128] and q_pe [B*s_q, H, 64]
-     ~ N(0, 1); W_UK [H, 128, 512] and W_UV [H, 512, 128] ~ N(0, 1/512) (variance).
+     ~ N(0, 1); W_UK [H, 128, 512] and W_UV [H, 512, 128] ~ N(0, 1/512) (variance);
+  7. optional top-k lists (sparse decode): per request, the first min(topk, L) of a
+     random permutation of its positions, sorted ascending (-1 pads the rest).
 Poison: pool pages no request uses, and slots at or beyond seqlen in a
 request's last page, hold NaN; block-table entries past a request's last page
 hold -1.  A correct kernel never reads any of them into its result.
@@ -46,6 +48,7 @@ class Workload:
     outlier_scale: float = 1.0
     with_projections: bool = False
     fixed_seqlens: tuple = field(default_factory=tuple)
+    topk: int = 0                # sparse decode: each request lists min(topk, L) of its tokens
 
     @property
     def softmax_scale(self) -> float:
@@ -65,7 +68,9 @@ RAGGED = Workload("ragged_b128_h128_l1_8192", B=128, s_q=1, H=128, ragged_max=81
 MTP = Workload("mtp_b64_sq2_causal_h128_l8192", B=64, s_q=2, H=128, seqlen=8192, causal=True)
 LONG = Workload("long_b4_h128_l131072_outliers", B=4, s_q=1, H=128, seqlen=131072,
                 outlier_p=0.01, outlier_scale=8.0)
-ALL = (TINY, V3, RAGGED, MTP, LONG)
+# DeepSeek-V3.2-shaped sparse decode (top-k = 2048 of each request's tokens)
+SPARSE = Workload("sparse_b64_h128_l16384_top2048", B=64, s_q=1, H=128, seqlen=16384, topk=2048)
+ALL = (TINY, V3, RAGGED, MTP, LONG, SPARSE)
 BY_NAME = {w.name: w for w in ALL}
 
 
@@ -122,6 +127,16 @@ def make_inputs(w: Workload, seed: int = 0, seqlens: torch.Tensor | None = None,
         std = 1.0 / math.sqrt(512.0)
         out["w_uk"] = (torch.randn((w.H, D_NOPE, D_LATENT), generator=g) * std).to(torch.bfloat16)
         out["w_uv"] = (torch.randn((w.H, D_LATENT, D_V), generator=g) * std).to(torch.bfloat16)
+    if w.topk:   # the selector's output: min(topk, L) distinct positions per request, ascending
+        idx = torch.full((B, w.topk), -1, dtype=torch.int32)
+        kl = torch.zeros(B, dtype=torch.int32)
+        for b in range(B):
+            L = int(sl[b])
+            k = min(w.topk, L)
+            idx[b, :k] = torch.randperm(L, generator=g)[:k].sort().values.to(torch.int32)
+            kl[b] = k
+        out["indices"] = idx
+        out["topk_lens"] = kl
     return out
 
 
