@@ -157,9 +157,17 @@ def oracle_sample_step(inp, kv_np, sel, with_proj):
         flops += acc.bmm_work(len(sel) * s_q, H, True)[0]
     else:
         q = inp["q"][sel].double().numpy()
-    out, _ = oracle.decode_absorbed(q, kv_np, inp["block_table"][sel].numpy(), inp["seqlens"][sel].numpy(),
-                                    inp["softmax_scale"], causal=inp["causal"])
-    flops += acc.decode_work(inp["seqlens"][sel].tolist(), s_q, H, inp["causal"])[0]
+    if "indices" in inp:   # sparse (top-k) decode over each request's list
+        idx = inp["indices"][sel].numpy()
+        kl = inp["topk_lens"][sel].numpy()
+        out, _ = oracle.decode_sparse(q, kv_np, inp["block_table"][sel].numpy(), inp["seqlens"][sel].numpy(), idx,
+                                      kl, inp["softmax_scale"], causal=inp["causal"])
+        flops += acc.sparse_decode_work(inp["seqlens"][sel].tolist(), kl.tolist(), s_q, H, inp["causal"],
+                                        indices=idx.tolist())[0]
+    else:
+        out, _ = oracle.decode_absorbed(q, kv_np, inp["block_table"][sel].numpy(), inp["seqlens"][sel].numpy(),
+                                        inp["softmax_scale"], causal=inp["causal"])
+        flops += acc.decode_work(inp["seqlens"][sel].tolist(), s_q, H, inp["causal"])[0]
     if with_proj:
         oracle.unabsorb_o(out.reshape(-1, H, 512), inp["_w_uv_np"])
         flops += acc.bmm_work(len(sel) * s_q, H, False)[0]
@@ -211,7 +219,9 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "s_q": w.s_q, "H": w.H,
-                   "sample": f"request 0 of {w.B} per step (absorb, decode, un-absorb on the CPU oracle)"},
+                   "sample": f"request 0 of {w.B} per step ("
+                             + ("absorb, decode, un-absorb" if w.with_projections else
+                                "sparse decode" if w.topk else "decode") + " on the CPU oracle)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
                          "sample": f"request 0 of {w.B} per step"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -272,8 +282,12 @@ def run_ours(args, w):
     kv = inp["kv_cache"].to(dev)
     bt = inp["block_table"].to(dev)
     sl = inp["seqlens"].to(dev)
+    sparse = w.topk > 0   # sparse (top-k) decode: each request attends to its listed tokens only
+    idx = inp["indices"].to(dev) if sparse else None
+    kl = inp["topk_lens"].to(dev) if sparse else None
     parts = args.parts or mla.num_sm_parts(s_q, H)
-    step = mla.DecodeStep(B, s_q, H, sl, w.causal, w.softmax_scale, parts=parts, device=dev)
+    # the split schedule walks what the decode walks: the tokens, or the top-k lists
+    step = mla.DecodeStep(B, s_q, H, kl if sparse else sl, w.causal, w.softmax_scale, parts=parts, device=dev)
     q_direct = inp["q"].to(dev)
     stream = torch.cuda.current_stream()
     # Between timed steps L2 is flushed: a 256 MiB write (larger than the 126 MB L2),
@@ -293,8 +307,12 @@ def run_ours(args, w):
     q_dec = step.q if w.with_projections else q_direct
 
     def decode_only():
-        mla.decode(q_dec, kv, bt, sl, w.softmax_scale, w.causal, step.metadata, parts, workspace=step.workspace,
-                   out=step.out, lse=step.lse)
+        if sparse:
+            mla.decode_sparse(q_dec, kv, bt, sl, idx, kl, w.softmax_scale, w.causal, step.metadata, parts,
+                              workspace=step.workspace, out=step.out, lse=step.lse)
+        else:
+            mla.decode(q_dec, kv, bt, sl, w.softmax_scale, w.causal, step.metadata, parts, workspace=step.workspace,
+                       out=step.out, lse=step.lse)
 
     def one_step():
         step.plan()
@@ -372,7 +390,11 @@ def run_ours(args, w):
     t_dec = statistics.mean(dec_ms) / 1e3
     t_step, t_dec = max_over_ranks([t_step, t_dec], dist, dev)
 
-    dflops, dbytes = acc.decode_work(inp["seqlens"].tolist(), s_q, H, w.causal)
+    if sparse:
+        dflops, dbytes = acc.sparse_decode_work(inp["seqlens"].tolist(), inp["topk_lens"].tolist(), s_q, H, w.causal,
+                                                indices=inp["indices"].tolist())
+    else:
+        dflops, dbytes = acc.decode_work(inp["seqlens"].tolist(), s_q, H, w.causal)
     bflops = bbytes = 0
     if w.with_projections:
         for absorb in (True, False):
@@ -397,10 +419,14 @@ def run_ours(args, w):
         host_sl = inp["seqlens"].pin_memory()
         host_bt = inp["block_table"].pin_memory()
         dev_in = [t.to(dev) for t in host_in]
+        # sparse: the lists and their lengths are inputs of the step too (copied into the
+        # tensors the schedule and the decode read)
+        host_sp = [(inp["indices"].pin_memory(), idx), (inp["topk_lens"].pin_memory(), kl)] if sparse else []
         res_dev = step.o if w.with_projections else step.out
         host_out = torch.empty(res_dev.shape, dtype=res_dev.dtype).pin_memory()
         host_lse = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host_in) + host_sl.numel() * 4 + host_bt.numel() * 4
+        h2d = (sum(t.numel() * t.element_size() for t in host_in) + host_sl.numel() * 4 + host_bt.numel() * 4
+               + (inp["indices"].numel() * 4 + inp["topk_lens"].numel() * 4 if sparse else 0))
         d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
 
         def e2e_step():
@@ -408,14 +434,20 @@ def run_ours(args, w):
                 dst.copy_(src, non_blocking=True)
             sl.copy_(host_sl, non_blocking=True)
             bt.copy_(host_bt, non_blocking=True)
+            for src, dst in host_sp:
+                dst.copy_(src, non_blocking=True)
             step.plan()
             if w.with_projections:
                 mla.absorb_q(dev_in[0], w_uk, step.q, q_pe=dev_in[1], positions=dev_in[2])
                 q_in = step.q
             else:
                 q_in = dev_in[0]
-            mla.decode(q_in, kv, bt, sl, w.softmax_scale, w.causal, step.metadata, parts,
-                       workspace=step.workspace, out=step.out, lse=step.lse)
+            if sparse:
+                mla.decode_sparse(q_in, kv, bt, sl, idx, kl, w.softmax_scale, w.causal, step.metadata, parts,
+                                  workspace=step.workspace, out=step.out, lse=step.lse)
+            else:
+                mla.decode(q_in, kv, bt, sl, w.softmax_scale, w.causal, step.metadata, parts,
+                           workspace=step.workspace, out=step.out, lse=step.lse)
             if w.with_projections:
                 mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
             host_out.copy_(res_dev, non_blocking=True)
@@ -451,7 +483,7 @@ def run_ours(args, w):
                 "frac": ach / peaks["bf16_tflops"]}
     roof["peak_source"] = peaks["source"]
     roof["traffic"] = _traffic_per_launch(w.name)
-    roof["kernel"] = "mla_decode (decode kernel + LSE combine)"
+    roof["kernel"] = ("mla_decode_sparse" if sparse else "mla_decode") + " (decode kernel + LSE combine)"
     roof["algorithmic_per_launch"] = {"bytes": dbytes, "flops": dflops}
     roof["ms_per_launch"] = t_dec * 1e3
     roof["frac_of_spec_roofline"] = acc.roofline_time(dflops, dbytes, SPEC_FLOPS, SPEC_BW) / t_dec
@@ -472,6 +504,7 @@ def run_ours(args, w):
                        "seqlens": (w.seqlen or f"ragged 1..{w.ragged_max}" if not w.fixed_seqlens
                                    else list(w.fixed_seqlens)),
                        "page": 64, "parts": parts, "parallelism": f"replicas x{n}",
+                       **({"topk": w.topk, "path": "mla_decode_sparse"} if sparse else {}),
                        "l2": "flushed between timed steps (256 MiB write, then 256 MiB read; outside the step events)",
                        "decode_timing": "K further decode calls inside the timed region, L2 flushed before each",
                        "launch": "eager" if args.eager else "CUDA graph of the step's library calls"},

@@ -83,6 +83,36 @@ def decode_work(seqlens, s_q: int, H: int, causal: bool):
     return flops, kv_bytes + q_bytes + out_bytes + table_bytes
 
 
+def sparse_decode_work(seqlens, topk_lens, s_q: int, H: int, causal: bool, indices=None):
+    """Algorithmic (flops, bytes) of one mla_decode_sparse call: each listed token is
+    gathered once per request (1152 bytes) and takes part in every visible pair.
+    Without causal masking every query position sees the whole list; with it, position
+    i sees the listed positions t <= seqlens[b] - s_q + i (indices needed).  Bytes add
+    q, out, lse, the list entries (4 bytes each), one block-table entry per page the
+    list touches, and the two per-request lengths."""
+    seqlens = [int(x) for x in seqlens]
+    topk_lens = [int(x) for x in topk_lens]
+    B = len(seqlens)
+    pairs = 0
+    pages = 0
+    for b, (L, k) in enumerate(zip(seqlens, topk_lens)):
+        if causal:
+            lst = [int(t) for t in indices[b][:k]]
+            pairs += sum(sum(1 for t in lst if t < L - s_q + i + 1) for i in range(s_q))
+        else:
+            pairs += k * s_q
+        if indices is not None:
+            pages += len({int(t) // PAGE for t in indices[b][:k]})
+        else:
+            pages += min(k, (L + PAGE - 1) // PAGE)
+    flops = pairs * H * 2 * ((D_C + D_R) + D_C)
+    kv_bytes = sum(topk_lens) * (D_C + D_R) * BF16
+    rows = B * s_q * H
+    q_bytes = rows * (D_C + D_R) * BF16
+    out_bytes = rows * D_C * BF16 + rows * 4
+    return flops, kv_bytes + q_bytes + out_bytes + sum(topk_lens) * 4 + pages * 4 + B * 8
+
+
 def bmm_work(n_tokens: int, H: int, absorb: bool):
     """(flops, bytes) of q_nope@W_UK (absorb) or o_lat@W_UV (un-absorb) for n_tokens rows."""
     flops = 2 * n_tokens * H * D_NOPE * D_C

@@ -246,29 +246,60 @@ __device__ __forceinline__ const __nv_bfloat16* sparse_row(const DecodeParams& p
   return p.kv + (static_cast<int64_t>(blk) * kPageTokens + t % kPageTokens) * kDimQK;
 }
 
-// The warp copies 16-byte units [u0, u1) (unit u = dims 8u..8u+7, chunk u / 8) of the
-// page's rows into `stage` (chunk c at c * 8192, row r at r * 128, 128-byte swizzle):
-// one row at a time, the lanes taking consecutive units of it.  rows_lo / rows_hi are
-// this lane's row addresses for rows lane and lane + 32 (nullptr: not gathered).
-__device__ __forceinline__ void gather_units(uint32_t stage, const __nv_bfloat16* rows_lo, const __nv_bfloat16* rows_hi,
-                                             int u0, int u1, int lane) {
-#pragma unroll 1
-  for (int r = 0; r < 64; ++r) {
-    const uint64_t mine = reinterpret_cast<uint64_t>(r < 32 ? rows_lo : rows_hi);
-    const __nv_bfloat16* row = reinterpret_cast<const __nv_bfloat16*>(__shfl_sync(0xffffffffu, mine, r & 31));
-    if (row == nullptr) continue;
-    for (int u = u0 + lane; u < u1; u += 32) {
-      const int c = u >> 3, v = u & 7;
-      cp_async16(stage + c * 8192 + r * 128 + ((v ^ (r & 7)) << 4), row + u * 8);
+// Gathering warps: the S-CTA gathers with warps 0, 2 and 3, the O-CTA with warps 0 and
+// 3 (one warp alone cannot keep a page's 4608 copies in flight).  Gathering warp slot ws
+// owns rows [gather_r0(ws), gather_r0(ws + 1)) of each page; lane l looks up row
+// gather_r0(ws) + l.
+constexpr int kSGatherWarps = 3, kOGatherWarps = 2;
+__device__ __forceinline__ int gather_r0(int ws, int nwarps) { return ws * 64 / nwarps; }
+
+// Row address of entry k * 64 + r of request b's list, or nullptr (past the list, or a
+// bad entry: recorded as a bounds error, the row is not gathered).
+__device__ __forceinline__ const __nv_bfloat16* sparse_page_row(const DecodeParams& p, int b, int k, int r) {
+  const int e = k * 64 + r;
+  return (r < 64 && e < __ldg(p.lens + b)) ? sparse_row(p, b, e) : nullptr;
+}
+
+// The warp copies units [u0, u0 + kPerRow) (unit u = dims 8u..8u+7, chunk u / 8) of rows
+// [r0, r0 + nrows) of the page into `stage` (chunk c at c * 8192, row r at r * 128,
+// 128-byte swizzle), the (row, unit) pairs spread evenly over the lanes; `mine` is the
+// address of row r0 + lane (nullptr: not gathered).
+template <int kPerRow>
+__device__ __forceinline__ void gather_rows(uint32_t stage, const __nv_bfloat16* mine, int r0, int nrows, int u0,
+                                            int lane) {
+  const int total = nrows * kPerRow;
+  for (int j0 = 0; j0 < total; j0 += 32) {
+    const int j = j0 + lane;
+    const int rr = j < total ? j / kPerRow : 0;
+    const uint64_t src = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(mine), rr);
+    if (j < total && src != 0) {
+      const int u = u0 + j % kPerRow, r = r0 + rr, c = u >> 3, v = u & 7;
+      cp_async16(stage + c * 8192 + r * 128 + ((v ^ (r & 7)) << 4), reinterpret_cast<const __nv_bfloat16*>(src) + u * 8);
     }
   }
 }
 
-// Warp 0 of the S-CTA, sparse decode: the q blocks by TMA (lane 0) and the pages by
-// warp-wide gathers, both through the same two stages as the dense producer.
+// The page after page k of segment s in this part's walk: (b, k) or b = -1 at the end.
+__device__ __forceinline__ void next_page(const SegmentWalker& w, const Segment& s, int k, int& nb, int& nk) {
+  if (k + 1 < s.ke) {
+    nb = s.b, nk = k + 1;
+    return;
+  }
+  SegmentWalker nx = w;
+  Segment ns;
+  if (nx.next(ns)) nb = ns.b, nk = ns.kb;
+  else nb = -1, nk = 0;
+}
+
+// Gathering warp ws of the S-CTA, sparse decode: the q blocks by TMA (lane 0 of warp
+// 0) and its rows of every page by cp.async, through the same stages as the dense
+// producer; a stage's barriers expect one arrival per gathering lane.  The row
+// addresses of the next page are looked up while the current page's copies fly.
 __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
-                                  uint32_t cl, int rb, bool withhold) {
+                                  uint32_t cl, int rb, bool withhold, int ws) {
   const int lane = threadIdx.x & 31;
+  const bool issuer = (ws == 0 && lane == 0);
+  const int r0 = gather_r0(ws, kSGatherWarps), nrows = gather_r0(ws + 1, kSGatherWarps) - r0;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
@@ -276,7 +307,8 @@ __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Sha
   int issued[kKStages];
   uint32_t issued_phase[kKStages];
   for (int j = 0; j < kKStages; ++j) issued[j] = 0, issued_phase[j] = 0;
-  bool ok = true;
+  bool ok = true, have_next = false;
+  const __nv_bfloat16* next_row = nullptr;
   while (ok && w.next(s)) {
     const int qrow0 = s.b * p.rows + rb * 128;
     for (int j = 0; j < 2 && ok; ++j, ++i) {
@@ -288,7 +320,7 @@ __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Sha
       }
       mbar_arrive(smem_u32(&sh.bar.full_b[st]));   // a q block lands whole; its second half needs no bytes
       const uint32_t full = smem_u32(&sh.bar.full[st]);
-      if (lane != 0) {
+      if (!issuer) {
         mbar_arrive(full);
       } else if (!(withhold && i == 0)) {   // test hook: this block never arrives
         mbar_arrive_expect_tx(full, kKStageBytes);
@@ -296,49 +328,56 @@ __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Sha
         issued[st] = 1, issued_phase[st] = ph;
       }
     }
-    const int n = __ldg(p.lens + s.b);
     for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
       const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
       const uint32_t stage = smem + kOffStage + st * kKStageBytes;
+      const __nv_bfloat16* mine = have_next ? next_row : sparse_page_row(p, s.b, k, r0 + lane);
+      if (lane >= nrows) mine = nullptr;
+      int nb, nk;
+      next_page(w, s, k, nb, nk);
+      have_next = nb >= 0;
+      next_row = (have_next && lane < nrows) ? sparse_page_row(p, nb, nk, r0 + lane) : nullptr;
       if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      const int e0 = k * 64 + lane;
-      const __nv_bfloat16* lo = e0 < n ? sparse_row(p, s.b, e0) : nullptr;
-      const __nv_bfloat16* hi = e0 + 32 < n ? sparse_row(p, s.b, e0 + 32) : nullptr;
-      gather_units(stage, lo, hi, 0, kKPartA * 8, lane);
+      gather_rows<kKPartA * 8>(stage, mine, r0, nrows, 0, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full[st]));
       if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      gather_units(stage, lo, hi, kKPartA * 8, 72, lane);
+      gather_rows<72 - kKPartA * 8>(stage, mine, r0, nrows, kKPartA * 8, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full_b[st]));
     }
+    // the next segment's first page was looked up with this segment's walker state
   }
   cp_async_wait_all();   // this lane's copies land before the CTA may exit
-  if (lane == 0)
+  if (issuer)
     for (int st = 0; st < kKStages; ++st)
       if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
   __syncwarp();
 }
 
-// Warp 0 of the O-CTA, sparse decode: the 512 value dims of every gathered page.
-__device__ void o_producer_sparse(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl) {
+// Gathering warp ws of the O-CTA, sparse decode: its rows' 512 value dims of every page.
+__device__ void o_producer_sparse(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int ws) {
   const int lane = threadIdx.x & 31;
+  const int r0 = gather_r0(ws, kOGatherWarps), nrows = gather_r0(ws + 1, kOGatherWarps) - r0;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
   uint32_t T = 0;
-  bool ok = true;
+  bool ok = true, have_next = false;
+  const __nv_bfloat16* next_row = nullptr;
   while (ok && w.next(s)) {
-    const int n = __ldg(p.lens + s.b);
     for (int k = s.kb; k < s.ke && ok; ++k, ++T) {
       const uint32_t st = T % kVStages, ph = (T / kVStages) & 1;
       const uint32_t stage = smem + kOffStage + st * kVStageBytes;
+      const __nv_bfloat16* mine = have_next ? next_row : sparse_page_row(p, s.b, k, r0 + lane);
+      if (lane >= nrows) mine = nullptr;
+      int nb, nk;
+      next_page(w, s, k, nb, nk);
+      have_next = nb >= 0;
+      next_row = (have_next && lane < nrows) ? sparse_page_row(p, nb, nk, r0 + lane) : nullptr;
       if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      const int e0 = k * 64 + lane;
-      const __nv_bfloat16* lo = e0 < n ? sparse_row(p, s.b, e0) : nullptr;
-      const __nv_bfloat16* hi = e0 + 32 < n ? sparse_row(p, s.b, e0 + 32) : nullptr;
-      gather_units(stage, lo, hi, 0, 32, lane);
+      gather_rows<32>(stage, mine, r0, nrows, 0, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full[st]));
       if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      gather_units(stage, lo, hi, 32, 64, lane);
+      gather_rows<32>(stage, mine, r0, nrows, 32, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full_b[st]));
     }
   }
@@ -909,7 +948,8 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     prefetch_tensormap(&maps.c4);
     sh.abort = 0;
     sh.cmd = 0;
-    constexpr uint32_t fills = kSparse ? 32u : 1u;   // sparse: one arrival per gathering lane
+    // sparse: one arrival per gathering lane
+    const uint32_t fills = kSparse ? 32u * static_cast<uint32_t>(is_s ? kSGatherWarps : kOGatherWarps) : 1u;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&sh.bar.full[i]), fills);
       mbar_init(smem_u32(&sh.bar.empty[i]), 1);
@@ -947,22 +987,20 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
   }
 
   if (is_s) {
-    if (warp == 0) {
-      if constexpr (kSparse)
-        s_producer_sparse(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
-      else if ((threadIdx.x & 31) == 0)
-        s_producer(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
+    if (kSparse && (warp == 0 || warp == 2 || warp == 3)) {   // the gathering warps
+      s_producer_sparse(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0, warp == 0 ? 0 : warp - 1);
+    } else if (warp == 0) {
+      if ((threadIdx.x & 31) == 0) s_producer(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
     } else if (warp == 1) {
       s_cta_mma<kSparse>(p, sh, smem, part, cl);
     } else if (warp >= 4) {
       s_cta_softmax<kSparse>(p, sh, smem, part, cl, rb, peer);
     }
   } else {
-    if (warp == 0) {
-      if constexpr (kSparse)
-        o_producer_sparse(p, sh, smem, part, cl);
-      else if ((threadIdx.x & 31) == 0)
-        o_producer(p, &maps, sh, smem, part, cl);
+    if (kSparse && (warp == 0 || warp == 3)) {   // the gathering warps
+      o_producer_sparse(p, sh, smem, part, cl, warp == 0 ? 0 : 1);
+    } else if (warp == 0) {
+      if ((threadIdx.x & 31) == 0) o_producer(p, &maps, sh, smem, part, cl);
     } else if (warp == 1) {
       o_cta_mma<kSparse>(p, sh, smem, part, cl);
     } else if (warp == 2) {

@@ -85,3 +85,21 @@ def test_bmm_work(absorb):
     f, b = acc.bmm_work(64, 128, absorb)
     assert f == 2 * 64 * 128 * 128 * 512
     assert b > 128 * 128 * 512 * 2
+
+
+def test_sparse_decode_work_counts():
+    # every token of a request listed once: the same pairs and cache bytes as the dense
+    # decode; on top, 4 bytes per list entry and the list length
+    L = 4096
+    full = list(range(L))
+    f, b = acc.sparse_decode_work([L], [L], 1, 128, False, indices=[full])
+    fd, bd = acc.decode_work([L], 1, 128, False)
+    assert f == fd
+    assert b == bd + L * 4 + 4
+    # 2048 of 16384 tokens: pairs = k per query, bytes = k cached rows + q/out/lse + lists
+    f, b = acc.sparse_decode_work([16384], [2048], 1, 128, False)
+    assert f == 2048 * 278528
+    assert b == 2048 * 1152 + 128 * (1152 + 1024 + 4) + 2048 * 4 + min(2048, 256) * 4 + 8
+    # causal, s_q = 2, seqlen 10: listed positions 3, 8, 9; query 0 sees t <= 8, query 1 t <= 9
+    f, _ = acc.sparse_decode_work([10], [3], 2, 16, True, indices=[[3, 8, 9]])
+    assert f == (2 + 3) * 16 * 2176
