@@ -80,7 +80,8 @@ constexpr uint32_t kOffLpart = kOffPm + 1024;                     // S-CTA: part
 constexpr uint32_t kOffInvL = kOffRecv + kSlots * kPktStride;     // O-CTA: 1/l of the segment [128]
 constexpr uint32_t kOffSharedO = kOffInvL + 512;
 constexpr uint32_t kOffShared = kOffSharedO > kOffLpart + 512 ? kOffSharedO : kOffLpart + 512;  // both roles
-constexpr uint32_t kSmemBytes = kOffShared + 640;
+constexpr uint32_t kOffEpi = kOffShared + 640;                    // O-CTA: 2 KiB transpose buffer per epilogue warp
+constexpr uint32_t kSmemBytes = kOffEpi + 8 * 2048;
 static_assert(kOffLpart + 512 <= kOffShared, "S-CTA layout");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kQCol = 0, kSCol0 = 320;           // S-CTA TMEM columns: Q [0,288), S buffers 320, 384
@@ -840,8 +841,6 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
   const int wg = t >> 7;
   const int r = t & 127;
   const int wq = r >> 5, lane = r & 31;
-  const int g = rb * 128 + r;
-  const bool row_valid = g < p.rows;
   const uint32_t tmem_lane = sh.tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + wg * 256;
   SegmentWalker w;
   w.init(p, part);
@@ -881,8 +880,20 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
     const int ns0 = __ldg(p.num_splits + s.b);
     const int nsplit = __ldg(p.num_splits + s.b + 1) - ns0;
     const bool final_out = (nsplit == 1);
-    __nv_bfloat16* orow = p.out + (static_cast<int64_t>(s.b) * p.rows + g) * 512 + wg * 256;
-    float* prow = p.o_part + (static_cast<int64_t>(ns0 + s.split) * p.rows + g) * 512 + wg * 256;
+    // Stores go through the warp's transpose buffer: a thread holds one row's columns, so
+    // direct stores would touch 32 rows per instruction; transposed, each store
+    // instruction writes 64 contiguous bytes of 8 rows.  Buffer row x (64 B) holds
+    // 16-byte unit u at ((u ^ (x & 3)) * 16).
+    const int g0 = rb * 128 + wq * 32;    // the warp's first row within the request
+    __nv_bfloat16* obase = p.out + (static_cast<int64_t>(s.b) * p.rows + g0) * 512 + wg * 256;
+    float* pbase = p.o_part + (static_cast<int64_t>(ns0 + s.split) * p.rows + g0) * 512 + wg * 256;
+    const uint32_t stg = smem + kOffEpi + ((wg << 2) | wq) * 2048;
+    const int tq = lane & 3;                // transposed: 16-byte quad tq of rows 8j + (lane >> 2)
+    auto put = [&](int j, uint4 u) { st_shared_v4(stg + lane * 64 + ((j ^ (lane & 3)) << 4), u); };
+    auto get = [&](int j) {
+      const int x = 8 * j + (lane >> 2);
+      return ld_shared_v4(stg + x * 64 + ((tq ^ (x & 3)) << 4));
+    };
 #pragma unroll 1
     for (int c = 0; c < 256; c += 32) {
       uint32_t v[32];
@@ -893,9 +904,7 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.bar.o_free));
       }
-      if (!row_valid) continue;
-      if (final_out) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+      if (final_out) {   // 32 bf16 columns: 64 B per row
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint4 u;
@@ -903,14 +912,35 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
           u.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv_l, __uint_as_float(v[8 * j + 3]) * inv_l);
           u.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv_l, __uint_as_float(v[8 * j + 5]) * inv_l);
           u.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv_l, __uint_as_float(v[8 * j + 7]) * inv_l);
-          dst[j] = u;
+          put(j, u);
         }
-      } else {
-        float4* dst = reinterpret_cast<float4*>(prow + c);
+        __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          dst[j] = make_float4(__uint_as_float(v[4 * j]) * inv_l, __uint_as_float(v[4 * j + 1]) * inv_l,
-                               __uint_as_float(v[4 * j + 2]) * inv_l, __uint_as_float(v[4 * j + 3]) * inv_l);
+        for (int j = 0; j < 4; ++j) {
+          const int x = 8 * j + (lane >> 2);
+          const uint4 u = get(j);
+          if (g0 + x < p.rows) *reinterpret_cast<uint4*>(obase + static_cast<int64_t>(x) * 512 + c + 8 * tq) = u;
+        }
+        __syncwarp();
+      } else {           // fp32 partials: two passes of 16 columns (64 B per row)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int e = 16 * h + 4 * j;
+            put(j, make_uint4(__float_as_uint(__uint_as_float(v[e]) * inv_l), __float_as_uint(__uint_as_float(v[e + 1]) * inv_l),
+                              __float_as_uint(__uint_as_float(v[e + 2]) * inv_l), __float_as_uint(__uint_as_float(v[e + 3]) * inv_l)));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int x = 8 * j + (lane >> 2);
+            const uint4 u = get(j);
+            if (g0 + x < p.rows)
+              *reinterpret_cast<uint4*>(pbase + static_cast<int64_t>(x) * 512 + c + 16 * h + 4 * tq) = u;
+          }
+          __syncwarp();
+        }
       }
     }
     ++seg;
