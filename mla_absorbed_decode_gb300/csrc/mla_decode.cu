@@ -88,7 +88,6 @@ constexpr uint32_t kQCol = 0, kSCol0 = 320;           // S-CTA TMEM columns: Q [
 constexpr float kRescaleLog2 = 8.0f;                  // rebase the row max when it grows by more than 2^8
 constexpr uint64_t kTimeoutNs = 500ull * 1000 * 1000;
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr uint32_t kSoftThreads = 256;                // two warpgroups
 
 struct Bars {
   uint64_t full[kStages];   // O: chunks 0..3 of V landed; S: chunks 0..4 of K, or a whole q block
@@ -247,11 +246,18 @@ __device__ __forceinline__ const __nv_bfloat16* sparse_row(const DecodeParams& p
   return p.kv + (static_cast<int64_t>(blk) * kPageTokens + t % kPageTokens) * kDimQK;
 }
 
-// Gathering warps: the S-CTA gathers with warps 0, 2 and 3, the O-CTA with warps 0 and
-// 3 (one warp alone cannot keep a page's 4608 copies in flight).  Gathering warp slot ws
-// owns rows [gather_r0(ws), gather_r0(ws + 1)) of each page; lane l looks up row
-// gather_r0(ws) + l.
-constexpr int kSGatherWarps = 3, kOGatherWarps = 2;
+// Gathering warps: the S-CTA gathers with warps 0, 2, 3 and 8..11, the O-CTA with warps
+// 0, 3 and 8..11 (one warp sustains only ~5 GB/s of 16-byte copies; in sparse mode the
+// softmax and the epilogue run on warps 4..7 alone).  Gathering warp slot ws owns rows
+// [gather_r0(ws), gather_r0(ws + 1)) of each page; lane l looks up row gather_r0(ws) + l.
+constexpr int kSGatherWarps = 7, kOGatherWarps = 6;
+// Gathering warp slot of warp `warp`, or -1: S-CTA 0, 2, 3, 8..11 -> 0..6; O-CTA 0, 3, 8..11 -> 0..5.
+__device__ __forceinline__ int gather_slot(bool is_s, int warp) {
+  if (warp == 0) return 0;
+  if (warp >= 8) return warp - (is_s ? 5 : 6);
+  if (is_s) return (warp == 2 || warp == 3) ? warp - 1 : -1;
+  return warp == 3 ? 1 : -1;
+}
 __device__ __forceinline__ int gather_r0(int ws, int nwarps) { return ws * 64 / nwarps; }
 
 // Row address of entry k * 64 + r of request b's list, or nullptr (past the list, or a
@@ -563,6 +569,11 @@ __device__ __forceinline__ void copy_q_to_tmem(uint32_t smem, uint32_t tmem_lane
 template <bool sparse>
 __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb,
                               uint32_t peer) {
+  // Dense: two warpgroups, each covering 32 of a page's 64 columns.  Sparse: one
+  // warpgroup covering all 64 in two passes (the other four warps gather).
+  constexpr int kWG = sparse ? 1 : 2;
+  constexpr uint32_t kST = kWG * 128;      // softmax threads
+  constexpr int kPieces = 2 / kWG;         // 32-column pieces per thread and page
   const int t = threadIdx.x - 128;
   const int wg = t >> 7;
   const int r = t & 127;                    // row within the block == TMEM lane
@@ -594,11 +605,12 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       const uint32_t mine = (r < 64) ? q0 : q1;
       const uint32_t mph = ((i + ((r < 64) ? 0u : 1u)) / kKStages) & 1;
       const bool got = wait_bar(sh, smem_u32(&sh.bar.full[mine]), mph, p.status, cl);
-      if (named_bar_or(1, kSoftThreads, !got)) break;
-      copy_q_to_tmem(smem, tmem_lane, q0, q1, wg, r);
+      if (named_bar_or(1, kST, !got)) break;
+#pragma unroll
+      for (int h = 0; h < kPieces; ++h) copy_q_to_tmem(smem, tmem_lane, q0, q1, wg + h, r);
       tmem_wait_st();
       tc_fence_before();
-      named_bar_sync(1, kSoftThreads);
+      named_bar_sync(1, kST);
       if (t == 0) {
         mbar_arrive(smem_u32(&sh.bar.q_full));
         mbar_arrive(smem_u32(&sh.bar.empty[q0]));
@@ -612,6 +624,7 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       i += 2 + static_cast<uint32_t>(s.ke - s.kb);   // ring items of this segment
     }
     float m_ref = -INFINITY, l = 0.f;   // reference maximum (log2 units) and running sum of the rows
+    float l_hi = 0.f;                   // one warpgroup: the running sum of columns 32..63
     for (int k = s.kb; k < s.ke; ++k, ++T) {
       const uint32_t sb = T & 1, ph = (T >> 1) & 1;
       const uint32_t rs = T % kSlots, rph = (T / kSlots) & 1;
@@ -625,30 +638,43 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       }
       tc_fence_after();
       float sv[32];
-      tmem_ld32(tmem_lane + kSCol0 + sb * 64 + c0, *reinterpret_cast<uint32_t(*)[32]>(sv));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.bar.s_empty[sb]));
-
-      // raw scores; slots at or past `vis` are masked to -inf (only on the last pages)
-      const int nvalid = vis - (k * 64 + c0);   // columns c < nvalid are visible
-      if (nvalid < 32) {
+      // raw scores of 32 columns from column cb on; slots at or past `vis` are masked to
+      // -inf (only on the last pages)
+      auto load_scores = [&](int cb) {
+        tmem_ld32(tmem_lane + kSCol0 + sb * 64 + cb, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tmem_wait_ld();
+        const int nvalid = vis - (k * 64 + cb);   // columns c < nvalid are visible
+        if (nvalid < 32) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) sv[c] = (c < nvalid) ? sv[c] : -INFINITY;
-      }
-      if (sparse && p.causal) {   // token positions of this thread's 32 columns (sparse only)
-        const int32_t* ix = p.indices + static_cast<int64_t>(s.b) * p.idx_stride + k * 64 + c0;
+          for (int c = 0; c < 32; ++c) sv[c] = (c < nvalid) ? sv[c] : -INFINITY;
+        }
+        if (sparse && p.causal) {   // token positions of these 32 columns (sparse only)
+          const int32_t* ix = p.indices + static_cast<int64_t>(s.b) * p.idx_stride + k * 64 + cb;
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (c < nvalid && __ldg(ix + c) >= vis_pos) sv[c] = -INFINITY;
+          for (int c = 0; c < 32; ++c)
+            if (c < nvalid && __ldg(ix + c) >= vis_pos) sv[c] = -INFINITY;
+        }
+      };
+      auto release_s = [&]() {   // every column of S has been read
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.bar.s_empty[sb]));
+      };
+      load_scores(c0);
+      float my_max = max32(sv);
+      if constexpr (kWG == 1) {
+        load_scores(32);
+        my_max = fmaxf(my_max, max32(sv));
       }
-      const float my_max = max32(sv);
-      asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine), "f"(my_max) : "memory");
+      if constexpr (kWG == 2) {
+        release_s();
+        asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine), "f"(my_max) : "memory");
+      }
       // one barrier both exchanges the row maxima and makes the abort decision uniform
-      if (named_bar_or(1, kSoftThreads, !ok_t)) { ok = false; break; }
+      if (named_bar_or(1, kST, !ok_t)) { ok = false; break; }
       // softmax_scale > 0, so the scaled maximum is the scaled raw maximum
-      const float m_new = fmaxf(m_ref, fmaxf(my_max, ld_shared_f32(pm_other)) * p.scale_log2);
+      const float row_max = (kWG == 2) ? fmaxf(my_max, ld_shared_f32(pm_other)) : my_max;
+      const float m_new = fmaxf(m_ref, row_max * p.scale_log2);
       float alpha = 1.f;
       const bool rebase = m_new > m_ref + kRescaleLog2;
       if (rebase) {
@@ -656,28 +682,43 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
         m_ref = m_new;
       }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      uint32_t pk[16];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {   // l sums the fp32 probabilities; P goes to the MMA in bf16
-        const float e0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, neg_m));
-        const float e1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, neg_m));
-        pk[c] = pack_bf16x2(e0, e1);
-        ps[c & 3] += e0 + e1;
-      }
-      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      const bool last = (k == s.ke - 1);
-      if (last) {   // the row sum over both warpgroups is needed for 1/l
-        if (wg == 1) asm volatile("st.shared.f32 [%0], %1;" :: "r"(lpart), "f"(l) : "memory");
-        named_bar_sync(1, kSoftThreads);
-        if (wg == 0) l += ld_shared_f32(lpart);
-      }
       const uint32_t slot = smem + kOffSend + sb * kPktStride;
       const uint32_t row = slot + r * 128;
+      float lsum[kPieces];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int cc = wg * 4 + j;              // 16-byte chunk: tokens 8cc .. 8cc+7
-        st_shared_v4(row + ((cc ^ (r & 7)) << 4), make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
+      for (int h = 0; h < kPieces; ++h) {
+        const int cb = c0 + 32 * h;
+        if constexpr (kWG == 1) load_scores(cb);   // the second pass reads the scores again
+        uint32_t pk[16];
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {   // l sums the fp32 probabilities; P goes to the MMA in bf16
+          const float e0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, neg_m));
+          const float e1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, neg_m));
+          pk[c] = pack_bf16x2(e0, e1);
+          ps[c & 3] += e0 + e1;
+        }
+        lsum[h] = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int cc = cb / 8 + j;              // 16-byte chunk: tokens 8cc .. 8cc+7
+          st_shared_v4(row + ((cc ^ (r & 7)) << 4), make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
+        }
+      }
+      if constexpr (kWG == 1) release_s();
+      // one running sum per 32-column piece, added at the segment's end: the same
+      // arithmetic as two warpgroups with one piece each
+      l = l * alpha + lsum[0];
+      if constexpr (kPieces == 2) l_hi = l_hi * alpha + lsum[1];
+      const bool last = (k == s.ke - 1);
+      if (last) {   // the row sum over both halves is needed for 1/l
+        if constexpr (kWG == 2) {
+          if (wg == 1) asm volatile("st.shared.f32 [%0], %1;" :: "r"(lpart), "f"(l) : "memory");
+          named_bar_sync(1, kST);
+          if (wg == 0) l += ld_shared_f32(lpart);
+        } else {
+          l += l_hi;
+        }
       }
       if (wg == 0) {
         asm volatile("st.shared.f32 [%0], %1;" :: "r"(slot + kPktAlpha + r * 4), "f"(alpha) : "memory");
@@ -686,7 +727,7 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
                        : "memory");
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, kSoftThreads);
+      named_bar_sync(1, kST);
       if (t == 0) {
         bulk_copy_to_cluster(peer_recv + rs * kPktStride, slot, kPktStride, peer_pfull0 + rs * 8);
         bulk_commit_group();
@@ -836,12 +877,16 @@ __device__ void o_cta_forwarder(const DecodeParams& p, Shared& sh, int part, uin
 
 // Warps 4..11 of the O-CTA: rescale O rows, or normalise and store a finished
 // segment.  Warpgroup wg owns O columns [256 wg, 256 wg + 256).
+// Dense: two warpgroups, one per 256-column half of O; sparse: warps 4..7 alone cover both
+// halves (warps 8..11 gather).
+template <bool sparse>
 __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb) {
+  constexpr int kHalves = sparse ? 2 : 1;   // 256-column halves of O per thread
   const int t = threadIdx.x - 128;
   const int wg = t >> 7;
   const int r = t & 127;
   const int wq = r >> 5, lane = r & 31;
-  const uint32_t tmem_lane = sh.tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + wg * 256;
+  const uint32_t tmem_row = sh.tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
   SegmentWalker w;
   w.init(p, part);
   Segment s;
@@ -857,13 +902,14 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
       tc_fence_after();
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
+        for (int c = 0; c < 256 * kHalves; c += 32) {
+          const uint32_t col = tmem_row + wg * 256 + c;
           uint32_t v[32];
-          tmem_ld32(tmem_lane + c, v);
+          tmem_ld32(col, v);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-          tmem_st32(tmem_lane + c, v);
+          tmem_st32(col, v);
         }
         tmem_wait_st();
       }
@@ -885,8 +931,8 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
     // instruction writes 64 contiguous bytes of 8 rows.  Buffer row x (64 B) holds
     // 16-byte unit u at ((u ^ (x & 3)) * 16).
     const int g0 = rb * 128 + wq * 32;    // the warp's first row within the request
-    __nv_bfloat16* obase = p.out + (static_cast<int64_t>(s.b) * p.rows + g0) * 512 + wg * 256;
-    float* pbase = p.o_part + (static_cast<int64_t>(ns0 + s.split) * p.rows + g0) * 512 + wg * 256;
+    __nv_bfloat16* const obase0 = p.out + (static_cast<int64_t>(s.b) * p.rows + g0) * 512;
+    float* const pbase0 = p.o_part + (static_cast<int64_t>(ns0 + s.split) * p.rows + g0) * 512;
     const uint32_t stg = smem + kOffEpi + ((wg << 2) | wq) * 2048;
     const int tq = lane & 3;                // transposed: 16-byte quad tq of rows 8j + (lane >> 2)
     auto put = [&](int j, uint4 u) { st_shared_v4(stg + lane * 64 + ((j ^ (lane & 3)) << 4), u); };
@@ -895,11 +941,14 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
       return ld_shared_v4(stg + x * 64 + ((tq ^ (x & 3)) << 4));
     };
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
+    for (int hc = 0; hc < 256 * kHalves; hc += 32) {
+      const int half = wg + hc / 256, c = hc % 256;   // column c of O's half `half`
+      __nv_bfloat16* const obase = obase0 + half * 256;
+      float* const pbase = pbase0 + half * 256;
       uint32_t v[32];
-      tmem_ld32(tmem_lane + c, v);
+      tmem_ld32(tmem_row + half * 256 + c, v);
       tmem_wait_ld();
-      if (c == 224) {   // everything read: O may be overwritten by the next segment
+      if (hc == 256 * kHalves - 32) {   // everything read: O may be overwritten by the next segment
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.bar.o_free));
@@ -988,7 +1037,7 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.bar.s_full[i]), 1);
-      mbar_init(smem_u32(&sh.bar.s_empty[i]), 8);
+      mbar_init(smem_u32(&sh.bar.s_empty[i]), kSparse ? 4 : 8);   // one arrival per softmax warp
     }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(smem_u32(&sh.bar.credit[i]), 1);
@@ -997,10 +1046,10 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     }
     mbar_init(smem_u32(&sh.bar.q_full), 1);
     mbar_init(smem_u32(&sh.bar.o_full), 1);
-    mbar_init(smem_u32(&sh.bar.o_free), 8);
+    mbar_init(smem_u32(&sh.bar.o_free), kSparse ? 4 : 8);          // one arrival per epilogue warp
     mbar_init(smem_u32(&sh.bar.o_sync), 1);
     mbar_init(smem_u32(&sh.bar.corr_go), 1);
-    mbar_init(smem_u32(&sh.bar.corr_done), 8);
+    mbar_init(smem_u32(&sh.bar.corr_done), kSparse ? 4 : 8);
     mbar_init(smem_u32(&sh.bar.drain), 1);
     fence_mbar_init();
   }
@@ -1017,8 +1066,8 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
   }
 
   if (is_s) {
-    if (kSparse && (warp == 0 || warp == 2 || warp == 3)) {   // the gathering warps
-      s_producer_sparse(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0, warp == 0 ? 0 : warp - 1);
+    if (kSparse && gather_slot(true, warp) >= 0) {   // the gathering warps
+      s_producer_sparse(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0, gather_slot(true, warp));
     } else if (warp == 0) {
       if ((threadIdx.x & 31) == 0) s_producer(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
     } else if (warp == 1) {
@@ -1027,8 +1076,8 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
       s_cta_softmax<kSparse>(p, sh, smem, part, cl, rb, peer);
     }
   } else {
-    if (kSparse && (warp == 0 || warp == 3)) {   // the gathering warps
-      o_producer_sparse(p, sh, smem, part, cl, warp == 0 ? 0 : 1);
+    if (kSparse && gather_slot(false, warp) >= 0) {   // the gathering warps
+      o_producer_sparse(p, sh, smem, part, cl, gather_slot(false, warp));
     } else if (warp == 0) {
       if ((threadIdx.x & 31) == 0) o_producer(p, &maps, sh, smem, part, cl);
     } else if (warp == 1) {
@@ -1036,7 +1085,7 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     } else if (warp == 2) {
       if ((threadIdx.x & 31) == 0) o_cta_forwarder(p, sh, part, cl, peer);
     } else if (warp >= 4) {
-      o_cta_epilogue(p, sh, smem, part, cl, rb);
+      o_cta_epilogue<kSparse>(p, sh, smem, part, cl, rb);
     }
   }
 
