@@ -345,6 +345,9 @@ __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Sha
       have_next = nb >= 0;
       next_row = (have_next && lane < nrows) ? sparse_page_row(p, nb, nk, r0 + lane) : nullptr;
       if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      // the stage's latest use is now a gathered page (waited for by cp.async.wait_all): the
+      // drain below must not wait for an older phase of its barrier, whose parity can alias
+      issued[st] = 0;
       gather_rows<kKPartA * 8>(stage, mine, r0, nrows, 0, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full[st]));
       if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
@@ -354,7 +357,7 @@ __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Sha
     // the next segment's first page was looked up with this segment's walker state
   }
   cp_async_wait_all();   // this lane's copies land before the CTA may exit
-  if (issuer)
+  if (issuer)   // a q block whose stage saw no later page may still be in flight (after an abort)
     for (int st = 0; st < kKStages; ++st)
       if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
   __syncwarp();

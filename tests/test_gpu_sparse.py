@@ -105,3 +105,27 @@ def test_sparse_v32_shaped_sampled():
                                             inp["block_table"][sel].numpy(), inp["seqlens"][sel].numpy(),
                                             idx[sel].numpy(), kl[sel].numpy(), inp["softmax_scale"])
     compare(out[sel], lse[sel], sub_out, sub_lse, what="sparse V3.2 shape")
+
+
+def test_sparse_calls_return_promptly():
+    """Every call finishes in far less than the kernel's 500 ms bounded-wait limit, for
+    batch sizes that give the parts segments of both parities of page counts (a drain
+    that waited for an aliased, older phase of a stage barrier once stalled 0.5-1 s at
+    exit, with the result still correct)."""
+    import mla_absorbed_decode_gb300 as mla
+    L, k = 4096, 640   # ten gathered pages per request
+    for B in (6, 7, 9, 12):
+        inp = _case(B, 1, 128, [L] * B, seed=B)
+        idx, kl = _lists([L] * B, [k] * B, seed=B)
+        q, kv, bt, sl = (inp[x].cuda() for x in ("q", "kv_cache", "block_table", "seqlens"))
+        idx, kl = idx.cuda(), kl.cuda()
+        P = mla.num_sm_parts(1, 128)
+        meta = mla.decode_metadata(kl, 1, 128, False, P)
+        for _ in range(2):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            mla.decode_sparse(q, kv, bt, sl, idx, kl, inp["softmax_scale"], False, meta, P)
+            e1.record()
+            torch.cuda.synchronize()
+            assert mla.get_device_status() == 0
+            assert e0.elapsed_time(e1) < 200.0, f"B={B}: {e0.elapsed_time(e1):.1f} ms"
