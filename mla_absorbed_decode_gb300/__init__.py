@@ -217,10 +217,22 @@ class DecodeStep:
         self.workspace = torch.empty(decode_workspace_size(B, s_q, H, self.parts), dtype=torch.uint8, device=dev)
         self.seqlens = seqlens
         self.metadata = decode_metadata(seqlens, s_q, H, causal, self.parts)
+        self._plan_stream = torch.cuda.Stream(device=dev)
 
     def plan(self, stream=None):
         """Recompute the split schedule (after seqlens changed)."""
         decode_metadata(self.seqlens, self.s_q, self.H, self.causal, self.parts, out=self.metadata, stream=stream)
+
+    def plan_beside(self, work):
+        """plan() on a side stream while `work()` (stream work that does not read the
+        metadata, such as the W_UK absorption) runs on the current stream; the current
+        stream then waits for both.  The schedule sees everything issued before the call."""
+        cur = torch.cuda.current_stream(self.q.device)
+        self._plan_stream.wait_stream(cur)
+        with torch.cuda.stream(self._plan_stream):
+            self.plan()
+        work()
+        cur.wait_stream(self._plan_stream)
 
     def run(self, q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, stream=None, positions=None,
             rope_theta: float = 10000.0):
@@ -239,12 +251,19 @@ class DecodeStep:
         copies of the step's inputs from pinned host buffers, or of its result back) is recorded in
         the same graph.  The graph holds the addresses of every buffer: refill them in place between
         replays.  The step runs once, uncaptured, first (one-time library set-up happens there)."""
+        def absorb():
+            absorb_q(q_nope, w_uk, self.q, q_pe=q_pe, positions=positions, rope_theta=rope_theta)
+
         def body():
             if before is not None:
                 before()
-            if plan:
-                self.plan()
-            self.run(q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, positions=positions, rope_theta=rope_theta)
+            if plan:   # the schedule beside the absorption, which does not need it
+                self.plan_beside(absorb)
+            else:
+                absorb()
+            decode(self.q, kv_cache, block_table, self.seqlens, self.scale, self.causal, self.metadata, self.parts,
+                   workspace=self.workspace, out=self.out, lse=self.lse)
+            unabsorb_o(self.out.view(self.B * self.s_q, self.H, 512), w_uv, o=self.o)
             if after is not None:
                 after()
         side = torch.cuda.Stream(device=self.q.device)
