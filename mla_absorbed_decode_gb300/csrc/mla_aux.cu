@@ -287,20 +287,6 @@ __device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-// 32 fp32 accumulator columns of one row -> 32 bf16 at dst (64 bytes, 16-byte aligned)
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t (&v)[32]) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint4 u;
-    u.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-    u.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-    u.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-    u.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-    d4[j] = u;
-  }
-}
-
 // RoPE of one q_pe row in place (64 bf16 values as 32 interleaved pairs; the page's tiny
 // example and "DeepSeekV2之MLA" 4.2: the pair (x[2j], x[2j+1]) turns by the angle
 // pos * theta^(-2j/64)).  The angle is carried as a float pair: pos is exact in fp32, the
@@ -427,16 +413,44 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
   const bool store = got && !fail_s && n < p.N;
   __nv_bfloat16* dst = p.out + static_cast<int64_t>(n) * p.out_row_stride + static_cast<int64_t>(h) * p.out_head_stride + n0;
   const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  // The stores go through a 2 KiB transpose buffer per warp in the (now idle) first stage: a
+  // thread holds one token row, so direct stores would touch 32 rows per instruction; here
+  // each store instruction writes 64 contiguous bytes of 8 rows.  Buffer row x (64 B) holds
+  // 16-byte unit u at ((u ^ (x & 3)) * 16).
+  const uint32_t stg = smem + warp * 2048;
+  const int tq = lane & 3, nw0 = m0 + warp * 32;   // transposed: quad tq of rows 8j + (lane >> 2)
+  const bool ok_all = got && !fail_s;
+  __nv_bfloat16* const dst0 = p.out + static_cast<int64_t>(h) * p.out_head_stride + n0;
+  auto store32 = [&](int c, const uint32_t (&v)[32]) {   // columns [c, c + 32) of the warp's 32 rows
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 u;
+      u.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+      u.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+      u.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+      u.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+      st_shared_v4(stg + lane * 64 + ((j ^ (lane & 3)) << 4), u);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int x = 8 * j + (lane >> 2);
+      const uint4 u = ld_shared_v4(stg + x * 64 + ((tq ^ (x & 3)) << 4));
+      if (ok_all && nw0 + x < p.N)
+        *reinterpret_cast<uint4*>(dst0 + static_cast<int64_t>(nw0 + x) * p.out_row_stride + c + 8 * tq) = u;
+    }
+    __syncwarp();
+  };
   uint32_t va[32], vb[32];
   tmem_ld32(tl, va);
 #pragma unroll 1
   for (int c = 0; c < NT; c += 64) {
     tmem_wait_ld();
     tmem_ld32(tl + c + 32, vb);
-    if (store) store_bf16x32(dst + c, va);
+    store32(c, va);
     tmem_wait_ld();
     if (c + 64 < NT) tmem_ld32(tl + c + 64, va);
-    if (store) store_bf16x32(dst + c + 32, vb);
+    store32(c + 32, vb);
   }
   tmem_wait_ld();
   if (store && copy_pe) {

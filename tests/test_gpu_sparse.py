@@ -107,6 +107,31 @@ def test_sparse_v32_shaped_sampled():
     compare(out[sel], lse[sel], sub_out, sub_lse, what="sparse V3.2 shape")
 
 
+def test_sparse_bench_workload_sampled():
+    """The sparse workload bench.py times (64 requests, top 2048 of 16384 tokens, the
+    workload generator's lists), in the bench's launch configuration; requests 0, 31 and 63
+    against the oracle.  Their pages are copied into a compact cache (the block table
+    remapped) so that the oracle reads exactly the same rows."""
+    import mla_absorbed_decode_gb300 as mla
+    w = W.SPARSE
+    inp = W.make_inputs(w)
+    q, kv, bt, sl = (inp[x].cuda() for x in ("q", "kv_cache", "block_table", "seqlens"))
+    idx, kl = inp["indices"], inp["topk_lens"]
+    P = mla.num_sm_parts(w.s_q, w.H)
+    meta = mla.decode_metadata(kl.cuda(), w.s_q, w.H, w.causal, P)
+    out, lse = mla.decode_sparse(q, kv, bt, sl, idx.cuda(), kl.cuda(), w.softmax_scale, w.causal, meta, P)
+    assert mla.get_device_status() == 0
+    out, lse = out.cpu(), lse.cpu()
+    sel = [0, 31, 63]
+    npages = (int(sl[0]) + 63) // 64
+    rows = inp["block_table"][sel, :npages]
+    kv_small = inp["kv_cache"][rows.reshape(-1)].float().numpy()
+    bt_small = np.arange(len(sel) * npages, dtype=np.int64).reshape(len(sel), npages)
+    ref_out, ref_lse = oracle.decode_sparse(to_np(inp["q"][sel]), kv_small, bt_small, inp["seqlens"][sel].numpy(),
+                                            idx[sel].numpy(), kl[sel].numpy(), w.softmax_scale, causal=w.causal)
+    compare(out[sel], lse[sel], ref_out, ref_lse, what="sparse bench workload")
+
+
 def test_sparse_calls_return_promptly():
     """Every call finishes in far less than the kernel's 500 ms bounded-wait limit, for
     batch sizes that give the parts segments of both parities of page counts (a drain
