@@ -413,43 +413,47 @@ def run_ours(args, w):
     # the step, D2H of its result, every step
     e2e = None
     if not args.no_e2e:
-        host_in = []
-        if w.with_projections:
-            host_in = [inp["q_nope"].pin_memory(), inp["q_pe"].pin_memory(), pos_host.pin_memory()]
-        else:
-            host_in = [inp["q"].pin_memory()]
-        host_sl = inp["seqlens"].pin_memory()
-        host_bt = inp["block_table"].pin_memory()
-        dev_in = [t.to(dev) for t in host_in]
-        # sparse: the lists and their lengths are inputs of the step too (copied into the
-        # tensors the schedule and the decode read)
-        host_sp = [(inp["indices"].pin_memory(), idx), (inp["topk_lens"].pin_memory(), kl)] if sparse else []
+        # The step's inputs are staged in one pinned host buffer and arrive with one
+        # host-to-device copy per step (their device tensors are views of one buffer, each
+        # 256-byte aligned); the result comes back with one copy for o and one for lse.
+        specs = [("q_nope", inp["q_nope"]), ("q_pe", inp["q_pe"]), ("pos", pos_host)] if w.with_projections \
+            else [("q", inp["q"])]
+        specs += [("sl", inp["seqlens"]), ("bt", inp["block_table"])]
+        if sparse:
+            specs += [("idx", inp["indices"]), ("kl", inp["topk_lens"])]
+        offs, total = {}, 0
+        for name, t in specs:
+            nb = t.numel() * t.element_size()
+            offs[name] = (total, nb)
+            total += (nb + 255) // 256 * 256
+        host_pack = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        dev_pack = torch.empty(total, dtype=torch.uint8, device=dev)
+        dv = {}
+        for name, t in specs:
+            o, nb = offs[name]
+            host_pack[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
+            dv[name] = dev_pack[o:o + nb].view(t.dtype).view(t.shape)
         res_dev = step.o if w.with_projections else step.out
         host_out = torch.empty(res_dev.shape, dtype=res_dev.dtype).pin_memory()
         host_lse = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
-        h2d = (sum(t.numel() * t.element_size() for t in host_in) + host_sl.numel() * 4 + host_bt.numel() * 4
-               + (inp["indices"].numel() * 4 + inp["topk_lens"].numel() * 4 if sparse else 0))
+        h2d = total
         d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
+        step.seqlens = dv["kl"] if sparse else dv["sl"]   # the schedule reads the staged lengths
 
         def e2e_step():
-            for src, dst in zip(host_in, dev_in):
-                dst.copy_(src, non_blocking=True)
-            sl.copy_(host_sl, non_blocking=True)
-            bt.copy_(host_bt, non_blocking=True)
-            for src, dst in host_sp:
-                dst.copy_(src, non_blocking=True)
+            dev_pack.copy_(host_pack, non_blocking=True)
 
             def absorb_in():
                 if w.with_projections:
-                    mla.absorb_q(dev_in[0], w_uk, step.q, q_pe=dev_in[1], positions=dev_in[2])
+                    mla.absorb_q(dv["q_nope"], w_uk, step.q, q_pe=dv["q_pe"], positions=dv["pos"])
 
             step.plan_beside(absorb_in)
-            q_in = step.q if w.with_projections else dev_in[0]
+            q_in = step.q if w.with_projections else dv["q"]
             if sparse:
-                mla.decode_sparse(q_in, kv, bt, sl, idx, kl, w.softmax_scale, w.causal, step.metadata, parts,
-                                  workspace=step.workspace, out=step.out, lse=step.lse)
+                mla.decode_sparse(q_in, kv, dv["bt"], dv["sl"], dv["idx"], dv["kl"], w.softmax_scale, w.causal,
+                                  step.metadata, parts, workspace=step.workspace, out=step.out, lse=step.lse)
             else:
-                mla.decode(q_in, kv, bt, sl, w.softmax_scale, w.causal, step.metadata, parts,
+                mla.decode(q_in, kv, dv["bt"], dv["sl"], w.softmax_scale, w.causal, step.metadata, parts,
                            workspace=step.workspace, out=step.out, lse=step.lse)
             if w.with_projections:
                 mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
