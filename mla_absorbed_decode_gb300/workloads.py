@@ -16,9 +16,12 @@ with `seed`, in this fixed order):
      ~ N(0, 1); W_UK [H, 128, 512] and W_UV [H, 512, 128] ~ N(0, 1/512) (variance);
   7. optional top-k lists (sparse decode): per request, the first min(topk, L) of a
      random permutation of its positions, sorted ascending (-1 pads the rest).
+FP8 cache (kv_fp8): the draws are the same; the cache is stored as E4M3 codes of
+kv / kv_scale (clamped to +-448, torch's round-to-nearest conversion) instead of bf16,
+with one per-tensor kv_scale.
 Poison: pool pages no request uses, and slots at or beyond seqlen in a
-request's last page, hold NaN; block-table entries past a request's last page
-hold -1.  A correct kernel never reads any of them into its result.
+request's last page, hold NaN (code 0x7F in an FP8 cache); block-table entries past
+a request's last page hold -1.  A correct kernel never reads any of them into its result.
 """
 from __future__ import annotations
 
@@ -49,6 +52,8 @@ class Workload:
     with_projections: bool = False
     fixed_seqlens: tuple = field(default_factory=tuple)
     topk: int = 0                # sparse decode: each request lists min(topk, L) of its tokens
+    kv_fp8: bool = False         # cache stored as FP8 E4M3 codes with one per-tensor scale
+    kv_scale: float = 1.0 / 64.0  # dequantized value = code value * kv_scale (N(0,1) draws -> codes within +-448)
 
     @property
     def softmax_scale(self) -> float:
@@ -70,7 +75,10 @@ LONG = Workload("long_b4_h128_l131072_outliers", B=4, s_q=1, H=128, seqlen=13107
                 outlier_p=0.01, outlier_scale=8.0)
 # DeepSeek-V3.2-shaped sparse decode (top-k = 2048 of each request's tokens)
 SPARSE = Workload("sparse_b64_h128_l16384_top2048", B=64, s_q=1, H=128, seqlen=16384, topk=2048)
-ALL = (TINY, V3, RAGGED, MTP, LONG, SPARSE)
+# the DeepSeek-V3 shape over an FP8 (E4M3) latent cache
+FP8 = Workload("fp8_deepseek_v3_b64_h128_l4096", B=64, s_q=1, H=128, seqlen=4096, with_projections=True,
+               kv_fp8=True)
+ALL = (TINY, V3, RAGGED, MTP, LONG, SPARSE, FP8)
 BY_NAME = {w.name: w for w in ALL}
 
 
@@ -85,8 +93,9 @@ def make_seqlens(w: Workload, g: torch.Generator) -> torch.Tensor:
 def make_inputs(w: Workload, seed: int = 0, seqlens: torch.Tensor | None = None,
                 poison: bool = True, max_blocks: int | None = None) -> dict:
     """All CPU tensors of one workload.  Keys:
-    q [B,s_q,H,576] bf16, kv_cache [pool,64,576] bf16, block_table [B,max_blocks] int32,
-    seqlens [B] int32, softmax_scale, causal, and with projections also
+    q [B,s_q,H,576] bf16, kv_cache [pool,64,576] bf16 (uint8 E4M3 codes with kv_fp8, plus
+    kv_scale), block_table [B,max_blocks] int32, seqlens [B] int32, softmax_scale, causal,
+    and with projections also
     q_nope [B*s_q,H,128], q_pe [B*s_q,H,64], w_uk [H,128,512], w_uv [H,512,128] (bf16).
     """
     g = torch.Generator().manual_seed(seed)
@@ -109,17 +118,24 @@ def make_inputs(w: Workload, seed: int = 0, seqlens: torch.Tensor | None = None,
     if w.outlier_p > 0:
         hit = torch.rand((pool, PAGE), generator=g) < w.outlier_p
         kv[hit] *= w.outlier_scale
-    kv = kv.to(torch.bfloat16)
+    if w.kv_fp8:
+        kv = (kv / w.kv_scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        nan = 0x7F
+    else:
+        kv = kv.to(torch.bfloat16)
+        nan = float("nan")
     if poison:
         in_use = torch.zeros(pool, dtype=torch.bool)
         in_use[perm[:used].long()] = True
-        kv[~in_use] = float("nan")
+        kv[~in_use] = nan
         for b in range(B):
             L = int(sl[b])
             if nb[b] and L % PAGE:
-                kv[int(bt[b, nb[b] - 1]), L % PAGE:] = float("nan")
+                kv[int(bt[b, nb[b] - 1]), L % PAGE:] = nan
     out = dict(q=q, kv_cache=kv, block_table=bt, seqlens=sl,
                softmax_scale=w.softmax_scale, causal=w.causal)
+    if w.kv_fp8:
+        out["kv_scale"] = w.kv_scale
     if w.with_projections:
         n = B * w.s_q
         out["q_nope"] = torch.randn((n, w.H, D_NOPE), generator=g).to(torch.bfloat16)

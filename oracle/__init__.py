@@ -9,8 +9,9 @@ input generator, which holds none of the method's arithmetic.
 Everything here is plain numpy in float64 (or pure Python for the brute-force
 checks), written for a reader to check against the pages by eye:
 
-* ``mla.py``      -- the absorbed decode definition (dense, and over a selected
-                    top-k token list), the expanded (un-absorbed) chain, the
+* ``mla.py``      -- the absorbed decode definition (dense, over an FP8 E4M3
+                    cache with a per-tensor scale, and over a selected top-k
+                    token list), the expanded (un-absorbed) chain, the
                     LSE merge, a pure-Python brute force and the tiny full-MLA
                     example with decoupled RoPE.
 * ``schedule.py`` -- a restatement of the split-KV schedule rule and the
@@ -21,8 +22,8 @@ Parity status: every function is pinned by a ``-m "not gpu"`` test in
 """
 from .mla import (  # noqa: F401
     PAGE, D_LATENT, D_ROPE, D_QK,
-    gather_request, visible_tokens,
-    decode_absorbed, decode_sparse, decode_expanded, absorb_q, assemble_q, unabsorb_o,
+    gather_request, visible_tokens, e4m3_value, E4M3_VALUES, dequantize_e4m3,
+    decode_absorbed, decode_fp8, decode_sparse, decode_expanded, absorb_q, assemble_q, unabsorb_o,
     lse_merge, decode_bruteforce, tiny_full_mla, rope_interleaved,
 )
 from .schedule import schedule_reference, check_schedule  # noqa: F401

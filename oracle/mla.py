@@ -35,15 +35,54 @@ D_ROPE = 64        # shared RoPE key k^R
 D_QK = D_LATENT + D_ROPE  # 576: width of the absorbed key / query
 
 
-def gather_request(kv_cache: np.ndarray, block_row: np.ndarray, n_tokens: int) -> np.ndarray:
+def e4m3_value(code: int) -> float:
+    """The number an FP8 E4M3 byte stands for (the "e4m3fn" encoding of FP8 KV caches).
+
+    Bit 7 is the sign, bits 6..3 the exponent e (bias 7), bits 2..0 the mantissa m:
+        e > 0:  (-1)^s * (1 + m/8) * 2^(e - 7)
+        e = 0:  (-1)^s * (m/8) * 2^-6            (subnormal)
+    The two codes with e = 15 and m = 7 are NaN; there is no infinity, so the largest
+    finite magnitude is 1.75 * 2^8 = 448.
+    """
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_VALUES = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def dequantize_e4m3(codes, scale: float) -> np.ndarray:
+    """Cached FP8 values as float64: the code's E4M3 value times the per-tensor scale.
+
+    [MLA-paths], exercise 2 ("FP8 的 KV Cache"): a token's 576 latent values are stored
+    one byte each, with scale factors beside them.  The reading taken here is one scale
+    for the whole cache, the per-tensor convention of the FP8 bmm in the SGLang page
+    (bmm_fp8 with a scale per operand).
+    """
+    return E4M3_VALUES[np.asarray(codes, dtype=np.uint8)] * float(scale)
+
+
+def gather_request(kv_cache: np.ndarray, block_row: np.ndarray, n_tokens: int, kv_scale=None) -> np.ndarray:
     """Rows 0..n_tokens-1 of one request's latent cache, as float64 [n_tokens, 576].
 
     kv_cache is [num_blocks, 64, 576]; block_row is that request's row of the
-    block table.  Token t sits in page block_row[t // 64] at slot t % 64.
+    block table.  Token t sits in page block_row[t // 64] at slot t % 64.  With
+    kv_scale given, the cache holds E4M3 codes (uint8) and each gathered row is
+    dequantized (dequantize_e4m3).
     """
     t = np.arange(n_tokens)
     pages = np.asarray(block_row)[t // PAGE]
-    return np.asarray(kv_cache[pages, t % PAGE], dtype=np.float64)
+    rows = np.asarray(kv_cache[pages, t % PAGE])
+    if kv_scale is not None:
+        return dequantize_e4m3(rows, kv_scale)
+    return np.asarray(rows, dtype=np.float64)
 
 
 def visible_tokens(seqlen: int, s_q: int, i: int, causal: bool) -> int:
@@ -53,7 +92,8 @@ def visible_tokens(seqlen: int, s_q: int, i: int, causal: bool) -> int:
     return max(0, min(int(seqlen), int(seqlen) - s_q + i + 1))
 
 
-def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=False, with_abs=False):
+def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=False, with_abs=False,
+                    kv_scale=None):
     """The absorbed decode definition: an MQA with a 576-wide key and 512-wide value.
 
     For every request b, query position i and head h, with n = visible tokens:
@@ -68,6 +108,8 @@ def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=Fal
     With with_abs=True it also returns out_abs = sum_t p_t |kv_t[:512]|, the
     attention-weighted magnitude of the values, which sizes the rounding error of
     a kernel that rounds p_t to bf16 (test tolerance, not part of the method).
+    With kv_scale given, kv_cache holds FP8 E4M3 codes and kv_t is the dequantized
+    row (gather_request); see decode_fp8.
     """
     q = np.asarray(q, dtype=np.float64)
     B, s_q, H, dq = q.shape
@@ -79,7 +121,7 @@ def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=Fal
         L = int(seqlens[b])
         if L <= 0:
             continue
-        kv = gather_request(kv_cache, block_table[b], L)
+        kv = gather_request(kv_cache, block_table[b], L, kv_scale)
         for i in range(s_q):
             n = visible_tokens(L, s_q, i, causal)
             if n == 0:
@@ -95,6 +137,17 @@ def decode_absorbed(q, kv_cache, block_table, seqlens, softmax_scale, causal=Fal
     if with_abs:
         return out, lse, out_abs
     return out, lse
+
+
+def decode_fp8(q, kv_codes, kv_scale, block_table, seqlens, softmax_scale, causal=False, with_abs=False):
+    """Absorbed decode over an FP8 (E4M3) latent cache with one per-tensor scale.
+
+    [MLA-paths], FlashMLA paragraph (the kernel supports an FP8 KV cache) and exercise 2
+    (576 bytes per cached token plus scale factors): the attention is the one of
+    decode_absorbed, over kv_t = dequantize_e4m3(kv_codes[page, slot], kv_scale);
+    q stays bf16.  kv_codes: [num_blocks, 64, 576] uint8.
+    """
+    return decode_absorbed(q, kv_codes, block_table, seqlens, softmax_scale, causal, with_abs, kv_scale=kv_scale)
 
 
 def decode_sparse(q, kv_cache, block_table, seqlens, indices, topk_lens, softmax_scale, causal=False,
