@@ -271,9 +271,10 @@ def test_pins_catch_planted_mistakes(monkeypatch):
 
     mutants = {
         "drop the last token": lambda m: m.setattr(om, "gather_request",
-            lambda kv, row, n: np.concatenate([real_gather(kv, row, n)[:-1], real_gather(kv, row, n)[:1] * 0], 0)),
+            lambda kv, row, n, sc=None: np.concatenate([real_gather(kv, row, n, sc)[:-1],
+                                                       real_gather(kv, row, n, sc)[:1] * 0], 0)),
         "shift one page": lambda m: m.setattr(om, "gather_request",
-            lambda kv, row, n: real_gather(kv, np.roll(np.asarray(row), 1), n)),
+            lambda kv, row, n, sc=None: real_gather(kv, np.roll(np.asarray(row), 1), n, sc)),
         "causal off by one": lambda m: m.setattr(om, "visible_tokens",
             lambda L, s_q, i, c: max(0, real_vis(L, s_q, i, c) - (1 if c else 0))),
         "value includes rope dims": lambda m: m.setattr(om, "D_LATENT", 511),
