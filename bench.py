@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode TFLOP/s and HBM GB/s, % of GB300 roofline (1 GPU)"
 SPEC_FLOPS = 2.25e15
+SPEC_FLOPS_FP8 = 4.5e15   # nominal dense FP8 tensor rate (twice bf16)
 SPEC_BW = 8.0e12
 DECODE_KERNEL_SOURCES = ("mla_absorbed_decode_gb300/csrc/mla_decode.cu", "mla_absorbed_decode_gb300/csrc/mla_ptx.cuh")
 
@@ -164,6 +165,10 @@ def oracle_sample_step(inp, kv_np, sel, with_proj):
                                       kl, inp["softmax_scale"], causal=inp["causal"])
         flops += acc.sparse_decode_work(inp["seqlens"][sel].tolist(), kl.tolist(), s_q, H, inp["causal"],
                                         indices=idx.tolist())[0]
+    elif "kv_scale" in inp:   # FP8 cache: kv_np holds its E4M3 codes
+        out, _ = oracle.decode_fp8(q, kv_np, inp["kv_scale"], inp["block_table"][sel].numpy(),
+                                   inp["seqlens"][sel].numpy(), inp["softmax_scale"], causal=inp["causal"])
+        flops += acc.decode_work(inp["seqlens"][sel].tolist(), s_q, H, inp["causal"])[0]
     else:
         out, _ = oracle.decode_absorbed(q, kv_np, inp["block_table"][sel].numpy(), inp["seqlens"][sel].numpy(),
                                         inp["softmax_scale"], causal=inp["causal"])
@@ -174,11 +179,18 @@ def oracle_sample_step(inp, kv_np, sel, with_proj):
     return flops
 
 
+def _kv_for_oracle(inp):
+    """The cache as the oracle takes it: float values, or an FP8 cache's codes."""
+    if "kv_scale" in inp:
+        return inp["kv_cache"].numpy()
+    return inp["kv_cache"].float().numpy()
+
+
 def cpu_sample(inp, w, target_s=10.0, max_reqs=None):
     """Time the oracle on a bounded sample of the workload (about target_s seconds)."""
     import numpy as np
     if "_kv_np" not in inp:
-        inp["_kv_np"] = inp["kv_cache"].float().numpy()
+        inp["_kv_np"] = _kv_for_oracle(inp)
     if w.with_projections and "_w_uk_np" not in inp:
         inp["_w_uk_np"] = inp["w_uk"].double().numpy()
         inp["_w_uv_np"] = inp["w_uv"].double().numpy()
@@ -200,7 +212,7 @@ def run_reference(args, w):
         return 0
     from mla_absorbed_decode_gb300 import workloads as W
     inp = W.make_inputs(w)
-    inp["_kv_np"] = inp["kv_cache"].float().numpy()
+    inp["_kv_np"] = _kv_for_oracle(inp)
     if w.with_projections:
         inp["_w_uk_np"] = inp["w_uk"].double().numpy()
         inp["_w_uv_np"] = inp["w_uv"].double().numpy()
@@ -283,11 +295,14 @@ def run_ours(args, w):
     bt = inp["block_table"].to(dev)
     sl = inp["seqlens"].to(dev)
     sparse = w.topk > 0   # sparse (top-k) decode: each request attends to its listed tokens only
+    fp8 = w.kv_fp8        # FP8 (E4M3) cache with a per-tensor scale
+    kv_scale = inp.get("kv_scale")
     idx = inp["indices"].to(dev) if sparse else None
     kl = inp["topk_lens"].to(dev) if sparse else None
     parts = args.parts or mla.num_sm_parts(s_q, H)
     # the split schedule walks what the decode walks: the tokens, or the top-k lists
-    step = mla.DecodeStep(B, s_q, H, kl if sparse else sl, w.causal, w.softmax_scale, parts=parts, device=dev)
+    step = mla.DecodeStep(B, s_q, H, kl if sparse else sl, w.causal, w.softmax_scale, parts=parts, device=dev,
+                          kv_scale=kv_scale)
     q_direct = inp["q"].to(dev)
     stream = torch.cuda.current_stream()
     # Between timed steps L2 is flushed: a 256 MiB write (larger than the 126 MB L2),
@@ -310,6 +325,9 @@ def run_ours(args, w):
         if sparse:
             mla.decode_sparse(q_dec, kv, bt, sl, idx, kl, w.softmax_scale, w.causal, step.metadata, parts,
                               workspace=step.workspace, out=step.out, lse=step.lse)
+        elif fp8:
+            mla.decode_fp8(q_dec, kv, kv_scale, bt, sl, w.softmax_scale, w.causal, step.metadata, parts,
+                           workspace=step.workspace, out=step.out, lse=step.lse)
         else:
             mla.decode(q_dec, kv, bt, sl, w.softmax_scale, w.causal, step.metadata, parts, workspace=step.workspace,
                        out=step.out, lse=step.lse)
@@ -396,7 +414,9 @@ def run_ours(args, w):
         dflops, dbytes = acc.sparse_decode_work(inp["seqlens"].tolist(), inp["topk_lens"].tolist(), s_q, H, w.causal,
                                                 indices=inp["indices"].tolist())
     else:
-        dflops, dbytes = acc.decode_work(inp["seqlens"].tolist(), s_q, H, w.causal)
+        dflops, dbytes = acc.decode_work(inp["seqlens"].tolist(), s_q, H, w.causal,
+                                         kv_value_bytes=acc.FP8 if fp8 else acc.BF16)
+    spec_dec_flops = SPEC_FLOPS_FP8 if fp8 else SPEC_FLOPS   # the decode's MMAs run at the FP8 rate
     bflops = bbytes = 0
     if w.with_projections:
         for absorb in (True, False):
@@ -407,7 +427,7 @@ def run_ours(args, w):
     n = ws
     value = n * step_flops / t_step / 1e12
     gbs = n * step_bytes / t_step / 1e9
-    rl_time = acc.roofline_time(step_flops, step_bytes, SPEC_FLOPS, SPEC_BW)
+    rl_time = max(dflops / spec_dec_flops + bflops / SPEC_FLOPS, step_bytes / SPEC_BW)
 
     # end to end through the public API with host buffers: H2D of the step's inputs,
     # the step, D2H of its result, every step
@@ -452,6 +472,9 @@ def run_ours(args, w):
             if sparse:
                 mla.decode_sparse(q_in, kv, dv["bt"], dv["sl"], dv["idx"], dv["kl"], w.softmax_scale, w.causal,
                                   step.metadata, parts, workspace=step.workspace, out=step.out, lse=step.lse)
+            elif fp8:
+                mla.decode_fp8(q_in, kv, kv_scale, dv["bt"], dv["sl"], w.softmax_scale, w.causal, step.metadata,
+                               parts, workspace=step.workspace, out=step.out, lse=step.lse)
             else:
                 mla.decode(q_in, kv, dv["bt"], dv["sl"], w.softmax_scale, w.causal, step.metadata, parts,
                            workspace=step.workspace, out=step.out, lse=step.lse)
@@ -480,20 +503,21 @@ def run_ours(args, w):
 
     peaks = _peaks()
     dec_achieved = dbytes / t_dec / 1e9
-    roof_bound = "hbm" if dflops / SPEC_FLOPS < dbytes / SPEC_BW else "tensor"
+    roof_bound = "hbm" if dflops / spec_dec_flops < dbytes / SPEC_BW else "tensor"
     if roof_bound == "hbm":
         roof = {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": dec_achieved / peaks["hbm_gbs"]}
-    else:
+    else:   # FP8: the measured bf16 rate times the nominal FP8 / bf16 ratio (2)
         ach = dflops / t_dec / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / peaks["bf16_tflops"]}
+        tpeak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+        roof = {"bound": "tensor", "achieved": ach, "peak": tpeak, "unit": "TFLOP/s", "frac": ach / tpeak}
     roof["peak_source"] = peaks["source"]
     roof["traffic"] = _traffic_per_launch(w.name)
-    roof["kernel"] = ("mla_decode_sparse" if sparse else "mla_decode") + " (decode kernel + LSE combine)"
+    roof["kernel"] = ("mla_decode_sparse" if sparse else "mla_decode_fp8" if fp8 else "mla_decode") \
+        + " (decode kernel + LSE combine)"
     roof["algorithmic_per_launch"] = {"bytes": dbytes, "flops": dflops}
     roof["ms_per_launch"] = t_dec * 1e3
-    roof["frac_of_spec_roofline"] = acc.roofline_time(dflops, dbytes, SPEC_FLOPS, SPEC_BW) / t_dec
+    roof["frac_of_spec_roofline"] = acc.roofline_time(dflops, dbytes, spec_dec_flops, SPEC_BW) / t_dec
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
@@ -506,12 +530,15 @@ def run_ours(args, w):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": n, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": t_step * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": B, "s_q": s_q, "H": H,
                        "seqlens": (w.seqlen or f"ragged 1..{w.ragged_max}" if not w.fixed_seqlens
                                    else list(w.fixed_seqlens)),
                        "page": 64, "parts": parts, "parallelism": f"replicas x{n}",
                        **({"topk": w.topk, "path": "mla_decode_sparse"} if sparse else {}),
+                       **({"kv_cache": f"e4m3 codes, per-tensor scale {kv_scale}", "path": "mla_decode_fp8",
+                           "mma": "kind::f8f6f4; q and P each as two E4M3 terms, fp32 accumulation"}
+                          if fp8 else {}),
                        "l2": "flushed between timed steps (256 MiB write, then 256 MiB read; outside the step events)",
                        "decode_timing": "K further decode calls inside the timed region, L2 flushed before each",
                        "launch": ("eager" if args.eager else "CUDA graph of the step's library calls")

@@ -140,6 +140,25 @@ mla_status_t mla_decode_sparse(const mla_bf16_t* q, const mla_bf16_t* kv_cache, 
                                void* workspace, size_t workspace_bytes, mla_bf16_t* out, float* lse,
                                mla_stream_t stream);
 
+/* Absorbed decode over an FP8 latent cache (page "MLA 推理：两条计算路径与 FlashMLA":
+ * the FlashMLA paragraph -- the kernel supports an FP8 KV cache -- and exercise 2 --
+ * 576 bytes per cached token plus scale factors, which moves the decode from the
+ * bandwidth limit to the tensor cores).
+ *  kv_cache  [num_blocks, 64, 576] bytes: E4M3 codes (sign, 4 exponent bits with bias
+ *            7, 3 mantissa bits; no infinities, codes 0x7F / 0xFF are NaN).  Cached
+ *            value = code value * kv_scale.
+ *  kv_scale  one scale for the whole cache, finite and > 0 (else MLA_ERR_INVALID_ARG)
+ * The attention is that of mla_decode over the dequantized values; q stays bf16.
+ * Inside, q (per row, scaled to the E4M3 range) and the probabilities are each carried
+ * as a sum of two E4M3 terms for the FP8 tensor-core MMAs, which keeps the result
+ * within the bf16 path's error.  Other arguments, results and errors as for mla_decode.
+ * Async on stream. */
+mla_status_t mla_decode_fp8(const mla_bf16_t* q, const uint8_t* kv_cache, float kv_scale, int64_t num_blocks,
+                            const int32_t* block_table, int max_blocks, const int32_t* seqlens, int B, int s_q, int H,
+                            float softmax_scale, int causal_s_q, const void* metadata, int num_sm_parts,
+                            void* workspace, size_t workspace_bytes, mla_bf16_t* out, float* lse,
+                            mla_stream_t stream);
+
 /* W_UK absorption and assembly of the decode query ("DeepSeekV2之MLA" 4.5:
  * q_nope_out = bmm(q_nope, w_kc) goes into q[..., :kv_lora_rank], the RoPE'd
  * q_pe into the last 64 values):

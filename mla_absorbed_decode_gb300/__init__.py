@@ -15,7 +15,7 @@ import torch
 
 __all__ = [
     "MLAError", "lib", "library_path", "num_sm_parts", "metadata_size", "decode_metadata",
-    "decode_workspace_size", "decode", "decode_sparse", "absorb_q", "unabsorb_o", "get_device_status",
+    "decode_workspace_size", "decode", "decode_sparse", "decode_fp8", "absorb_q", "unabsorb_o", "get_device_status",
     "schedule_params", "debug_withhold_first_load", "DecodeStep", "EXPORTED_SYMBOLS",
 ]
 
@@ -38,6 +38,8 @@ _SIGNATURES = {
                             _p, _c_int, _p, _c_size, _p, _p, _p]),
     "mla_decode_sparse": (_c_int, [_p, _p, _c_ll, _p, _c_int, _p, _p, _c_ll, _p, _c_int, _c_int, _c_int, _c_float,
                                    _c_int, _p, _c_int, _p, _c_size, _p, _p, _p]),
+    "mla_decode_fp8": (_c_int, [_p, _p, _c_float, _c_ll, _p, _c_int, _p, _c_int, _c_int, _c_int, _c_float, _c_int,
+                                _p, _c_int, _p, _c_size, _p, _p, _p]),
     "mla_absorb_q": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _p, _c_int, _c_int, _p]),
     "mla_absorb_q_rope": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _p, _c_int, _c_int, _p]),
     "mla_unabsorb_o": (_c_int, [_p, _p, _p, _c_int, _c_int, _p]),
@@ -162,6 +164,27 @@ def decode_sparse(q, kv_cache, block_table, seqlens, indices, topk_lens, softmax
     return out, lse
 
 
+def decode_fp8(q, kv_cache, kv_scale: float, block_table, seqlens, softmax_scale: float, causal: bool, metadata,
+               parts: int, workspace=None, out=None, lse=None, stream=None):
+    """Absorbed MLA decode over an FP8 cache: kv_cache [num_blocks,64,576] uint8 E4M3 codes (or a
+    float8_e4m3fn tensor), cached value = code value * kv_scale.  Returns (out, lse) as decode."""
+    B, s_q, H, _ = q.shape
+    dev = q.device
+    if kv_cache.element_size() != 1:
+        raise TypeError("decode_fp8: kv_cache must hold one byte per value (E4M3 codes)")
+    if out is None:
+        out = torch.empty((B, s_q, H, 512), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_size(B, s_q, H, parts), dtype=torch.uint8, device=dev)
+    _check(lib().mla_decode_fp8(_ptr(q), _ptr(kv_cache), float(kv_scale), kv_cache.shape[0], _ptr(block_table),
+                                block_table.shape[1], _ptr(seqlens), B, s_q, H, float(softmax_scale), int(causal),
+                                _ptr(metadata), parts, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _ptr(out), _ptr(lse), _stream(stream)), "mla_decode_fp8")
+    return out, lse
+
+
 def absorb_q(q_nope: torch.Tensor, w_uk: torch.Tensor, q: torch.Tensor, q_pe: torch.Tensor | None = None,
              stream=None, positions: torch.Tensor | None = None, rope_theta: float = 10000.0) -> torch.Tensor:
     """q[n, h, 0:512] = q_nope[n, h, :] @ w_uk[h] and q[n, h, 512:576] = q_pe[n, h, :], RoPE-rotated
@@ -201,13 +224,15 @@ class DecodeStep:
     absorbed decode over the paged latent cache, LSE combine, W_UV un-absorption.
 
     Buffers (q, out, lse, o, metadata, workspace) are allocated once here, with
-    torch, and reused; `run` launches only library kernels.
+    torch, and reused; `run` launches only library kernels.  With kv_scale given, the
+    cache passed to `run` / `capture` is an FP8 (E4M3) cache with that per-tensor scale.
     """
 
     def __init__(self, B: int, s_q: int, H: int, seqlens: torch.Tensor, causal: bool, softmax_scale: float,
-                 parts: int | None = None, device="cuda"):
+                 parts: int | None = None, device="cuda", kv_scale: float | None = None):
         self.B, self.s_q, self.H = B, s_q, H
         self.causal, self.scale = causal, softmax_scale
+        self.kv_scale = kv_scale
         self.parts = parts if parts is not None else num_sm_parts(s_q, H)
         dev = torch.device(device)
         self.q = torch.empty((B, s_q, H, 576), dtype=torch.bfloat16, device=dev)
@@ -234,13 +259,20 @@ class DecodeStep:
         work()
         cur.wait_stream(self._plan_stream)
 
+    def _decode(self, kv_cache, block_table, stream=None):
+        if self.kv_scale is None:
+            decode(self.q, kv_cache, block_table, self.seqlens, self.scale, self.causal, self.metadata, self.parts,
+                   workspace=self.workspace, out=self.out, lse=self.lse, stream=stream)
+        else:
+            decode_fp8(self.q, kv_cache, self.kv_scale, block_table, self.seqlens, self.scale, self.causal,
+                       self.metadata, self.parts, workspace=self.workspace, out=self.out, lse=self.lse, stream=stream)
+
     def run(self, q_nope, q_pe, w_uk, w_uv, kv_cache, block_table, stream=None, positions=None,
             rope_theta: float = 10000.0):
         """q_nope [B*s_q,H,128], q_pe [B*s_q,H,64] -> o [B*s_q,H,128] (bf16); with positions
         (int32 [B*s_q]) q_pe is RoPE-rotated inside the absorption."""
         absorb_q(q_nope, w_uk, self.q, q_pe=q_pe, stream=stream, positions=positions, rope_theta=rope_theta)
-        decode(self.q, kv_cache, block_table, self.seqlens, self.scale, self.causal, self.metadata, self.parts,
-               workspace=self.workspace, out=self.out, lse=self.lse, stream=stream)
+        self._decode(kv_cache, block_table, stream=stream)
         unabsorb_o(self.out.view(self.B * self.s_q, self.H, 512), w_uv, o=self.o, stream=stream)
         return self.o
 
@@ -261,8 +293,7 @@ class DecodeStep:
                 self.plan_beside(absorb)
             else:
                 absorb()
-            decode(self.q, kv_cache, block_table, self.seqlens, self.scale, self.causal, self.metadata, self.parts,
-                   workspace=self.workspace, out=self.out, lse=self.lse)
+            self._decode(kv_cache, block_table)
             unabsorb_o(self.out.view(self.B * self.s_q, self.H, 512), w_uv, o=self.o)
             if after is not None:
                 after()

@@ -20,6 +20,7 @@ D_R = 64       # shared RoPE key width (qk_rope_head_dim)
 D_NOPE = 128   # per-head non-positional q/k width
 D_V = 128      # per-head value width
 BF16 = 2
+FP8 = 1        # an FP8 (E4M3) cache: 576 bytes per token ("MLA 推理：两条计算路径与FlashMLA", exercise 2)
 
 
 def pair_flops(H: int, absorbed: bool) -> int:
@@ -68,13 +69,14 @@ def visible(seqlen: int, s_q: int, i: int, causal: bool) -> int:
     return max(0, min(seqlen, seqlen - s_q + i + 1))
 
 
-def decode_work(seqlens, s_q: int, H: int, causal: bool):
-    """Algorithmic (flops, bytes) of one mla_decode call."""
+def decode_work(seqlens, s_q: int, H: int, causal: bool, kv_value_bytes: int = BF16):
+    """Algorithmic (flops, bytes) of one mla_decode call (kv_value_bytes = FP8: one
+    mla_decode_fp8 call; its scale is one number, not counted)."""
     seqlens = [int(x) for x in seqlens]
     B = len(seqlens)
     pairs = sum(visible(L, s_q, i, causal) for L in seqlens for i in range(s_q))
     flops = pairs * H * 2 * ((D_C + D_R) + D_C)
-    kv_bytes = sum(max(L, 0) for L in seqlens) * (D_C + D_R) * BF16
+    kv_bytes = sum(max(L, 0) for L in seqlens) * (D_C + D_R) * kv_value_bytes
     rows = B * s_q * H
     q_bytes = rows * (D_C + D_R) * BF16
     out_bytes = rows * D_C * BF16 + rows * 4

@@ -58,42 +58,72 @@ namespace mla {
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kKStages = 2;                           // S-CTA: pages in flight
-constexpr int kVStages = 2;                           // O-CTA: pages in flight (its loads hit L2)
-constexpr int kStages = 2;                            // barrier slots (the larger of the two)
+constexpr int kMaxStages = 4;                         // barrier slots: the deepest page ring
 constexpr int kSlots = 4;                             // O-CTA packet receive slots: a slot's credit
                                                       // round trip over DSMEM is hidden 4 pages deep
-constexpr uint32_t kKStageBytes = 9 * 8192;           // S-CTA: 64 tokens x 576 dims, 9 swizzled chunks
-constexpr uint32_t kKPartA = 5;                       // chunks 0..4 of a page stage are released and
-                                                      // refilled as soon as QK^T is done with them
-constexpr uint32_t kVStageBytes = 8 * 8192;           // O-CTA: 64 tokens x 512 dims
-constexpr uint32_t kPBytes = 128 * 128;               // P: 128 rows x 64 tokens bf16 (MMA A layout)
+constexpr uint32_t kChunk = 8192;                     // one swizzled chunk of a page: 64 rows x 128 B
+constexpr uint32_t kPBytes = 128 * 128;               // P: 128 rows x 128 B in the MMA A layout (bf16: 64
+                                                      // tokens; FP8: hi and lo codes of 64 tokens)
 constexpr uint32_t kPktAlpha = kPBytes;               // float[128] rescale factor per row
-constexpr uint32_t kPktInvL = kPBytes + 512;          // float[128] 1/l per row (last page of a segment)
+constexpr uint32_t kPktInvL = kPBytes + 512;          // float[128] output factor per row (last page of a segment)
 constexpr uint32_t kPktStride = kPBytes + 1024;       // 17 KiB, a multiple of 1024; all of it is copied
-// dynamic shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t kOffStage = 0;
-constexpr uint32_t kOffRecv = kVStages * kVStageBytes;            // O-CTA: kSlots packet receive slots
-constexpr uint32_t kOffSend = kKStages * kKStageBytes;            // S-CTA: 2 packet staging slots
-constexpr uint32_t kOffPm = kOffSend + 2 * kPktStride;            // S-CTA: row-max exchange [2][128]
-constexpr uint32_t kOffLpart = kOffPm + 1024;                     // S-CTA: partial row sums [128]
-constexpr uint32_t kOffInvL = kOffRecv + kSlots * kPktStride;     // O-CTA: 1/l of the segment [128]
-constexpr uint32_t kOffSharedO = kOffInvL + 512;
-constexpr uint32_t kOffShared = kOffSharedO > kOffLpart + 512 ? kOffSharedO : kOffLpart + 512;  // both roles
-constexpr uint32_t kOffEpi = kOffShared + 640;                    // O-CTA: 2 KiB transpose buffer per epilogue warp
-constexpr uint32_t kSmemBytes = kOffEpi + 8 * 2048;
-static_assert(kOffLpart + 512 <= kOffShared, "S-CTA layout");
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kQCol = 0, kSCol0 = 320;           // S-CTA TMEM columns: Q [0,288), S buffers 320, 384
-constexpr float kRescaleLog2 = 8.0f;                  // rebase the row max when it grows by more than 2^8
 constexpr uint64_t kTimeoutNs = 500ull * 1000 * 1000;
 constexpr float kLn2 = 0.69314718055994530942f;
 
+// Layout of the two cache formats.
+// bf16 cache: the S-CTA's page stage holds 64 tokens x 576 dims as 9 chunks of 64 dims,
+// the O-CTA's the 512 value dims as 8 chunks; two pages in flight on each side.
+// FP8 (E4M3) cache, 576 bytes a token: the S-CTA's stage holds dims 0..511 as 4 chunks of
+// 128 and the 64 RoPE dims in a fifth chunk whose upper half the TMA fills with zeros,
+// the O-CTA's the 512 value dims as 4 chunks; four pages in flight on each side.
+// A chunk is 64 rows of 128 bytes with the 128-byte swizzle in both formats, so the
+// MMA operand descriptors are the same; an FP8 MMA step covers K = 32 instead of 16.
+template <bool F8>
+struct Cfg {
+  static constexpr int kKStages = F8 ? 4 : 2;         // S-CTA: pages in flight
+  static constexpr int kVStages = F8 ? 4 : 2;         // O-CTA: pages in flight (its loads hit L2)
+  static constexpr uint32_t kKChunks = F8 ? 5 : 9;
+  static constexpr uint32_t kKPartA = F8 ? 4 : 5;     // chunks 0..kKPartA-1 of a page stage are released
+                                                      // and refilled as soon as QK^T is done with them
+  static constexpr uint32_t kVChunks = F8 ? 4 : 8;
+  static constexpr uint32_t kKStageBytes = kKChunks * kChunk;
+  static constexpr uint32_t kVStageBytes = kVChunks * kChunk;
+  static constexpr int kQItems = F8 ? 4 : 2;          // q blocks per segment: 128 bf16 rows in blocks of 32 or 64
+  static constexpr int kQRows = 128 / kQItems;
+  static constexpr uint32_t kQItemBytes = static_cast<uint32_t>(kQRows) * kDimQK * 2;
+  static constexpr int kKStep = F8 ? 32 : 16;         // K of one MMA step (32 bytes of a row either way)
+  // The row maximum is rebased when it grows by more than 2^kRescaleLog2; P is taken
+  // relative to 2^-kPOffset times the reference.  FP8: P < 2^(6+2) stays within E4M3's
+  // range (448) while typical values stay clearer of its subnormals (below 2^-6) than
+  // with no offset; a lower threshold would rebase O on many pages (with 2^4, about
+  // half the pages of a 4096-token request with unit-scale q).
+  static constexpr float kRescaleLog2 = F8 ? 6.0f : 8.0f;
+  static constexpr float kPOffset = F8 ? 2.0f : 0.0f;
+  // dynamic shared memory map (offsets from a 1024-byte aligned base)
+  static constexpr uint32_t kOffStage = 0;
+  static constexpr uint32_t kOffRecv = kVStages * kVStageBytes;            // O-CTA: kSlots packet receive slots
+  static constexpr uint32_t kOffSend = kKStages * kKStageBytes;            // S-CTA: 2 packet staging slots
+  static constexpr uint32_t kOffPm = kOffSend + 2 * kPktStride;            // S-CTA: row-max exchange [2][128]
+  static constexpr uint32_t kOffLpart = kOffPm + 1024;                     // S-CTA: partial row sums [128]
+  static constexpr uint32_t kOffInvL = kOffRecv + kSlots * kPktStride;     // O-CTA: output factor of the segment [128]
+  static constexpr uint32_t kOffSharedO = kOffInvL + 512;
+  static constexpr uint32_t kOffShared = kOffSharedO > kOffLpart + 512 ? kOffSharedO : kOffLpart + 512;  // both roles
+  static constexpr uint32_t kOffEpi = kOffShared + 640;                    // O-CTA: 2 KiB transpose buffer per epilogue warp
+  static constexpr uint32_t kSmemBytes = kOffEpi + 8 * 2048;
+  static_assert(kKStages <= kMaxStages && kVStages <= kMaxStages, "barrier slots");
+  static_assert(kQItemBytes <= kKStageBytes, "a q block fits a page stage");
+  static_assert(kQItems <= kKStages, "the q blocks of a segment are resident together");
+  static_assert(kOffLpart + 512 <= kOffShared, "S-CTA layout");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+using CfgB = Cfg<false>;   // bf16 cache (dense and sparse)
+
 struct Bars {
-  uint64_t full[kStages];   // O: chunks 0..3 of V landed; S: chunks 0..4 of K, or a whole q block
-  uint64_t empty[kStages];  // O: chunks 0..3 free again; S: chunks 0..4 free again
-  uint64_t full_b[kStages];   // S: chunks 5..8 of K landed (plain arrival for a q block); O: chunks 4..7 of V
-  uint64_t empty_b[kStages];  // S: chunks 5..8 free again; O: chunks 4..7 free again
+  uint64_t full[kMaxStages];     // O: first half of V landed; S: part A of K, or a whole q block
+  uint64_t empty[kMaxStages];    // O: first half of V free again; S: part A of K free again
+  uint64_t full_b[kMaxStages];   // S: part B of K landed (plain arrival for a q block); O: second half of V
+  uint64_t empty_b[kMaxStages];  // S: part B of K free again; O: second half of V free again
   uint64_t s_full[2];       // S-CTA: S = QK^T ready in TMEM
   uint64_t s_empty[2];      // S-CTA: S read by the softmax warps (8 arrivals)
   uint64_t q_full;          // S-CTA: Q of the segment stored in TMEM
@@ -311,15 +341,15 @@ __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Sha
   w.init(p, part);
   Segment s;
   uint32_t i = 0;
-  int issued[kKStages];
-  uint32_t issued_phase[kKStages];
-  for (int j = 0; j < kKStages; ++j) issued[j] = 0, issued_phase[j] = 0;
+  int issued[CfgB::kKStages];
+  uint32_t issued_phase[CfgB::kKStages];
+  for (int j = 0; j < CfgB::kKStages; ++j) issued[j] = 0, issued_phase[j] = 0;
   bool ok = true, have_next = false;
   const __nv_bfloat16* next_row = nullptr;
   while (ok && w.next(s)) {
     const int qrow0 = s.b * p.rows + rb * 128;
     for (int j = 0; j < 2 && ok; ++j, ++i) {
-      const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
+      const uint32_t st = i % CfgB::kKStages, ph = (i / CfgB::kKStages) & 1;
       if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl) ||
           !warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) {
         ok = false;
@@ -330,14 +360,14 @@ __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Sha
       if (!issuer) {
         mbar_arrive(full);
       } else if (!(withhold && i == 0)) {   // test hook: this block never arrives
-        mbar_arrive_expect_tx(full, kKStageBytes);
-        tma_load_3d(smem + kOffStage + st * kKStageBytes, &maps->q, full, 0, qrow0 + 64 * j, 0);
+        mbar_arrive_expect_tx(full, CfgB::kKStageBytes);
+        tma_load_3d(smem + CfgB::kOffStage + st * CfgB::kKStageBytes, &maps->q, full, 0, qrow0 + 64 * j, 0);
         issued[st] = 1, issued_phase[st] = ph;
       }
     }
     for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
-      const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
-      const uint32_t stage = smem + kOffStage + st * kKStageBytes;
+      const uint32_t st = i % CfgB::kKStages, ph = (i / CfgB::kKStages) & 1;
+      const uint32_t stage = smem + CfgB::kOffStage + st * CfgB::kKStageBytes;
       const __nv_bfloat16* mine = have_next ? next_row : sparse_page_row(p, s.b, k, r0 + lane);
       if (lane >= nrows) mine = nullptr;
       int nb, nk;
@@ -348,17 +378,17 @@ __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Sha
       // the stage's latest use is now a gathered page (waited for by cp.async.wait_all): the
       // drain below must not wait for an older phase of its barrier, whose parity can alias
       issued[st] = 0;
-      gather_rows<kKPartA * 8>(stage, mine, r0, nrows, 0, lane);
+      gather_rows<CfgB::kKPartA * 8>(stage, mine, r0, nrows, 0, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full[st]));
       if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      gather_rows<72 - kKPartA * 8>(stage, mine, r0, nrows, kKPartA * 8, lane);
+      gather_rows<72 - CfgB::kKPartA * 8>(stage, mine, r0, nrows, CfgB::kKPartA * 8, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full_b[st]));
     }
     // the next segment's first page was looked up with this segment's walker state
   }
   cp_async_wait_all();   // this lane's copies land before the CTA may exit
   if (issuer)   // a q block whose stage saw no later page may still be in flight (after an abort)
-    for (int st = 0; st < kKStages; ++st)
+    for (int st = 0; st < CfgB::kKStages; ++st)
       if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
   __syncwarp();
 }
@@ -375,8 +405,8 @@ __device__ void o_producer_sparse(const DecodeParams& p, Shared& sh, uint32_t sm
   const __nv_bfloat16* next_row = nullptr;
   while (ok && w.next(s)) {
     for (int k = s.kb; k < s.ke && ok; ++k, ++T) {
-      const uint32_t st = T % kVStages, ph = (T / kVStages) & 1;
-      const uint32_t stage = smem + kOffStage + st * kVStageBytes;
+      const uint32_t st = T % CfgB::kVStages, ph = (T / CfgB::kVStages) & 1;
+      const uint32_t stage = smem + CfgB::kOffStage + st * CfgB::kVStageBytes;
       const __nv_bfloat16* mine = have_next ? next_row : sparse_page_row(p, s.b, k, r0 + lane);
       if (lane >= nrows) mine = nullptr;
       int nb, nk;
@@ -395,63 +425,68 @@ __device__ void o_producer_sparse(const DecodeParams& p, Shared& sh, uint32_t sm
   __syncwarp();
 }
 
-// Lane 0 of warp 0 of the O-CTA: the 512 value dims of every page, as two 32 KiB
-// halves (chunks 0..3 and 4..7); each half is refilled as soon as the PV MMAs that
-// read it are done.
+// Lane 0 of warp 0 of the O-CTA: the 512 value dims of every page, as two halves
+// (bf16: chunks 0..3 and 4..7, 32 KiB each; FP8: chunks 0..1 and 2..3, 16 KiB each);
+// each half is refilled as soon as the PV MMAs that read it are done.
+template <bool F8>
 __device__ void o_producer(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
                            uint32_t cl) {
+  using C = Cfg<F8>;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
   uint32_t T = 0;
-  int issued[kVStages], issued_b[kVStages];
-  uint32_t issued_phase[kVStages], issued_phase_b[kVStages];
-  for (int j = 0; j < kVStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
+  int issued[C::kVStages], issued_b[C::kVStages];
+  uint32_t issued_phase[C::kVStages], issued_phase_b[C::kVStages];
+  for (int j = 0; j < C::kVStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
   const uint64_t policy = l2_policy_evict_first();
   bool ok = true;
   while (ok && w.next(s)) {
     for (int k = s.kb; k < s.ke && ok; ++k, ++T) {
-      const uint32_t st = T % kVStages, ph = (T / kVStages) & 1;
-      const uint32_t stage = smem + kOffStage + st * kVStageBytes;
+      const uint32_t st = T % C::kVStages, ph = (T / C::kVStages) & 1;
+      const uint32_t stage = smem + C::kOffStage + st * C::kVStageBytes;
       if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
       const int blk = request_block(p, s.b, k);
       const uint32_t full = smem_u32(&sh.bar.full[st]);
-      mbar_arrive_expect_tx(full, kVStageBytes / 2);
+      mbar_arrive_expect_tx(full, C::kVStageBytes / 2);
       tma_load_3d_hint(stage, &maps->c4, full, 0, blk * 64, 0, policy);
       issued[st] = 1, issued_phase[st] = ph;
       if (!wait_bar(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
       const uint32_t full_b = smem_u32(&sh.bar.full_b[st]);
-      mbar_arrive_expect_tx(full_b, kVStageBytes / 2);
-      tma_load_3d_hint(stage + kVStageBytes / 2, &maps->c4, full_b, 0, blk * 64, 4, policy);
+      mbar_arrive_expect_tx(full_b, C::kVStageBytes / 2);
+      tma_load_3d_hint(stage + C::kVStageBytes / 2, &maps->c4, full_b, 0, blk * 64, C::kVChunks / 2, policy);
       issued_b[st] = 1, issued_phase_b[st] = ph;
     }
   }
-  for (int st = 0; st < kVStages; ++st) {   // loads still in flight land before the CTA may exit
+  for (int st = 0; st < C::kVStages; ++st) {   // loads still in flight land before the CTA may exit
     if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
     if (issued_b[st]) drain_bar(smem_u32(&sh.bar.full_b[st]), issued_phase_b[st]);
   }
 }
 
 // ------------------------------------------------------------------ S-CTA --
-// The S-CTA ring walks, per segment, two q blocks (rows 0..63 and 64..127 of the
-// pair's row block) and then the segment's pages; ring item i uses stage i % 2.
+// The S-CTA ring walks, per segment, the q blocks of the pair's row block (bf16: rows
+// 0..63 and 64..127; FP8: four blocks of 32 rows) and then the segment's pages; ring
+// item i uses stage i % kKStages.
 
-// Lane 0 of warp 0: every ring item (a q block or a page, 72 KiB, one TMA box).
+// Lane 0 of warp 0: every ring item (a q block in one TMA box, or a page in two parts).
+template <bool F8>
 __device__ void s_producer(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
                            uint32_t cl, int rb, bool withhold) {
+  using C = Cfg<F8>;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
   uint32_t i = 0;
-  int issued[kKStages], issued_b[kKStages];
-  uint32_t issued_phase[kKStages], issued_phase_b[kKStages];
-  for (int j = 0; j < kKStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
+  int issued[C::kKStages], issued_b[C::kKStages];
+  uint32_t issued_phase[C::kKStages], issued_phase_b[C::kKStages];
+  for (int j = 0; j < C::kKStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
   const uint64_t policy = l2_policy_evict_first();
   bool ok = true;
   while (ok && w.next(s)) {
     const int qrow0 = s.b * p.rows + rb * 128;
-    for (int j = 0; j < 2 && ok; ++j, ++i) {
-      const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
+    for (int j = 0; j < C::kQItems && ok; ++j, ++i) {
+      const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;
       if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl) ||
           !wait_bar(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) {
         ok = false;
@@ -461,67 +496,91 @@ __device__ void s_producer(const DecodeParams& p, const KvMaps* maps, Shared& sh
       issued_b[st] = 1, issued_phase_b[st] = ph;
       if (withhold && i == 0) continue;   // test hook: this block never arrives
       const uint32_t full = smem_u32(&sh.bar.full[st]);
-      mbar_arrive_expect_tx(full, kKStageBytes);
-      tma_load_3d(smem + kOffStage + st * kKStageBytes, &maps->q, full, 0, qrow0 + 64 * j, 0);
+      mbar_arrive_expect_tx(full, C::kQItemBytes);
+      tma_load_3d(smem + C::kOffStage + st * C::kKStageBytes, &maps->q, full, 0, qrow0 + C::kQRows * j, 0);
       issued[st] = 1, issued_phase[st] = ph;
     }
     for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
-      const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
-      const uint32_t stage = smem + kOffStage + st * kKStageBytes;
+      const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;
+      const uint32_t stage = smem + C::kOffStage + st * C::kKStageBytes;
       if (!wait_bar(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
       const int blk = request_block(p, s.b, k);
       const uint32_t full = smem_u32(&sh.bar.full[st]);
-      mbar_arrive_expect_tx(full, kKPartA * 8192);
+      mbar_arrive_expect_tx(full, C::kKPartA * kChunk);
       tma_load_3d_hint(stage, &maps->k_a, full, 0, blk * 64, 0, policy);
       issued[st] = 1, issued_phase[st] = ph;
       if (!wait_bar(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
       const uint32_t full_b = smem_u32(&sh.bar.full_b[st]);
-      mbar_arrive_expect_tx(full_b, kKStageBytes - kKPartA * 8192);
-      tma_load_3d_hint(stage + kKPartA * 8192, &maps->c4, full_b, 0, blk * 64, kKPartA, policy);
+      mbar_arrive_expect_tx(full_b, C::kKStageBytes - C::kKPartA * kChunk);
+      if constexpr (F8)   // the RoPE chunk: bytes 512..639 of the row, 576..639 filled with zeros
+        tma_load_2d_hint(stage + C::kKPartA * kChunk, &maps->rope, full_b, kDimV, blk * 64, policy);
+      else
+        tma_load_3d_hint(stage + C::kKPartA * kChunk, &maps->c4, full_b, 0, blk * 64, C::kKPartA, policy);
       issued_b[st] = 1, issued_phase_b[st] = ph;
     }
   }
-  for (int st = 0; st < kKStages; ++st) {   // loads still in flight land before the CTA may exit
+  for (int st = 0; st < C::kKStages; ++st) {   // loads still in flight land before the CTA may exit
     if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
     if (issued_b[st]) drain_bar(smem_u32(&sh.bar.full_b[st]), issued_phase_b[st]);
   }
 }
 
 // Warp 1 of the S-CTA; all 32 lanes run the loop, one elected lane issues.
-template <bool sparse>
+// bf16: 36 steps of K = 16 (9 chunks x 4), Q in TMEM columns [0, 288).
+// FP8: Q is held as two E4M3 terms, hi in columns [0, 144) and lo in [144, 288)
+// (S = Q_hi K^T + Q_lo K^T, one accumulator); 36 steps of K = 32: chunks 0..3 x 4 steps
+// x {hi, lo}, then the RoPE chunk's 2 steps x {hi, lo}.
+template <bool sparse, bool F8>
 __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl) {
+  using C = Cfg<F8>;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
   uint32_t i = 0, T = 0, seg = 0;
   const uint32_t tmem = sh.tmem_base;
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+  constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(128, 64, 0, 0) : idesc_bf16_f32(128, 64, 0, 0);
+  // one QK^T step: chunk c, 32-byte step j within its rows, Q term x (FP8 only)
+  auto step = [&](uint32_t d, uint32_t kstage, int c, int j, int x, uint32_t acc) {
+    const uint64_t bdesc = smem_desc_sw128(kstage + c * kChunk + j * 32, 16, 1024);
+    if constexpr (F8)
+      mma_f8_ts_warp(d, tmem + kQCol + x * 144 + c * 32 + j * 8, bdesc, idesc, acc);
+    else
+      mma_bf16_ts_warp(d, tmem + kQCol + c * 32 + j * 8, bdesc, idesc, acc);
+  };
   bool ok = true, any = false;
   while (ok && w.next(s)) {
-    i += 2;   // the q blocks are consumed by the softmax warps
+    i += C::kQItems;   // the q blocks are consumed by the softmax warps
     if (!warp_wait(sh, smem_u32(&sh.bar.q_full), seg & 1, p.status, cl)) break;
     for (int k = s.kb; k < s.ke; ++k, ++T, ++i) {
-      const uint32_t st = i % kKStages, ph = (i / kKStages) & 1;
+      const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;
       const uint32_t sb = T & 1, sph = (T >> 1) & 1;
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.s_empty[sb]), sph ^ 1, p.status, cl)) { ok = false; break; }
       if constexpr (sparse) fence_proxy_async_smem();   // gathered by cp.async: generic-proxy writes
       tc_fence_after();
-      const uint32_t kstage = smem + kOffStage + st * kKStageBytes;
+      const uint32_t kstage = smem + C::kOffStage + st * C::kKStageBytes;
       const uint32_t d = tmem + kSCol0 + sb * 64;
+      constexpr int kTerms = F8 ? 2 : 1;
 #pragma unroll
-      for (int kk = 0; kk < 4 * kKPartA; ++kk) {
-        const uint64_t bdesc = smem_desc_sw128(kstage + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-        mma_bf16_ts_warp(d, tmem + kQCol + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
-      }
-      mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // chunks 0..4 may be refilled
+      for (int c = 0; c < static_cast<int>(C::kKPartA); ++c)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int x = 0; x < kTerms; ++x) step(d, kstage, c, j, x, (c | j | x) ? 1u : 0u);
+      mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // part A may be refilled
       if (!warp_wait(sh, smem_u32(&sh.bar.full_b[st]), ph, p.status, cl)) { ok = false; break; }
       if constexpr (sparse) fence_proxy_async_smem();
       tc_fence_after();
+      if constexpr (F8) {
 #pragma unroll
-      for (int kk = 4 * kKPartA; kk < 36; ++kk) {
-        const uint64_t bdesc = smem_desc_sw128(kstage + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-        mma_bf16_ts_warp(d, tmem + kQCol + kk * 8, bdesc, idesc, 1u);
+        for (int j = 0; j < 2; ++j)   // dims 512..575: the first 64 bytes of the RoPE chunk
+#pragma unroll
+          for (int x = 0; x < 2; ++x) step(d, kstage, 4, j, x, 1u);
+      } else {
+#pragma unroll
+        for (int c = C::kKPartA; c < 9; ++c)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) step(d, kstage, c, j, 0, 1u);
       }
       mma_commit_warp(smem_u32(&sh.bar.empty_b[st]));
       mma_commit_warp(smem_u32(&sh.bar.s_full[sb]));
@@ -547,31 +606,78 @@ __device__ __forceinline__ float max32(const float (&x)[32]) {
   return m[0];
 }
 
-// Q rows of the segment from the two q-block stages into TMEM columns [0, 288):
-// thread (wg, r) moves dims [288 wg, 288 wg + 288) of row r (36 16-byte units).
-__device__ __forceinline__ void copy_q_to_tmem(uint32_t smem, uint32_t tmem_lane, uint32_t qstage0, uint32_t qstage1,
-                                               int wg, int r) {
-  const int rl = r & 63;
-  const uint32_t base = smem + kOffStage + ((r < 64) ? qstage0 : qstage1) * kKStageBytes + rl * 128;
+// bf16 cache: row r's q values into TMEM columns [0, 288), 2 per column.  `qrow` is
+// the address of the row's first 128 bytes in its q block (chunks of kQRows rows x 128 B);
+// thread (wg, r) moves dims [288 wg, 288 wg + 288) (36 16-byte units).
+__device__ __forceinline__ void copy_q_to_tmem(uint32_t qrow, uint32_t chunk_bytes, uint32_t tmem_lane, int wg, int rl) {
 #pragma unroll
   for (int c = 0; c < 9; ++c) {          // 9 groups of 4 units = 16 TMEM columns
     uint32_t v[16];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int u = wg * 36 + c * 4 + j;   // unit over the 576 dims: chunk u / 8, unit u % 8
-      const uint4 x = ld_shared_v4(base + (u >> 3) * 8192 + (((u & 7) ^ (rl & 7)) << 4));
+      const uint4 x = ld_shared_v4(qrow + (u >> 3) * chunk_bytes + (((u & 7) ^ (rl & 7)) << 4));
       v[4 * j] = x.x, v[4 * j + 1] = x.y, v[4 * j + 2] = x.z, v[4 * j + 3] = x.w;
     }
     tmem_st16(tmem_lane + kQCol + wg * 144 + c * 16, v);
   }
 }
 
+// FP8 cache: row r's q values as two E4M3 terms, 4 values per TMEM column.  sc is the
+// power of two that puts max|q| over the row in (224, 448]; hi = e4m3(q sc) goes to
+// columns [0, 144) and lo = e4m3(q sc - hi) to [144, 288).  A bf16 value has 8
+// significant bits: hi keeps the top 4 and the remainder, a multiple of q's last bit
+// no larger than 8 of them, fits lo exactly, so hi + lo = q sc and QK^T is exact up to
+// fp32 accumulation (values below ~2^-5 after scaling may lose their last bits).  One
+// E4M3 term alone (2^-4 relative) would move the scores too much.  Thread (wg, r)
+// converts dims [288 wg, 288 wg + 288); the two warpgroups agree on the row's maximum
+// through pm_mine / pm_other (named barrier 1).  Returns 1 / sc.
+__device__ __forceinline__ float copy_q_to_tmem_f8(uint32_t qrow, uint32_t chunk_bytes, uint32_t tmem_lane, int wg,
+                                                   int rl, uint32_t pm_mine, uint32_t pm_other) {
+  auto unit = [&](int u) { return ld_shared_v4(qrow + (u >> 3) * chunk_bytes + (((u & 7) ^ (rl & 7)) << 4)); };
+  auto amax2 = [](float m, uint32_t w) { return fmaxf(m, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w)))); };
+  float amax = 0.f;
+#pragma unroll 4
+  for (int j = 0; j < 36; ++j) {
+    const uint4 x = unit(wg * 36 + j);
+    amax = amax2(amax2(amax2(amax2(amax, x.x), x.y), x.z), x.w);
+  }
+  asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine), "f"(amax) : "memory");
+  named_bar_sync(1, 256);
+  amax = fmaxf(amax, ld_shared_f32(pm_other));
+  const float t = amax > 0.f ? fminf(448.f / amax, 0x1p100f) : 1.f;
+  const float sc = __uint_as_float(__float_as_uint(t) & 0x7F800000u);   // 2^floor(log2 t)
+#pragma unroll 1
+  for (int c = 0; c < 9; ++c) {          // 4 units = 32 dims = 8 columns of each term
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 x = unit(wg * 36 + c * 4 + j);
+      const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {      // dims 4e..4e+3 of the unit -> one column
+        const float v0 = bf16_lo(wv[2 * e]) * sc, v1 = bf16_hi(wv[2 * e]) * sc;
+        const float v2 = bf16_lo(wv[2 * e + 1]) * sc, v3 = bf16_hi(wv[2 * e + 1]) * sc;
+        const uint32_t h01 = cvt_e4m3x2(v0, v1), h23 = cvt_e4m3x2(v2, v3);
+        const float2 f01 = e4m3x2_to_float2(h01), f23 = e4m3x2_to_float2(h23);
+        hi[2 * j + e] = h01 | (h23 << 16);
+        lo[2 * j + e] = cvt_e4m3x2(v0 - f01.x, v1 - f01.y) | (cvt_e4m3x2(v2 - f23.x, v3 - f23.y) << 16);
+      }
+    }
+    tmem_st8(tmem_lane + kQCol + wg * 72 + c * 8, hi);
+    tmem_st8(tmem_lane + kQCol + 144 + wg * 72 + c * 8, lo);
+  }
+  return 1.f / sc;
+}
+
 // Warps 4..11 of the S-CTA.  Warpgroup wg (0 or 1) handles columns [32*wg, 32*wg+32)
 // of every page for its 128 rows; the two exchange row maxima and partial sums
 // through shared memory and use named barrier 1 (256 threads).
-template <bool sparse>
+template <bool sparse, bool F8>
 __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb,
                               uint32_t peer) {
+  using C = Cfg<F8>;
+  static_assert(!(sparse && F8), "the sparse decode reads a bf16 cache");
   // Dense: two warpgroups, each covering 32 of a page's 64 columns.  Sparse: one
   // warpgroup covering all 64 in two passes (the other four warps gather).
   constexpr int kWG = sparse ? 1 : 2;
@@ -586,11 +692,12 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
   const bool row_valid = g < p.rows;
   const int pos_i = row_valid ? g / p.H : 0;
   const uint32_t tmem_lane = sh.tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
-  const uint32_t peer_recv = map_to_rank(smem + kOffRecv, peer);
+  const uint32_t peer_recv = map_to_rank(smem + C::kOffRecv, peer);
   const uint32_t peer_pfull0 = map_to_rank(smem_u32(&sh.bar.p_full[0]), peer);
-  const uint32_t pm_mine = smem + kOffPm + (wg * 128 + r) * 4;
-  const uint32_t pm_other = smem + kOffPm + ((1 - wg) * 128 + r) * 4;
-  const uint32_t lpart = smem + kOffLpart + r * 4;
+  const uint32_t pm_mine = smem + C::kOffPm + (wg * 128 + r) * 4;
+  const uint32_t pm_other = smem + C::kOffPm + ((1 - wg) * 128 + r) * 4;
+  const uint32_t lpart = smem + C::kOffLpart + r * 4;
+  float sl2 = p.scale_log2;                 // raw score -> log2 units (FP8: per row, set with Q)
   SegmentWalker w;
   w.init(p, part);
   Segment s;
@@ -604,27 +711,35 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
     const int vis_pos = (sparse && p.causal) ? __ldg(p.seqlens + s.b) - p.s_q + (row_valid ? pos_i : 0) + 1 : 0;
     {   // Q of this request into TMEM (every QK^T of the previous segment is complete:
         // its last S was waited for below)
-      const uint32_t q0 = i % kKStages, q1 = (i + 1) % kKStages;
-      const uint32_t mine = (r < 64) ? q0 : q1;
-      const uint32_t mph = ((i + ((r < 64) ? 0u : 1u)) / kKStages) & 1;
+      const uint32_t qi = static_cast<uint32_t>(r / C::kQRows);   // this row's q block
+      const uint32_t mine = (i + qi) % C::kKStages;
+      const uint32_t mph = ((i + qi) / C::kKStages) & 1;
       const bool got = wait_bar(sh, smem_u32(&sh.bar.full[mine]), mph, p.status, cl);
       if (named_bar_or(1, kST, !got)) break;
+      constexpr uint32_t kQChunk = C::kQRows * 128;   // bytes per 64-dim chunk of a q block
+      const int rl = r % C::kQRows;
+      const uint32_t qrow = smem + C::kOffStage + mine * C::kKStageBytes + rl * 128;
+      if constexpr (F8) {
+        sl2 = p.scale_log2 * p.kv_scale * copy_q_to_tmem_f8(qrow, kQChunk, tmem_lane, wg, rl, pm_mine, pm_other);
+      } else {
 #pragma unroll
-      for (int h = 0; h < kPieces; ++h) copy_q_to_tmem(smem, tmem_lane, q0, q1, wg + h, r);
+        for (int h = 0; h < kPieces; ++h) copy_q_to_tmem(qrow, kQChunk, tmem_lane, wg + h, rl);
+      }
       tmem_wait_st();
       tc_fence_before();
       named_bar_sync(1, kST);
       if (t == 0) {
         mbar_arrive(smem_u32(&sh.bar.q_full));
-        mbar_arrive(smem_u32(&sh.bar.empty[q0]));
-        mbar_arrive(smem_u32(&sh.bar.empty_b[q0]));
-        mbar_arrive(smem_u32(&sh.bar.empty[q1]));
-        mbar_arrive(smem_u32(&sh.bar.empty_b[q1]));
+        for (int j = 0; j < C::kQItems; ++j) {
+          const uint32_t qs = (i + j) % C::kKStages;
+          mbar_arrive(smem_u32(&sh.bar.empty[qs]));
+          mbar_arrive(smem_u32(&sh.bar.empty_b[qs]));
+        }
         SegmentWalker nx = w;   // the next segment's q rows and block-table row, into L2 now
         Segment ns;
         if (nx.next(ns)) prefetch_request(p, ns.b);
       }
-      i += 2 + static_cast<uint32_t>(s.ke - s.kb);   // ring items of this segment
+      i += C::kQItems + static_cast<uint32_t>(s.ke - s.kb);   // ring items of this segment
     }
     float m_ref = -INFINITY, l = 0.f;   // reference maximum (log2 units) and running sum of the rows
     float l_hi = 0.f;                   // one warpgroup: the running sum of columns 32..63
@@ -677,15 +792,15 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       if (named_bar_or(1, kST, !ok_t)) { ok = false; break; }
       // softmax_scale > 0, so the scaled maximum is the scaled raw maximum
       const float row_max = (kWG == 2) ? fmaxf(my_max, ld_shared_f32(pm_other)) : my_max;
-      const float m_new = fmaxf(m_ref, row_max * p.scale_log2);
+      const float m_new = fmaxf(m_ref, row_max * (F8 ? sl2 : p.scale_log2));
       float alpha = 1.f;
-      const bool rebase = m_new > m_ref + kRescaleLog2;
+      const bool rebase = m_new > m_ref + C::kRescaleLog2;
       if (rebase) {
         alpha = fast_exp2(m_ref - m_new);       // 0 when m_ref = -inf
         m_ref = m_new;
       }
-      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      const uint32_t slot = smem + kOffSend + sb * kPktStride;
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : (F8 ? C::kPOffset - m_ref : -m_ref);
+      const uint32_t slot = smem + C::kOffSend + sb * kPktStride;
       const uint32_t row = slot + r * 128;
       float lsum[kPieces];
 #pragma unroll
@@ -694,18 +809,38 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
         if constexpr (kWG == 1) load_scores(cb);   // the second pass reads the scores again
         uint32_t pk[16];
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        // l sums the fp32 probabilities; P goes to the MMA in bf16, or (FP8) as two E4M3
+        // terms hi + lo: bytes 0..63 of the row hold hi of tokens 0..63, bytes 64..127 lo
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {   // l sums the fp32 probabilities; P goes to the MMA in bf16
-          const float e0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, neg_m));
-          const float e1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, neg_m));
-          pk[c] = pack_bf16x2(e0, e1);
+        for (int c = 0; c < 16; ++c) {
+          const float e0 = fast_exp2(fmaf(sv[2 * c], F8 ? sl2 : p.scale_log2, neg_m));
+          const float e1 = fast_exp2(fmaf(sv[2 * c + 1], F8 ? sl2 : p.scale_log2, neg_m));
+          if constexpr (F8) {
+            const uint32_t h2 = cvt_e4m3x2(e0, e1);
+            const float2 hf = e4m3x2_to_float2(h2);
+            const uint32_t l2 = cvt_e4m3x2(e0 - hf.x, e1 - hf.y);
+            if (c & 1) pk[c >> 1] |= h2 << 16, pk[8 + (c >> 1)] |= l2 << 16;
+            else pk[c >> 1] = h2, pk[8 + (c >> 1)] = l2;
+          } else {
+            pk[c] = pack_bf16x2(e0, e1);
+          }
           ps[c & 3] += e0 + e1;
         }
         lsum[h] = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        if constexpr (F8) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int cc = cb / 8 + j;              // 16-byte chunk: tokens 8cc .. 8cc+7
-          st_shared_v4(row + ((cc ^ (r & 7)) << 4), make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
+          for (int j = 0; j < 2; ++j) {
+            const int cc = cb / 16 + j;             // 16-byte chunk: tokens 16cc .. 16cc+15
+            st_shared_v4(row + ((cc ^ (r & 7)) << 4), make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
+            st_shared_v4(row + (((4 + cc) ^ (r & 7)) << 4),
+                         make_uint4(pk[8 + 4 * j], pk[9 + 4 * j], pk[10 + 4 * j], pk[11 + 4 * j]));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int cc = cb / 8 + j;              // 16-byte chunk: tokens 8cc .. 8cc+7
+            st_shared_v4(row + ((cc ^ (r & 7)) << 4), make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
+          }
         }
       }
       if constexpr (kWG == 1) release_s();
@@ -725,9 +860,9 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       }
       if (wg == 0) {
         asm volatile("st.shared.f32 [%0], %1;" :: "r"(slot + kPktAlpha + r * 4), "f"(alpha) : "memory");
-        if (last)
-          asm volatile("st.shared.f32 [%0], %1;" :: "r"(slot + kPktInvL + r * 4), "f"(l > 0.f ? 1.f / l : 0.f)
-                       : "memory");
+        if (last)   // the output factor: 1/l (FP8: kv_scale / l, the value codes' scale)
+          asm volatile("st.shared.f32 [%0], %1;" :: "r"(slot + kPktInvL + r * 4),
+                       "f"(l > 0.f ? (F8 ? p.kv_scale : 1.f) / l : 0.f) : "memory");
       }
       fence_proxy_async_smem();
       named_bar_sync(1, kST);
@@ -738,7 +873,7 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
     }
     if (!ok) break;
     if (row_valid && wg == 0) {
-      const float lse = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+      const float lse = l > 0.f ? ((F8 ? m_ref - C::kPOffset : m_ref) + log2f(l)) * kLn2 : -INFINITY;
       const int ns0 = __ldg(p.num_splits + s.b);
       const int nsplit = __ldg(p.num_splits + s.b + 1) - ns0;
       if (nsplit == 1)
@@ -751,40 +886,45 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
 }
 
 // ------------------------------------------------------------------ O-CTA --
-// Warp 1 of the O-CTA (all 32 lanes; one elected lane issues the MMAs).
-template <bool sparse>
+// Warp 1 of the O-CTA (all 32 lanes; one elected lane issues the MMAs).  Per page and
+// 256-column half of O: bf16, one MMA per 16 tokens; FP8, two per 32 tokens (the hi and
+// the lo term of P against the same value rows).
+template <bool sparse, bool F8>
 __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl) {
+  using C = Cfg<F8>;
+  constexpr int kHalfChunks = static_cast<int>(C::kVChunks / 2);
+  constexpr int kTerms = F8 ? 2 : 1;
   const int lane = threadIdx.x & 31;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
   uint32_t T = 0, seg = 0, nresc = 0;
   const uint32_t tmem = sh.tmem_base;
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
+  constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(128, 256, 0, 1) : idesc_bf16_f32(128, 256, 0, 1);
   bool ok = true, any = false;
   while (ok && w.next(s)) {
     if (seg > 0 && !warp_wait(sh, smem_u32(&sh.bar.o_free), (seg - 1) & 1, p.status, cl)) break;
     const int L = __ldg(p.lens + s.b);
     for (int k = s.kb; k < s.ke; ++k, ++T) {
-      const uint32_t st = T % kVStages, ph = (T / kVStages) & 1;
+      const uint32_t st = T % C::kVStages, ph = (T / C::kVStages) & 1;
       const uint32_t ps = T % kSlots, pph = (T / kSlots) & 1;
-      const uint32_t vstage = smem + kOffStage + st * kVStageBytes;
-      const uint32_t pkt = smem + kOffRecv + ps * kPktStride;
+      const uint32_t vstage = smem + C::kOffStage + st * C::kVStageBytes;
+      const uint32_t pkt = smem + C::kOffRecv + ps * kPktStride;
       if (lane == 0) mbar_arrive_expect_tx(smem_u32(&sh.bar.p_full[ps]), kPktStride);
       __syncwarp();
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.p_full[ps]), pph, p.status, cl, true)) { ok = false; break; }
       if constexpr (sparse) fence_proxy_async_smem();
-      // tail page: zero the value rows past the sequence end up to the next 16-row
+      // tail page: zero the value rows past the sequence end up to the next MMA-step
       // boundary, so that P = 0 never meets a non-finite value in the MMA (per half)
       const int nvalid = min(64, L - k * 64);
-      const int krows = (nvalid + 15) & ~15;
+      const int krows = (nvalid + C::kKStep - 1) & ~(C::kKStep - 1);
       auto zero_tail = [&](uint32_t half) {
         if (nvalid < krows) {
-          const int nz = krows - nvalid;                 // rows to clear, < 16
-          for (int i = lane; i < nz * 4 * 8; i += 32) {  // rows x chunks x 16-byte units
-            const int row = nvalid + i / 32, chunk = (i / 8) % 4, u = i % 8;
-            st_shared_v4(half + chunk * 8192 + row * 128 + u * 16, make_uint4(0, 0, 0, 0));
+          const int nz = krows - nvalid;                           // rows to clear, < kKStep
+          for (int i = lane; i < nz * kHalfChunks * 8; i += 32) {  // rows x chunks x 16-byte units
+            const int row = nvalid + i / (kHalfChunks * 8), chunk = (i / 8) % kHalfChunks, u = i % 8;
+            st_shared_v4(half + chunk * kChunk + row * 128 + u * 16, make_uint4(0, 0, 0, 0));
           }
           fence_proxy_async_smem();
         }
@@ -792,7 +932,7 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       zero_tail(vstage);
       const bool last = (k == s.ke - 1);
       if (last)     // keep 1/l of the segment's rows before the slot can be reused
-        st_shared_v4(smem + kOffInvL + lane * 16, ld_shared_v4(pkt + kPktInvL + lane * 16));
+        st_shared_v4(smem + C::kOffInvL + lane * 16, ld_shared_v4(pkt + kPktInvL + lane * 16));
       bool need = false;
       if (k != s.kb) {   // did any row rebase its maximum on this page?
         const uint4 a = ld_shared_v4(pkt + kPktAlpha + lane * 16);
@@ -815,23 +955,28 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       __syncwarp();
       tc_fence_after();
       {
-        const int ksteps = krows / 16;
-        for (int js = 0; js < ksteps; ++js) {   // output columns 0..255 from value chunks 0..3
-          const uint64_t adesc = smem_desc_sw128(pkt + js * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(vstage + js * 2048, 8192, 1024);
-          mma_bf16_ss_warp(tmem, adesc, bdesc, idesc, (k == s.kb && js == 0) ? 0u : 1u);
-        }
-        mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // chunks 0..3 may be refilled
+        const int ksteps = krows / C::kKStep;
+        // O[:, 256 h .. 256 h + 255] += P V over the value chunks of half h; step js covers
+        // tokens [kKStep js, kKStep js + kKStep) (P: 32 bytes of the row, term x at byte 64 x)
+        auto pv = [&](int h, uint32_t vhalf) {
+          for (int js = 0; js < ksteps; ++js)
+#pragma unroll
+            for (int x = 0; x < kTerms; ++x) {
+              const uint64_t adesc = smem_desc_sw128(pkt + x * 64 + js * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc_sw128(vhalf + js * C::kKStep * 128, 8192, 1024);
+              const uint32_t acc = (k == s.kb && js == 0 && x == 0) ? 0u : 1u;
+              if constexpr (F8) mma_f8_ss_warp(tmem + 256 * h, adesc, bdesc, idesc, acc);
+              else mma_bf16_ss_warp(tmem + 256 * h, adesc, bdesc, idesc, acc);
+            }
+        };
+        pv(0, vstage);                                  // output columns 0..255
+        mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // the first half may be refilled
         if (!warp_wait(sh, smem_u32(&sh.bar.full_b[st]), ph, p.status, cl)) { ok = false; break; }
         if constexpr (sparse) fence_proxy_async_smem();
-        zero_tail(vstage + kVStageBytes / 2);
+        zero_tail(vstage + C::kVStageBytes / 2);
         __syncwarp();
         tc_fence_after();
-        for (int js = 0; js < ksteps; ++js) {   // output columns 256..511 from value chunks 4..7
-          const uint64_t adesc = smem_desc_sw128(pkt + js * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(vstage + kVStageBytes / 2 + js * 2048, 8192, 1024);
-          mma_bf16_ss_warp(tmem + 256, adesc, bdesc, idesc, (k == s.kb && js == 0) ? 0u : 1u);
-        }
+        pv(1, vstage + C::kVStageBytes / 2);            // output columns 256..511
         mma_commit_warp(smem_u32(&sh.bar.empty_b[st]));
         mma_commit_warp(smem_u32(&sh.bar.p_free[ps]));
         if (last) mma_commit_warp(smem_u32(&sh.bar.o_full));
@@ -882,8 +1027,9 @@ __device__ void o_cta_forwarder(const DecodeParams& p, Shared& sh, int part, uin
 // segment.  Warpgroup wg owns O columns [256 wg, 256 wg + 256).
 // Dense: two warpgroups, one per 256-column half of O; sparse: warps 4..7 alone cover both
 // halves (warps 8..11 gather).
-template <bool sparse>
+template <bool sparse, bool F8>
 __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb) {
+  using C = Cfg<F8>;
   constexpr int kHalves = sparse ? 2 : 1;   // 256-column halves of O per thread
   const int t = threadIdx.x - 128;
   const int wg = t >> 7;
@@ -901,7 +1047,7 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
     const int cmd = sh.cmd, arg = sh.cmd_arg;
     if (cmd == 3) break;
     if (cmd == 1) {
-      const float alpha = ld_shared_f32(smem + kOffRecv + arg * kPktStride + kPktAlpha + r * 4);
+      const float alpha = ld_shared_f32(smem + C::kOffRecv + arg * kPktStride + kPktAlpha + r * 4);
       tc_fence_after();
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
@@ -925,7 +1071,7 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
     if (!have_seg) break;
     if (!warp_wait(sh, smem_u32(&sh.bar.o_full), seg & 1, p.status, cl)) break;
     tc_fence_after();
-    const float inv_l = ld_shared_f32(smem + kOffInvL + r * 4);
+    const float inv_l = ld_shared_f32(smem + C::kOffInvL + r * 4);
     const int ns0 = __ldg(p.num_splits + s.b);
     const int nsplit = __ldg(p.num_splits + s.b + 1) - ns0;
     const bool final_out = (nsplit == 1);
@@ -936,7 +1082,7 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
     const int g0 = rb * 128 + wq * 32;    // the warp's first row within the request
     __nv_bfloat16* const obase0 = p.out + (static_cast<int64_t>(s.b) * p.rows + g0) * 512;
     float* const pbase0 = p.o_part + (static_cast<int64_t>(ns0 + s.split) * p.rows + g0) * 512;
-    const uint32_t stg = smem + kOffEpi + ((wg << 2) | wq) * 2048;
+    const uint32_t stg = smem + C::kOffEpi + ((wg << 2) | wq) * 2048;
     const int tq = lane & 3;                // transposed: 16-byte quad tq of rows 8j + (lane >> 2)
     auto put = [&](int j, uint4 u) { st_shared_v4(stg + lane * 64 + ((j ^ (lane & 3)) << 4), u); };
     auto get = [&](int j) {
@@ -1003,9 +1149,12 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
 }  // namespace
 
 // kSparse: the pages are gathered from the top-k lists (p.indices) instead of read whole.
-template <bool kSparse>
+// kF8: the cache holds E4M3 codes with one per-tensor scale (p.kv_scale).
+template <bool kSparse, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
+  static_assert(!(kSparse && kF8), "the sparse decode reads a bf16 cache");
+  using C = Cfg<kF8>;
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   const uint32_t base = smem_u32(dyn_smem);
   if (base & 1023u) {   // the layout needs a 1024-byte aligned base (no static shared memory is declared)
@@ -1013,7 +1162,7 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     return;             // every CTA of the grid takes this branch alike
   }
   const uint32_t smem = base;
-  Shared& sh = *reinterpret_cast<Shared*>(dyn_smem + kOffShared);
+  Shared& sh = *reinterpret_cast<Shared*>(dyn_smem + C::kOffShared);
   const int warp = threadIdx.x >> 5;
   const uint32_t rank = cluster_ctarank();
   const uint32_t cl = 2u * static_cast<uint32_t>(p.n_rb);   // CTAs per cluster
@@ -1026,13 +1175,14 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     if (is_s) {
       prefetch_tensormap(&maps.q);
       prefetch_tensormap(&maps.k_a);
+      if (kF8) prefetch_tensormap(&maps.rope);
     }
     prefetch_tensormap(&maps.c4);
     sh.abort = 0;
     sh.cmd = 0;
     // sparse: one arrival per gathering lane
     const uint32_t fills = kSparse ? 32u * static_cast<uint32_t>(is_s ? kSGatherWarps : kOGatherWarps) : 1u;
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(smem_u32(&sh.bar.full[i]), fills);
       mbar_init(smem_u32(&sh.bar.empty[i]), 1);
       mbar_init(smem_u32(&sh.bar.full_b[i]), fills);
@@ -1072,23 +1222,23 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     if (kSparse && gather_slot(true, warp) >= 0) {   // the gathering warps
       s_producer_sparse(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0, gather_slot(true, warp));
     } else if (warp == 0) {
-      if ((threadIdx.x & 31) == 0) s_producer(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
+      if ((threadIdx.x & 31) == 0) s_producer<kF8>(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
     } else if (warp == 1) {
-      s_cta_mma<kSparse>(p, sh, smem, part, cl);
+      s_cta_mma<kSparse, kF8>(p, sh, smem, part, cl);
     } else if (warp >= 4) {
-      s_cta_softmax<kSparse>(p, sh, smem, part, cl, rb, peer);
+      s_cta_softmax<kSparse, kF8>(p, sh, smem, part, cl, rb, peer);
     }
   } else {
     if (kSparse && gather_slot(false, warp) >= 0) {   // the gathering warps
       o_producer_sparse(p, sh, smem, part, cl, gather_slot(false, warp));
     } else if (warp == 0) {
-      if ((threadIdx.x & 31) == 0) o_producer(p, &maps, sh, smem, part, cl);
+      if ((threadIdx.x & 31) == 0) o_producer<kF8>(p, &maps, sh, smem, part, cl);
     } else if (warp == 1) {
-      o_cta_mma<kSparse>(p, sh, smem, part, cl);
+      o_cta_mma<kSparse, kF8>(p, sh, smem, part, cl);
     } else if (warp == 2) {
       if ((threadIdx.x & 31) == 0) o_cta_forwarder(p, sh, part, cl, peer);
     } else if (warp >= 4) {
-      o_cta_epilogue<kSparse>(p, sh, smem, part, cl, rb);
+      o_cta_epilogue<kSparse, kF8>(p, sh, smem, part, cl, rb);
     }
   }
 
@@ -1104,18 +1254,23 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
 }
 
 cudaError_t decode_set_attributes() {
-  const cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(Cfg<false>::kSmemBytes));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemBytes));
+  e = cudaFuncSetAttribute(mla_decode_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(Cfg<false>::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(Cfg<true>::kSmemBytes));
 }
 
 // attr[0] = the cluster shape; with pdl, attr[1] = programmatic stream serialisation
+// (both cache formats use the same amount of shared memory)
+static_assert(Cfg<false>::kSmemBytes == Cfg<true>::kSmemBytes, "one launch shape for both formats");
 static cudaLaunchConfig_t decode_config(int grid_ctas, int cluster_ctas, cudaStream_t stream,
                                         cudaLaunchAttribute* attr, bool pdl) {
-  cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(grid_ctas), 1, 1), dim3(kThreads, 1, 1), kSmemBytes,
-                                      stream, attr + 1);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(grid_ctas), 1, 1), dim3(kThreads, 1, 1),
+                                      Cfg<false>::kSmemBytes, stream, attr + 1);
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_ctas);
   attr[0].val.clusterDim.y = 1;
@@ -1129,7 +1284,7 @@ int decode_max_clusters(int cluster_ctas) {
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = decode_config(cluster_ctas, cluster_ctas, nullptr, attr, false);
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, mla_decode_kernel<false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, mla_decode_kernel<false, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1139,8 +1294,9 @@ int decode_max_clusters(int cluster_ctas) {
 cudaError_t launch_decode(const KvMaps& maps, const DecodeParams& p, int cluster_ctas, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = decode_config(p.num_parts * cluster_ctas, cluster_ctas, stream, attr, true);
-  if (p.indices) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, maps, p);
-  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, maps, p);
+  if (p.indices) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, false>, maps, p);
+  if (p.kv_fp8) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, true>, maps, p);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, false>, maps, p);
 }
 
 }  // namespace mla

@@ -104,6 +104,34 @@ bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, cons
          enc(&maps->q, q, q_rows, kDimQK / 64);
 }
 
+bool encode_kv_maps_fp8(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache,
+                        int64_t num_blocks, const void* q, int64_t q_rows) {
+  const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks * kPageTokens);
+  const cuuint32_t es[3] = {1, 1, 1};
+  auto enc3 = [&](CUtensorMap* m, uint32_t chunks) {   // [chunk][row][128 codes] of dims 0..511
+    const cuuint64_t dims[3] = {128, rows, kDimV / 128};
+    const cuuint64_t strides[2] = {kDimQK, 128};
+    const cuuint32_t box[3] = {128, 64, chunks};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv_cache), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  const cuuint64_t rdims[2] = {kDimQK, rows};
+  const cuuint64_t rstrides[1] = {kDimQK};
+  const cuuint32_t rbox[2] = {128, 64};
+  const bool rope_ok = encode(&maps->rope, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv_cache), rdims,
+                              rstrides, rbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  // q: bf16 [chunk 0..8][q row][64 dims] in boxes of 32 rows
+  const cuuint64_t qdims[3] = {64, static_cast<cuuint64_t>(q_rows), kDimQK / 64};
+  const cuuint64_t qstrides[2] = {kDimQK * 2, 128};
+  const cuuint32_t qbox[3] = {64, 32, kDimQK / 64};
+  const bool q_ok = encode(&maps->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qdims, qstrides, qbox,
+                           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc3(&maps->k_a, 4) && enc3(&maps->c4, 2) && rope_ok && q_ok;
+}
+
 namespace {
 
 size_t max_splits(int B, int num_parts) { return static_cast<size_t>(B) + static_cast<size_t>(num_parts); }
@@ -185,12 +213,14 @@ size_t mla_decode_workspace_size(int B, int s_q, int H, int num_sm_parts) {
 
 namespace {
 
-// Shared body of mla_decode (indices == nullptr) and mla_decode_sparse.
-mla_status_t decode_impl(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_t num_blocks,
-                         const int32_t* block_table, int max_blocks, const int32_t* seqlens, const int32_t* indices,
-                         int64_t idx_stride, const int32_t* topk_lens, int B, int s_q, int H, float softmax_scale,
-                         int causal_s_q, const void* metadata, int num_sm_parts, void* workspace,
-                         size_t workspace_bytes, mla_bf16_t* out, float* lse, mla_stream_t stream) {
+// Shared body of mla_decode (indices == nullptr), mla_decode_sparse and mla_decode_fp8
+// (kv_fp8: kv_cache holds E4M3 codes scaled by kv_scale).
+mla_status_t decode_impl(const void* q, const void* kv_cache, int64_t num_blocks, const int32_t* block_table,
+                         int max_blocks, const int32_t* seqlens, const int32_t* indices, int64_t idx_stride,
+                         const int32_t* topk_lens, int B, int s_q, int H, float softmax_scale, int causal_s_q,
+                         const void* metadata, int num_sm_parts, void* workspace, size_t workspace_bytes,
+                         mla_bf16_t* out, float* lse, mla_stream_t stream, bool kv_fp8 = false,
+                         float kv_scale = 1.f) {
   if (!q || !kv_cache || !block_table || !seqlens || !metadata || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (B < 1 || s_q < 1 || H < 1 || num_blocks < 1 || max_blocks < 1 || num_sm_parts < 1) return MLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
@@ -201,6 +231,7 @@ mla_status_t decode_impl(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_
                   (reinterpret_cast<uintptr_t>(topk_lens) & 3u)))
     return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (kv_fp8 && (!std::isfinite(kv_scale) || !(kv_scale > 0.f))) return MLA_ERR_INVALID_ARG;
   const int n_rb = pairs_for(s_q, H);
   if (n_rb > kMaxPairsPerCluster) return MLA_ERR_UNSUPPORTED;
   if (num_blocks * kPageTokens > (int64_t(1) << 31) - kPageTokens) return MLA_ERR_UNSUPPORTED;
@@ -212,7 +243,9 @@ mla_status_t decode_impl(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_
   if (st != MLA_OK) return st;
 
   KvMaps kv_maps;
-  if (!encode_kv_maps(g_encode, &kv_maps, kv_cache, num_blocks, q, static_cast<int64_t>(B) * s_q * H))
+  const int64_t q_rows = static_cast<int64_t>(B) * s_q * H;
+  if (!(kv_fp8 ? encode_kv_maps_fp8(g_encode, &kv_maps, kv_cache, num_blocks, q, q_rows)
+               : encode_kv_maps(g_encode, &kv_maps, kv_cache, num_blocks, q, q_rows)))
     return MLA_ERR_CUDA;
 
   const int rows = s_q * H;
@@ -244,6 +277,8 @@ mla_status_t decode_impl(const mla_bf16_t* q, const mla_bf16_t* kv_cache, int64_
   p.status = d->status;
   p.withhold_first_load = g_withhold_first_load;
   g_withhold_first_load = 0;
+  p.kv_fp8 = kv_fp8 ? 1 : 0;
+  p.kv_scale = kv_fp8 ? kv_scale : 1.f;
 
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (launch_decode(kv_maps, p, 2 * n_rb, cs) != cudaSuccess) return MLA_ERR_CUDA;
@@ -273,6 +308,16 @@ mla_status_t mla_decode_sparse(const mla_bf16_t* q, const mla_bf16_t* kv_cache, 
   return decode_impl(q, kv_cache, num_blocks, block_table, max_blocks, seqlens, indices, index_stride, topk_lens, B,
                      s_q, H, softmax_scale, causal_s_q, metadata, num_sm_parts, workspace, workspace_bytes, out, lse,
                      stream);
+}
+
+mla_status_t mla_decode_fp8(const mla_bf16_t* q, const uint8_t* kv_cache, float kv_scale, int64_t num_blocks,
+                            const int32_t* block_table, int max_blocks, const int32_t* seqlens, int B, int s_q, int H,
+                            float softmax_scale, int causal_s_q, const void* metadata, int num_sm_parts,
+                            void* workspace, size_t workspace_bytes, mla_bf16_t* out, float* lse,
+                            mla_stream_t stream) {
+  return decode_impl(q, kv_cache, num_blocks, block_table, max_blocks, seqlens, nullptr, 0, nullptr, B, s_q, H,
+                     softmax_scale, causal_s_q, metadata, num_sm_parts, workspace, workspace_bytes, out, lse, stream,
+                     true, kv_scale);
 }
 
 }  // extern "C"

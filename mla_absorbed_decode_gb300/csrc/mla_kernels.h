@@ -51,24 +51,36 @@ struct DecodeParams {
   float* lse;                           // [B][rows]
   int* status;
   int withhold_first_load;
+  // FP8 cache: kv holds E4M3 codes (576 bytes a token) and a cached value is its code's
+  // value times kv_scale.
+  int kv_fp8 = 0;
+  float kv_scale = 1.f;
 };
 
-// Tensor maps of the decode kernel.  The paged latent cache and q are both viewed
-// as [chunk 0..8][row][64 dims]: dim 0 = 64 dims of a chunk (128 B, contiguous),
-// dim 1 = rows (stride 1152 B: cache tokens, or q rows b * s_q * H + i * H + h),
-// dim 2 = chunk (stride 128 B).  A box lands in the swizzled, chunk-major shared-
-// memory layout the MMAs read: k_a = chunks 0..4 of a page (40 KiB), c4 = four
-// chunks of a page (32 KiB: K chunks 5..8, V chunks 0..3 or 4..7), q = 64 q rows
-// (72 KiB).
+// Tensor maps of the decode kernel.  Every box lands in the swizzled (128-byte),
+// chunk-major shared-memory layout the MMAs read: chunks of 128-byte rows.
+// bf16 cache: the cache and q are both viewed as [chunk 0..8][row][64 dims]: dim 0 =
+// 64 dims of a chunk (128 B, contiguous), dim 1 = rows (stride 1152 B: cache tokens,
+// or q rows b * s_q * H + i * H + h), dim 2 = chunk (stride 128 B); k_a = chunks 0..4
+// of a page (40 KiB), c4 = four chunks (32 KiB: K chunks 5..8, V chunks 0..3 or 4..7),
+// q = 64 q rows (72 KiB).
+// FP8 cache: the cache is viewed as [chunk 0..3][row][128 codes] (row stride 576 B):
+// k_a = chunks 0..3 of a page (32 KiB), c4 = two chunks (16 KiB: V chunks 0..1 or
+// 2..3); rope = the cache as [row][576 codes], read as a 128-code box at code 512 (the
+// 64 RoPE codes, the rest of the box filled with zeros); q = 32 q rows (36 KiB).
 struct KvMaps {
   CUtensorMap k_a;
   CUtensorMap c4;
   CUtensorMap q;
+  CUtensorMap rope;   // FP8 cache only
 };
-// Encodes the three maps for a cache of num_blocks pages and q_rows rows of q;
-// false on failure.
+// Encodes the maps for a bf16 cache of num_blocks pages and q_rows rows of q; false on
+// failure.
 bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache, int64_t num_blocks,
                     const void* q, int64_t q_rows);
+// The same for an FP8 (E4M3) cache.
+bool encode_kv_maps_fp8(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache,
+                        int64_t num_blocks, const void* q, int64_t q_rows);
 
 // Device address of the kernels' status word on the current device (set-up on
 // first use); nullptr on error.

@@ -13,6 +13,12 @@ Tolerances (written here, used by every parity test):
   being loose when |out| is small;
 * lse: |delta| <= 1e-3 * max(1, |ref|);
 * integer schedule and indexing: bit-exact.
+The FP8-cache decode is held to the same bounds against the oracle's decode over the
+dequantized cache: inside the kernel q (scaled by a power of two) and P each travel as
+a sum of two E4M3 terms -- exact for q's 8 significant bits, 2^-9 relative for P, the
+size of the bf16 path's rounding of P -- which a CPU emulation of that arithmetic puts
+at ~2e-3 relative L2, <= 5e-3 absolute and ~1e-7 relative on lse for unit-scale inputs
+(the rebase threshold 2^6 with P offset 2^2 keeps small P values near E4M3's subnormals).
 """
 from __future__ import annotations
 
@@ -42,7 +48,10 @@ def run_library(inp: dict, parts: int | None = None, device="cuda"):
     B, s_q, H, _ = q.shape
     P = parts if parts is not None else mla.num_sm_parts(s_q, H)
     meta = mla.decode_metadata(sl, s_q, H, inp["causal"], P)
-    out, lse = mla.decode(q, kv, bt, sl, inp["softmax_scale"], inp["causal"], meta, P)
+    if "kv_scale" in inp:   # FP8 (E4M3) cache
+        out, lse = mla.decode_fp8(q, kv, inp["kv_scale"], bt, sl, inp["softmax_scale"], inp["causal"], meta, P)
+    else:
+        out, lse = mla.decode(q, kv, bt, sl, inp["softmax_scale"], inp["causal"], meta, P)
     st = mla.get_device_status()
     assert st == 0, f"device status {st}"
     return out.cpu(), lse.cpu(), meta.cpu(), P
@@ -51,15 +60,20 @@ def run_library(inp: dict, parts: int | None = None, device="cuda"):
 def oracle_decode(inp: dict, batches=None):
     """Oracle on all requests (or a subset); returns float64 arrays for those requests."""
     sel = list(range(inp["q"].shape[0])) if batches is None else list(batches)
+    fp8 = "kv_scale" in inp
     kv = inp.get("_kv_np")
-    if kv is None:
-        kv = inp["kv_cache"].float().numpy()
+    if kv is None:   # an FP8 cache stays as its codes: the oracle dequantizes the rows it gathers
+        kv = inp["kv_cache"].numpy() if fp8 else inp["kv_cache"].float().numpy()
         inp["_kv_np"] = kv
     q = to_np(inp["q"][sel])
     bt = inp["block_table"][sel].numpy()
     sl = inp["seqlens"][sel].numpy()
-    out, lse, out_abs = oracle.decode_absorbed(q, kv, bt, sl, inp["softmax_scale"], causal=inp["causal"],
-                                               with_abs=True)
+    if fp8:
+        out, lse, out_abs = oracle.decode_fp8(q, kv, inp["kv_scale"], bt, sl, inp["softmax_scale"],
+                                              causal=inp["causal"], with_abs=True)
+    else:
+        out, lse, out_abs = oracle.decode_absorbed(q, kv, bt, sl, inp["softmax_scale"], causal=inp["causal"],
+                                                   with_abs=True)
     return out, lse, out_abs
 
 

@@ -72,6 +72,16 @@ def test_host_argument_checks(mla):
     for bad in (0.0, -0.5):   # the kernel takes the row maximum on unscaled scores
         neg_scale = list(args); neg_scale[9] = bad
         assert L.mla_decode(*neg_scale) == 1
+    # the FP8 entry: the same checks, plus its scale
+    f8 = args[:2] + [1.0] + args[2:]
+    assert L.mla_decode_fp8(*f8[:1], None, *f8[2:]) == 1      # no cache
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        bad_kv = list(f8); bad_kv[2] = bad
+        assert L.mla_decode_fp8(*bad_kv) == 1
+    bad_shape8 = list(f8); bad_shape8[8] = 5; bad_shape8[9] = 128
+    assert L.mla_decode_fp8(*bad_shape8) == 2
+    small_ws8 = list(f8); small_ws8[15] = ws - 1
+    assert L.mla_decode_fp8(*small_ws8) == 3
     assert L.mla_decode_metadata(None, 2, 1, 16, 0, 4, A, None) == 1
     assert L.mla_decode_metadata(A, 2, 8, 128, 0, 4, A, None) == 2
     assert L.mla_decode_metadata(A, 16385, 1, 128, 0, 4, A, None) == 2   # more requests than supported

@@ -78,6 +78,12 @@ def test_decode_work_counts():
     # empty request does no work and reads no cache
     f0, b0 = acc.decode_work([0], 1, 16, False)
     assert f0 == 0 and b0 == 16 * (1152 + 1024 + 4) + 4
+    # FP8 cache: 576 bytes per cached token, the rest unchanged; per-pair FLOPs over the
+    # cached bytes is the printed ~484 FLOP/B of exercise 2
+    f8, b8 = acc.decode_work([4096], 1, 128, False, kv_value_bytes=acc.FP8)
+    assert f8 == f and b8 == b - 4096 * 576
+    p = _load("flop_counter_mla_paths.json")["printed"]
+    assert round(f8 / (4096 * 576)) == p["fp8_kv_ai_flop_per_byte_approx"]
 
 
 @pytest.mark.parametrize("absorb", [True, False])
