@@ -18,7 +18,7 @@ Readings taken where the pages are silent:
 * lse is the natural log of the sum of exp of the *scaled* scores.
 * With s_q > 1 and causal masking, seqlens counts the s_q new tokens and new
   token i (0 = earliest) sees tokens t <= seqlen - s_q + i  ([MLA-paths],
-  FLOP counter: "k includes the new tokens", pairs = q*k - q(q-1)/2).
+  FLOP counter: its key count takes in the new tokens, pairs = q*k - q(q-1)/2).
 * A query row with no visible token has out = 0 and lse = -inf.
 * Token t of request b lives at kv_cache[block_table[b, t // 64], t % 64]; the
   page size 64 is the one FlashMLA uses ([MLA-paths], FlashMLA paragraph).
