@@ -115,3 +115,35 @@ def test_fp8_full_size_v3_sampled():
     sel = sorted({0, w.B - 1, *np.random.default_rng(1).choice(w.B, size=4, replace=False).tolist()})
     ref_out, ref_lse, _ = oracle_decode(inp, sel)
     compare(out[sel], lse[sel], ref_out, ref_lse, what=f"{w.name} sampled {sel}")
+
+
+def test_fp8_step_chain_and_graph_vs_expanded_definition():
+    # DecodeStep over an FP8 cache (absorb with RoPE -> mla_decode_fp8 -> un-absorb), run eagerly
+    # and replayed from a CUDA graph, against the expanded (un-absorbed) definition over the
+    # dequantized cache
+    import oracle
+    import mla_absorbed_decode_gb300 as mla
+    from _harness import OUT_ABS, to_np
+    w = W.small_variant(W.FP8, B=3, seqlen=700)
+    inp = make(w)
+    B, s_q, H = w.B, w.s_q, w.H
+    pos = (inp["seqlens"] - 1).to(torch.int32)
+    step = mla.DecodeStep(B, s_q, H, inp["seqlens"].cuda(), w.causal, w.softmax_scale, kv_scale=inp["kv_scale"])
+    args = (inp["q_nope"].cuda(), inp["q_pe"].cuda(), inp["w_uk"].cuda(), inp["w_uv"].cuda(),
+            inp["kv_cache"].cuda(), inp["block_table"].cuda())
+    o = step.run(*args, positions=pos.cuda()).clone()
+    assert mla.get_device_status() == 0
+    step.capture(*args, positions=pos.cuda())
+    o2 = step.replay().clone()
+    torch.cuda.synchronize()
+    assert mla.get_device_status() == 0
+    assert torch.equal(o, o2)
+    qp = np.swapaxes(oracle.rope_interleaved(np.swapaxes(to_np(inp["q_pe"]), 0, 1), pos.numpy()), 0, 1)
+    kv = oracle.dequantize_e4m3(inp["kv_cache"].numpy(), inp["kv_scale"])
+    ref, _ = oracle.decode_expanded(to_np(inp["q_nope"]).reshape(B, s_q, H, 128), qp.reshape(B, s_q, H, 64),
+                                    to_np(inp["w_uk"]), to_np(inp["w_uv"]), kv, inp["block_table"].numpy(),
+                                    inp["seqlens"].numpy(), w.softmax_scale)
+    got = to_np(o.view(B, s_q, H, 128).cpu())
+    d = np.abs(got - ref)
+    assert d.max() <= OUT_ABS, d.max()
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2e-2
