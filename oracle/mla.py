@@ -151,7 +151,7 @@ def decode_fp8(q, kv_codes, kv_scale, block_table, seqlens, softmax_scale, causa
 
 
 def decode_sparse(q, kv_cache, block_table, seqlens, indices, topk_lens, softmax_scale, causal=False,
-                  with_abs=False):
+                  with_abs=False, kv_scale=None):
     """Sparse (top-k) absorbed decode: the same attention, over a selected list of tokens.
 
     [AI-note] section 6 ("Sparse attention 把方向反过来"): a selector picks k of the L
@@ -163,6 +163,8 @@ def decode_sparse(q, kv_cache, block_table, seqlens, indices, topk_lens, softmax
         s_t = softmax_scale * <q[b,i,h,:576], kv_t[:576]>,  t listed and visible
         lse = ln sum_t exp(s_t),   out = sum_t exp(s_t - lse) * kv_t[:512]
     A listed token counts once per listing.  Returns out [B, s_q, H, 512], lse [B, s_q, H].
+    With kv_scale given, kv_cache holds FP8 E4M3 codes and kv_t is the dequantized row
+    (dequantize_e4m3), as in decode_fp8.
     """
     q = np.asarray(q, dtype=np.float64)
     B, s_q, H, dq = q.shape
@@ -176,7 +178,8 @@ def decode_sparse(q, kv_cache, block_table, seqlens, indices, topk_lens, softmax
         if sel.size == 0:
             continue
         assert sel.min() >= 0 and sel.max() < L
-        kv = np.asarray(kv_cache[np.asarray(block_table[b])[sel // PAGE], sel % PAGE], dtype=np.float64)
+        rows = np.asarray(kv_cache[np.asarray(block_table[b])[sel // PAGE], sel % PAGE])
+        kv = dequantize_e4m3(rows, kv_scale) if kv_scale is not None else np.asarray(rows, dtype=np.float64)
         for i in range(s_q):
             keep = sel < visible_tokens(L, s_q, i, causal)
             if not keep.any():

@@ -62,3 +62,22 @@ def test_block_table_out_of_range_is_reported():
     # request 0 does not use the bad entry and is still exact
     ref_out, ref_lse, ref_abs = oracle_decode(inp, [0])
     compare(out[:1].cpu(), lse[:1].cpu(), ref_out, ref_lse, what="request 0 beside a bad entry")
+
+
+def test_bounded_wait_times_out_fp8_cache():
+    # the same withheld load in the FP8-cache kernel (four page stages, four q blocks): the
+    # wait runs out, the CTAs drain what they issued, and the next FP8 call is correct
+    import mla_absorbed_decode_gb300 as mla
+    w = W.Workload("fault_fp8", B=2, s_q=1, H=128, fixed_seqlens=(300, 200), kv_fp8=True)
+    inp = make(w, seed=2)
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    P = 2
+    meta = mla.decode_metadata(dev["seqlens"], 1, 128, False, P)
+    mla.debug_withhold_first_load(True)
+    mla.decode_fp8(dev["q"], dev["kv_cache"], inp["kv_scale"], dev["block_table"], dev["seqlens"],
+                   inp["softmax_scale"], False, meta, P)
+    assert mla.get_device_status() == 5          # MLA_ERR_TIMEOUT
+    assert mla.get_device_status() == 0
+    out, lse, _, _ = run_library(inp, parts=P)
+    ref_out, ref_lse, _ = oracle_decode(inp)
+    compare(out, lse, ref_out, ref_lse, what="fp8 after timeout")

@@ -82,3 +82,18 @@ def test_fp8_workload_codes_round_the_draws(scale):
     err = np.abs(x - np.clip(draws, -448, 448))
     bound = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10)
     assert np.all(err <= bound * (1 + 1e-12))
+
+
+def test_fp8_sparse_decode_equals_bf16_sparse_of_the_dequantized_cache():
+    # the sparse (top-k) decode over an FP8 cache: the bf16 sparse decode of the dequantized
+    # cache, exactly (E4M3 values times 2^-6 are bf16 numbers)
+    w = W.Workload("fp8_sparse_probe", B=2, s_q=2, H=4, seqlen=300, topk=100, causal=True, kv_fp8=True)
+    d = W.make_inputs(w, seed=4)
+    codes, scale = d["kv_cache"].numpy(), d["kv_scale"]
+    deq = torch.from_numpy(oracle.dequantize_e4m3(codes, scale)).to(torch.bfloat16).float().numpy()
+    q, bt, sl = d["q"].float().numpy(), d["block_table"].numpy(), d["seqlens"].numpy()
+    idx, kl = d["indices"].numpy(), d["topk_lens"].numpy()
+    o8, l8 = oracle.decode_sparse(q, codes, bt, sl, idx, kl, w.softmax_scale, causal=True, kv_scale=scale)
+    ob, lb = oracle.decode_sparse(q, deq, bt, sl, idx, kl, w.softmax_scale, causal=True)
+    assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
+    assert np.isfinite(o8).all()
