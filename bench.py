@@ -162,7 +162,7 @@ def oracle_sample_step(inp, kv_np, sel, with_proj):
         idx = inp["indices"][sel].numpy()
         kl = inp["topk_lens"][sel].numpy()
         out, _ = oracle.decode_sparse(q, kv_np, inp["block_table"][sel].numpy(), inp["seqlens"][sel].numpy(), idx,
-                                      kl, inp["softmax_scale"], causal=inp["causal"])
+                                      kl, inp["softmax_scale"], causal=inp["causal"], kv_scale=inp.get("kv_scale"))
         flops += acc.sparse_decode_work(inp["seqlens"][sel].tolist(), kl.tolist(), s_q, H, inp["causal"],
                                         indices=idx.tolist())[0]
     elif "kv_scale" in inp:   # FP8 cache: kv_np holds its E4M3 codes
@@ -322,7 +322,10 @@ def run_ours(args, w):
     q_dec = step.q if w.with_projections else q_direct
 
     def decode_only():
-        if sparse:
+        if sparse and fp8:
+            mla.decode_sparse_fp8(q_dec, kv, kv_scale, bt, sl, idx, kl, w.softmax_scale, w.causal, step.metadata,
+                                  parts, workspace=step.workspace, out=step.out, lse=step.lse)
+        elif sparse:
             mla.decode_sparse(q_dec, kv, bt, sl, idx, kl, w.softmax_scale, w.causal, step.metadata, parts,
                               workspace=step.workspace, out=step.out, lse=step.lse)
         elif fp8:
@@ -412,7 +415,8 @@ def run_ours(args, w):
 
     if sparse:
         dflops, dbytes = acc.sparse_decode_work(inp["seqlens"].tolist(), inp["topk_lens"].tolist(), s_q, H, w.causal,
-                                                indices=inp["indices"].tolist())
+                                                indices=inp["indices"].tolist(),
+                                                kv_value_bytes=acc.FP8 if fp8 else acc.BF16)
     else:
         dflops, dbytes = acc.decode_work(inp["seqlens"].tolist(), s_q, H, w.causal,
                                          kv_value_bytes=acc.FP8 if fp8 else acc.BF16)
@@ -469,7 +473,11 @@ def run_ours(args, w):
 
             step.plan_beside(absorb_in)
             q_in = step.q if w.with_projections else dv["q"]
-            if sparse:
+            if sparse and fp8:
+                mla.decode_sparse_fp8(q_in, kv, kv_scale, dv["bt"], dv["sl"], dv["idx"], dv["kl"], w.softmax_scale,
+                                      w.causal, step.metadata, parts, workspace=step.workspace, out=step.out,
+                                      lse=step.lse)
+            elif sparse:
                 mla.decode_sparse(q_in, kv, dv["bt"], dv["sl"], dv["idx"], dv["kl"], w.softmax_scale, w.causal,
                                   step.metadata, parts, workspace=step.workspace, out=step.out, lse=step.lse)
             elif fp8:
@@ -513,7 +521,8 @@ def run_ours(args, w):
         roof = {"bound": "tensor", "achieved": ach, "peak": tpeak, "unit": "TFLOP/s", "frac": ach / tpeak}
     roof["peak_source"] = peaks["source"]
     roof["traffic"] = _traffic_per_launch(w.name)
-    roof["kernel"] = ("mla_decode_sparse" if sparse else "mla_decode_fp8" if fp8 else "mla_decode") \
+    roof["kernel"] = ("mla_decode_sparse_fp8" if sparse and fp8 else "mla_decode_sparse" if sparse
+                      else "mla_decode_fp8" if fp8 else "mla_decode") \
         + " (decode kernel + LSE combine)"
     roof["algorithmic_per_launch"] = {"bytes": dbytes, "flops": dflops}
     roof["ms_per_launch"] = t_dec * 1e3
@@ -536,7 +545,8 @@ def run_ours(args, w):
                                    else list(w.fixed_seqlens)),
                        "page": 64, "parts": parts, "parallelism": f"replicas x{n}",
                        **({"topk": w.topk, "path": "mla_decode_sparse"} if sparse else {}),
-                       **({"kv_cache": f"e4m3 codes, per-tensor scale {kv_scale}", "path": "mla_decode_fp8",
+                       **({"kv_cache": f"e4m3 codes, per-tensor scale {kv_scale}",
+                           "path": "mla_decode_sparse_fp8" if sparse else "mla_decode_fp8",
                            "mma": "kind::f8f6f4; q and P each as two E4M3 terms, fp32 accumulation"}
                           if fp8 else {}),
                        "l2": "flushed between timed steps (256 MiB write, then 256 MiB read; outside the step events)",

@@ -159,6 +159,16 @@ mla_status_t mla_decode_fp8(const mla_bf16_t* q, const uint8_t* kv_cache, float 
                             void* workspace, size_t workspace_bytes, mla_bf16_t* out, float* lse,
                             mla_stream_t stream);
 
+/* The sparse (top-k) decode of mla_decode_sparse over an FP8 cache as in mla_decode_fp8:
+ * the listed tokens' rows are E4M3 codes (576 bytes each) scaled by kv_scale.  Arguments,
+ * results and errors as for those two calls.  Async on stream. */
+mla_status_t mla_decode_sparse_fp8(const mla_bf16_t* q, const uint8_t* kv_cache, float kv_scale, int64_t num_blocks,
+                                   const int32_t* block_table, int max_blocks, const int32_t* seqlens,
+                                   const int32_t* indices, int64_t index_stride, const int32_t* topk_lens, int B,
+                                   int s_q, int H, float softmax_scale, int causal_s_q, const void* metadata,
+                                   int num_sm_parts, void* workspace, size_t workspace_bytes, mla_bf16_t* out,
+                                   float* lse, mla_stream_t stream);
+
 /* W_UK absorption and assembly of the decode query ("DeepSeekV2之MLA" 4.5:
  * q_nope_out = bmm(q_nope, w_kc) goes into q[..., :kv_lora_rank], the RoPE'd
  * q_pe into the last 64 values):

@@ -15,7 +15,7 @@ import torch
 
 __all__ = [
     "MLAError", "lib", "library_path", "num_sm_parts", "metadata_size", "decode_metadata",
-    "decode_workspace_size", "decode", "decode_sparse", "decode_fp8", "absorb_q", "unabsorb_o", "get_device_status",
+    "decode_workspace_size", "decode", "decode_sparse", "decode_fp8", "decode_sparse_fp8", "absorb_q", "unabsorb_o", "get_device_status",
     "schedule_params", "debug_withhold_first_load", "DecodeStep", "EXPORTED_SYMBOLS",
 ]
 
@@ -40,6 +40,8 @@ _SIGNATURES = {
                                    _c_int, _p, _c_int, _p, _c_size, _p, _p, _p]),
     "mla_decode_fp8": (_c_int, [_p, _p, _c_float, _c_ll, _p, _c_int, _p, _c_int, _c_int, _c_int, _c_float, _c_int,
                                 _p, _c_int, _p, _c_size, _p, _p, _p]),
+    "mla_decode_sparse_fp8": (_c_int, [_p, _p, _c_float, _c_ll, _p, _c_int, _p, _p, _c_ll, _p, _c_int, _c_int, _c_int,
+                                       _c_float, _c_int, _p, _c_int, _p, _c_size, _p, _p, _p]),
     "mla_absorb_q": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _p, _c_int, _c_int, _p]),
     "mla_absorb_q_rope": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _p, _c_int, _c_int, _p]),
     "mla_unabsorb_o": (_c_int, [_p, _p, _p, _c_int, _c_int, _p]),
@@ -182,6 +184,27 @@ def decode_fp8(q, kv_cache, kv_scale: float, block_table, seqlens, softmax_scale
                                 block_table.shape[1], _ptr(seqlens), B, s_q, H, float(softmax_scale), int(causal),
                                 _ptr(metadata), parts, _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _ptr(out), _ptr(lse), _stream(stream)), "mla_decode_fp8")
+    return out, lse
+
+
+def decode_sparse_fp8(q, kv_cache, kv_scale: float, block_table, seqlens, indices, topk_lens, softmax_scale: float,
+                      causal: bool, metadata, parts: int, workspace=None, out=None, lse=None, stream=None):
+    """decode_sparse over an FP8 cache (E4M3 codes scaled by kv_scale, as in decode_fp8)."""
+    B, s_q, H, _ = q.shape
+    dev = q.device
+    if kv_cache.element_size() != 1:
+        raise TypeError("decode_sparse_fp8: kv_cache must hold one byte per value (E4M3 codes)")
+    if out is None:
+        out = torch.empty((B, s_q, H, 512), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_size(B, s_q, H, parts), dtype=torch.uint8, device=dev)
+    _check(lib().mla_decode_sparse_fp8(_ptr(q), _ptr(kv_cache), float(kv_scale), kv_cache.shape[0], _ptr(block_table),
+                                       block_table.shape[1], _ptr(seqlens), _ptr(indices), indices.stride(0),
+                                       _ptr(topk_lens), B, s_q, H, float(softmax_scale), int(causal), _ptr(metadata),
+                                       parts, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+                                       _ptr(lse), _stream(stream)), "mla_decode_sparse_fp8")
     return out, lse
 
 

@@ -85,13 +85,14 @@ def decode_work(seqlens, s_q: int, H: int, causal: bool, kv_value_bytes: int = B
     return flops, kv_bytes + q_bytes + out_bytes + table_bytes
 
 
-def sparse_decode_work(seqlens, topk_lens, s_q: int, H: int, causal: bool, indices=None):
+def sparse_decode_work(seqlens, topk_lens, s_q: int, H: int, causal: bool, indices=None, kv_value_bytes: int = BF16):
     """Algorithmic (flops, bytes) of one mla_decode_sparse call: each listed token is
     gathered once per request (1152 bytes) and takes part in every visible pair.
     Without causal masking every query position sees the whole list; with it, position
     i sees the listed positions t <= seqlens[b] - s_q + i (indices needed).  Bytes add
     q, out, lse, the list entries (4 bytes each), one block-table entry per page the
-    list touches, and the two per-request lengths."""
+    list touches, and the two per-request lengths.  kv_value_bytes = FP8: 576 bytes per
+    listed token (mla_decode_sparse_fp8)."""
     seqlens = [int(x) for x in seqlens]
     topk_lens = [int(x) for x in topk_lens]
     B = len(seqlens)
@@ -108,7 +109,7 @@ def sparse_decode_work(seqlens, topk_lens, s_q: int, H: int, causal: bool, indic
         else:
             pages += min(k, (L + PAGE - 1) // PAGE)
     flops = pairs * H * 2 * ((D_C + D_R) + D_C)
-    kv_bytes = sum(topk_lens) * (D_C + D_R) * BF16
+    kv_bytes = sum(topk_lens) * (D_C + D_R) * kv_value_bytes
     rows = B * s_q * H
     q_bytes = rows * (D_C + D_R) * BF16
     out_bytes = rows * D_C * BF16 + rows * 4

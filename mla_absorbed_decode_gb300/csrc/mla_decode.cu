@@ -39,7 +39,8 @@
 // Roles (384 threads): warp 0 = TMA producer, warp 1 = MMA issuer (warp-uniform,
 // one elected lane issues), warp 2 = credit forwarder (O-CTA), warps 4..7 and
 // 8..11 = two softmax (S-CTA) or rescale/epilogue (O-CTA) warpgroups; a thread
-// of a warpgroup owns one query row (its TMEM lane).
+// of a warpgroup owns one query row (its TMEM lane).  The sparse decode gathers its
+// pages with warps (SparseWarps below); over an FP8 cache it runs 512 threads.
 // Every barrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT,
 // raises an abort flag in every CTA of its cluster, drains what it has in
 // flight and exits.
@@ -47,6 +48,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <climits>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -57,7 +59,9 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 384;          // 12 warps; the sparse decode over an FP8 cache runs 16 (see SparseWarps)
+template <bool kSparse, bool kF8>
+constexpr int threads_of() { return (kSparse && kF8) ? 512 : kThreads; }
 constexpr int kMaxStages = 4;                         // barrier slots: the deepest page ring
 constexpr int kSlots = 4;                             // O-CTA packet receive slots: a slot's credit
                                                       // round trip over DSMEM is hidden 4 pages deep
@@ -117,8 +121,6 @@ struct Cfg {
   static_assert(kOffLpart + 512 <= kOffShared, "S-CTA layout");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
-using CfgB = Cfg<false>;   // bf16 cache (dense and sparse)
-
 struct Bars {
   uint64_t full[kMaxStages];     // O: first half of V landed; S: part A of K, or a whole q block
   uint64_t empty[kMaxStages];    // O: first half of V free again; S: part A of K free again
@@ -263,41 +265,118 @@ __device__ __forceinline__ int request_block(const DecodeParams& p, int b, int k
 // the same swizzled layout a TMA box would produce; the stage's barrier expects one
 // arrival per lane (cp.async.mbarrier.arrive.noinc when the lane's copies land).
 
-// Address of list entry e's cached row, or nullptr (and a recorded bounds error) if
-// the entry is not a position of the request or its page is out of range.
-__device__ __forceinline__ const __nv_bfloat16* sparse_row(const DecodeParams& p, int b, int e) {
-  const int t = __ldg(p.indices + static_cast<int64_t>(b) * p.idx_stride + e);
-  if (t < 0 || t >= __ldg(p.seqlens + b)) {
+// The row lookups run ahead of the copies: a lane loads the list entry of its row two
+// pages ahead and that token's block-table entry one page ahead, so that the two
+// dependent loads of a page are spread over the two previous pages' gathers instead of
+// stalling the warp between pages.
+constexpr int kNoEntry = INT_MIN;   // a row past the request's list: nothing to gather
+
+// Walks the (request, page) pairs of one part in the order the kernel processes them.
+struct PageIter {
+  SegmentWalker w;
+  Segment s;
+  int k;
+  bool valid;
+  __device__ void init(const DecodeParams& p, int part) {
+    w.init(p, part);
+    valid = w.next(s);
+    k = valid ? s.kb : 0;
+  }
+  __device__ void advance() {
+    if (valid && ++k >= s.ke) {
+      valid = w.next(s);
+      k = valid ? s.kb : 0;
+    }
+  }
+};
+
+// Token position of row r of the iterator's page (list entry 64 k + r), or kNoEntry.
+__device__ __forceinline__ int sparse_entry(const DecodeParams& p, const PageIter& it, int r, bool active) {
+  if (!it.valid || !active) return kNoEntry;
+  const int e = it.k * 64 + r;
+  if (r >= 64 || e >= __ldg(p.lens + it.s.b)) return kNoEntry;
+  return __ldg(p.indices + static_cast<int64_t>(it.s.b) * p.idx_stride + e);
+}
+// Block-table entry of token t of request b (checked by sparse_address), or -1 when t
+// cannot be looked up.
+__device__ __forceinline__ int sparse_block(const DecodeParams& p, int b, int t) {
+  if (t == kNoEntry || t < 0 || t / kPageTokens >= p.max_blocks) return -1;
+  return __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + t / kPageTokens);
+}
+// Address of token t's cached row (bf16: 1152 bytes; FP8: 576) given its block-table
+// entry, or nullptr: past the list, or a bad entry -- a token outside [0, seqlens[b]), a
+// page past the table's width or outside [0, num_blocks) -- which is recorded as a bounds
+// error and not gathered.  The gather copies bytes, so the row is handed on untyped.
+template <bool F8>
+__device__ __forceinline__ const __nv_bfloat16* sparse_address(const DecodeParams& p, int b, int t, int blk) {
+  if (t == kNoEntry) return nullptr;
+  if (t < 0 || t >= __ldg(p.seqlens + b) || t / kPageTokens >= p.max_blocks || blk < 0 || blk >= p.num_blocks) {
     atomicCAS(p.status, 0, MLA_ERR_DEVICE_BOUNDS);
     return nullptr;
   }
-  const int blk = request_block(p, b, t / kPageTokens);
-  if (blk < 0) return nullptr;
-  return p.kv + (static_cast<int64_t>(blk) * kPageTokens + t % kPageTokens) * kDimQK;
+  const int64_t row = static_cast<int64_t>(blk) * kPageTokens + t % kPageTokens;
+  return reinterpret_cast<const __nv_bfloat16*>(reinterpret_cast<const uint8_t*>(p.kv) +
+                                                row * (F8 ? kDimQK : 2 * kDimQK));
 }
 
-// Gathering warps: the S-CTA gathers with warps 0, 2, 3 and 8..11, the O-CTA with warps
-// 0, 3 and 8..11 (one warp sustains only ~5 GB/s of 16-byte copies; in sparse mode the
-// softmax and the epilogue run on warps 4..7 alone).  Gathering warp slot ws owns rows
+// One gathering lane's lookups: (b0, t0, blk0) for the page being gathered, (b1, t1)
+// for the next one; `ahead` walks two pages ahead.
+template <bool F8>
+struct RowLookahead {
+  PageIter ahead;
+  int b0, t0, blk0, b1, t1, r;
+  bool active;
+  __device__ void init(const DecodeParams& p, int part, int row, bool act) {
+    r = row;
+    active = act;
+    ahead.init(p, part);
+    b0 = ahead.valid ? ahead.s.b : 0;
+    t0 = sparse_entry(p, ahead, r, active);
+    ahead.advance();
+    blk0 = sparse_block(p, b0, t0);
+    b1 = ahead.valid ? ahead.s.b : 0;
+    t1 = sparse_entry(p, ahead, r, active);
+    ahead.advance();
+  }
+  // The current page's row address; issues the next page's block-table load and the
+  // list-entry load two pages ahead, then moves on by one page.
+  __device__ const __nv_bfloat16* step(const DecodeParams& p) {
+    const __nv_bfloat16* mine = sparse_address<F8>(p, b0, t0, blk0);
+    const int blk1 = sparse_block(p, b1, t1);
+    const int b2 = ahead.valid ? ahead.s.b : 0;
+    const int t2 = sparse_entry(p, ahead, r, active);
+    ahead.advance();
+    b0 = b1, t0 = t1, blk0 = blk1, b1 = b2, t1 = t2;
+    return mine;
+  }
+};
+
+// Gathering warps of the sparse decode.  Gathering warp slot ws owns rows
 // [gather_r0(ws), gather_r0(ws + 1)) of each page; lane l looks up row gather_r0(ws) + l.
-constexpr int kSGatherWarps = 7, kOGatherWarps = 6;
-// Gathering warp slot of warp `warp`, or -1: S-CTA 0, 2, 3, 8..11 -> 0..6; O-CTA 0, 3, 8..11 -> 0..5.
-__device__ __forceinline__ int gather_slot(bool is_s, int warp) {
-  if (warp == 0) return 0;
-  if (warp >= 8) return warp - (is_s ? 5 : 6);
-  if (is_s) return (warp == 2 || warp == 3) ? warp - 1 : -1;
-  return warp == 3 ? 1 : -1;
-}
+// bf16 cache (12 warps): the S-CTA gathers with warps 0, 2, 3 and 8..11, the O-CTA with
+// warps 0, 3 and 8..11 (one warp sustains only a few GB/s of 16-byte copies), and the
+// softmax and the epilogue run on warps 4..7 alone.  FP8 cache: the kernel runs 16 warps
+// (its registers fit 128 a thread); warps 12..15 gather as well, and the softmax and the
+// epilogue keep both warpgroups (4..11) as in the dense decode.  With one warpgroup the
+// FP8 softmax took ~2 us a page and set the period; with two but only warps 0, 2, 3 / 0, 3
+// gathering, the gather did.
+template <bool F8>
+struct SparseWarps {
+  static constexpr bool kOneWG = !F8;     // the softmax / epilogue on warps 4..7 only
+  static constexpr int kS = 7, kO = 6;
+  static constexpr int kFirstExtra = kOneWG ? 8 : 12;   // warps kFirstExtra..kFirstExtra+3 gather
+  // gathering warp slot of warp `warp`, or -1
+  __device__ static int slot(bool is_s, int warp) {
+    if (warp == 0) return 0;
+    if (warp >= kFirstExtra) return warp - kFirstExtra + (is_s ? 3 : 2);
+    if (is_s) return (warp == 2 || warp == 3) ? warp - 1 : -1;
+    return warp == 3 ? 1 : -1;
+  }
+};
 __device__ __forceinline__ int gather_r0(int ws, int nwarps) { return ws * 64 / nwarps; }
 
-// Row address of entry k * 64 + r of request b's list, or nullptr (past the list, or a
-// bad entry: recorded as a bounds error, the row is not gathered).
-__device__ __forceinline__ const __nv_bfloat16* sparse_page_row(const DecodeParams& p, int b, int k, int r) {
-  const int e = k * 64 + r;
-  return (r < 64 && e < __ldg(p.lens + b)) ? sparse_row(p, b, e) : nullptr;
-}
-
-// The warp copies units [u0, u0 + kPerRow) (unit u = dims 8u..8u+7, chunk u / 8) of rows
+// The warp copies units [u0, u0 + kPerRow) (unit u = bytes 16u..16u+15 of a row: bf16 dims
+// 8u..8u+7 or FP8 dims 16u..16u+15; chunk u / 8) of rows
 // [r0, r0 + nrows) of the page into `stage` (chunk c at c * 8192, row r at r * 128,
 // 128-byte swizzle), the (row, unit) pairs spread evenly over the lanes; `mine` is the
 // address of row r0 + lane (nullptr: not gathered).
@@ -316,40 +395,35 @@ __device__ __forceinline__ void gather_rows(uint32_t stage, const __nv_bfloat16*
   }
 }
 
-// The page after page k of segment s in this part's walk: (b, k) or b = -1 at the end.
-__device__ __forceinline__ void next_page(const SegmentWalker& w, const Segment& s, int k, int& nb, int& nk) {
-  if (k + 1 < s.ke) {
-    nb = s.b, nk = k + 1;
-    return;
-  }
-  SegmentWalker nx = w;
-  Segment ns;
-  if (nx.next(ns)) nb = ns.b, nk = ns.kb;
-  else nb = -1, nk = 0;
-}
-
 // Gathering warp ws of the S-CTA, sparse decode: the q blocks by TMA (lane 0 of warp
 // 0) and its rows of every page by cp.async, through the same stages as the dense
 // producer; a stage's barriers expect one arrival per gathering lane.  The row
 // addresses of the next page are looked up while the current page's copies fly.
+// Part A of a page is its first kKPartA chunks (bf16: dims 0..319; FP8: 0..511), part B
+// the rest of the row (FP8: the 64 RoPE codes, the first half of the fifth chunk).
+template <bool F8>
 __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
                                   uint32_t cl, int rb, bool withhold, int ws) {
+  using C = Cfg<F8>;
+  constexpr int kRowUnits = F8 ? kDimQK / 16 : kDimQK / 8;   // 16-byte units of a cached row
+  constexpr int kUnitsA = static_cast<int>(C::kKPartA) * 8;
   const int lane = threadIdx.x & 31;
   const bool issuer = (ws == 0 && lane == 0);
-  const int r0 = gather_r0(ws, kSGatherWarps), nrows = gather_r0(ws + 1, kSGatherWarps) - r0;
+  const int r0 = gather_r0(ws, SparseWarps<F8>::kS), nrows = gather_r0(ws + 1, SparseWarps<F8>::kS) - r0;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
   uint32_t i = 0;
-  int issued[CfgB::kKStages];
-  uint32_t issued_phase[CfgB::kKStages];
-  for (int j = 0; j < CfgB::kKStages; ++j) issued[j] = 0, issued_phase[j] = 0;
-  bool ok = true, have_next = false;
-  const __nv_bfloat16* next_row = nullptr;
+  int issued[C::kKStages];
+  uint32_t issued_phase[C::kKStages];
+  for (int j = 0; j < C::kKStages; ++j) issued[j] = 0, issued_phase[j] = 0;
+  bool ok = true;
+  RowLookahead<F8> look;
+  look.init(p, part, r0 + lane, lane < nrows);
   while (ok && w.next(s)) {
     const int qrow0 = s.b * p.rows + rb * 128;
-    for (int j = 0; j < 2 && ok; ++j, ++i) {
-      const uint32_t st = i % CfgB::kKStages, ph = (i / CfgB::kKStages) & 1;
+    for (int j = 0; j < C::kQItems && ok; ++j, ++i) {
+      const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;
       if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl) ||
           !warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) {
         ok = false;
@@ -360,64 +434,58 @@ __device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Sha
       if (!issuer) {
         mbar_arrive(full);
       } else if (!(withhold && i == 0)) {   // test hook: this block never arrives
-        mbar_arrive_expect_tx(full, CfgB::kKStageBytes);
-        tma_load_3d(smem + CfgB::kOffStage + st * CfgB::kKStageBytes, &maps->q, full, 0, qrow0 + 64 * j, 0);
+        mbar_arrive_expect_tx(full, C::kQItemBytes);
+        tma_load_3d(smem + C::kOffStage + st * C::kKStageBytes, &maps->q, full, 0, qrow0 + C::kQRows * j, 0);
         issued[st] = 1, issued_phase[st] = ph;
       }
     }
     for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
-      const uint32_t st = i % CfgB::kKStages, ph = (i / CfgB::kKStages) & 1;
-      const uint32_t stage = smem + CfgB::kOffStage + st * CfgB::kKStageBytes;
-      const __nv_bfloat16* mine = have_next ? next_row : sparse_page_row(p, s.b, k, r0 + lane);
-      if (lane >= nrows) mine = nullptr;
-      int nb, nk;
-      next_page(w, s, k, nb, nk);
-      have_next = nb >= 0;
-      next_row = (have_next && lane < nrows) ? sparse_page_row(p, nb, nk, r0 + lane) : nullptr;
+      const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;
+      const uint32_t stage = smem + C::kOffStage + st * C::kKStageBytes;
+      const __nv_bfloat16* mine = look.step(p);   // page k of request s.b (the walks agree)
       if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
       // the stage's latest use is now a gathered page (waited for by cp.async.wait_all): the
       // drain below must not wait for an older phase of its barrier, whose parity can alias
       issued[st] = 0;
-      gather_rows<CfgB::kKPartA * 8>(stage, mine, r0, nrows, 0, lane);
+      gather_rows<kUnitsA>(stage, mine, r0, nrows, 0, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full[st]));
       if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      gather_rows<72 - CfgB::kKPartA * 8>(stage, mine, r0, nrows, CfgB::kKPartA * 8, lane);
+      gather_rows<kRowUnits - kUnitsA>(stage, mine, r0, nrows, kUnitsA, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full_b[st]));
     }
-    // the next segment's first page was looked up with this segment's walker state
   }
   cp_async_wait_all();   // this lane's copies land before the CTA may exit
   if (issuer)   // a q block whose stage saw no later page may still be in flight (after an abort)
-    for (int st = 0; st < CfgB::kKStages; ++st)
+    for (int st = 0; st < C::kKStages; ++st)
       if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
   __syncwarp();
 }
 
-// Gathering warp ws of the O-CTA, sparse decode: its rows' 512 value dims of every page.
+// Gathering warp ws of the O-CTA, sparse decode: its rows' 512 value dims of every page,
+// as two halves of kVChunks / 2 chunks.
+template <bool F8>
 __device__ void o_producer_sparse(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int ws) {
+  using C = Cfg<F8>;
+  constexpr int kHalfUnits = static_cast<int>(C::kVChunks / 2) * 8;
   const int lane = threadIdx.x & 31;
-  const int r0 = gather_r0(ws, kOGatherWarps), nrows = gather_r0(ws + 1, kOGatherWarps) - r0;
+  const int r0 = gather_r0(ws, SparseWarps<F8>::kO), nrows = gather_r0(ws + 1, SparseWarps<F8>::kO) - r0;
   SegmentWalker w;
   w.init(p, part);
   Segment s;
   uint32_t T = 0;
-  bool ok = true, have_next = false;
-  const __nv_bfloat16* next_row = nullptr;
+  bool ok = true;
+  RowLookahead<F8> look;
+  look.init(p, part, r0 + lane, lane < nrows);
   while (ok && w.next(s)) {
     for (int k = s.kb; k < s.ke && ok; ++k, ++T) {
-      const uint32_t st = T % CfgB::kVStages, ph = (T / CfgB::kVStages) & 1;
-      const uint32_t stage = smem + CfgB::kOffStage + st * CfgB::kVStageBytes;
-      const __nv_bfloat16* mine = have_next ? next_row : sparse_page_row(p, s.b, k, r0 + lane);
-      if (lane >= nrows) mine = nullptr;
-      int nb, nk;
-      next_page(w, s, k, nb, nk);
-      have_next = nb >= 0;
-      next_row = (have_next && lane < nrows) ? sparse_page_row(p, nb, nk, r0 + lane) : nullptr;
+      const uint32_t st = T % C::kVStages, ph = (T / C::kVStages) & 1;
+      const uint32_t stage = smem + C::kOffStage + st * C::kVStageBytes;
+      const __nv_bfloat16* mine = look.step(p);   // page k of request s.b
       if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      gather_rows<32>(stage, mine, r0, nrows, 0, lane);
+      gather_rows<kHalfUnits>(stage, mine, r0, nrows, 0, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full[st]));
       if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      gather_rows<32>(stage, mine, r0, nrows, 32, lane);
+      gather_rows<kHalfUnits>(stage, mine, r0, nrows, kHalfUnits, lane);
       cp_async_arrive_noinc(smem_u32(&sh.bar.full_b[st]));
     }
   }
@@ -629,30 +697,36 @@ __device__ __forceinline__ void copy_q_to_tmem(uint32_t qrow, uint32_t chunk_byt
 // significant bits: hi keeps the top 4 and the remainder, a multiple of q's last bit
 // no larger than 8 of them, fits lo exactly, so hi + lo = q sc and QK^T is exact up to
 // fp32 accumulation (values below ~2^-5 after scaling may lose their last bits).  One
-// E4M3 term alone (2^-4 relative) would move the scores too much.  Thread (wg, r)
-// converts dims [288 wg, 288 wg + 288); the two warpgroups agree on the row's maximum
-// through pm_mine / pm_other (named barrier 1).  Returns 1 / sc.
+// E4M3 term alone (2^-4 relative) would move the scores too much.  With two warpgroups
+// thread (wg, r) converts dims [288 wg, 288 wg + 288) and the two agree on the row's
+// maximum through pm_mine / pm_other (named barrier 1); with one, thread r converts the
+// whole row.  Returns 1 / sc.
+template <int kWG>
 __device__ __forceinline__ float copy_q_to_tmem_f8(uint32_t qrow, uint32_t chunk_bytes, uint32_t tmem_lane, int wg,
                                                    int rl, uint32_t pm_mine, uint32_t pm_other) {
+  constexpr int kUnits = 72 / kWG;        // 16-byte units (8 bf16 values) of the row per thread
+  const int u0 = wg * 36;
   auto unit = [&](int u) { return ld_shared_v4(qrow + (u >> 3) * chunk_bytes + (((u & 7) ^ (rl & 7)) << 4)); };
   auto amax2 = [](float m, uint32_t w) { return fmaxf(m, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w)))); };
   float amax = 0.f;
 #pragma unroll 4
-  for (int j = 0; j < 36; ++j) {
-    const uint4 x = unit(wg * 36 + j);
+  for (int j = 0; j < kUnits; ++j) {
+    const uint4 x = unit(u0 + j);
     amax = amax2(amax2(amax2(amax2(amax, x.x), x.y), x.z), x.w);
   }
-  asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine), "f"(amax) : "memory");
-  named_bar_sync(1, 256);
-  amax = fmaxf(amax, ld_shared_f32(pm_other));
+  if constexpr (kWG == 2) {
+    asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine), "f"(amax) : "memory");
+    named_bar_sync(1, 256);
+    amax = fmaxf(amax, ld_shared_f32(pm_other));
+  }
   const float t = amax > 0.f ? fminf(448.f / amax, 0x1p100f) : 1.f;
   const float sc = __uint_as_float(__float_as_uint(t) & 0x7F800000u);   // 2^floor(log2 t)
 #pragma unroll 1
-  for (int c = 0; c < 9; ++c) {          // 4 units = 32 dims = 8 columns of each term
+  for (int c = 0; c < kUnits / 4; ++c) {   // 4 units = 32 dims = 8 columns of each term
     uint32_t hi[8], lo[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint4 x = unit(wg * 36 + c * 4 + j);
+      const uint4 x = unit(u0 + c * 4 + j);
       const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {      // dims 4e..4e+3 of the unit -> one column
@@ -664,8 +738,8 @@ __device__ __forceinline__ float copy_q_to_tmem_f8(uint32_t qrow, uint32_t chunk
         lo[2 * j + e] = cvt_e4m3x2(v0 - f01.x, v1 - f01.y) | (cvt_e4m3x2(v2 - f23.x, v3 - f23.y) << 16);
       }
     }
-    tmem_st8(tmem_lane + kQCol + wg * 72 + c * 8, hi);
-    tmem_st8(tmem_lane + kQCol + 144 + wg * 72 + c * 8, lo);
+    tmem_st8(tmem_lane + kQCol + 2 * u0 + c * 8, hi);          // dims 8 u0 + 32 c: column (8 u0 + 32 c) / 4
+    tmem_st8(tmem_lane + kQCol + 144 + 2 * u0 + c * 8, lo);
   }
   return 1.f / sc;
 }
@@ -677,10 +751,9 @@ template <bool sparse, bool F8>
 __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb,
                               uint32_t peer) {
   using C = Cfg<F8>;
-  static_assert(!(sparse && F8), "the sparse decode reads a bf16 cache");
-  // Dense: two warpgroups, each covering 32 of a page's 64 columns.  Sparse: one
-  // warpgroup covering all 64 in two passes (the other four warps gather).
-  constexpr int kWG = sparse ? 1 : 2;
+  // Two warpgroups, each covering 32 of a page's 64 columns; sparse over a bf16 cache:
+  // one warpgroup covering all 64 in two passes (the other four warps gather).
+  constexpr int kWG = (sparse && SparseWarps<F8>::kOneWG) ? 1 : 2;
   constexpr uint32_t kST = kWG * 128;      // softmax threads
   constexpr int kPieces = 2 / kWG;         // 32-column pieces per thread and page
   const int t = threadIdx.x - 128;
@@ -720,7 +793,7 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       const int rl = r % C::kQRows;
       const uint32_t qrow = smem + C::kOffStage + mine * C::kKStageBytes + rl * 128;
       if constexpr (F8) {
-        sl2 = p.scale_log2 * p.kv_scale * copy_q_to_tmem_f8(qrow, kQChunk, tmem_lane, wg, rl, pm_mine, pm_other);
+        sl2 = p.scale_log2 * p.kv_scale * copy_q_to_tmem_f8<kWG>(qrow, kQChunk, tmem_lane, wg, rl, pm_mine, pm_other);
       } else {
 #pragma unroll
         for (int h = 0; h < kPieces; ++h) copy_q_to_tmem(qrow, kQChunk, tmem_lane, wg + h, rl);
@@ -1025,12 +1098,12 @@ __device__ void o_cta_forwarder(const DecodeParams& p, Shared& sh, int part, uin
 
 // Warps 4..11 of the O-CTA: rescale O rows, or normalise and store a finished
 // segment.  Warpgroup wg owns O columns [256 wg, 256 wg + 256).
-// Dense: two warpgroups, one per 256-column half of O; sparse: warps 4..7 alone cover both
-// halves (warps 8..11 gather).
+// Two warpgroups, one per 256-column half of O; sparse over a bf16 cache: warps 4..7 alone
+// cover both halves (warps 8..11 gather).
 template <bool sparse, bool F8>
 __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb) {
   using C = Cfg<F8>;
-  constexpr int kHalves = sparse ? 2 : 1;   // 256-column halves of O per thread
+  constexpr int kHalves = (sparse && SparseWarps<F8>::kOneWG) ? 2 : 1;   // 256-column halves of O per thread
   const int t = threadIdx.x - 128;
   const int wg = t >> 7;
   const int r = t & 127;
@@ -1151,9 +1224,8 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
 // kSparse: the pages are gathered from the top-k lists (p.indices) instead of read whole.
 // kF8: the cache holds E4M3 codes with one per-tensor scale (p.kv_scale).
 template <bool kSparse, bool kF8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<kSparse, kF8>(), 1)
 mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
-  static_assert(!(kSparse && kF8), "the sparse decode reads a bf16 cache");
   using C = Cfg<kF8>;
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   const uint32_t base = smem_u32(dyn_smem);
@@ -1181,7 +1253,9 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     sh.abort = 0;
     sh.cmd = 0;
     // sparse: one arrival per gathering lane
-    const uint32_t fills = kSparse ? 32u * static_cast<uint32_t>(is_s ? kSGatherWarps : kOGatherWarps) : 1u;
+    using SW = SparseWarps<kF8>;
+    constexpr uint32_t kGroupWarps = (kSparse && SW::kOneWG) ? 4 : 8;   // softmax / epilogue warps
+    const uint32_t fills = kSparse ? 32u * static_cast<uint32_t>(is_s ? SW::kS : SW::kO) : 1u;
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(smem_u32(&sh.bar.full[i]), fills);
       mbar_init(smem_u32(&sh.bar.empty[i]), 1);
@@ -1190,7 +1264,7 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.bar.s_full[i]), 1);
-      mbar_init(smem_u32(&sh.bar.s_empty[i]), kSparse ? 4 : 8);   // one arrival per softmax warp
+      mbar_init(smem_u32(&sh.bar.s_empty[i]), kGroupWarps);   // one arrival per softmax warp
     }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(smem_u32(&sh.bar.credit[i]), 1);
@@ -1199,10 +1273,10 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     }
     mbar_init(smem_u32(&sh.bar.q_full), 1);
     mbar_init(smem_u32(&sh.bar.o_full), 1);
-    mbar_init(smem_u32(&sh.bar.o_free), kSparse ? 4 : 8);          // one arrival per epilogue warp
+    mbar_init(smem_u32(&sh.bar.o_free), kGroupWarps);            // one arrival per epilogue warp
     mbar_init(smem_u32(&sh.bar.o_sync), 1);
     mbar_init(smem_u32(&sh.bar.corr_go), 1);
-    mbar_init(smem_u32(&sh.bar.corr_done), kSparse ? 4 : 8);
+    mbar_init(smem_u32(&sh.bar.corr_done), kGroupWarps);
     mbar_init(smem_u32(&sh.bar.drain), 1);
     fence_mbar_init();
   }
@@ -1219,8 +1293,9 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
   }
 
   if (is_s) {
-    if (kSparse && gather_slot(true, warp) >= 0) {   // the gathering warps
-      s_producer_sparse(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0, gather_slot(true, warp));
+    if (kSparse && SparseWarps<kF8>::slot(true, warp) >= 0) {   // the gathering warps
+      s_producer_sparse<kF8>(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0,
+                             SparseWarps<kF8>::slot(true, warp));
     } else if (warp == 0) {
       if ((threadIdx.x & 31) == 0) s_producer<kF8>(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
     } else if (warp == 1) {
@@ -1229,8 +1304,8 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
       s_cta_softmax<kSparse, kF8>(p, sh, smem, part, cl, rb, peer);
     }
   } else {
-    if (kSparse && gather_slot(false, warp) >= 0) {   // the gathering warps
-      o_producer_sparse(p, sh, smem, part, cl, gather_slot(false, warp));
+    if (kSparse && SparseWarps<kF8>::slot(false, warp) >= 0) {   // the gathering warps
+      o_producer_sparse<kF8>(p, sh, smem, part, cl, SparseWarps<kF8>::slot(false, warp));
     } else if (warp == 0) {
       if ((threadIdx.x & 31) == 0) o_producer<kF8>(p, &maps, sh, smem, part, cl);
     } else if (warp == 1) {
@@ -1260,7 +1335,10 @@ cudaError_t decode_set_attributes() {
   e = cudaFuncSetAttribute(mla_decode_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(Cfg<false>::kSmemBytes));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mla_decode_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(mla_decode_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(Cfg<true>::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(Cfg<true>::kSmemBytes));
 }
 
@@ -1268,9 +1346,10 @@ cudaError_t decode_set_attributes() {
 // (both cache formats use the same amount of shared memory)
 static_assert(Cfg<false>::kSmemBytes == Cfg<true>::kSmemBytes, "one launch shape for both formats");
 static cudaLaunchConfig_t decode_config(int grid_ctas, int cluster_ctas, cudaStream_t stream,
-                                        cudaLaunchAttribute* attr, bool pdl) {
-  cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(grid_ctas), 1, 1), dim3(kThreads, 1, 1),
-                                      Cfg<false>::kSmemBytes, stream, attr + 1);
+                                        cudaLaunchAttribute* attr, bool pdl, int threads = kThreads) {
+  cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(grid_ctas), 1, 1),
+                                      dim3(static_cast<unsigned>(threads), 1, 1), Cfg<false>::kSmemBytes, stream,
+                                      attr + 1);
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_ctas);
   attr[0].val.clusterDim.y = 1;
@@ -1293,6 +1372,11 @@ int decode_max_clusters(int cluster_ctas) {
 
 cudaError_t launch_decode(const KvMaps& maps, const DecodeParams& p, int cluster_ctas, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
+  if (p.indices && p.kv_fp8) {   // 16 warps (one CTA per SM either way: shared memory bounds it)
+    cudaLaunchConfig_t cfg16 = decode_config(p.num_parts * cluster_ctas, cluster_ctas, stream, attr, true,
+                                             threads_of<true, true>());
+    return cudaLaunchKernelEx(&cfg16, mla_decode_kernel<true, true>, maps, p);
+  }
   cudaLaunchConfig_t cfg = decode_config(p.num_parts * cluster_ctas, cluster_ctas, stream, attr, true);
   if (p.indices) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, false>, maps, p);
   if (p.kv_fp8) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, true>, maps, p);

@@ -310,6 +310,18 @@ mla_status_t mla_decode_sparse(const mla_bf16_t* q, const mla_bf16_t* kv_cache, 
                      stream);
 }
 
+mla_status_t mla_decode_sparse_fp8(const mla_bf16_t* q, const uint8_t* kv_cache, float kv_scale, int64_t num_blocks,
+                                   const int32_t* block_table, int max_blocks, const int32_t* seqlens,
+                                   const int32_t* indices, int64_t index_stride, const int32_t* topk_lens, int B,
+                                   int s_q, int H, float softmax_scale, int causal_s_q, const void* metadata,
+                                   int num_sm_parts, void* workspace, size_t workspace_bytes, mla_bf16_t* out,
+                                   float* lse, mla_stream_t stream) {
+  if (!indices) return MLA_ERR_INVALID_ARG;
+  return decode_impl(q, kv_cache, num_blocks, block_table, max_blocks, seqlens, indices, index_stride, topk_lens, B,
+                     s_q, H, softmax_scale, causal_s_q, metadata, num_sm_parts, workspace, workspace_bytes, out, lse,
+                     stream, true, kv_scale);
+}
+
 mla_status_t mla_decode_fp8(const mla_bf16_t* q, const uint8_t* kv_cache, float kv_scale, int64_t num_blocks,
                             const int32_t* block_table, int max_blocks, const int32_t* seqlens, int B, int s_q, int H,
                             float softmax_scale, int causal_s_q, const void* metadata, int num_sm_parts,

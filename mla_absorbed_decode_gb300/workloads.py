@@ -78,7 +78,9 @@ SPARSE = Workload("sparse_b64_h128_l16384_top2048", B=64, s_q=1, H=128, seqlen=1
 # the DeepSeek-V3 shape over an FP8 (E4M3) latent cache
 FP8 = Workload("fp8_deepseek_v3_b64_h128_l4096", B=64, s_q=1, H=128, seqlen=4096, with_projections=True,
                kv_fp8=True)
-ALL = (TINY, V3, RAGGED, MTP, LONG, SPARSE, FP8)
+# the DeepSeek-V3.2-shaped sparse decode over an FP8 (E4M3) cache
+SPARSE_FP8 = Workload("sparse_fp8_b64_h128_l16384_top2048", B=64, s_q=1, H=128, seqlen=16384, topk=2048, kv_fp8=True)
+ALL = (TINY, V3, RAGGED, MTP, LONG, SPARSE, FP8, SPARSE_FP8)
 BY_NAME = {w.name: w for w in ALL}
 
 

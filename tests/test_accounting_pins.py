@@ -109,3 +109,6 @@ def test_sparse_decode_work_counts():
     # causal, s_q = 2, seqlen 10: listed positions 3, 8, 9; query 0 sees t <= 8, query 1 t <= 9
     f, _ = acc.sparse_decode_work([10], [3], 2, 16, True, indices=[[3, 8, 9]])
     assert f == (2 + 3) * 16 * 2176
+    # over an FP8 cache a listed token costs 576 bytes, the rest unchanged
+    f8, b8 = acc.sparse_decode_work([16384], [2048], 1, 128, False, kv_value_bytes=acc.FP8)
+    assert f8 == 2048 * 278528 and b8 == 2048 * 576 + 128 * (1152 + 1024 + 4) + 2048 * 4 + min(2048, 256) * 4 + 8

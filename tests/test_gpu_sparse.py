@@ -154,3 +154,69 @@ def test_sparse_calls_return_promptly():
             torch.cuda.synchronize()
             assert mla.get_device_status() == 0
             assert e0.elapsed_time(e1) < 200.0, f"B={B}: {e0.elapsed_time(e1):.1f} ms"
+
+
+# ------------------------------------------------------------------ FP8 cache --
+
+def _case8(B, s_q, H, seqlens, causal=False, seed=0):
+    w = W.Workload("sparse_fp8_case", B=B, s_q=s_q, H=H, causal=causal, fixed_seqlens=tuple(seqlens), kv_fp8=True)
+    return make(w, seed=seed)
+
+
+def _run8(inp, idx, kl, parts=None):
+    import mla_absorbed_decode_gb300 as mla
+    q, kv, bt, sl = (inp[k].cuda() for k in ("q", "kv_cache", "block_table", "seqlens"))
+    B, s_q, H, _ = q.shape
+    P = parts or mla.num_sm_parts(s_q, H)
+    meta = mla.decode_metadata(kl.cuda(), s_q, H, inp["causal"], P)
+    out, lse = mla.decode_sparse_fp8(q, kv, inp["kv_scale"], bt, sl, idx.cuda(), kl.cuda(), inp["softmax_scale"],
+                                     inp["causal"], meta, P)
+    assert mla.get_device_status() == 0
+    return out.cpu(), lse.cpu()
+
+
+def _ref8(inp, idx, kl):
+    return oracle.decode_sparse(to_np(inp["q"]), inp["kv_cache"].numpy(), inp["block_table"].numpy(),
+                                inp["seqlens"].numpy(), idx.numpy(), kl.numpy(), inp["softmax_scale"],
+                                causal=inp["causal"], kv_scale=inp["kv_scale"])
+
+
+@pytest.mark.parametrize("H,s_q,causal", [(16, 1, False), (128, 1, False), (128, 2, True), (64, 2, False)])
+def test_sparse_fp8_small(H, s_q, causal):
+    seqlens = [5000, 130, 64, 3000]
+    ks = [2048, 130, 1, 777]
+    inp = _case8(len(seqlens), s_q, H, seqlens, causal=causal, seed=H + s_q)
+    idx, kl = _lists(seqlens, ks, seed=H)
+    ref_out, ref_lse = _ref8(inp, idx, kl)
+    for parts in (None, 3):
+        out, lse = _run8(inp, idx, kl, parts)
+        compare(out, lse, ref_out, ref_lse, what=f"sparse fp8 H={H} s_q={s_q} parts={parts}")
+
+
+def test_sparse_fp8_empty_list_and_unsorted_order():
+    seqlens = [300, 900]
+    inp = _case8(2, 1, 64, seqlens, seed=5)
+    idx, kl = _lists(seqlens, [0, 500], seed=5)
+    idx[1, :500] = idx[1, :500][torch.randperm(500, generator=torch.Generator().manual_seed(1))]
+    out, lse = _run8(inp, idx, kl)
+    ref_out, ref_lse = _ref8(inp, idx, kl)
+    compare(out, lse, ref_out, ref_lse, what="sparse fp8 empty/unsorted")
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+
+
+def test_sparse_fp8_every_token_listed_matches_the_dense_fp8_kernel():
+    # listing every token in order gathers the same rows the dense FP8 kernel loads by TMA;
+    # the arithmetic after the load is the same, so the results agree bit for bit
+    import mla_absorbed_decode_gb300 as mla
+    seqlens = [700, 64, 1]
+    inp = _case8(3, 1, 128, seqlens, seed=8)
+    idx = torch.full((3, 700), -1, dtype=torch.int32)
+    for b, L in enumerate(seqlens):
+        idx[b, :L] = torch.arange(L, dtype=torch.int32)
+    kl = torch.tensor(seqlens, dtype=torch.int32)
+    out_s, lse_s = _run8(inp, idx, kl, parts=2)
+    q, kv, bt, sl = (inp[k].cuda() for k in ("q", "kv_cache", "block_table", "seqlens"))
+    meta = mla.decode_metadata(sl, 1, 128, False, 2)
+    out_d, lse_d = mla.decode_fp8(q, kv, inp["kv_scale"], bt, sl, inp["softmax_scale"], False, meta, 2)
+    assert mla.get_device_status() == 0
+    assert torch.equal(out_s, out_d.cpu()) and torch.equal(lse_s, lse_d.cpu())
