@@ -11,6 +11,11 @@ rates the dominant kernel (the mla_decode call) against the measured HBM peak.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
+--workload picks another shape (mla_absorbed_decode_gb300/workloads.py): the
+ragged, MTP (s_q = 2, causal) and long-context ones, the V3 shape over an FP8
+(E4M3) cache (fp8_deepseek_v3_b64_h128_l4096: mla_decode_fp8, the FP8 tensor rate
+in the roofline), and the V3.2-shaped top-2048 sparse decode over a bf16 or an
+FP8 cache (sparse_b64_h128_l16384_top2048, sparse_fp8_b64_h128_l16384_top2048).
 --impl reference times the CPU oracle (numpy float64) on a bounded sample of
 the same workload per step.  With N > 1 (torchrun) every rank runs its own
 replica of the workload (requests shard across GPUs with no exchange).
