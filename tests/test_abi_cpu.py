@@ -82,6 +82,20 @@ def test_host_argument_checks(mla):
     assert L.mla_decode_fp8(*bad_shape8) == 2
     small_ws8 = list(f8); small_ws8[15] = ws - 1
     assert L.mla_decode_fp8(*small_ws8) == 3
+    # the sparse FP8 entry: a list is required, the scale must be finite and positive, and
+    # the sparse decode's own checks apply
+    # (q, kv, scale, num_blocks, table, max_blocks, seqlens, indices, stride, topk_lens, B, s_q, H,
+    #  softmax_scale, causal, metadata, parts, workspace, bytes, out, lse, stream)
+    sp8 = [A, A, 1.0, 10, A, 8, A, A, 8, A, 2, 1, 16, 0.1, 0, A, 4, A, ws, A, A, None]
+    no_list = list(sp8); no_list[7] = None
+    assert L.mla_decode_sparse_fp8(*no_list) == 1
+    for bad in (0.0, -2.0, float("nan")):
+        bad_kv = list(sp8); bad_kv[2] = bad
+        assert L.mla_decode_sparse_fp8(*bad_kv) == 1
+    bad_stride = list(sp8); bad_stride[8] = 0
+    assert L.mla_decode_sparse_fp8(*bad_stride) == 1
+    bad_rows = list(sp8); bad_rows[11] = 5; bad_rows[12] = 128
+    assert L.mla_decode_sparse_fp8(*bad_rows) == 2
     assert L.mla_decode_metadata(None, 2, 1, 16, 0, 4, A, None) == 1
     assert L.mla_decode_metadata(A, 2, 8, 128, 0, 4, A, None) == 2
     assert L.mla_decode_metadata(A, 16385, 1, 128, 0, 4, A, None) == 2   # more requests than supported
