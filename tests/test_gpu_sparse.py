@@ -220,3 +220,32 @@ def test_sparse_fp8_every_token_listed_matches_the_dense_fp8_kernel():
     out_d, lse_d = mla.decode_fp8(q, kv, inp["kv_scale"], bt, sl, inp["softmax_scale"], False, meta, 2)
     assert mla.get_device_status() == 0
     assert torch.equal(out_s, out_d.cpu()) and torch.equal(lse_s, lse_d.cpu())
+
+
+def test_fp8_calls_return_promptly():
+    """The same guard for the FP8-cache kernels (four page stages, four q blocks), sparse
+    and dense, over batch sizes and part counts that split requests."""
+    import mla_absorbed_decode_gb300 as mla
+    L, k = 4096, 640
+    for B in (6, 7, 9, 12):
+        inp = _case8(B, 1, 128, [L] * B, seed=B)
+        idx, kl = _lists([L] * B, [k] * B, seed=B)
+        q, kv, bt, sl = (inp[x].cuda() for x in ("q", "kv_cache", "block_table", "seqlens"))
+        idx, kl = idx.cuda(), kl.cuda()
+        P = mla.num_sm_parts(1, 128)
+        calls = [("sparse", mla.decode_metadata(kl, 1, 128, False, P), P)]
+        for parts in (P, 5):
+            calls.append(("dense", mla.decode_metadata(sl, 1, 128, False, parts), parts))
+        for kind, meta, parts in calls:
+            for _ in range(2):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                if kind == "sparse":
+                    mla.decode_sparse_fp8(q, kv, inp["kv_scale"], bt, sl, idx, kl, inp["softmax_scale"], False,
+                                          meta, parts)
+                else:
+                    mla.decode_fp8(q, kv, inp["kv_scale"], bt, sl, inp["softmax_scale"], False, meta, parts)
+                e1.record()
+                torch.cuda.synchronize()
+                assert mla.get_device_status() == 0
+                assert e0.elapsed_time(e1) < 200.0, f"{kind} B={B} parts={parts}: {e0.elapsed_time(e1):.1f} ms"
