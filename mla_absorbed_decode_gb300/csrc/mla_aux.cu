@@ -181,7 +181,7 @@ cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fi
 // written by the decode kernel; requests with none get out = 0, lse = -inf.
 __global__ void __launch_bounds__(128)
 mla_combine_kernel(const float* o_part, const float* lse_part, const int32_t* num_splits, int B, int rows,
-                   __nv_bfloat16* out, float* lse) {
+                   int max_splits, __nv_bfloat16* out, float* lse, int* status) {
   griddep_wait();
   griddep_launch_dependents();
   const int b = blockIdx.x;
@@ -191,6 +191,10 @@ mla_combine_kernel(const float* o_part, const float* lse_part, const int32_t* nu
   const int s0 = num_splits[b];
   const int n = num_splits[b + 1] - s0;
   if (n == 1) return;
+  if (s0 < 0 || n < 0 || s0 + n > max_splits) {   // offsets that do not fit the workspace: reported, not read
+    if (lane == 0) atomicCAS(status, 0, MLA_ERR_DEVICE_BOUNDS);
+    return;
+  }
   __nv_bfloat16* orow = out + (static_cast<int64_t>(b) * rows + g) * kDimV + lane * 16;
   if (n == 0) {
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -497,7 +501,7 @@ cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap&
 
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* num_splits, int B, int rows,
-                           __nv_bfloat16* out, float* lse, cudaStream_t stream) {
+                           int max_splits, __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream) {
   // The decode kernel never signals its dependents early, so the combine's CTAs are
   // placed only once the whole decode grid is done (spread over every SM) and the
   // programmatic launch just hides the launch latency.  An early signal would let them
@@ -506,7 +510,8 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, const int
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg =
       pdl_config(dim3(static_cast<unsigned>(B), static_cast<unsigned>((rows + 3) / 4), 1), dim3(128), 0, stream, attr);
-  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, o_part, lse_part, num_splits, B, rows, out, lse);
+  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, o_part, lse_part, num_splits, B, rows, max_splits, out, lse,
+                            status);
 }
 
 }  // namespace mla

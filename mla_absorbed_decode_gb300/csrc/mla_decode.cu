@@ -168,6 +168,13 @@ struct SegmentWalker {
     split0 = m[4];
     first = true;
     done = (b < 0);
+    // A record that does not fit this call (metadata built for another batch, or
+    // overwritten) would send the walk past the caller's buffers: report it and walk
+    // nothing.  Every role reads the same record, so all of them stop alike.
+    if (!done && (b >= prm.B || b_last < b || b_last >= prm.B || kb < 0 || k_end < 0 || split0 < 0)) {
+      atomicCAS(prm.status, 0, MLA_ERR_DEVICE_BOUNDS);
+      done = true;
+    }
   }
   __device__ static int pages_of(int L) { return L > 0 ? (L + 63) / 64 : 0; }
   __device__ bool next(Segment& s) {
@@ -242,6 +249,15 @@ __device__ __forceinline__ void prefetch_request(const DecodeParams& p, int b) {
   prefetch_l2(reinterpret_cast<const void*>(a0), static_cast<uint32_t>(a1 - a0));
 }
 
+// Whether split slot `slot` (partial output and lse) lies in the workspace, which holds
+// B + num_parts slots; a slot outside it (metadata that does not fit the call) is
+// recorded as a bounds error and its stores are skipped.
+__device__ __forceinline__ bool split_slot_ok(const DecodeParams& p, int slot) {
+  if (slot >= 0 && slot < p.B + p.num_parts) return true;
+  atomicCAS(p.status, 0, MLA_ERR_DEVICE_BOUNDS);
+  return false;
+}
+
 // Page id of page k of request b, or -1 (and a recorded bounds error) if the
 // table entry is outside [0, num_blocks) or k is past the table's width.
 __device__ __forceinline__ int request_block(const DecodeParams& p, int b, int k) {
@@ -295,6 +311,10 @@ __device__ __forceinline__ int sparse_entry(const DecodeParams& p, const PageIte
   if (!it.valid || !active) return kNoEntry;
   const int e = it.k * 64 + r;
   if (r >= 64 || e >= __ldg(p.lens + it.s.b)) return kNoEntry;
+  if (e >= p.idx_stride) {   // a list longer than its row of indices: reported, not read
+    atomicCAS(p.status, 0, MLA_ERR_DEVICE_BOUNDS);
+    return kNoEntry;
+  }
   return __ldg(p.indices + static_cast<int64_t>(it.s.b) * p.idx_stride + e);
 }
 // Block-table entry of token t of request b (checked by sparse_address), or -1 when t
@@ -842,8 +862,8 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
         if (sparse && p.causal) {   // token positions of these 32 columns (sparse only)
           const int32_t* ix = p.indices + static_cast<int64_t>(s.b) * p.idx_stride + k * 64 + cb;
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c < nvalid && __ldg(ix + c) >= vis_pos) sv[c] = -INFINITY;
+          for (int c = 0; c < 32; ++c)   // entries past the row of indices are not read (the gather reports them)
+            if (c < nvalid && k * 64 + cb + c < p.idx_stride && __ldg(ix + c) >= vis_pos) sv[c] = -INFINITY;
         }
       };
       auto release_s = [&]() {   // every column of S has been read
@@ -951,7 +971,7 @@ __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, 
       const int nsplit = __ldg(p.num_splits + s.b + 1) - ns0;
       if (nsplit == 1)
         p.lse[static_cast<int64_t>(s.b) * p.rows + g] = lse;
-      else
+      else if (split_slot_ok(p, ns0 + s.split))
         p.lse_part[static_cast<int64_t>(ns0 + s.split) * p.rows + g] = lse;
     }
   }
@@ -1148,6 +1168,7 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
     const int ns0 = __ldg(p.num_splits + s.b);
     const int nsplit = __ldg(p.num_splits + s.b + 1) - ns0;
     const bool final_out = (nsplit == 1);
+    const bool slot_ok = final_out || split_slot_ok(p, ns0 + s.split);   // partial stores stay in the workspace
     // Stores go through the warp's transpose buffer: a thread holds one row's columns, so
     // direct stores would touch 32 rows per instruction; transposed, each store
     // instruction writes 64 contiguous bytes of 8 rows.  Buffer row x (64 B) holds
@@ -1207,7 +1228,7 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
           for (int j = 0; j < 4; ++j) {
             const int x = 8 * j + (lane >> 2);
             const uint4 u = get(j);
-            if (g0 + x < p.rows)
+            if (g0 + x < p.rows && slot_ok)
               *reinterpret_cast<uint4*>(pbase + static_cast<int64_t>(x) * 512 + c + 16 * h + 4 * tq) = u;
           }
           __syncwarp();

@@ -282,7 +282,9 @@ mla_status_t decode_impl(const void* q, const void* kv_cache, int64_t num_blocks
 
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (launch_decode(kv_maps, p, 2 * n_rb, cs) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_combine(p.o_part, p.lse_part, p.num_splits, B, rows, p.out, lse, cs) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_combine(p.o_part, p.lse_part, p.num_splits, B, rows, static_cast<int>(ms), p.out, lse, p.status, cs) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
   return MLA_OK;
 }
 

@@ -110,8 +110,10 @@ cudaError_t launch_decode(const KvMaps& maps, const DecodeParams& p, int cluster
 
 cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
                             int split_cost, int32_t* meta, int32_t* num_splits, cudaStream_t stream);
+// max_splits: partial slots in the workspace (B + num_parts); split offsets beyond it
+// are reported as MLA_ERR_DEVICE_BOUNDS in *status instead of read.
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* num_splits, int B, int rows,
-                           __nv_bfloat16* out, float* lse, cudaStream_t stream);
+                           int max_splits, __nv_bfloat16* out, float* lse, int* status, cudaStream_t stream);
 
 struct BmmParams {
   __nv_bfloat16* out;

@@ -137,6 +137,8 @@ extern "C" mla_status_t mla_decode_noalloc(const mla_bf16_t* q, const mla_bf16_t
   p.status = status;
   p.withhold_first_load = 0;
   if (launch_decode(kv_maps, p, 2 * n_rb, cs) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_combine(p.o_part, p.lse_part, p.num_splits, B, rows, p.out, lse, cs) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_combine(p.o_part, p.lse_part, p.num_splits, B, rows, static_cast<int>(ms), p.out, lse, p.status, cs) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -345,61 +345,64 @@ def rope_interleaved(x, positions, base=10000.0):
 
 
 def tiny_full_mla(seed=0, T=6, D=64, H=4, NOPE=8, ROPE=4, DV=8, DC=16):
-    """The worked tiny full-MLA example with decoupled RoPE, both paths.
+    """A tiny full MLA layer with decoupled RoPE, evaluated both ways.
 
-    Follows [MLA-paths] section "两条等价的路径": hidden states h [T, D];
-    latent c = h W_dkv (cached); shared RoPE key k^R = rope(h W_kr) (cached);
-    per-head query split into q^N (NOPE) and q^R = rope(.) (ROPE);
-    scale = 1/sqrt(NOPE + ROPE); causal prefill mask (token t sees s <= t).
-      path 1 (expand): k = [c W_uk[h], k^R], v = c W_uv[h]; ordinary MHA.
-      path 2 (absorb): q_lat = W_uk[h] q^N; score = q_lat.c + q^R.k^R;
-                       out = (sum_s p_s c_s) W_uv[h].
-    Both are projected by W_o.  The page's weights come from a seeded torch RNG
-    it does not print; any draw works, since the claim is the equality itself.
-    Returns dict with y_expand, y_absorb [T, D] and the per-token cache counts.
+    [MLA-paths] section "两条等价的路径" states the score of head h between query
+    token i and cached token j as
+        s = q^N_{h,i} . k^N_{h,j} + q^R_{h,i} . k^R_j,   k^N_{h,j} = U_k[h] c_j,
+    with c_j the cached latent (DC values) and k^R_j the shared RoPE key (ROPE values),
+    and the value as v_{h,j} = U_v[h] c_j.  Since q^N . (U_k c) = (U_k^T q^N) . c, the
+    same numbers come out of
+      * path 1 (expand): build k^N_{h,j} and v_{h,j} for every cached token, then
+        ordinary attention;
+      * path 2 (absorb): move q^N into the latent space once per query token, score
+        against c_j directly, sum p_j c_j in the latent space and apply U_v[h] last.
+    Each head's outputs (DV values) are concatenated and projected back to D.  The
+    page checks the two paths with allclose and counts the cached numbers per token
+    (per-head K and V against c plus k^R); those are the claims kept here.  Weights
+    are seeded Gaussians scaled by 1/sqrt(fan-in); prefill-style causal masking (token
+    i sees j <= i); softmax scale 1/sqrt(NOPE + ROPE); RoPE at positions 0..T-1.
+    Returns y_expand, y_absorb ([T, D]) and the per-token cache counts.
     """
     rng = np.random.default_rng(seed)
-    W_q = rng.standard_normal((D, H * (NOPE + ROPE))) / 8
-    W_dkv = rng.standard_normal((D, DC)) / 8
-    W_kr = rng.standard_normal((D, ROPE)) / 8
-    W_uk = rng.standard_normal((H, DC, NOPE)) / 4     # latent -> per-head k^N
-    W_uv = rng.standard_normal((H, DC, DV)) / 4       # latent -> per-head v
-    W_o = rng.standard_normal((H * DV, D)) / 8
-    hid = rng.standard_normal((T, D))
-    pos = np.arange(T)
-    allowed = np.tril(np.ones((T, T), dtype=bool))
 
-    c = hid @ W_dkv                                   # [T, DC]
-    k_r = rope_interleaved(hid @ W_kr, pos)           # [T, ROPE]
-    q = (hid @ W_q).reshape(T, H, NOPE + ROPE).transpose(1, 0, 2)   # [H, T, NOPE+ROPE]
-    q_n = q[..., :NOPE]
-    q_r = rope_interleaved(q[..., NOPE:], pos)
+    def gauss(rows, cols):   # a (rows x cols) map applied as M @ x, scaled by its fan-in
+        return rng.standard_normal((rows, cols)) / math.sqrt(cols)
+
+    x = rng.standard_normal((T, D))                      # hidden states of the T tokens
+    to_latent, to_rope_key = gauss(DC, D), gauss(ROPE, D)
+    heads = [dict(q_n=gauss(NOPE, D), q_r=gauss(ROPE, D), u_k=gauss(NOPE, DC), u_v=gauss(DV, DC))
+             for _ in range(H)]
+    out_proj = gauss(D, H * DV)
+    pos = np.arange(T)
     scale = 1.0 / math.sqrt(NOPE + ROPE)
 
-    def masked_softmax(s):
-        s = np.where(allowed, s, -np.inf)
-        s = s - s.max(axis=-1, keepdims=True)
-        e = np.exp(s)
-        return e / e.sum(axis=-1, keepdims=True)
+    latent = np.stack([to_latent @ x[t] for t in range(T)])                        # cached: c_j
+    rope_key = rope_interleaved(np.stack([to_rope_key @ x[t] for t in range(T)]), pos)   # cached: k^R_j
 
-    # path 1: expand the latent into per-head keys and values
-    k_n = np.einsum("tc,hcd->htd", c, W_uk)
-    k = np.concatenate([k_n, np.broadcast_to(k_r, (H, T, ROPE))], axis=-1)
-    v = np.einsum("tc,hcd->htd", c, W_uv)
-    qq = np.concatenate([q_n, q_r], axis=-1)
-    out1 = masked_softmax(np.einsum("hid,hjd->hij", qq, k) * scale) @ v        # [H, T, DV]
+    def probabilities(scores):   # softmax over the visible tokens, maximum subtracted
+        e = np.exp(np.asarray(scores) - max(scores))
+        return e / e.sum()
 
-    # path 2: absorb W_uk into the query, sum in the latent space, then W_uv
-    q_lat = np.einsum("htd,hcd->htc", q_n, W_uk)                               # [H, T, DC]
-    p = masked_softmax((q_lat @ c.T + q_r @ k_r.T) * scale)                    # [H, T, T]
-    lat = p @ c                                                                 # [H, T, DC]
-    out2 = np.einsum("htc,hcd->htd", lat, W_uv)
-
-    y1 = out1.transpose(1, 0, 2).reshape(T, H * DV) @ W_o
-    y2 = out2.transpose(1, 0, 2).reshape(T, H * DV) @ W_o
+    concat = {"expand": np.zeros((T, H * DV)), "absorb": np.zeros((T, H * DV))}
+    for h, w in enumerate(heads):
+        qn_all = np.stack([w["q_n"] @ x[t] for t in range(T)])
+        qr_all = rope_interleaved(np.stack([w["q_r"] @ x[t] for t in range(T)]), pos)
+        cols = slice(h * DV, (h + 1) * DV)
+        for i in range(T):
+            qn, qr = qn_all[i], qr_all[i]
+            # path 1: per-head keys and values expanded from the latent
+            s1 = [scale * (qn @ (w["u_k"] @ latent[j]) + qr @ rope_key[j]) for j in range(i + 1)]
+            p1 = probabilities(s1)
+            concat["expand"][i, cols] = sum(p1[j] * (w["u_v"] @ latent[j]) for j in range(i + 1))
+            # path 2: the query moves into the latent space; the output leaves it at the end
+            q_lat = w["u_k"].T @ qn
+            s2 = [scale * (q_lat @ latent[j] + qr @ rope_key[j]) for j in range(i + 1)]
+            p2 = probabilities(s2)
+            concat["absorb"][i, cols] = w["u_v"] @ sum(p2[j] * latent[j] for j in range(i + 1))
     return {
-        "y_expand": y1,
-        "y_absorb": y2,
+        "y_expand": concat["expand"] @ out_proj.T,
+        "y_absorb": concat["absorb"] @ out_proj.T,
         "cache_per_token_mha": H * (NOPE + ROPE) + H * DV,
         "cache_per_token_mla": DC + ROPE,
     }
