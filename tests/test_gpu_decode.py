@@ -171,3 +171,49 @@ def test_full_size_workload_sampled(w):
     ref_out, ref_lse, ref_abs = oracle_decode(inp, sel)
     compare(out[sel], lse[sel], ref_out, ref_lse, ref_abs=ref_abs if w.outlier_p > 0 else None,
             what=f"{w.name} sampled {sel}")
+
+
+# ------------------------------------------------------------------ mutations --
+
+def _marker_case(seed=13):
+    """One 4096-token request whose result hinges on eight marker tokens.  Every head's
+    RoPE query part is set to one vector u (|u|^2 = 64) and the markers' RoPE key part to
+    3u, so each marker scores ~14 nats above the random tokens for every head and the
+    eight of them carry nearly all the softmax weight; their latent (value) parts stay
+    N(0,1) draws, so the output keeps unit scale.  A kernel that drops any marker, or
+    reads the wrong page for one, moves the output by ~1/8 of a unit value -- far
+    outside the parity bounds -- whereas with random inputs alone a single token's
+    weight (~1/4096) would sit inside them."""
+    inp = _case(1, 1, 128, [4096], seed=seed)
+    g = torch.Generator().manual_seed(seed)
+    u = torch.randn(64, generator=g)
+    u = u / u.norm() * 8.0
+    inp["q"][..., 512:576] = u.to(torch.bfloat16)
+    markers = [63, 64, 511, 1000, 2047, 2048, 3333, 4095]       # page ends and starts among them
+    bt = inp["block_table"][0]
+    for t in markers:
+        inp["kv_cache"][bt[t // 64], t % 64, 512:576] = (3.0 * u).to(torch.bfloat16)
+    return inp, markers
+
+
+def test_harness_catches_a_dropped_token_and_a_wrong_page():
+    import mla_absorbed_decode_gb300 as mla
+    inp, markers = _marker_case()
+    ref_out, ref_lse, _ = oracle_decode(inp)
+    out, lse, _, _ = run_library(inp, parts=4)                  # split over parts, as the bench runs it
+    compare(out, lse, ref_out, ref_lse, what="marker case")
+    # mutation 1: the last token (a marker) dropped by the kernel's input
+    short = dict(inp)
+    short["seqlens"] = inp["seqlens"] - 1
+    out1, lse1, _, _ = run_library(short, parts=4)
+    with pytest.raises(AssertionError):
+        compare(out1, lse1, ref_out, ref_lse, what="dropped token")
+    # mutation 2: the page holding marker 1000 replaced by its neighbour page (one page read twice)
+    shifted = dict(inp)
+    bt = inp["block_table"].clone()
+    bt[0, 1000 // 64] = bt[0, 1000 // 64 + 1]
+    shifted["block_table"] = bt
+    out2, lse2, _, _ = run_library(shifted, parts=4)
+    with pytest.raises(AssertionError):
+        compare(out2, lse2, ref_out, ref_lse, what="wrong page")
+    assert mla.get_device_status() == 0

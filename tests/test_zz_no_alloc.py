@@ -7,8 +7,8 @@ split partials in a fixed array of device memory inside the library instead.
 This test calls it through the C ABI twice in a row, with different requests
 (the second call finds the first call's data in the shared array), and checks
 each result against mla_decode on the same inputs, within the parity
-tolerance.  It sits in a file collected last so that a failure here does not
-hide any other test.
+tolerance, and against the CPU oracle directly.  It sits in a file collected
+last so that a failure here does not hide any other test.
 """
 import ctypes
 
@@ -17,7 +17,7 @@ import torch
 
 from mla_absorbed_decode_gb300 import workloads as W
 
-from _harness import compare, to_np
+from _harness import compare, oracle_decode, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -68,6 +68,9 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row():
         out, lse = _call_noalloc(inp, parts)
         ref_out, ref_lse = _call_existing(inp, parts)
         compare(out, lse, to_np(ref_out), to_np(ref_lse), what="noalloc vs mla_decode")
+        # and directly against the CPU oracle, within the same parity bounds
+        o_out, o_lse, _ = oracle_decode(inp)
+        compare(out, lse, o_out, o_lse, what="noalloc vs oracle")
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
