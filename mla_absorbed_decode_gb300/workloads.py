@@ -19,6 +19,9 @@ with `seed`, in this fixed order):
 FP8 cache (kv_fp8): the draws are the same; the cache is stored as E4M3 codes of
 kv / kv_scale (clamped to +-448, torch's round-to-nearest conversion) instead of bf16,
 with one per-tensor kv_scale.
+FP8 projection weights (proj_fp8): the same W_UK / W_UV draws, each head's matrix stored
+transposed ([H, 512, 128] and [H, 128, 512], K contiguous) as E4M3 codes of W / w_scale
+with one fixed per-tensor w_scale (torch's round-to-nearest conversion, clamped to +-448).
 Poison: pool pages no request uses, and slots at or beyond seqlen in a
 request's last page, hold NaN (code 0x7F in an FP8 cache); block-table entries past
 a request's last page hold -1.  A correct kernel never reads any of them into its result.
@@ -54,6 +57,8 @@ class Workload:
     topk: int = 0                # sparse decode: each request lists min(topk, L) of its tokens
     kv_fp8: bool = False         # cache stored as FP8 E4M3 codes with one per-tensor scale
     kv_scale: float = 1.0 / 64.0  # dequantized value = code value * kv_scale (N(0,1) draws -> codes within +-448)
+    proj_fp8: bool = False       # W_UK / W_UV also given as FP8 E4M3 codes (transposed) with one per-tensor scale
+    w_scale: float = 2.0 ** -9   # N(0, 1/512) weights / 2^-9 -> codes of standard deviation ~23, within +-448
 
     @property
     def softmax_scale(self) -> float:
@@ -80,7 +85,10 @@ FP8 = Workload("fp8_deepseek_v3_b64_h128_l4096", B=64, s_q=1, H=128, seqlen=4096
                kv_fp8=True)
 # the DeepSeek-V3.2-shaped sparse decode over an FP8 (E4M3) cache
 SPARSE_FP8 = Workload("sparse_fp8_b64_h128_l16384_top2048", B=64, s_q=1, H=128, seqlen=16384, topk=2048, kv_fp8=True)
-ALL = (TINY, V3, RAGGED, MTP, LONG, SPARSE, FP8, SPARSE_FP8)
+# the DeepSeek-V3 step with the W_UK / W_UV projections on FP8 weights (bmm_fp8), bf16 cache
+FP8_PROJ = Workload("fp8proj_deepseek_v3_b64_h128_l4096", B=64, s_q=1, H=128, seqlen=4096, with_projections=True,
+                    proj_fp8=True)
+ALL = (TINY, V3, RAGGED, MTP, LONG, SPARSE, FP8, SPARSE_FP8, FP8_PROJ)
 BY_NAME = {w.name: w for w in ALL}
 
 
@@ -145,6 +153,13 @@ def make_inputs(w: Workload, seed: int = 0, seqlens: torch.Tensor | None = None,
         std = 1.0 / math.sqrt(512.0)
         out["w_uk"] = (torch.randn((w.H, D_NOPE, D_LATENT), generator=g) * std).to(torch.bfloat16)
         out["w_uv"] = (torch.randn((w.H, D_LATENT, D_V), generator=g) * std).to(torch.bfloat16)
+        if w.proj_fp8:
+            def codes(t):   # [H, K, J] weights -> [H, J, K] E4M3 codes of t / w_scale
+                u = (t.float().transpose(1, 2) / w.w_scale).clamp(-448.0, 448.0)
+                return u.to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+            out["w_uk_t_fp8"] = codes(out["w_uk"])
+            out["w_uv_t_fp8"] = codes(out["w_uv"])
+            out["w_scale"] = w.w_scale
     if w.topk:   # the selector's output: min(topk, L) distinct positions per request, ascending
         idx = torch.full((B, w.topk), -1, dtype=torch.int32)
         kl = torch.zeros(B, dtype=torch.int32)

@@ -12,8 +12,9 @@ checks), written for a reader to check against the pages by eye:
 * ``mla.py``      -- the absorbed decode definition (dense, over an FP8 E4M3
                     cache with a per-tensor scale, and over a selected top-k
                     token list), the expanded (un-absorbed) chain, the
-                    LSE merge, a pure-Python brute force and the tiny full-MLA
-                    example with decoupled RoPE.
+                    LSE merge, a pure-Python brute force, the tiny full-MLA
+                    example with decoupled RoPE, and the FP8 projections
+                    (per-tensor input quantization, bmm_fp8).
 * ``schedule.py`` -- a restatement of the split-KV schedule rule and the
                     invariants any valid schedule must satisfy.
 
@@ -25,5 +26,6 @@ from .mla import (  # noqa: F401
     gather_request, visible_tokens, e4m3_value, E4M3_VALUES, dequantize_e4m3,
     decode_absorbed, decode_fp8, decode_sparse, decode_expanded, absorb_q, assemble_q, unabsorb_o,
     lse_merge, decode_bruteforce, tiny_full_mla, rope_interleaved,
+    E4M3_MAX, e4m3_round, input_to_float8, bmm_fp8, absorb_q_fp8, assemble_q_fp8, unabsorb_o_fp8,
 )
 from .schedule import schedule_reference, check_schedule  # noqa: F401

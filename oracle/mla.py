@@ -406,3 +406,85 @@ def tiny_full_mla(seed=0, T=6, D=64, H=4, NOPE=8, ROPE=4, DV=8, DC=16):
         "cache_per_token_mha": H * (NOPE + ROPE) + H * DV,
         "cache_per_token_mla": DC + ROPE,
     }
+
+
+# ------------------------------------------------------- FP8 projections (bmm_fp8) --
+# [SGL-compile] "SGLang v0.3 MLA / torch.compile", the weight-absorption code walk-through:
+# with FP8 weights the absorption runs as
+#     x_val, x_scale = input_to_float8(x)            (x = q_nope, or the attention output)
+#     y = bmm_fp8(x_val, w, x_scale, w_scale) -> bf16
+# one scale per operand.  The page shows the calls, not their bodies; the reading taken
+# here is the plain per-tensor one: the activation's scale maps its largest magnitude onto
+# E4M3's largest finite value, 448, and the product is the float64 sum of the decoded
+# codes times both scales.  The quantization is done in float32 (the scale's reciprocal
+# multiplies each float32 value, then one rounding to E4M3), so that a kernel doing the same
+# float32 steps reaches the same codes.
+
+E4M3_MAX = 448.0
+_E4M3_POS = E4M3_VALUES[:127]          # codes 0x00..0x7E: 0, the subnormals, the normals up to 448
+
+
+def e4m3_round(v) -> np.ndarray:
+    """E4M3 codes (uint8) of float values: the nearest representable value, ties to the
+    even code (mantissa bit 0 clear), magnitudes of 448 and above saturated to 448, the sign
+    kept (negative values that round to zero give -0, 0x80), NaN to the NaN code 0x7F."""
+    v = np.asarray(v, dtype=np.float64)
+    mag = np.minimum(np.abs(v), E4M3_MAX)
+    hi = np.clip(np.searchsorted(_E4M3_POS, mag, side="left"), 0, 126)   # first code with value >= mag
+    lo = np.clip(hi - 1, 0, 126)
+    d_hi = _E4M3_POS[hi] - mag
+    d_lo = mag - _E4M3_POS[lo]
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    code = np.where(pick_lo, lo, hi).astype(np.uint8)
+    code = np.where(np.signbit(v), code | 0x80, code)   # the sign bit is kept, also on values rounding to zero
+    return np.where(np.isnan(v), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def input_to_float8(x):
+    """Per-tensor dynamic FP8 quantization of an activation tensor (the page's
+    input_to_float8): amax = max |x| over the whole tensor; in float32,
+    inv = 448 / amax and scale = amax / 448 (both 1 when amax = 0); codes =
+    e4m3_round(float32(x) * inv).  Returns (codes uint8, scale float); x ~= codes' values * scale."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(x32))) if x32.size else np.float32(0.0)
+    if amax > 0:
+        inv = np.float32(E4M3_MAX) / amax
+        scale = amax / np.float32(E4M3_MAX)
+    else:
+        inv = np.float32(1.0)
+        scale = np.float32(1.0)
+    return e4m3_round((x32 * inv).astype(np.float32)), float(scale)
+
+
+def bmm_fp8(x_codes, x_scale, w_t_codes, w_scale):
+    """Per-head product of FP8 operands (the page's bmm_fp8 with one scale per operand):
+        y[n, h, j] = sum_k e4m3(x[n, h, k]) * e4m3(w_t[h, j, k]) * x_scale * w_scale
+    x_codes [N, H, K] uint8, w_t_codes [H, J, K] uint8 (each head's weight stored with its K
+    values contiguous: W[h] transposed).  Returns float64 [N, H, J]."""
+    xv = E4M3_VALUES[np.asarray(x_codes, dtype=np.uint8)]
+    wv = E4M3_VALUES[np.asarray(w_t_codes, dtype=np.uint8)]
+    return np.einsum("nhk,hjk->nhj", xv, wv) * (float(x_scale) * float(w_scale))
+
+
+def absorb_q_fp8(q_nope, w_uk_t_codes, w_uk_scale):
+    """q_lat = bmm_fp8(input_to_float8(q_nope), W_UK) ([SGL-compile]; [DSV2-MLA] 4.5):
+    q_nope [N, H, 128] -> [N, H, 512] float64; w_uk_t_codes [H, 512, 128] (W_UK[h]^T)."""
+    codes, scale = input_to_float8(q_nope)
+    return bmm_fp8(codes, scale, w_uk_t_codes, w_uk_scale)
+
+
+def assemble_q_fp8(q_nope, q_pe, w_uk_t_codes, w_uk_scale, positions=None, base=10000.0):
+    """The decode query with the FP8 absorption: [absorb_q_fp8(q_nope), q_pe rotated by RoPE
+    at positions (copied when positions is None)] -> [N, H, 576] float64 (as assemble_q)."""
+    q_lat = absorb_q_fp8(q_nope, w_uk_t_codes, w_uk_scale)
+    pe = np.asarray(q_pe, dtype=np.float64)
+    if positions is not None:
+        pe = np.swapaxes(rope_interleaved(np.swapaxes(pe, 0, 1), positions, base), 0, 1)
+    return np.concatenate([q_lat, pe], axis=-1)
+
+
+def unabsorb_o_fp8(o_lat, w_uv_t_codes, w_uv_scale):
+    """o = bmm_fp8(input_to_float8(o_lat), W_UV) ([SGL-compile]; [DSV2-MLA] 4.5):
+    o_lat [N, H, 512] -> [N, H, 128] float64; w_uv_t_codes [H, 128, 512] (W_UV[h]^T)."""
+    codes, scale = input_to_float8(o_lat)
+    return bmm_fp8(codes, scale, w_uv_t_codes, w_uv_scale)
