@@ -159,7 +159,11 @@ def oracle_sample_step(inp, kv_np, sel, with_proj):
         qp = inp["q_pe"].float().numpy().reshape(B, s_q, H, 64)[sel].reshape(-1, H, 64)
         sl = inp["seqlens"][sel].numpy()
         pos = (np.repeat(sl, s_q) - s_q + np.tile(np.arange(s_q), len(sel))).clip(min=0)
-        q = oracle.assemble_q(qn, qp, inp["_w_uk_np"], positions=pos).reshape(len(sel), s_q, H, 576)
+        if "w_uk_t_fp8" in inp:   # FP8 projections (bmm_fp8 with per-tensor input quantization)
+            q = oracle.assemble_q_fp8(qn, qp, inp["w_uk_t_fp8"].numpy(), inp["w_scale"], positions=pos)
+        else:
+            q = oracle.assemble_q(qn, qp, inp["_w_uk_np"], positions=pos)
+        q = q.reshape(len(sel), s_q, H, 576)
         flops += acc.bmm_work(len(sel) * s_q, H, True)[0]
     else:
         q = inp["q"][sel].double().numpy()
@@ -179,7 +183,10 @@ def oracle_sample_step(inp, kv_np, sel, with_proj):
                                         inp["softmax_scale"], causal=inp["causal"])
         flops += acc.decode_work(inp["seqlens"][sel].tolist(), s_q, H, inp["causal"])[0]
     if with_proj:
-        oracle.unabsorb_o(out.reshape(-1, H, 512), inp["_w_uv_np"])
+        if "w_uv_t_fp8" in inp:
+            oracle.unabsorb_o_fp8(out.reshape(-1, H, 512), inp["w_uv_t_fp8"].numpy(), inp["w_scale"])
+        else:
+            oracle.unabsorb_o(out.reshape(-1, H, 512), inp["_w_uv_np"])
         flops += acc.bmm_work(len(sel) * s_q, H, False)[0]
     return flops
 
@@ -296,6 +303,10 @@ def run_ours(args, w):
     q_pe = inp["q_pe"].to(dev) if w.with_projections else None
     w_uk = inp["w_uk"].to(dev) if w.with_projections else None
     w_uv = inp["w_uv"].to(dev) if w.with_projections else None
+    proj_fp8 = w.with_projections and w.proj_fp8   # W_UK / W_UV as E4M3 codes: bmm_fp8
+    w_uk_t = inp["w_uk_t_fp8"].to(dev) if proj_fp8 else None
+    w_uv_t = inp["w_uv_t_fp8"].to(dev) if proj_fp8 else None
+    fp8_ws = torch.empty(mla.bmm_fp8_workspace_size(), dtype=torch.uint8, device=dev) if proj_fp8 else None
     kv = inp["kv_cache"].to(dev)
     bt = inp["block_table"].to(dev)
     sl = inp["seqlens"].to(dev)
@@ -340,15 +351,27 @@ def run_ours(args, w):
             mla.decode(q_dec, kv, bt, sl, w.softmax_scale, w.causal, step.metadata, parts, workspace=step.workspace,
                        out=step.out, lse=step.lse)
 
+    def absorb_call(qn, qp, pos_d):
+        if proj_fp8:
+            mla.absorb_q_fp8(qn, w_uk_t, w.w_scale, step.q, q_pe=qp, positions=pos_d, workspace=fp8_ws)
+        else:
+            mla.absorb_q(qn, w_uk, step.q, q_pe=qp, positions=pos_d)
+
+    def unabsorb_call():
+        if proj_fp8:
+            mla.unabsorb_o_fp8(step.out.view(B * s_q, H, 512), w_uv_t, w.w_scale, o=step.o, workspace=fp8_ws)
+        else:
+            mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
+
     def absorb():
         if w.with_projections:
-            mla.absorb_q(q_nope, w_uk, step.q, q_pe=q_pe, positions=positions)
+            absorb_call(q_nope, q_pe, positions)
 
     def one_step():
         step.plan_beside(absorb)   # the split schedule on a side stream, beside the absorption
         decode_only()
         if w.with_projections:
-            mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
+            unabsorb_call()
 
     launches_per_step = 1 + 2 + (2 if w.with_projections else 0)   # schedule, decode+combine, bmms
     for _ in range(max(args.warmup, 3)):
@@ -400,12 +423,12 @@ def run_ours(args, w):
         step.plan()
         ev[1].record()
         if w.with_projections:
-            mla.absorb_q(q_nope, w_uk, step.q, q_pe=q_pe, positions=positions)
+            absorb_call(q_nope, q_pe, positions)
         ev[2].record()
         decode_only()
         ev[3].record()
         if w.with_projections:
-            mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
+            unabsorb_call()
         ev[4].record()
         torch.cuda.synchronize()
         for j, k in enumerate(comp):
@@ -429,7 +452,7 @@ def run_ours(args, w):
     bflops = bbytes = 0
     if w.with_projections:
         for absorb in (True, False):
-            f, b = acc.bmm_work(B * s_q, H, absorb)
+            f, b = acc.bmm_work(B * s_q, H, absorb, weight_bytes=acc.FP8 if proj_fp8 else acc.BF16)
             bflops += f
             bbytes += b
     step_flops, step_bytes = dflops + bflops, dbytes + bbytes
@@ -474,7 +497,7 @@ def run_ours(args, w):
 
             def absorb_in():
                 if w.with_projections:
-                    mla.absorb_q(dv["q_nope"], w_uk, step.q, q_pe=dv["q_pe"], positions=dv["pos"])
+                    absorb_call(dv["q_nope"], dv["q_pe"], dv["pos"])
 
             step.plan_beside(absorb_in)
             q_in = step.q if w.with_projections else dv["q"]
@@ -492,7 +515,7 @@ def run_ours(args, w):
                 mla.decode(q_in, kv, dv["bt"], dv["sl"], w.softmax_scale, w.causal, step.metadata, parts,
                            workspace=step.workspace, out=step.out, lse=step.lse)
             if w.with_projections:
-                mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
+                unabsorb_call()
             host_out.copy_(res_dev, non_blocking=True)
             host_lse.copy_(step.lse, non_blocking=True)
 
@@ -550,6 +573,8 @@ def run_ours(args, w):
                                    else list(w.fixed_seqlens)),
                        "page": 64, "parts": parts, "parallelism": f"replicas x{n}",
                        **({"topk": w.topk, "path": "mla_decode_sparse"} if sparse else {}),
+                       **({"projections": f"bmm_fp8: E4M3 weights (per-tensor scale {w.w_scale}), activations "
+                                          "quantized per tensor on the fly (input_to_float8)"} if proj_fp8 else {}),
                        **({"kv_cache": f"e4m3 codes, per-tensor scale {kv_scale}",
                            "path": "mla_decode_sparse_fp8" if sparse else "mla_decode_fp8",
                            "mma": "kind::f8f6f4; q and P each as two E4M3 terms, fp32 accumulation"}

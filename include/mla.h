@@ -206,6 +206,42 @@ mla_status_t mla_absorb_q_rope(const mla_bf16_t* q_nope, int64_t q_nope_row_stri
 mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* o,
                             int N, int H, mla_stream_t stream);
 
+/* FP8 projections (page "SGLang v0.3 MLA / torch.compile", the weight-absorption code
+ * walk-through, its FP8 branches):  x_val, x_scale = input_to_float8(x);
+ * y = bmm_fp8(x_val, w, x_scale, w_scale), one scale per operand, bf16 out.
+ * The activation x is quantized per tensor inside the call: amax = max |x| over the whole
+ * [N, H, K] tensor, inv = 448 / amax and x_scale = amax / 448 in float32 (1 and 1 when
+ * amax = 0), codes = E4M3 round-to-nearest-even, saturating, of float32(x) * inv.  The
+ * weights are E4M3 codes (sign, 4 exponent bits with bias 7, 3 mantissa bits) with one
+ * per-tensor scale, each head's matrix stored transposed (K contiguous):
+ *   y[n, h, j] = sum_k code_x[n, h, k] * code_w[h, j, k] * x_scale * w_scale
+ * (fp32 accumulation on FP8 tensor cores, bf16 out).  A call runs two kernels on `stream`
+ * (the maxima of |x|, then the product); `workspace` (device, 16-byte aligned, at least
+ * mla_bmm_fp8_workspace_size() bytes, owned by the caller) carries the partial maxima
+ * between them and may be reused by the next call on the same stream.  Too small or NULL:
+ * MLA_ERR_WORKSPACE. */
+size_t mla_bmm_fp8_workspace_size(void);
+
+/* mla_absorb_q with FP8 weights (see above), K = 128:
+ *   q[n, h, 0:512]   = bmm_fp8(input_to_float8(q_nope), W_UK)[n, h, :]
+ *   q[n, h, 512:576] = q_pe[n, h, :], RoPE-rotated by positions[n] as in
+ *                      mla_absorb_q_rope when positions is not NULL (copied when it is;
+ *                      skipped when q_pe is NULL)
+ *  w_uk_t      [H, 512, 128] E4M3 codes: W_UK[h] transposed;  w_uk_scale finite and > 0
+ *  q_nope, q_pe, positions, rope_theta, q as for mla_absorb_q / mla_absorb_q_rope.
+ * Async on stream. */
+mla_status_t mla_absorb_q_fp8(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                              int64_t q_pe_row_stride, const int32_t* positions, float rope_theta,
+                              const uint8_t* w_uk_t, float w_uk_scale, mla_bf16_t* q, int N, int H,
+                              void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* mla_unabsorb_o with FP8 weights (see above), K = 512:
+ *   o[n, h, 0:128] = bmm_fp8(input_to_float8(o_lat), W_UV)[n, h, :]
+ *  o_lat [N, H, 512] bf16;  w_uv_t [H, 128, 512] E4M3 codes: W_UV[h] transposed;
+ *  w_uv_scale finite and > 0;  o [N, H, 128] bf16.  Async on stream. */
+mla_status_t mla_unabsorb_o_fp8(const mla_bf16_t* o_lat, const uint8_t* w_uv_t, float w_uv_scale, mla_bf16_t* o,
+                                int N, int H, void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
 /* mla_decode without caller-provided scratch.  The paper has no counterpart:
  * this entry point exists for callers that cannot allocate device memory or pass
  * a workspace -- code inside an inference engine or plugin whose memory pool

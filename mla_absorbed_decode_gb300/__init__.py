@@ -15,7 +15,8 @@ import torch
 
 __all__ = [
     "MLAError", "lib", "library_path", "num_sm_parts", "metadata_size", "decode_metadata",
-    "decode_workspace_size", "decode", "decode_sparse", "decode_fp8", "decode_sparse_fp8", "absorb_q", "unabsorb_o", "get_device_status",
+    "decode_workspace_size", "decode", "decode_sparse", "decode_fp8", "decode_sparse_fp8", "absorb_q", "unabsorb_o",
+    "bmm_fp8_workspace_size", "absorb_q_fp8", "unabsorb_o_fp8", "get_device_status",
     "schedule_params", "debug_withhold_first_load", "DecodeStep", "EXPORTED_SYMBOLS",
 ]
 
@@ -45,6 +46,9 @@ _SIGNATURES = {
     "mla_absorb_q": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _p, _c_int, _c_int, _p]),
     "mla_absorb_q_rope": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _p, _c_int, _c_int, _p]),
     "mla_unabsorb_o": (_c_int, [_p, _p, _p, _c_int, _c_int, _p]),
+    "mla_bmm_fp8_workspace_size": (_c_size, []),
+    "mla_absorb_q_fp8": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _c_float, _p, _c_int, _c_int, _p, _c_size, _p]),
+    "mla_unabsorb_o_fp8": (_c_int, [_p, _p, _c_float, _p, _c_int, _c_int, _p, _c_size, _p]),
     "mla_decode_noalloc": (_c_int, [_p, _p, _c_ll, _p, _c_int, _p, _c_int, _c_int, _c_int, _c_float, _c_int,
                                     _c_int, _p, _p, _p]),
     "mla_get_device_status": (_c_int, [_p]),
@@ -230,6 +234,49 @@ def unabsorb_o(o_lat: torch.Tensor, w_uv: torch.Tensor, o: torch.Tensor | None =
     if o is None:
         o = torch.empty((N, H, 128), dtype=torch.bfloat16, device=o_lat.device)
     _check(lib().mla_unabsorb_o(_ptr(o_lat), _ptr(w_uv), _ptr(o), N, H, _stream(stream)), "mla_unabsorb_o")
+    return o
+
+
+def bmm_fp8_workspace_size() -> int:
+    return lib().mla_bmm_fp8_workspace_size()
+
+
+def _fp8_workspace(dev, workspace):
+    if workspace is None:
+        workspace = torch.empty(bmm_fp8_workspace_size(), dtype=torch.uint8, device=dev)
+    return workspace
+
+
+def absorb_q_fp8(q_nope: torch.Tensor, w_uk_t: torch.Tensor, w_uk_scale: float, q: torch.Tensor,
+                 q_pe: torch.Tensor | None = None, positions: torch.Tensor | None = None,
+                 rope_theta: float = 10000.0, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q[n, h, 0:512] = bmm_fp8(input_to_float8(q_nope), W_UK)[n, h] with w_uk_t [H, 512, 128] E4M3
+    codes (uint8 or float8_e4m3fn) and scale w_uk_scale; q[n, h, 512:576] = q_pe[n, h], RoPE-rotated
+    by positions[n] when positions is given."""
+    N, H, _ = q_nope.shape
+    if w_uk_t.element_size() != 1:
+        raise TypeError("absorb_q_fp8: w_uk_t must hold one E4M3 code per value")
+    ws = _fp8_workspace(q_nope.device, workspace)
+    pe_ptr, pe_stride = (0, 0) if q_pe is None else (_ptr(q_pe), q_pe.stride(0))
+    _check(lib().mla_absorb_q_fp8(_ptr(q_nope), q_nope.stride(0), pe_ptr or None, pe_stride,
+                                  None if positions is None else _ptr(positions), float(rope_theta), _ptr(w_uk_t),
+                                  float(w_uk_scale), _ptr(q), N, H, _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)), "mla_absorb_q_fp8")
+    return q
+
+
+def unabsorb_o_fp8(o_lat: torch.Tensor, w_uv_t: torch.Tensor, w_uv_scale: float, o: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """o[n, h, :] = bmm_fp8(input_to_float8(o_lat), W_UV)[n, h] with w_uv_t [H, 128, 512] E4M3 codes
+    and scale w_uv_scale; o_lat is [N, H, 512] -> o [N, H, 128] bf16."""
+    N, H = o_lat.shape[0], o_lat.shape[1]
+    if w_uv_t.element_size() != 1:
+        raise TypeError("unabsorb_o_fp8: w_uv_t must hold one E4M3 code per value")
+    if o is None:
+        o = torch.empty((N, H, 128), dtype=torch.bfloat16, device=o_lat.device)
+    ws = _fp8_workspace(o_lat.device, workspace)
+    _check(lib().mla_unabsorb_o_fp8(_ptr(o_lat), _ptr(w_uv_t), float(w_uv_scale), _ptr(o), N, H, _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)), "mla_unabsorb_o_fp8")
     return o
 
 

@@ -116,10 +116,12 @@ def sparse_decode_work(seqlens, topk_lens, s_q: int, H: int, causal: bool, indic
     return flops, kv_bytes + q_bytes + out_bytes + sum(topk_lens) * 4 + pages * 4 + B * 8
 
 
-def bmm_work(n_tokens: int, H: int, absorb: bool):
-    """(flops, bytes) of q_nope@W_UK (absorb) or o_lat@W_UV (un-absorb) for n_tokens rows."""
+def bmm_work(n_tokens: int, H: int, absorb: bool, weight_bytes: int = BF16):
+    """(flops, bytes) of q_nope@W_UK (absorb) or o_lat@W_UV (un-absorb) for n_tokens rows;
+    weight_bytes = FP8 for E4M3 weights (bmm_fp8; the bf16 activation is read once and
+    quantized on chip, so it still counts 2 bytes a value)."""
     flops = 2 * n_tokens * H * D_NOPE * D_C
-    w = H * D_NOPE * D_C * BF16
+    w = H * D_NOPE * D_C * weight_bytes
     if absorb:
         io = n_tokens * H * (D_NOPE + D_C) * BF16
     else:

@@ -49,6 +49,7 @@ mla_status_t device_state(int dev, DeviceState** out) {
     if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
     if (decode_set_attributes() != cudaSuccess) return MLA_ERR_CUDA;
     if (bmm_set_attributes() != cudaSuccess) return MLA_ERR_CUDA;
+    if (bmm_fp8_set_attributes() != cudaSuccess) return MLA_ERR_CUDA;
     for (int n = 1; n <= kMaxPairsPerCluster; ++n) d.parts[n] = decode_max_clusters(2 * n);
     d.ready = true;
   }
@@ -421,6 +422,99 @@ mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla
   p.pe_row_stride = 0;
   return launch_bmm(false, a_map, w_map, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
                                                                                                 : MLA_ERR_CUDA;
+}
+
+size_t mla_bmm_fp8_workspace_size(void) { return static_cast<size_t>(kAmaxParts) * sizeof(float); }
+
+}  // extern "C"
+
+namespace {
+
+// Shared body of mla_absorb_q_fp8 (absorb: x = q_nope, K = 128, 512 columns, optional q_pe
+// copy / RoPE) and mla_unabsorb_o_fp8 (x = o_lat, K = 512, 128 columns).
+mla_status_t bmm_fp8_impl(bool absorb, const mla_bf16_t* x, int64_t x_row_stride, const mla_bf16_t* q_pe,
+                          int64_t q_pe_row_stride, const int32_t* positions, double rope_theta, const uint8_t* w_t,
+                          float w_scale, mla_bf16_t* out, int N, int H, void* workspace, size_t workspace_bytes,
+                          mla_stream_t stream) {
+  const int K = absorb ? 128 : kDimV;
+  const int J = absorb ? kDimV : 128;
+  if (!x || !w_t || !out || N < 1 || H < 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_t) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  if (x_row_stride < static_cast<int64_t>(H) * K || (x_row_stride % 8) != 0) return MLA_ERR_INVALID_ARG;
+  if (q_pe && (!aligned16(q_pe) || q_pe_row_stride < static_cast<int64_t>(H) * 64 || (q_pe_row_stride % 8) != 0))
+    return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(w_scale) || !(w_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < mla_bmm_fp8_workspace_size() || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+    return workspace_bytes < mla_bmm_fp8_workspace_size() || !workspace ? MLA_ERR_WORKSPACE : MLA_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  mla_status_t st = current_device(&d);
+  if (st != MLA_OK) return st;
+  CUtensorMap x_map, w_map;
+  // x as [K, H, N] with the token stride given: one box = 64 values of 128 tokens of one head
+  if (!encode_3d(&x_map, x, static_cast<uint64_t>(K), static_cast<uint64_t>(H), static_cast<uint64_t>(N),
+                 static_cast<uint64_t>(K) * 2, static_cast<uint64_t>(x_row_stride) * 2, 64, 1, 128))
+    return MLA_ERR_CUDA;
+  {   // the E4M3 weight codes as [H * J rows][K codes]: one box = 128 codes of the tile's rows
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(H) * J};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(absorb ? 256 : 128)};
+    const cuuint32_t es[2] = {1, 1};
+    if (g_encode(&w_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w_t), dims, strides, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MLA_ERR_CUDA;
+  }
+  BmmFp8Params p = {};
+  p.base.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.base.out_row_stride = static_cast<int64_t>(H) * (absorb ? kDimQK : 128);
+  p.base.out_head_stride = absorb ? kDimQK : 128;
+  p.base.N = N;
+  p.base.H = H;
+  p.base.status = d->status;
+  p.base.pe = reinterpret_cast<const __nv_bfloat16*>(q_pe);
+  p.base.pe_row_stride = q_pe_row_stride;
+  p.base.positions = positions;
+  if (positions) {   // inverse frequencies theta^(-2j/64) and 2*pi, each as a float pair (hi + lo)
+    for (int j = 0; j < 32; ++j) {
+      const double inv = std::pow(rope_theta, -2.0 * j / 64.0);
+      p.base.rope_hi[j] = static_cast<float>(inv);
+      p.base.rope_lo[j] = static_cast<float>(inv - static_cast<double>(p.base.rope_hi[j]));
+    }
+    const double two_pi = 6.283185307179586476925286766559;
+    p.base.two_pi_hi = static_cast<float>(two_pi);
+    p.base.two_pi_lo = static_cast<float>(two_pi - static_cast<double>(p.base.two_pi_hi));
+  }
+  p.partials = static_cast<const float*>(workspace);
+  p.w = w_t;
+  p.J = J;
+  p.w_scale = w_scale;
+  return launch_bmm_fp8(absorb, reinterpret_cast<const __nv_bfloat16*>(x), x_row_stride, K, x_map, w_map, p,
+                        static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_absorb_q_fp8(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                              int64_t q_pe_row_stride, const int32_t* positions, float rope_theta,
+                              const uint8_t* w_uk_t, float w_uk_scale, mla_bf16_t* q, int N, int H, void* workspace,
+                              size_t workspace_bytes, mla_stream_t stream) {
+  if (positions && (!q_pe || (reinterpret_cast<uintptr_t>(positions) & 3u) || !std::isfinite(rope_theta) ||
+                    !(rope_theta > 1.f)))
+    return MLA_ERR_INVALID_ARG;
+  return bmm_fp8_impl(true, q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, positions,
+                      static_cast<double>(rope_theta), w_uk_t, w_uk_scale, q, N, H, workspace, workspace_bytes,
+                      stream);
+}
+
+mla_status_t mla_unabsorb_o_fp8(const mla_bf16_t* o_lat, const uint8_t* w_uv_t, float w_uv_scale, mla_bf16_t* o, int N,
+                                int H, void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  if (!o_lat) return MLA_ERR_INVALID_ARG;
+  return bmm_fp8_impl(false, o_lat, static_cast<int64_t>(H) * kDimV, nullptr, 0, nullptr, 0.0, w_uv_t, w_uv_scale, o, N,
+                      H, workspace, workspace_bytes, stream);
 }
 
 mla_status_t mla_get_device_status(mla_stream_t stream) {

@@ -136,4 +136,19 @@ cudaError_t bmm_set_attributes();
 cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap& w_map, const BmmParams& p,
                        cudaStream_t stream);
 
+// FP8 projections: x (bf16) quantized per tensor on the fly, E4M3 weights stored transposed
+// ([H, J, K], K contiguous) with one per-tensor scale.  `partials` (kAmaxParts floats of
+// caller workspace) receives the partial maxima of |x| that the bmm kernel reduces.
+constexpr int kAmaxParts = 128;
+struct BmmFp8Params {
+  BmmParams base;           // output, strides, N, H, status, the optional q_pe copy / RoPE
+  const float* partials;    // [kAmaxParts]
+  const uint8_t* w;         // [H, J, K] E4M3 codes
+  int J;                    // output columns per head (512: absorption, 128: un-absorption)
+  float w_scale;
+};
+cudaError_t bmm_fp8_set_attributes();
+cudaError_t launch_bmm_fp8(bool absorb, const __nv_bfloat16* x, int64_t x_row_stride, int K, const CUtensorMap& x_map,
+                           const CUtensorMap& w_map, const BmmFp8Params& p, float* partials, cudaStream_t stream);
+
 }  // namespace mla

@@ -103,3 +103,35 @@ def test_host_argument_checks(mla):
     assert L.mla_absorb_q(A, 128, A, 8, A, A, 4, 1, None) == 1         # q_pe stride below H*64
     assert L.mla_unabsorb_o(A + 8, A, A, 4, 1, None) == 1
     assert L.mla_num_sm_parts(0, 5, 128) < 0
+
+
+def test_fp8_projection_argument_checks(mla):
+    L = mla.lib()
+    A = 0x10000  # 16-byte aligned, never dereferenced: every case returns before any launch
+    ws = mla.bmm_fp8_workspace_size()
+    assert ws >= 4 * 128
+    # (q_nope, stride, q_pe, pe_stride, positions, theta, w_uk_t, w_scale, q, N, H, workspace, bytes, stream)
+    ab = [A, 128, A, 64, A, 10000.0, A, 2.0 ** -9, A, 4, 1, A, ws, None]
+    for i in (0, 6, 8):                                             # q_nope, weights, q
+        bad = list(ab); bad[i] = None
+        assert L.mla_absorb_q_fp8(*bad) == 1                        # MLA_ERR_INVALID_ARG
+    for bad_scale in (0.0, -1.0, float("nan"), float("inf")):
+        bad = list(ab); bad[7] = bad_scale
+        assert L.mla_absorb_q_fp8(*bad) == 1
+    bad = list(ab); bad[1] = 100                                    # stride below H*128
+    assert L.mla_absorb_q_fp8(*bad) == 1
+    bad = list(ab); bad[2] = None                                   # positions without q_pe
+    assert L.mla_absorb_q_fp8(*bad) == 1
+    bad = list(ab); bad[5] = 1.0                                    # rope_theta must exceed 1
+    assert L.mla_absorb_q_fp8(*bad) == 1
+    bad = list(ab); bad[12] = ws - 1
+    assert L.mla_absorb_q_fp8(*bad) == 3                            # MLA_ERR_WORKSPACE
+    bad = list(ab); bad[11] = None
+    assert L.mla_absorb_q_fp8(*bad) == 3
+    # (o_lat, w_uv_t, w_scale, o, N, H, workspace, bytes, stream)
+    un = [A, A, 2.0 ** -9, A, 4, 1, A, ws, None]
+    assert L.mla_unabsorb_o_fp8(*([A + 8] + un[1:])) == 1            # misaligned o_lat
+    bad = list(un); bad[2] = 0.0
+    assert L.mla_unabsorb_o_fp8(*bad) == 1
+    bad = list(un); bad[7] = 0
+    assert L.mla_unabsorb_o_fp8(*bad) == 3
