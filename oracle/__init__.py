@@ -13,8 +13,9 @@ checks), written for a reader to check against the pages by eye:
                     cache with a per-tensor scale, and over a selected top-k
                     token list), the expanded (un-absorbed) chain, the
                     LSE merge, a pure-Python brute force, the tiny full-MLA
-                    example with decoupled RoPE, and the FP8 projections
-                    (per-tensor input quantization, bmm_fp8).
+                    example with decoupled RoPE, the FP8 projections
+                    (per-tensor input quantization, bmm_fp8), and the chunked
+                    expanded extend (MHA_CHUNKED_KV: chunks merged by LSE).
 * ``schedule.py`` -- a restatement of the split-KV schedule rule and the
                     invariants any valid schedule must satisfy.
 
@@ -27,5 +28,6 @@ from .mla import (  # noqa: F401
     decode_absorbed, decode_fp8, decode_sparse, decode_expanded, absorb_q, assemble_q, unabsorb_o,
     lse_merge, decode_bruteforce, tiny_full_mla, rope_interleaved,
     E4M3_MAX, e4m3_round, input_to_float8, bmm_fp8, absorb_q_fp8, assemble_q_fp8, unabsorb_o_fp8,
+    expand_chunk, attend_chunk, extend_chunked_expanded,
 )
 from .schedule import schedule_reference, check_schedule  # noqa: F401

@@ -488,3 +488,67 @@ def unabsorb_o_fp8(o_lat, w_uv_t_codes, w_uv_scale):
     o_lat [N, H, 512] -> [N, H, 128] float64; w_uv_t_codes [H, 128, 512] (W_UV[h]^T)."""
     codes, scale = input_to_float8(o_lat)
     return bmm_fp8(codes, scale, w_uv_t_codes, w_uv_scale)
+
+
+# --------------------------------------------- chunked expanded extend (MHA_CHUNKED_KV) --
+# [MLA-paths] end of section "两条等价的路径" and exercise 3: with a long cached prefix, an
+# extend (T new tokens after P cached ones) runs on the expanded path with the prefix
+# expanded chunk by chunk -- per head K = [W_UK c, k^R] and V = W_UV^T c for the chunk's
+# tokens only -- attention of the new tokens to each chunk on its own, and the per-chunk
+# results merged by LSE (the merge of context parallelism), so that the whole expanded
+# prefix (~80 KB a token) never exists at once.
+
+def expand_chunk(kv_rows, w_uk, w_uv):
+    """The expanded keys and values of a run of cached rows ([MLA-paths] path 1):
+    k_nope[h, t] = W_UK[h] c_t (128), k_pe[t] = k^R_t (64, shared by the heads),
+    v[h, t] = W_UV[h]^T c_t (128).  kv_rows [n, 576]; returns k_nope [H, n, 128],
+    k_pe [n, 64], v [H, n, 128] float64."""
+    c = np.asarray(kv_rows, dtype=np.float64)[:, :D_LATENT]
+    k_pe = np.asarray(kv_rows, dtype=np.float64)[:, D_LATENT:]
+    k_nope = np.einsum("hdc,tc->htd", np.asarray(w_uk, dtype=np.float64), c)
+    v = np.einsum("tc,hcd->htd", c, np.asarray(w_uv, dtype=np.float64))
+    return k_nope, k_pe, v
+
+
+def attend_chunk(q_nope, q_pe, k_nope, k_pe, v, key_pos, query_pos, softmax_scale):
+    """Multi-head attention of T queries to one expanded chunk, causal by position: query i
+    (at position query_pos[i]) sees key t if key_pos[t] <= query_pos[i].  q_nope [T, H, 128],
+    q_pe [T, H, 64]; k_nope [H, n, 128], k_pe [n, 64], v [H, n, 128].  Returns the chunk's
+    normalised output o [T, H, 128] and lse [T, H] (o = 0, lse = -inf for a query that sees
+    no key of the chunk)."""
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    q_pe = np.asarray(q_pe, dtype=np.float64)
+    T, H, _ = q_nope.shape
+    o = np.zeros((T, H, v.shape[2]))
+    lse = np.full((T, H), -np.inf)
+    for i in range(T):
+        seen = np.asarray(key_pos) <= query_pos[i]
+        if not seen.any():
+            continue
+        s = softmax_scale * (np.einsum("hd,htd->ht", q_nope[i], k_nope[:, seen]) + q_pe[i] @ k_pe[seen].T)
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        z = e.sum(axis=1, keepdims=True)
+        lse[i] = (m + np.log(z))[:, 0]
+        o[i] = np.einsum("ht,htd->hd", e / z, v[:, seen])
+    return o, lse
+
+
+def extend_chunked_expanded(q_nope, q_pe, w_uk, w_uv, kv_cache, block_row, seqlen, softmax_scale, chunk_tokens):
+    """Extend of one request on the expanded path with its context in chunks: the T new
+    tokens are the last T of the request's seqlen cached tokens (new token i at position
+    seqlen - T + i, causal); the cached rows [c0, c0 + chunk_tokens) are expanded
+    (expand_chunk), attended to (attend_chunk), and the chunks' (o, lse) merged by lse_merge.
+    q_nope [T, H, 128], q_pe [T, H, 64] (RoPE already applied).  Returns o [T, H, 128], lse [T, H]."""
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    T = q_nope.shape[0]
+    rows = gather_request(kv_cache, block_row, int(seqlen))
+    qpos = np.arange(int(seqlen) - T, int(seqlen))
+    parts_o, parts_l = [], []
+    for c0 in range(0, int(seqlen), int(chunk_tokens)):
+        c1 = min(int(seqlen), c0 + int(chunk_tokens))
+        k_nope, k_pe, v = expand_chunk(rows[c0:c1], w_uk, w_uv)
+        o, l = attend_chunk(q_nope, q_pe, k_nope, k_pe, v, np.arange(c0, c1), qpos, softmax_scale)
+        parts_o.append(o)
+        parts_l.append(l)
+    return lse_merge(np.stack(parts_o), np.stack(parts_l))
