@@ -242,6 +242,35 @@ mla_status_t mla_absorb_q_fp8(const mla_bf16_t* q_nope, int64_t q_nope_row_strid
 mla_status_t mla_unabsorb_o_fp8(const mla_bf16_t* o_lat, const uint8_t* w_uv_t, float w_uv_scale, mla_bf16_t* o,
                                 int N, int H, void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
+/* Chunked extend on the expanded path (MHA_CHUNKED_KV; page "MLA 推理：两条计算路径与
+ * FlashMLA", end of section "两条等价的路径", and its exercise 3): T new tokens of one request
+ * attend, causally, to the request's seqlen cached tokens, the new tokens being the last T
+ * of them (new token i sits at position seqlen - T + i and sees positions <= its own).  The
+ * cache is expanded chunk by chunk -- per head h and cached token t with latent c_t and RoPE
+ * key k^R_t:  k_t = [W_UK[h] c_t (128), k^R_t (64)],  v_t = W_UV[h]^T c_t (128) -- each chunk
+ * is attended to on its own, and the chunks' results are merged by log-sum-exp:
+ *     s_t = softmax_scale * <[q_nope, q_pe][i, h], k_t>,   out = sum_t softmax(s)_t v_t,
+ *     lse = ln sum_t exp(s_t)  (natural log, scaled scores)
+ * so that the expanded context (~80 KB a token at H = 128) never exists at once.  The result
+ * equals the absorbed path's (mla_absorb_q, then attention over the latent, then
+ * mla_unabsorb_o) up to rounding.
+ *  q_nope [T, H, 128], q_pe [T, H, 64] (RoPE applied) bf16;  w_uk [H, 128, 512] and
+ *  w_uv [H, 512, 128] bf16 as for mla_absorb_q / mla_unabsorb_o;  kv_cache as for mla_decode;
+ *  block_row: the request's block-table row, int32 device, entries for pages
+ *  0 .. ceil(seqlen / 64) - 1 in [0, num_blocks) (others are reported as
+ *  MLA_ERR_DEVICE_BOUNDS and read as zeros);  seqlen (host) >= T >= 1;
+ *  chunk_tokens: cached tokens expanded at a time, a positive multiple of 64;
+ *  workspace >= mla_extend_workspace_size(T, H, chunk_tokens) bytes, 256-byte aligned
+ *  (the expanded keys and values of one chunk, ~512 * H bytes a chunk token, and the
+ *  running fp32 merge of the output);  out [T, H, 128] bf16;  lse [T, H] fp32.
+ * Launches two kernels per chunk on `stream`, in order.  Async on stream. */
+size_t mla_extend_workspace_size(int T, int H, int chunk_tokens);
+mla_status_t mla_extend_chunked(const mla_bf16_t* q_nope, const mla_bf16_t* q_pe, const mla_bf16_t* w_uk,
+                                const mla_bf16_t* w_uv, const mla_bf16_t* kv_cache, int64_t num_blocks,
+                                const int32_t* block_row, int seqlen, int T, int H, float softmax_scale,
+                                int chunk_tokens, void* workspace, size_t workspace_bytes, mla_bf16_t* out,
+                                float* lse, mla_stream_t stream);
+
 /* mla_decode without caller-provided scratch.  The paper has no counterpart:
  * this entry point exists for callers that cannot allocate device memory or pass
  * a workspace -- code inside an inference engine or plugin whose memory pool

@@ -16,7 +16,8 @@ import torch
 __all__ = [
     "MLAError", "lib", "library_path", "num_sm_parts", "metadata_size", "decode_metadata",
     "decode_workspace_size", "decode", "decode_sparse", "decode_fp8", "decode_sparse_fp8", "absorb_q", "unabsorb_o",
-    "bmm_fp8_workspace_size", "absorb_q_fp8", "unabsorb_o_fp8", "get_device_status",
+    "bmm_fp8_workspace_size", "absorb_q_fp8", "unabsorb_o_fp8", "extend_workspace_size", "extend_chunked",
+    "get_device_status",
     "schedule_params", "debug_withhold_first_load", "DecodeStep", "EXPORTED_SYMBOLS",
 ]
 
@@ -49,6 +50,9 @@ _SIGNATURES = {
     "mla_bmm_fp8_workspace_size": (_c_size, []),
     "mla_absorb_q_fp8": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _c_float, _p, _c_int, _c_int, _p, _c_size, _p]),
     "mla_unabsorb_o_fp8": (_c_int, [_p, _p, _c_float, _p, _c_int, _c_int, _p, _c_size, _p]),
+    "mla_extend_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
+    "mla_extend_chunked": (_c_int, [_p, _p, _p, _p, _p, _c_ll, _p, _c_int, _c_int, _c_int, _c_float, _c_int, _p, _c_size,
+                                    _p, _p, _p]),
     "mla_decode_noalloc": (_c_int, [_p, _p, _c_ll, _p, _c_int, _p, _c_int, _c_int, _c_int, _c_float, _c_int,
                                     _c_int, _p, _p, _p]),
     "mla_get_device_status": (_c_int, [_p]),
@@ -278,6 +282,33 @@ def unabsorb_o_fp8(o_lat: torch.Tensor, w_uv_t: torch.Tensor, w_uv_scale: float,
     _check(lib().mla_unabsorb_o_fp8(_ptr(o_lat), _ptr(w_uv_t), float(w_uv_scale), _ptr(o), N, H, _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)), "mla_unabsorb_o_fp8")
     return o
+
+
+def extend_workspace_size(T: int, H: int, chunk_tokens: int) -> int:
+    return lib().mla_extend_workspace_size(T, H, chunk_tokens)
+
+
+def extend_chunked(q_nope: torch.Tensor, q_pe: torch.Tensor, w_uk: torch.Tensor, w_uv: torch.Tensor,
+                   kv_cache: torch.Tensor, block_row: torch.Tensor, seqlen: int, softmax_scale: float,
+                   chunk_tokens: int = 2048, workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                   lse: torch.Tensor | None = None, stream=None):
+    """Chunked extend on the expanded path (MHA_CHUNKED_KV): the T new tokens (the last T of the
+    request's seqlen cached tokens, causal) attend to the cache expanded chunk by chunk, merged by
+    LSE.  q_nope [T,H,128], q_pe [T,H,64] (RoPE applied), w_uk [H,128,512], w_uv [H,512,128],
+    block_row int32 [>= ceil(seqlen/64)].  Returns (out [T,H,128] bf16, lse [T,H] fp32)."""
+    T, H, _ = q_nope.shape
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(extend_workspace_size(T, H, chunk_tokens), dtype=torch.uint8, device=dev)
+    _check(lib().mla_extend_chunked(_ptr(q_nope), _ptr(q_pe), _ptr(w_uk), _ptr(w_uv), _ptr(kv_cache),
+                                    kv_cache.shape[0], _ptr(block_row), int(seqlen), T, H, float(softmax_scale),
+                                    int(chunk_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _ptr(out), _ptr(lse), _stream(stream)), "mla_extend_chunked")
+    return out, lse
 
 
 def get_device_status(stream=None) -> int:

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmla.so")
-SOURCES = ["mla_host.cu", "mla_decode.cu", "mla_aux.cu", "mla_noalloc.cu", "mla_proj_fp8.cu"]
+SOURCES = ["mla_host.cu", "mla_decode.cu", "mla_aux.cu", "mla_noalloc.cu", "mla_proj_fp8.cu", "mla_extend.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]

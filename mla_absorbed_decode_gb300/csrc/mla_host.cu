@@ -50,6 +50,7 @@ mla_status_t device_state(int dev, DeviceState** out) {
     if (decode_set_attributes() != cudaSuccess) return MLA_ERR_CUDA;
     if (bmm_set_attributes() != cudaSuccess) return MLA_ERR_CUDA;
     if (bmm_fp8_set_attributes() != cudaSuccess) return MLA_ERR_CUDA;
+    if (extend_set_attributes() != cudaSuccess) return MLA_ERR_CUDA;
     for (int n = 1; n <= kMaxPairsPerCluster; ++n) d.parts[n] = decode_max_clusters(2 * n);
     d.ready = true;
   }
@@ -515,6 +516,87 @@ mla_status_t mla_unabsorb_o_fp8(const mla_bf16_t* o_lat, const uint8_t* w_uv_t, 
   if (!o_lat) return MLA_ERR_INVALID_ARG;
   return bmm_fp8_impl(false, o_lat, static_cast<int64_t>(H) * kDimV, nullptr, 0, nullptr, 0.0, w_uv_t, w_uv_scale, o, N,
                       H, workspace, workspace_bytes, stream);
+}
+
+namespace {
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+int extend_cap(int chunk_tokens) { return (chunk_tokens + 127) / 128 * 128; }
+}  // namespace
+
+size_t mla_extend_workspace_size(int T, int H, int chunk_tokens) {
+  if (T < 1 || H < 1 || chunk_tokens < kPageTokens || chunk_tokens % kPageTokens) return 0;
+  const size_t cap = static_cast<size_t>(extend_cap(chunk_tokens));
+  const size_t kv = round256(cap * H * 128 * sizeof(uint16_t));
+  return 2 * kv + round256(static_cast<size_t>(T) * H * 128 * sizeof(float)) +
+         round256(static_cast<size_t>(T) * H * sizeof(float));
+}
+
+mla_status_t mla_extend_chunked(const mla_bf16_t* q_nope, const mla_bf16_t* q_pe, const mla_bf16_t* w_uk,
+                                const mla_bf16_t* w_uv, const mla_bf16_t* kv_cache, int64_t num_blocks,
+                                const int32_t* block_row, int seqlen, int T, int H, float softmax_scale,
+                                int chunk_tokens, void* workspace, size_t workspace_bytes, mla_bf16_t* out,
+                                float* lse, mla_stream_t stream) {
+  if (!q_nope || !q_pe || !w_uk || !w_uv || !kv_cache || !block_row || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(kv_cache) ||
+      !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_row) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  if (T < 1 || H < 1 || seqlen < T || num_blocks < 1) return MLA_ERR_INVALID_ARG;
+  if (chunk_tokens < kPageTokens || chunk_tokens % kPageTokens) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (num_blocks * kPageTokens > (int64_t(1) << 31) - kPageTokens) return MLA_ERR_UNSUPPORTED;
+  const size_t need = mla_extend_workspace_size(T, H, chunk_tokens);
+  if (!workspace || workspace_bytes < need) return MLA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MLA_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  mla_status_t st = current_device(&d);
+  if (st != MLA_OK) return st;
+
+  const int cap = extend_cap(chunk_tokens);
+  const uint64_t uH = static_cast<uint64_t>(H);
+  ExtendMaps m;
+  const bool maps_ok =
+      encode_3d(&m.c, kv_cache, 64, static_cast<uint64_t>(num_blocks) * kPageTokens, kDimQK / 64, kDimQK * 2, 128, 64,
+                64, 1) &&
+      encode_2d(&m.wk, w_uk, kDimV, uH * 128, kDimV * 2, 64, 128) &&
+      encode_2d(&m.wv, w_uv, 128, uH * kDimV, 256, 64, 64) &&
+      encode_3d(&m.qn, q_nope, 128, uH, static_cast<uint64_t>(T), 256, uH * 256, 64, 1, 128) &&
+      encode_3d(&m.qp, q_pe, 64, uH, static_cast<uint64_t>(T), 128, uH * 128, 64, 1, 128);
+  char* ws = static_cast<char*>(workspace);
+  const size_t kv_bytes = round256(static_cast<size_t>(cap) * H * 128 * sizeof(uint16_t));
+  __nv_bfloat16* kx = reinterpret_cast<__nv_bfloat16*>(ws);
+  __nv_bfloat16* vx = reinterpret_cast<__nv_bfloat16*>(ws + kv_bytes);
+  float* acc_o = reinterpret_cast<float*>(ws + 2 * kv_bytes);
+  float* acc_lse = reinterpret_cast<float*>(ws + 2 * kv_bytes + round256(static_cast<size_t>(T) * H * 128 * 4));
+  if (!maps_ok || !encode_3d(&m.kx, kx, 128, uH, static_cast<uint64_t>(cap), 256, uH * 256, 64, 1, 64) ||
+      !encode_3d(&m.vx, vx, 128, uH, static_cast<uint64_t>(cap), 256, uH * 256, 64, 1, 64))
+    return MLA_ERR_CUDA;
+  m.kr = m.c;
+
+  ExtendParams p;
+  p.block_row = block_row;
+  p.num_blocks = num_blocks;
+  p.cap = cap;
+  p.T = T;
+  p.H = H;
+  p.qpos0 = seqlen - T;
+  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634074);
+  p.kx = kx;
+  p.vx = vx;
+  p.acc_o = acc_o;
+  p.acc_lse = acc_lse;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = d->status;
+  const int n_chunks = (seqlen + chunk_tokens - 1) / chunk_tokens;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  for (int j = 0; j < n_chunks; ++j) {
+    p.c0 = j * chunk_tokens;
+    p.n = seqlen - p.c0 < chunk_tokens ? seqlen - p.c0 : chunk_tokens;
+    p.first = j == 0;
+    p.last = j == n_chunks - 1;
+    if (launch_extend_chunk(m, p, cs) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
 }
 
 mla_status_t mla_get_device_status(mla_stream_t stream) {

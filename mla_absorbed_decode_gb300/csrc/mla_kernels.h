@@ -151,4 +151,32 @@ cudaError_t bmm_fp8_set_attributes();
 cudaError_t launch_bmm_fp8(bool absorb, const __nv_bfloat16* x, int64_t x_row_stride, int K, const CUtensorMap& x_map,
                            const CUtensorMap& w_map, const BmmFp8Params& p, float* partials, cudaStream_t stream);
 
+// Chunked extend on the expanded path: one chunk [c0, c0 + n) of a request's cache.
+struct ExtendParams {
+  const int32_t* block_row;     // the request's block-table row (device)
+  int64_t num_blocks;
+  int c0, n, cap;               // chunk start (a multiple of 64), its tokens, Kx / Vx rows
+  int T, H, qpos0;              // new tokens, heads, position of new token 0 (seqlen - T)
+  float scale_log2;             // softmax_scale * log2(e)
+  __nv_bfloat16* kx;            // [cap, H, 128] expanded keys (no RoPE part)
+  __nv_bfloat16* vx;            // [cap, H, 128] expanded values
+  float* acc_o;                 // [T, H, 128] running merged output (fp32)
+  float* acc_lse;               // [T, H] running merged lse
+  int first, last;              // the first / last chunk of the call
+  __nv_bfloat16* out;           // [T, H, 128] bf16 (written by the last chunk)
+  float* lse;                   // [T, H] (written by the last chunk)
+  int* status;
+};
+struct ExtendMaps {
+  CUtensorMap c;                // cache [chunk 0..8][row][64 dims], box 64 x 64 rows x 1 chunk
+  CUtensorMap wk;               // W_UK as [H * 128 rows][512], box 64 x 128
+  CUtensorMap wv;               // W_UV as [H * 512 rows][128], box 64 x 64
+  CUtensorMap qn;               // q_nope [128, H, T], box 64 x 1 x 128
+  CUtensorMap qp;               // q_pe [64, H, T], box 64 x 1 x 128
+  CUtensorMap kx, vx;           // [128, H, cap], box 64 x 1 x 64
+  CUtensorMap kr;               // the cache view of c, k^R = chunk 8
+};
+cudaError_t extend_set_attributes();
+cudaError_t launch_extend_chunk(const ExtendMaps& maps, const ExtendParams& p, cudaStream_t stream);
+
 }  // namespace mla
