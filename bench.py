@@ -15,7 +15,9 @@ rates the dominant kernel (the mla_decode call) against the measured HBM peak.
 ragged, MTP (s_q = 2, causal) and long-context ones, the V3 shape over an FP8
 (E4M3) cache (fp8_deepseek_v3_b64_h128_l4096: mla_decode_fp8, the FP8 tensor rate
 in the roofline), and the V3.2-shaped top-2048 sparse decode over a bf16 or an
-FP8 cache (sparse_b64_h128_l16384_top2048, sparse_fp8_b64_h128_l16384_top2048).
+FP8 cache (sparse_b64_h128_l16384_top2048, sparse_fp8_b64_h128_l16384_top2048), the V3
+step with FP8 projections (fp8proj_deepseek_v3_b64_h128_l4096: bmm_fp8), and the chunked
+extend on the expanded path (extend_t512_l32768_h128_chunk4096: mla_extend_chunked).
 --impl reference times the CPU oracle (numpy float64) on a bounded sample of
 the same workload per step.  With N > 1 (torchrun) every rank runs its own
 replica of the workload (requests shard across GPUs with no exchange).
@@ -224,6 +226,35 @@ def run_reference(args, w):
         return 0
     from mla_absorbed_decode_gb300 import workloads as W
     inp = W.make_inputs(w)
+    if w.chunk_tokens:   # chunked extend: the oracle on one head and the last 8 new tokens per step
+        import numpy as np
+        import oracle
+        from mla_absorbed_decode_gb300 import accounting as acc
+        T, L = w.s_q, w.seqlen
+        sel_t = np.arange(T - 8, T)
+        args_o = (inp["q_nope"][sel_t][:, :1].float().numpy(), inp["q_pe"][sel_t][:, :1].float().numpy(),
+                  inp["w_uk"][:1].float().numpy(), inp["w_uv"][:1].float().numpy(), inp["kv_cache"].float().numpy(),
+                  inp["block_table"][0].numpy(), L - (T - 8), inp["softmax_scale"], w.chunk_tokens)
+        for _ in range(args.warmup):
+            oracle.extend_chunked_expanded(*args_o)
+        times = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            oracle.extend_chunked_expanded(*args_o)
+            times.append(time.perf_counter() - t0)
+        t = statistics.mean(times)
+        value = acc.extend_work(L - (T - 8), 8, 1)[0] / t / 1e12
+        sample = f"one head, the last 8 new tokens (context {L - (T - 8)}) per step"
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "T_new": T, "H": w.H, "seqlen": L, "chunk_tokens": w.chunk_tokens,
+                       "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return 0
     inp["_kv_np"] = _kv_for_oracle(inp)
     if w.with_projections:
         inp["_w_uk_np"] = inp["w_uk"].double().numpy()
@@ -278,6 +309,133 @@ def _graphed(torch, fn, dev):
     with torch.cuda.graph(g):
         fn()
     return g.replay
+
+
+def run_extend(args, w):
+    """The chunked extend on the expanded path (mla_extend_chunked): T = w.s_q new tokens after
+    a (seqlen - T)-token prefix of one request, the cache expanded w.chunk_tokens at a time.
+    A step is one extend call; value = algorithmic TFLOP/s; the roofline object rates the
+    call against the measured bf16 tensor rate (the path is tensor-bound)."""
+    import torch
+    import mla_absorbed_decode_gb300 as mla
+    from mla_absorbed_decode_gb300 import accounting as acc, build_lib, workloads as W
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build_lib.build()
+    dev = torch.device("cuda", local)
+    inp = W.make_inputs(w, seed=rank)
+    T, H, L, chunk = w.s_q, w.H, w.seqlen, w.chunk_tokens
+    qn, qp = inp["q_nope"].to(dev), inp["q_pe"].to(dev)
+    wk, wv = inp["w_uk"].to(dev), inp["w_uv"].to(dev)
+    kv, row = inp["kv_cache"].to(dev), inp["block_table"][0].contiguous().to(dev)
+    work = torch.empty(mla.extend_workspace_size(T, H, chunk), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    flush_w = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        flush_r.sum()
+
+    def call(q_nope=qn, q_pe=qp):
+        mla.extend_chunked(q_nope, q_pe, wk, wv, kv, row, L, inp["softmax_scale"], chunk_tokens=chunk,
+                           workspace=work, out=out, lse=lse)
+
+    for _ in range(max(args.warmup, 3)):
+        flush()
+        call()
+    torch.cuda.synchronize()
+    if mla.get_device_status() != 0:
+        raise RuntimeError("device status during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush()
+            starts[i].record()
+            call()
+            ends[i].record()
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    if mla.get_device_status() != 0:
+        raise RuntimeError("device status in the timed region")
+    t_step = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3
+    t_step, = max_over_ranks([t_step], dist, dev)
+    flops, nbytes = acc.extend_work(L, T, H)
+    n = ws
+    value = n * flops / t_step / 1e12
+    # end to end: q_nope and q_pe from pinned host memory, out and lse back, every step
+    e2e = None
+    if not args.no_e2e:
+        hq, hp = inp["q_nope"].pin_memory(), inp["q_pe"].pin_memory()
+        dq, dp = torch.empty_like(qn), torch.empty_like(qp)
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps + 2):
+            flush()
+            if i >= 2:
+                es[i - 2].record()
+            dq.copy_(hq, non_blocking=True)
+            dp.copy_(hp, non_blocking=True)
+            call(dq, dp)
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            if i >= 2:
+                ee[i - 2].record()
+        torch.cuda.synchronize()
+        t_e2e = statistics.mean(a.elapsed_time(b) for a, b in zip(es, ee)) / 1e3
+        t_e2e, = max_over_ranks([t_e2e], dist, dev)
+        e2e = {"value": n * flops / t_e2e / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": hq.numel() * 2 + hp.numel() * 2,
+               "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4, "ms_per_step": t_e2e * 1e3}
+    peaks = _peaks()
+    ach = flops / t_step / 1e12
+    roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_tflops"], "peak_source": peaks["source"], "traffic": None,
+            "kernel": "mla_extend_chunked (expansion GEMM + flash attention per chunk)",
+            "algorithmic_per_launch": {"bytes": nbytes, "flops": flops}, "ms_per_launch": t_step * 1e3,
+            "frac_of_spec_roofline": acc.roofline_time(flops, nbytes, SPEC_FLOPS, SPEC_BW) / t_step}
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:   # the oracle on one head and 8 new tokens
+        import numpy as np
+        import oracle
+        sel_t = np.arange(T - 8, T)
+        t0 = time.perf_counter()
+        oracle.extend_chunked_expanded(inp["q_nope"][sel_t][:, :1].float().numpy(),
+                                       inp["q_pe"][sel_t][:, :1].float().numpy(), inp["w_uk"][:1].float().numpy(),
+                                       inp["w_uv"][:1].float().numpy(), inp["kv_cache"].float().numpy(),
+                                       inp["block_table"][0].numpy(), L - (T - 8), inp["softmax_scale"], chunk)
+        dt = time.perf_counter() - t0
+        f1, _ = acc.extend_work(L - (T - 8), 8, 1)
+        cpu = {"value": f1 / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"one head, the last 8 new tokens (context {L - (T - 8)}), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": n, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "T_new": T, "H": H, "seqlen": L, "chunk_tokens": chunk,
+                       "path": "mla_extend_chunked", "parallelism": f"replicas x{n}",
+                       "l2": "flushed between timed steps (256 MiB write, then 256 MiB read; outside the step events)"},
+            "pct_of_roofline": 100.0 * acc.roofline_time(flops, nbytes, SPEC_FLOPS, SPEC_BW) / t_step,
+            "roofline_spec": {"peak_tflops": SPEC_FLOPS / 1e12, "peak_gbs": SPEC_BW / 1e9},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 2 * ((L + chunk - 1) // chunk) * args.steps, "clocks": clocks.summary()}))
+    if dist:
+        dist.destroy_process_group()
+    return 0
 
 
 def run_ours(args, w):
@@ -620,6 +778,8 @@ def main():
         w = dataclasses.replace(w, B=args.batch, name=f"{w.name}_b{args.batch}")
     if args.impl == "reference":
         return run_reference(args, w)
+    if w.chunk_tokens:
+        return run_extend(args, w)
     return run_ours(args, w)
 
 

@@ -129,6 +129,20 @@ def bmm_work(n_tokens: int, H: int, absorb: bool, weight_bytes: int = BF16):
     return flops, w + io
 
 
+def extend_work(seqlen: int, T: int, H: int):
+    """Algorithmic (flops, bytes) of one chunked extend on the expanded path: every cached
+    token's latent is expanded once per head into a 128-value key and a 128-value value
+    (2 * 512 * 256 flops), and each visible (new token, cached token) pair costs
+    2 * (192 + 128) flops per head ("MLA 推理", the FLOP counter's expanded pair, 82K at
+    H = 128); new token i (at position seqlen - T + i) sees seqlen - T + i + 1 tokens.
+    Bytes: the cache read once (1152 per token), W_UK and W_UV, q_nope and q_pe in, out and
+    lse out; the expanded chunks are intermediates, not algorithmic bytes."""
+    pairs = sum(seqlen - T + i + 1 for i in range(T))
+    flops = seqlen * H * 2 * D_C * (D_NOPE + D_V) + pairs * H * 2 * (D_NOPE + D_R + D_V)
+    nbytes = seqlen * (D_C + D_R) * BF16 + 2 * H * D_NOPE * D_C * BF16 + T * H * (D_NOPE + D_R + D_V) * BF16 + T * H * 4
+    return flops, nbytes
+
+
 def roofline_time(flops: float, nbytes: float, peak_flops: float, peak_bw: float) -> float:
     """max(FLOPs / peak FLOP/s, bytes / peak bytes/s), in seconds."""
     return max(flops / peak_flops, nbytes / peak_bw)

@@ -59,6 +59,7 @@ class Workload:
     kv_scale: float = 1.0 / 64.0  # dequantized value = code value * kv_scale (N(0,1) draws -> codes within +-448)
     proj_fp8: bool = False       # W_UK / W_UV also given as FP8 E4M3 codes (transposed) with one per-tensor scale
     w_scale: float = 2.0 ** -9   # N(0, 1/512) weights / 2^-9 -> codes of standard deviation ~23, within +-448
+    chunk_tokens: int = 0        # chunked extend (expanded path): cached tokens expanded at a time; s_q new tokens
 
     @property
     def softmax_scale(self) -> float:
@@ -88,7 +89,11 @@ SPARSE_FP8 = Workload("sparse_fp8_b64_h128_l16384_top2048", B=64, s_q=1, H=128, 
 # the DeepSeek-V3 step with the W_UK / W_UV projections on FP8 weights (bmm_fp8), bf16 cache
 FP8_PROJ = Workload("fp8proj_deepseek_v3_b64_h128_l4096", B=64, s_q=1, H=128, seqlen=4096, with_projections=True,
                     proj_fp8=True)
-ALL = (TINY, V3, RAGGED, MTP, LONG, SPARSE, FP8, SPARSE_FP8, FP8_PROJ)
+# an extend on the expanded path: 512 new tokens after a 32K-token prefix, chunks of 4096
+# ("MLA 推理" exercise 3: a 32K prefix expands to ~2.6 GB per layer at once; chunked, 4096 tokens)
+EXTEND = Workload("extend_t512_l32768_h128_chunk4096", B=1, s_q=512, H=128, seqlen=32768, with_projections=True,
+                  chunk_tokens=4096)
+ALL = (TINY, V3, RAGGED, MTP, LONG, SPARSE, FP8, SPARSE_FP8, FP8_PROJ, EXTEND)
 BY_NAME = {w.name: w for w in ALL}
 
 
