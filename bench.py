@@ -623,41 +623,53 @@ def run_ours(args, w):
     # the step, D2H of its result, every step
     e2e = None
     if not args.no_e2e:
-        # The step's inputs are staged in one pinned host buffer and arrive with one
-        # host-to-device copy per step (their device tensors are views of one buffer, each
-        # 256-byte aligned); the result comes back with one copy for o and one for lse.
-        specs = [("q_nope", inp["q_nope"]), ("q_pe", inp["q_pe"]), ("pos", pos_host)] if w.with_projections \
+        # The step's inputs are staged in two pinned host buffers: the lengths and the block
+        # table (and the top-k lists) in a small one that arrives first on a side stream, where
+        # the split schedule runs on them at once, and the queries (with their RoPE positions)
+        # in a large one on the main stream, where the W_UK absorption waits for them.  The
+        # lse goes back on a side stream while the W_UV un-absorption runs, then o.  Device
+        # tensors are views of the two buffers, each 256-byte aligned.
+        big_specs = [("q_nope", inp["q_nope"]), ("q_pe", inp["q_pe"]), ("pos", pos_host)] if w.with_projections \
             else [("q", inp["q"])]
-        specs += [("sl", inp["seqlens"]), ("bt", inp["block_table"])]
+        small_specs = [("sl", inp["seqlens"]), ("bt", inp["block_table"])]
         if sparse:
-            specs += [("idx", inp["indices"]), ("kl", inp["topk_lens"])]
-        offs, total = {}, 0
-        for name, t in specs:
-            nb = t.numel() * t.element_size()
-            offs[name] = (total, nb)
-            total += (nb + 255) // 256 * 256
-        host_pack = torch.zeros(total, dtype=torch.uint8).pin_memory()
-        dev_pack = torch.empty(total, dtype=torch.uint8, device=dev)
+            small_specs += [("idx", inp["indices"]), ("kl", inp["topk_lens"])]
         dv = {}
-        for name, t in specs:
-            o, nb = offs[name]
-            host_pack[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
-            dv[name] = dev_pack[o:o + nb].view(t.dtype).view(t.shape)
+
+        def stage(specs):
+            offs, total = {}, 0
+            for name, t in specs:
+                nb = t.numel() * t.element_size()
+                offs[name] = (total, nb)
+                total += (nb + 255) // 256 * 256
+            host_pack = torch.zeros(total, dtype=torch.uint8).pin_memory()
+            dev_pack = torch.empty(total, dtype=torch.uint8, device=dev)
+            for name, t in specs:
+                o, nb = offs[name]
+                host_pack[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
+                dv[name] = dev_pack[o:o + nb].view(t.dtype).view(t.shape)
+            return host_pack, dev_pack, total
+
+        host_small, dev_small, n_small = stage(small_specs)
+        host_big, dev_big, n_big = stage(big_specs)
         res_dev = step.o if w.with_projections else step.out
         host_out = torch.empty(res_dev.shape, dtype=res_dev.dtype).pin_memory()
         host_lse = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
-        h2d = total
+        h2d = n_small + n_big
         d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * 4
         step.seqlens = dv["kl"] if sparse else dv["sl"]   # the schedule reads the staged lengths
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
         def e2e_step():
-            dev_pack.copy_(host_pack, non_blocking=True)
-
-            def absorb_in():
-                if w.with_projections:
-                    absorb_call(dv["q_nope"], dv["q_pe"], dv["pos"])
-
-            step.plan_beside(absorb_in)
+            cur = torch.cuda.current_stream(dev)
+            s_in.wait_stream(cur)
+            with torch.cuda.stream(s_in):   # lengths and table first; the schedule right behind them
+                dev_small.copy_(host_small, non_blocking=True)
+                step.plan()
+            dev_big.copy_(host_big, non_blocking=True)
+            if w.with_projections:
+                absorb_call(dv["q_nope"], dv["q_pe"], dv["pos"])
+            cur.wait_stream(s_in)
             q_in = step.q if w.with_projections else dv["q"]
             if sparse and fp8:
                 mla.decode_sparse_fp8(q_in, kv, kv_scale, dv["bt"], dv["sl"], dv["idx"], dv["kl"], w.softmax_scale,
@@ -672,10 +684,13 @@ def run_ours(args, w):
             else:
                 mla.decode(q_in, kv, dv["bt"], dv["sl"], w.softmax_scale, w.causal, step.metadata, parts,
                            workspace=step.workspace, out=step.out, lse=step.lse)
+            s_out.wait_stream(cur)
+            with torch.cuda.stream(s_out):   # lse back while the un-absorption runs
+                host_lse.copy_(step.lse, non_blocking=True)
             if w.with_projections:
                 unabsorb_call()
             host_out.copy_(res_dev, non_blocking=True)
-            host_lse.copy_(step.lse, non_blocking=True)
+            cur.wait_stream(s_out)
 
         for _ in range(3):
             flush.zero_()

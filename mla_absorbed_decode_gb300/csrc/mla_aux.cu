@@ -318,6 +318,11 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
     fence_mbar_init();
     prefetch_tensormap(&a_map);
     prefetch_tensormap(&w_map);
+    // this head's weight matrix (K x 512 or 512 x 128 bf16, 128 KiB) into L2 while the
+    // previous kernel of the stream may still run: only a prefetch, the TMA loads that use
+    // it come after griddepcontrol.wait (one CTA per head issues it)
+    if (p.w != nullptr && blockIdx.x == 0 && blockIdx.z == 0)
+      prefetch_l2(p.w + static_cast<int64_t>(h) * K * (K == 128 ? 512 : 128), static_cast<uint32_t>(K) * (K == 128 ? 512 : 128) * 2);
   }
   if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
   tc_fence_before();

@@ -1183,19 +1183,12 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
       const int x = 8 * j + (lane >> 2);
       return ld_shared_v4(stg + x * 64 + ((tq ^ (x & 3)) << 4));
     };
-#pragma unroll 1
-    for (int hc = 0; hc < 256 * kHalves; hc += 32) {
+    // column chunk hc (32 columns) of this warpgroup's part of O, then its stores
+    auto col_of = [&](int hc) { return tmem_row + (wg + hc / 256) * 256 + hc % 256; };
+    auto emit = [&](int hc, const uint32_t (&v)[32]) {
       const int half = wg + hc / 256, c = hc % 256;   // column c of O's half `half`
       __nv_bfloat16* const obase = obase0 + half * 256;
       float* const pbase = pbase0 + half * 256;
-      uint32_t v[32];
-      tmem_ld32(tmem_row + half * 256 + c, v);
-      tmem_wait_ld();
-      if (hc == 256 * kHalves - 32) {   // everything read: O may be overwritten by the next segment
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.bar.o_free));
-      }
       if (final_out) {   // 32 bf16 columns: 64 B per row
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -1234,6 +1227,25 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
           __syncwarp();
         }
       }
+    };
+    // the TMEM load of the next 32 columns is in flight while the current ones are stored
+    constexpr int kSteps = 256 * kHalves;
+    uint32_t va[32], vb[32];
+    tmem_ld32(col_of(0), va);
+#pragma unroll 1
+    for (int hc = 0; hc < kSteps; hc += 64) {
+      tmem_wait_ld();
+      tmem_ld32(col_of(hc + 32), vb);
+      emit(hc, va);
+      tmem_wait_ld();
+      if (hc + 64 < kSteps) {
+        tmem_ld32(col_of(hc + 64), va);
+      } else {   // everything read: O may be overwritten by the next segment
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.bar.o_free));
+      }
+      emit(hc + 32, vb);
     }
     ++seg;
     have_seg = w.next(s);

@@ -367,6 +367,7 @@ mla_status_t absorb_impl(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, co
   p.pe = reinterpret_cast<const __nv_bfloat16*>(q_pe);
   p.pe_row_stride = q_pe_row_stride;
   p.positions = positions;
+  p.w = reinterpret_cast<const __nv_bfloat16*>(w_uk);
   if (positions) {   // inverse frequencies theta^(-2j/64) and 2*pi, each as a float pair (hi + lo)
     for (int j = 0; j < 32; ++j) {
       const double inv = std::pow(rope_theta, -2.0 * j / 64.0);
@@ -421,6 +422,8 @@ mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla
   p.status = d->status;
   p.pe = nullptr;
   p.pe_row_stride = 0;
+  p.positions = nullptr;
+  p.w = reinterpret_cast<const __nv_bfloat16*>(w_uv);
   return launch_bmm(false, a_map, w_map, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
                                                                                                 : MLA_ERR_CUDA;
 }

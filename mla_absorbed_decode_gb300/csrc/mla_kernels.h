@@ -130,6 +130,9 @@ struct BmmParams {
   const int32_t* positions;
   float rope_hi[32], rope_lo[32];
   float two_pi_hi, two_pi_lo;
+  // the weights [H][K * N] (bf16 kernels): each head's matrix is prefetched into L2 before
+  // the kernel waits for the previous one (a prefetch only; the TMA loads come after)
+  const __nv_bfloat16* w = nullptr;
 };
 cudaError_t bmm_set_attributes();
 // absorb: K = 128 -> 512 columns; unabsorb: K = 512 -> 128 columns
