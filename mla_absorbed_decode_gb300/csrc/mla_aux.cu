@@ -402,7 +402,8 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
   // The stores go through a 2 KiB transpose buffer per warp in the (now idle) first stage: a
   // thread holds one token row, so direct stores would touch 32 rows per instruction; here
   // each store instruction writes 64 contiguous bytes of 8 rows.  Buffer row x (64 B) holds
-  // 16-byte unit u at ((u ^ (x & 3)) * 16).
+  // 16-byte unit u at ((u ^ ((x >> 1) & 3)) * 16): the 8 rows a quarter-warp stores (or
+  // the 2 rows it loads) then touch 8 distinct 16-byte bank groups.
   const uint32_t stg = smem + warp * 2048;
   const int tq = lane & 3, nw0 = m0 + warp * 32;   // transposed: quad tq of rows 8j + (lane >> 2)
   const bool ok_all = got && !fail_s;
@@ -415,13 +416,13 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
       u.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
       u.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
       u.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-      st_shared_v4(stg + lane * 64 + ((j ^ (lane & 3)) << 4), u);
+      st_shared_v4(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), u);
     }
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int x = 8 * j + (lane >> 2);
-      const uint4 u = ld_shared_v4(stg + x * 64 + ((tq ^ (x & 3)) << 4));
+      const uint4 u = ld_shared_v4(stg + x * 64 + ((tq ^ ((x >> 1) & 3)) << 4));
       if (ok_all && nw0 + x < p.N)
         *reinterpret_cast<uint4*>(dst0 + static_cast<int64_t>(nw0 + x) * p.out_row_stride + c + 8 * tq) = u;
     }

@@ -1172,16 +1172,17 @@ __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem,
     // Stores go through the warp's transpose buffer: a thread holds one row's columns, so
     // direct stores would touch 32 rows per instruction; transposed, each store
     // instruction writes 64 contiguous bytes of 8 rows.  Buffer row x (64 B) holds
-    // 16-byte unit u at ((u ^ (x & 3)) * 16).
+    // 16-byte unit u at ((u ^ ((x >> 1) & 3)) * 16): the 8 rows a quarter-warp stores (or
+    // the 2 rows it loads) then touch 8 distinct 16-byte bank groups.
     const int g0 = rb * 128 + wq * 32;    // the warp's first row within the request
     __nv_bfloat16* const obase0 = p.out + (static_cast<int64_t>(s.b) * p.rows + g0) * 512;
     float* const pbase0 = p.o_part + (static_cast<int64_t>(ns0 + s.split) * p.rows + g0) * 512;
     const uint32_t stg = smem + C::kOffEpi + ((wg << 2) | wq) * 2048;
     const int tq = lane & 3;                // transposed: 16-byte quad tq of rows 8j + (lane >> 2)
-    auto put = [&](int j, uint4 u) { st_shared_v4(stg + lane * 64 + ((j ^ (lane & 3)) << 4), u); };
+    auto put = [&](int j, uint4 u) { st_shared_v4(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), u); };
     auto get = [&](int j) {
       const int x = 8 * j + (lane >> 2);
-      return ld_shared_v4(stg + x * 64 + ((tq ^ (x & 3)) << 4));
+      return ld_shared_v4(stg + x * 64 + ((tq ^ ((x >> 1) & 3)) << 4));
     };
     // column chunk hc (32 columns) of this warpgroup's part of O, then its stores
     auto col_of = [&](int hc) { return tmem_row + (wg + hc / 256) * 256 + hc % 256; };

@@ -48,13 +48,13 @@ __device__ __forceinline__ void store_rows32(uint32_t stg, const uint32_t (&pk)[
                                              int64_t row_stride, int c, int lane, F rows_ok) {
 #pragma unroll
   for (int j = 0; j < 4; ++j)
-    st_shared_v4(stg + lane * 64 + ((j ^ (lane & 3)) << 4), make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
+    st_shared_v4(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]));
   __syncwarp();
   const int tq = lane & 3;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int x = 8 * j + (lane >> 2);
-    const uint4 u = ld_shared_v4(stg + x * 64 + ((tq ^ (x & 3)) << 4));
+    const uint4 u = ld_shared_v4(stg + x * 64 + ((tq ^ ((x >> 1) & 3)) << 4));
     if (rows_ok(x)) *reinterpret_cast<uint4*>(base + static_cast<int64_t>(x) * row_stride + c + 8 * tq) = u;
   }
   __syncwarp();

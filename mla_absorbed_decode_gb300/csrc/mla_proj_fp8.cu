@@ -246,13 +246,13 @@ mla_bmm_fp8_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_const
       u.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * out_scale, __uint_as_float(v[8 * j + 3]) * out_scale);
       u.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * out_scale, __uint_as_float(v[8 * j + 5]) * out_scale);
       u.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * out_scale, __uint_as_float(v[8 * j + 7]) * out_scale);
-      st_shared_v4(stg + lane * 64 + ((j ^ (lane & 3)) << 4), u);
+      st_shared_v4(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), u);
     }
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int x = 8 * j + (lane >> 2);
-      const uint4 u = ld_shared_v4(stg + x * 64 + ((tq ^ (x & 3)) << 4));
+      const uint4 u = ld_shared_v4(stg + x * 64 + ((tq ^ ((x >> 1) & 3)) << 4));
       if (ok_all && nw0 + x < b.N)
         *reinterpret_cast<uint4*>(dst0 + static_cast<int64_t>(nw0 + x) * b.out_row_stride + c + 8 * tq) = u;
     }
