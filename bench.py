@@ -521,17 +521,24 @@ def run_ours(args, w):
         else:
             mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
 
-    def absorb():
-        if w.with_projections:
-            absorb_call(q_nope, q_pe, positions)
+    # bf16 projections: the split schedule runs in the absorption's launch (one more CTA);
+    # otherwise on a side stream beside the absorption
+    fused_plan = w.with_projections and not proj_fp8 and B <= mla.absorb_plan_max_batch()
+
+    def absorb_and_plan(qn, qp, pos_d):
+        if fused_plan:
+            step.absorb_and_plan(qn, qp, w_uk, positions=pos_d)
+        else:
+            step.plan_beside(lambda: absorb_call(qn, qp, pos_d) if w.with_projections else None)
 
     def one_step():
-        step.plan_beside(absorb)   # the split schedule on a side stream, beside the absorption
+        absorb_and_plan(q_nope, q_pe, positions)
         decode_only()
         if w.with_projections:
             unabsorb_call()
 
-    launches_per_step = 1 + 2 + (2 if w.with_projections else 0)   # schedule, decode+combine, bmms
+    # schedule (alone or in the absorption's launch), decode + combine, the bmms
+    launches_per_step = (0 if fused_plan else 1) + 2 + (2 if w.with_projections else 0)
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
         one_step()
@@ -591,6 +598,16 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         for j, k in enumerate(comp):
             comp[k].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+    if fused_plan:   # the launch the step uses: absorption and schedule together
+        comp["absorb_and_schedule"] = []
+        for i in range(args.steps):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev[0].record()
+            absorb_and_plan(q_nope, q_pe, positions)
+            ev[1].record()
+            torch.cuda.synchronize()
+            comp["absorb_and_schedule"].append(ev[0].elapsed_time(ev[1]) * 1e3)
     components = {k: round(statistics.mean(v), 2) for k, v in comp.items()
                   if w.with_projections or k not in ("absorb", "unabsorb")}
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -624,11 +641,12 @@ def run_ours(args, w):
     e2e = None
     if not args.no_e2e:
         # The step's inputs are staged in two pinned host buffers: the lengths and the block
-        # table (and the top-k lists) in a small one that arrives first on a side stream, where
-        # the split schedule runs on them at once, and the queries (with their RoPE positions)
-        # in a large one on the main stream, where the W_UK absorption waits for them.  The
-        # lse goes back on a side stream while the W_UV un-absorption runs, then o.  Device
-        # tensors are views of the two buffers, each 256-byte aligned.
+        # table (and the top-k lists) in a small one on a side stream (where a separate split
+        # schedule runs on them at once), and the queries (with their RoPE positions) in a
+        # large one on the main stream, where the W_UK absorption (with the schedule in its
+        # launch, for bf16 projections) waits for them.  The lse goes back on a side stream
+        # while the W_UV un-absorption runs, then o.  Device tensors are views of the two
+        # buffers, each 256-byte aligned.
         big_specs = [("q_nope", inp["q_nope"]), ("q_pe", inp["q_pe"]), ("pos", pos_host)] if w.with_projections \
             else [("q", inp["q"])]
         small_specs = [("sl", inp["seqlens"]), ("bt", inp["block_table"])]
@@ -665,9 +683,13 @@ def run_ours(args, w):
             s_in.wait_stream(cur)
             with torch.cuda.stream(s_in):   # lengths and table first; the schedule right behind them
                 dev_small.copy_(host_small, non_blocking=True)
-                step.plan()
+                if not fused_plan:
+                    step.plan()
             dev_big.copy_(host_big, non_blocking=True)
-            if w.with_projections:
+            if fused_plan:   # the schedule in the absorption's launch, once both packs are in
+                cur.wait_stream(s_in)
+                step.absorb_and_plan(dv["q_nope"], dv["q_pe"], w_uk, positions=dv["pos"])
+            elif w.with_projections:
                 absorb_call(dv["q_nope"], dv["q_pe"], dv["pos"])
             cur.wait_stream(s_in)
             q_in = step.q if w.with_projections else dv["q"]
@@ -755,7 +777,8 @@ def run_ours(args, w):
                        "l2": "flushed between timed steps (256 MiB write, then 256 MiB read; outside the step events)",
                        "decode_timing": "K further decode calls inside the timed region, L2 flushed before each",
                        "launch": ("eager" if args.eager else "CUDA graph of the step's library calls")
-                                 + "; split schedule on a side stream beside the W_UK absorption"},
+                                 + ("; split schedule computed in the W_UK absorption's launch (one more CTA)"
+                                    if fused_plan else "; split schedule on a side stream beside the W_UK absorption")},
             "hbm_gbs": gbs,
             "pct_of_roofline": 100.0 * rl_time / t_step,
             "roofline_spec": {"peak_tflops": SPEC_FLOPS / 1e12, "peak_gbs": SPEC_BW / 1e9},

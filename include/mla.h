@@ -199,6 +199,26 @@ mla_status_t mla_absorb_q_rope(const mla_bf16_t* q_nope, int64_t q_nope_row_stri
                                int64_t q_pe_row_stride, const int32_t* positions, float rope_theta,
                                const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H, mla_stream_t stream);
 
+/* The W_UK absorption (mla_absorb_q_rope, or mla_absorb_q when positions is NULL)
+ * and the split-KV schedule (mla_decode_metadata) in one launch: one CTA beyond the
+ * absorption's tiles computes the schedule while the others multiply, so that the
+ * decode issued next on the stream depends on a single kernel (its programmatic
+ * launch then overlaps the absorption's tail instead of waiting on two).  Results
+ * are those of the two separate calls, bit for bit.
+ *  seqlens, B, num_sm_parts, metadata  as for mla_decode_metadata, with s_q = N / B
+ *                                      (N a multiple of B) and the same H;
+ *                                      B <= mla_absorb_plan_max_batch(), else
+ *                                      MLA_ERR_UNSUPPORTED (the schedule's prefix sums
+ *                                      live in that CTA's shared memory)
+ *  the rest                            as for mla_absorb_q_rope (positions, rope_theta)
+ *                                      or mla_absorb_q (positions NULL).
+ * Async on stream. */
+int mla_absorb_plan_max_batch(void);
+mla_status_t mla_absorb_q_plan(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                               int64_t q_pe_row_stride, const int32_t* positions, float rope_theta,
+                               const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H, const int32_t* seqlens, int B,
+                               int num_sm_parts, void* metadata, mla_stream_t stream);
+
 /* W_UV un-absorption ("DeepSeekV2之MLA" 4.5: bmm(attn_output, w_vc)):
  *   o[n, h, 0:128] = o_lat[n, h, 0:512] @ w_uv[h]      (fp32 accumulate, bf16 out)
  *  o_lat [N, H, 512] bf16 (the decode out), w_uv [H, 512, 128] bf16, o [N, H, 128] bf16.

@@ -16,6 +16,7 @@ import torch
 __all__ = [
     "MLAError", "lib", "library_path", "num_sm_parts", "metadata_size", "decode_metadata",
     "decode_workspace_size", "decode", "decode_sparse", "decode_fp8", "decode_sparse_fp8", "absorb_q", "unabsorb_o",
+    "absorb_plan_max_batch", "absorb_q_plan",
     "bmm_fp8_workspace_size", "absorb_q_fp8", "unabsorb_o_fp8", "extend_workspace_size", "extend_chunked",
     "get_device_status",
     "schedule_params", "debug_withhold_first_load", "DecodeStep", "EXPORTED_SYMBOLS",
@@ -46,6 +47,9 @@ _SIGNATURES = {
                                        _c_float, _c_int, _p, _c_int, _p, _c_size, _p, _p, _p]),
     "mla_absorb_q": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _p, _c_int, _c_int, _p]),
     "mla_absorb_q_rope": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _p, _c_int, _c_int, _p]),
+    "mla_absorb_plan_max_batch": (_c_int, []),
+    "mla_absorb_q_plan": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _p, _c_int, _c_int, _p, _c_int, _c_int, _p,
+                                   _p]),
     "mla_unabsorb_o": (_c_int, [_p, _p, _p, _c_int, _c_int, _p]),
     "mla_bmm_fp8_workspace_size": (_c_size, []),
     "mla_absorb_q_fp8": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _c_float, _p, _c_int, _c_int, _p, _c_size, _p]),
@@ -232,6 +236,24 @@ def absorb_q(q_nope: torch.Tensor, w_uk: torch.Tensor, q: torch.Tensor, q_pe: to
     return q
 
 
+def absorb_plan_max_batch() -> int:
+    return lib().mla_absorb_plan_max_batch()
+
+
+def absorb_q_plan(q_nope: torch.Tensor, w_uk: torch.Tensor, q: torch.Tensor, seqlens: torch.Tensor, num_parts: int,
+                  metadata: torch.Tensor, q_pe: torch.Tensor | None = None, positions: torch.Tensor | None = None,
+                  rope_theta: float = 10000.0, stream=None) -> torch.Tensor:
+    """absorb_q and decode_metadata(seqlens, ..., num_parts, out=metadata) in one launch
+    (B = len(seqlens), s_q = N / B); returns q."""
+    N, H, _ = q_nope.shape
+    pe_ptr, pe_stride = (0, 0) if q_pe is None else (_ptr(q_pe), q_pe.stride(0))
+    _check(lib().mla_absorb_q_plan(_ptr(q_nope), q_nope.stride(0), pe_ptr or None, pe_stride,
+                                   _ptr(positions) if positions is not None else None, float(rope_theta), _ptr(w_uk),
+                                   _ptr(q), N, H, _ptr(seqlens), seqlens.numel(), int(num_parts), _ptr(metadata),
+                                   _stream(stream)), "mla_absorb_q_plan")
+    return q
+
+
 def unabsorb_o(o_lat: torch.Tensor, w_uv: torch.Tensor, o: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """o[n, h, :] = o_lat[n, h, :] @ w_uv[h]; o_lat is [N, H, 512] -> o [N, H, 128]."""
     N, H = o_lat.shape[0], o_lat.shape[1]
@@ -360,6 +382,16 @@ class DecodeStep:
         work()
         cur.wait_stream(self._plan_stream)
 
+    def absorb_and_plan(self, q_nope, q_pe, w_uk, positions=None, rope_theta: float = 10000.0, stream=None):
+        """The W_UK absorption and plan() in one launch (B <= absorb_plan_max_batch(); else the
+        two calls, the schedule on a side stream beside the absorption)."""
+        if self.B <= absorb_plan_max_batch():
+            absorb_q_plan(q_nope, w_uk, self.q, self.seqlens, self.parts, self.metadata, q_pe=q_pe,
+                          positions=positions, rope_theta=rope_theta, stream=stream)
+        else:
+            self.plan_beside(lambda: absorb_q(q_nope, w_uk, self.q, q_pe=q_pe, stream=stream, positions=positions,
+                                              rope_theta=rope_theta))
+
     def _decode(self, kv_cache, block_table, stream=None):
         if self.kv_scale is None:
             decode(self.q, kv_cache, block_table, self.seqlens, self.scale, self.causal, self.metadata, self.parts,
@@ -390,8 +422,8 @@ class DecodeStep:
         def body():
             if before is not None:
                 before()
-            if plan:   # the schedule beside the absorption, which does not need it
-                self.plan_beside(absorb)
+            if plan:   # the schedule in the absorption's launch
+                self.absorb_and_plan(q_nope, q_pe, w_uk, positions=positions, rope_theta=rope_theta)
             else:
                 absorb()
             self._decode(kv_cache, block_table)

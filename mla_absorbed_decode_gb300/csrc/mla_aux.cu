@@ -23,11 +23,13 @@ namespace mla {
 // taking the pages whose positions lie in [p T, (p + 1) T).  The costs are
 // prefix-summed by all threads; each part then finds its first and last page with
 // two binary searches, independently of the other parts.
-// Exclusive prefix sum of one value per thread over the block (kScheduleThreads
-// threads): warp shuffles, then one warp over the warp totals.  `scratch` holds
-// kScheduleThreads / 32 + 1 entries; the block total is returned in *total.
+// Exclusive prefix sum of one value per thread over the block (kT threads): warp
+// shuffles, then one warp over the warp totals.  `scratch` holds kT / 32 + 1 entries;
+// the block total is returned in *total.
+template <int kT>
 __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* scratch, int64_t* total) {
-  constexpr int kWarps = kScheduleThreads / 32;
+  static_assert(kT % 32 == 0 && kT / 32 <= 32, "scan shape");
+  constexpr int kWarps = kT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int64_t x = v;   // inclusive scan within the warp
 #pragma unroll
@@ -54,18 +56,15 @@ __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* scra
   return before + x - v;
 }
 
-__global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const int32_t* seqlens, int B, int num_parts,
-                                                                        int fixed_cost, int hbm_parts, int split_cost,
-                                                                        int32_t* meta, int32_t* num_splits) {
-  extern __shared__ int64_t sched_c[];                                      // C[0..B]
-  int32_t* sched_nb = reinterpret_cast<int32_t*>(sched_c + B + 1);         // nb[0..B)
-  static_assert(kScheduleThreads % 32 == 0 && kScheduleThreads / 32 <= 32, "scan shape");
-  __shared__ int64_t s_scan[kScheduleThreads / 32 + 1];
+// The whole block (kT threads) computes the schedule; sched_c holds B + 1 int64 and
+// sched_nb B int32 of shared memory, s_scan kT / 32 + 1 int64.
+template <int kT>
+__device__ void schedule_body(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
+                              int split_cost, int32_t* meta, int32_t* num_splits, int64_t* sched_c, int32_t* sched_nb,
+                              int64_t* s_scan) {
   const int tid = threadIdx.x;
-  griddep_wait();
-  griddep_launch_dependents();
   const int64_t F = fixed_cost;
-  const int chunk = (B + kScheduleThreads - 1) / kScheduleThreads;
+  const int chunk = (B + kT - 1) / kT;
   const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
   // 1. page counts, per-thread sums of the costs, block-wide exclusive scan, C
   int64_t sum = 0;
@@ -76,7 +75,7 @@ __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const in
     sum += nb > 0 ? nb + F : 0;
   }
   int64_t block_total;
-  int64_t run = block_exclusive_scan(sum, s_scan, &block_total);
+  int64_t run = block_exclusive_scan<kT>(sum, s_scan, &block_total);
   if (tid == 0) sched_c[0] = 0;
   for (int i = lo; i < hi; ++i) {
     run += sched_nb[i] > 0 ? sched_nb[i] + F : 0;
@@ -100,7 +99,7 @@ __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const in
       int64_t extra = 0;
       for (int i = lo; i < hi; ++i) extra += sched_nb[i] > 0 ? segments(i, Tc) - 1 : 0;
       int64_t all_extra;
-      block_exclusive_scan(extra, s_scan, &all_extra);
+      block_exclusive_scan<kT>(extra, s_scan, &all_extra);
       const int64_t est = Tc + static_cast<int64_t>(split_cost) * ((all_extra + pe - 1) / pe);
       if (best_est < 0 || est < best_est) best_est = est, best_p = pe;
     }
@@ -117,7 +116,7 @@ __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const in
     return l;
   };
   // 2. one metadata record per part
-  for (int p = tid; p < num_parts; p += kScheduleThreads) {
+  for (int p = tid; p < num_parts; p += kT) {
     int32_t m[kMetaInts] = {-1, 0, 0, 0, 0, 0, 0, 0};
     const int64_t plo = static_cast<int64_t>(p) * T, phi = plo + T;
     if (total > 0 && p < p_eff && plo < total) {
@@ -151,12 +150,24 @@ __global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const in
   if (total > 0)
     for (int i = lo; i < hi; ++i) segs += segments(i, T);
   int64_t all_segs;
-  int32_t r = static_cast<int32_t>(block_exclusive_scan(segs, s_scan, &all_segs));
+  int32_t r = static_cast<int32_t>(block_exclusive_scan<kT>(segs, s_scan, &all_segs));
   if (tid == 0) num_splits[0] = 0;
   for (int i = lo; i < hi; ++i) {
     if (total > 0) r += static_cast<int32_t>(segments(i, T));
     num_splits[i + 1] = r;
   }
+}
+
+__global__ void __launch_bounds__(kScheduleThreads) mla_schedule_kernel(const int32_t* seqlens, int B, int num_parts,
+                                                                        int fixed_cost, int hbm_parts, int split_cost,
+                                                                        int32_t* meta, int32_t* num_splits) {
+  extern __shared__ int64_t sched_c[];                                      // C[0..B]
+  int32_t* sched_nb = reinterpret_cast<int32_t*>(sched_c + B + 1);         // nb[0..B)
+  __shared__ int64_t s_scan[kScheduleThreads / 32 + 1];
+  griddep_wait();
+  griddep_launch_dependents();
+  schedule_body<kScheduleThreads>(seqlens, B, num_parts, fixed_cost, hbm_parts, split_cost, meta, num_splits, sched_c,
+                                  sched_nb, s_scan);
 }
 
 cudaError_t launch_schedule(const int32_t* seqlens, int B, int num_parts, int fixed_cost, int hbm_parts,
@@ -300,12 +311,26 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
   constexpr int KC = K / 64;
   constexpr uint32_t kSB = bmm_stage_bytes<K, NT, STAGES>();
   constexpr uint32_t kTmemCols = NT;
+  constexpr int kNX = (K == 128 ? 512 : 128) / NT;   // column tiles per head
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   __shared__ uint64_t full[STAGES], empty[STAGES], acc_full;
   __shared__ uint32_t tmem_base_s;
   __shared__ int fail_s;
   const uint32_t smem = (smem_u32(dyn_smem) + 1023u) & ~1023u;
-  const int n0 = blockIdx.x * NT, h = blockIdx.y, m0 = blockIdx.z * 128;
+  // the grid is flat: column tile fastest, then head, then 128-token tile; with a
+  // schedule to compute, one CTA past the tiles does that and nothing else
+  const int tile = static_cast<int>(blockIdx.x);
+  if (p.sched_meta != nullptr && tile == kNX * p.H * ((p.N + 127) / 128)) {
+    __shared__ int64_t sched_scan[128 / 32 + 1];
+    int64_t* sched_c = reinterpret_cast<int64_t*>(dyn_smem + (smem - smem_u32(dyn_smem)));
+    griddep_wait();   // the lengths may come from the previous kernel
+    griddep_launch_dependents();
+    schedule_body<128>(p.sched_seqlens, p.sched_B, p.sched_parts, p.sched_fixed, p.sched_hbm, p.sched_split,
+                       p.sched_meta, p.sched_meta + kMetaInts * p.sched_parts, sched_c,
+                       reinterpret_cast<int32_t*>(sched_c + p.sched_B + 1), sched_scan);
+    return;
+  }
+  const int n0 = (tile % kNX) * NT, h = (tile / kNX) % p.H, m0 = (tile / (kNX * p.H)) * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -321,7 +346,7 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
     // this head's weight matrix (K x 512 or 512 x 128 bf16, 128 KiB) into L2 while the
     // previous kernel of the stream may still run: only a prefetch, the TMA loads that use
     // it come after griddepcontrol.wait (one CTA per head issues it)
-    if (p.w != nullptr && blockIdx.x == 0 && blockIdx.z == 0)
+    if (p.w != nullptr && n0 == 0 && m0 == 0)
       prefetch_l2(p.w + static_cast<int64_t>(h) * K * (K == 128 ? 512 : 128), static_cast<uint32_t>(K) * (K == 128 ? 512 : 128) * 2);
   }
   if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
@@ -353,7 +378,7 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
   const int n = m0 + threadIdx.x;
   // the RoPE part of the decode query is copied by the first column tile; it is
   // loaded (and rotated) while the tiles are in flight
-  const bool copy_pe = blockIdx.x == 0 && p.pe != nullptr && n < p.N;
+  const bool copy_pe = n0 == 0 && p.pe != nullptr && n < p.N;
   uint4 pe[8];
   if (copy_pe) {
     const uint4* src = reinterpret_cast<const uint4*>(p.pe + static_cast<int64_t>(n) * p.pe_row_stride + h * 64);
@@ -470,15 +495,24 @@ cudaError_t bmm_set_attributes() {
 
 cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap& w_map, const BmmParams& p,
                        cudaStream_t stream) {
-  const unsigned mt = static_cast<unsigned>((p.N + 127) / 128);
+  const int64_t mt = (p.N + 127) / 128;
   cudaLaunchAttribute attr[1];
   if (absorb) {
-    const cudaLaunchConfig_t cfg =
-        pdl_config(dim3(512 / 256, p.H, mt), dim3(128), bmm_smem_bytes<MLA_BMM_ABSORB>(), stream, attr);
+    if (p.sched_meta != nullptr &&
+        (p.sched_B < 1 || p.sched_B > kAbsorbPlanMaxB || p.sched_parts < 1 ||
+         sizeof(int64_t) * (p.sched_B + 1) + sizeof(int32_t) * p.sched_B + 1024 > bmm_smem_bytes<MLA_BMM_ABSORB>()))
+      return cudaErrorInvalidValue;
+    const int64_t ctas = (512 / 256) * static_cast<int64_t>(p.H) * mt + (p.sched_meta != nullptr ? 1 : 0);
+    if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
+    const cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(ctas)), dim3(128),
+                                              bmm_smem_bytes<MLA_BMM_ABSORB>(), stream, attr);
     return cudaLaunchKernelEx(&cfg, mla_bmm_kernel<MLA_BMM_ABSORB>, a_map, w_map, p);
   }
-  const cudaLaunchConfig_t cfg =
-      pdl_config(dim3(128 / 128, p.H, mt), dim3(128), bmm_smem_bytes<MLA_BMM_UNABSORB>(), stream, attr);
+  if (p.sched_meta != nullptr) return cudaErrorInvalidValue;
+  const int64_t ctas = (128 / 128) * static_cast<int64_t>(p.H) * mt;
+  if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(ctas)), dim3(128),
+                                            bmm_smem_bytes<MLA_BMM_UNABSORB>(), stream, attr);
   return cudaLaunchKernelEx(&cfg, mla_bmm_kernel<MLA_BMM_UNABSORB>, a_map, w_map, p);
 }
 

@@ -341,9 +341,12 @@ mla_status_t mla_decode_fp8(const mla_bf16_t* q, const uint8_t* kv_cache, float 
 namespace {
 
 // Shared body of mla_absorb_q and mla_absorb_q_rope (positions == nullptr: plain copy of q_pe).
+// With sched_meta set, one more CTA of the launch writes the split schedule of
+// (sched_seqlens, sched_B, sched_parts) -- mla_decode_metadata's output -- to sched_meta.
 mla_status_t absorb_impl(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
                          int64_t q_pe_row_stride, const int32_t* positions, double rope_theta, const mla_bf16_t* w_uk,
-                         mla_bf16_t* q, int N, int H, mla_stream_t stream) {
+                         mla_bf16_t* q, int N, int H, mla_stream_t stream, const int32_t* sched_seqlens = nullptr,
+                         int sched_B = 0, int sched_parts = 0, int32_t* sched_meta = nullptr) {
   if (!q_nope || !w_uk || !q || N < 1 || H < 1) return MLA_ERR_INVALID_ARG;
   if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q)) return MLA_ERR_INVALID_ARG;
   if (q_nope_row_stride < static_cast<int64_t>(H) * 128 || (q_nope_row_stride % 8) != 0) return MLA_ERR_INVALID_ARG;
@@ -368,6 +371,15 @@ mla_status_t absorb_impl(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, co
   p.pe_row_stride = q_pe_row_stride;
   p.positions = positions;
   p.w = reinterpret_cast<const __nv_bfloat16*>(w_uk);
+  if (sched_meta) {
+    p.sched_seqlens = sched_seqlens;
+    p.sched_meta = sched_meta;
+    p.sched_B = sched_B;
+    p.sched_parts = sched_parts;
+    p.sched_fixed = kSegmentCostPages;
+    p.sched_hbm = kHbmParts;
+    p.sched_split = kSplitCostPages;
+  }
   if (positions) {   // inverse frequencies theta^(-2j/64) and 2*pi, each as a float pair (hi + lo)
     for (int j = 0; j < 32; ++j) {
       const double inv = std::pow(rope_theta, -2.0 * j / 64.0);
@@ -399,6 +411,24 @@ mla_status_t mla_absorb_q_rope(const mla_bf16_t* q_nope, int64_t q_nope_row_stri
   if (!std::isfinite(rope_theta) || !(rope_theta > 1.f)) return MLA_ERR_INVALID_ARG;
   return absorb_impl(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, positions, static_cast<double>(rope_theta),
                      w_uk, q, N, H, stream);
+}
+
+int mla_absorb_plan_max_batch(void) { return kAbsorbPlanMaxB; }
+
+mla_status_t mla_absorb_q_plan(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                               int64_t q_pe_row_stride, const int32_t* positions, float rope_theta,
+                               const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H, const int32_t* seqlens, int B,
+                               int num_sm_parts, void* metadata, mla_stream_t stream) {
+  if (!seqlens || !metadata || B < 1 || num_sm_parts < 1 || N < 1 || H < 1 || N % B != 0) return MLA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(metadata) & 3u) != 0 || (reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0)
+    return MLA_ERR_INVALID_ARG;
+  if (B > kAbsorbPlanMaxB || pairs_for(N / B, H) > kMaxPairsPerCluster) return MLA_ERR_UNSUPPORTED;
+  if (positions) {
+    if (!q_pe || (reinterpret_cast<uintptr_t>(positions) & 3u)) return MLA_ERR_INVALID_ARG;
+    if (!std::isfinite(rope_theta) || !(rope_theta > 1.f)) return MLA_ERR_INVALID_ARG;
+  }
+  return absorb_impl(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, positions, static_cast<double>(rope_theta),
+                     w_uk, q, N, H, stream, seqlens, B, num_sm_parts, static_cast<int32_t*>(metadata));
 }
 
 mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla_bf16_t* o, int N, int H,

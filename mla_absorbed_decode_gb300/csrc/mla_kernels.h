@@ -133,7 +133,14 @@ struct BmmParams {
   // the weights [H][K * N] (bf16 kernels): each head's matrix is prefetched into L2 before
   // the kernel waits for the previous one (a prefetch only; the TMA loads come after)
   const __nv_bfloat16* w = nullptr;
+  // optional (bf16 absorption): one more CTA of the grid computes the split schedule
+  // (the rule and the bytes of mla_decode_metadata) for sched_B requests and sched_parts
+  // parts into sched_meta; its prefix sums use the CTA's shared memory (kAbsorbPlanMaxB)
+  const int32_t* sched_seqlens = nullptr;
+  int32_t* sched_meta = nullptr;
+  int sched_B = 0, sched_parts = 0, sched_fixed = 0, sched_hbm = 0, sched_split = 0;
 };
+constexpr int kAbsorbPlanMaxB = 8000;   // (B + 1) * 8 + B * 4 bytes within the absorption's 97 KB
 cudaError_t bmm_set_attributes();
 // absorb: K = 128 -> 512 columns; unabsorb: K = 512 -> 128 columns
 cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap& w_map, const BmmParams& p,

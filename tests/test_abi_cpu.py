@@ -135,3 +135,28 @@ def test_fp8_projection_argument_checks(mla):
     assert L.mla_unabsorb_o_fp8(*bad) == 1
     bad = list(un); bad[7] = 0
     assert L.mla_unabsorb_o_fp8(*bad) == 3
+
+
+def test_absorb_plan_argument_checks(mla):
+    L = mla.lib()
+    A = 0x10000  # 16-byte aligned, never dereferenced: every case returns before any launch
+    assert L.mla_absorb_plan_max_batch() >= 1024
+    # (q_nope, stride, q_pe, pe_stride, positions, theta, w_uk, q, N, H, seqlens, B, parts, metadata, stream)
+    ok = [A, 128, A, 64, A, 10000.0, A, A, 8, 1, A, 4, 76, A, None]
+    for i in (0, 6, 7, 10, 13):                                     # q_nope, w_uk, q, seqlens, metadata
+        bad = list(ok); bad[i] = None
+        assert L.mla_absorb_q_plan(*bad) == 1                       # MLA_ERR_INVALID_ARG
+    for i, v in ((11, 0), (11, 3), (12, 0), (8, 0), (9, 0)):        # B < 1, N not a multiple of B, parts, N, H
+        bad = list(ok); bad[i] = v
+        assert L.mla_absorb_q_plan(*bad) == 1
+    bad = list(ok); bad[13] = A + 2                                 # metadata must be 4-byte aligned
+    assert L.mla_absorb_q_plan(*bad) == 1
+    bad = list(ok); bad[2] = None                                   # positions without q_pe
+    assert L.mla_absorb_q_plan(*bad) == 1
+    bad = list(ok); bad[5] = 1.0                                    # rope_theta must exceed 1
+    assert L.mla_absorb_q_plan(*bad) == 1
+    big = L.mla_absorb_plan_max_batch() + 1
+    bad = list(ok); bad[11] = big; bad[8] = big                     # more requests than the CTA's shared memory holds
+    assert L.mla_absorb_q_plan(*bad) == 2                           # MLA_ERR_UNSUPPORTED
+    bad = list(ok); bad[9] = 1024; bad[8] = 4                       # s_q * H beyond a cluster's pairs
+    assert L.mla_absorb_q_plan(*bad) == 2

@@ -71,6 +71,34 @@ def test_absorb_q_with_rope(N, H):
     assert torch.equal(q[0, :, 512:].cpu(), q_pe[0])   # position 0 is the identity, bit for bit
 
 
+@pytest.mark.parametrize("B,s_q,H,parts", [(1, 1, 16, 1), (64, 1, 128, 76), (37, 2, 128, 76), (700, 1, 16, 148),
+                                           (8000, 1, 1, 148)])
+@pytest.mark.parametrize("rope", [False, True])
+def test_absorb_q_plan_matches_the_separate_calls(B, s_q, H, parts, rope):
+    """The absorption with the schedule in its launch gives the two separate calls' q and
+    metadata bit for bit (requests of length 0 included; every metadata int is written)."""
+    import mla_absorbed_decode_gb300 as mla
+    g = torch.Generator().manual_seed(B * 13 + s_q * 7 + H + rope)
+    N = B * s_q
+    q_nope = _bf(torch.randn((N, H, 128), generator=g)).cuda()
+    q_pe = _bf(torch.randn((N, H, 64), generator=g)).cuda()
+    w_uk = _bf(torch.randn((H, 128, 512), generator=g) / math.sqrt(512)).cuda()
+    seqlens = torch.randint(0, 9000, (B,), generator=g, dtype=torch.int32)
+    if B > 1:
+        seqlens[0] = 0
+    seqlens = seqlens.cuda()
+    pos = torch.randint(0, 1 << 20, (N,), generator=g, dtype=torch.int32).cuda() if rope else None
+    q1 = torch.full((N, H, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mla.absorb_q(q_nope, w_uk, q1, q_pe=q_pe, positions=pos)
+    meta1 = mla.decode_metadata(seqlens, s_q, H, False, parts)
+    q2 = torch.full((N, H, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    meta2 = torch.full_like(meta1, -7)
+    mla.absorb_q_plan(q_nope, w_uk, q2, seqlens, parts, meta2, q_pe=q_pe, positions=pos)
+    assert mla.get_device_status() == 0
+    assert torch.equal(q1.view(torch.int16), q2.view(torch.int16))
+    assert torch.equal(meta1, meta2)
+
+
 def test_absorb_q_rope_rejects_bad_arguments():
     import mla_absorbed_decode_gb300 as mla
     N, H = 4, 2
