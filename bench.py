@@ -18,6 +18,10 @@ in the roofline), and the V3.2-shaped top-2048 sparse decode over a bf16 or an
 FP8 cache (sparse_b64_h128_l16384_top2048, sparse_fp8_b64_h128_l16384_top2048), the V3
 step with FP8 projections (fp8proj_deepseek_v3_b64_h128_l4096: bmm_fp8), and the chunked
 extend on the expanded path (extend_t512_l32768_h128_chunk4096: mla_extend_chunked).
+Each timed step replays --inner passes (default 256) back to back from one CUDA graph,
+cycling over enough copies of the inputs, weights and buffers that more than 512 MiB
+is touched between two uses of a copy (L2 holds 126 MB), so that the timed region
+lasts long enough for the clock samples; ms_per_step is per pass.
 --impl reference times the CPU oracle (numpy float64) on a bounded sample of
 the same workload per step.  With N > 1 (torchrun) every rank runs its own
 replica of the workload (requests shard across GPUs with no exchange).
@@ -493,62 +497,96 @@ def run_ours(args, w):
 
     flush = _Flush()
 
-    q_dec = step.q if w.with_projections else q_direct
+    # Everything one pass reads or writes (the inputs, the weights and the step's buffers);
+    # the timed steps cycle through several copies of it (see --inner)
+    class InputSet:
+        pass
 
-    def decode_only():
+    S0 = InputSet()
+    S0.step, S0.kv, S0.bt, S0.sl, S0.idx, S0.kl = step, kv, bt, sl, idx, kl
+    S0.q_nope, S0.q_pe, S0.positions, S0.q_direct = q_nope, q_pe, positions, q_direct
+    S0.w_uk, S0.w_uv, S0.w_uk_t, S0.w_uv_t, S0.fp8_ws = w_uk, w_uv, w_uk_t, w_uv_t, fp8_ws
+
+    def copy_of(S):
+        C = InputSet()
+        for name, val in vars(S).items():
+            setattr(C, name, val.clone() if isinstance(val, torch.Tensor) else val)
+        C.step = mla.DecodeStep(B, s_q, H, C.kl if sparse else C.sl, w.causal, w.softmax_scale, parts=parts,
+                                device=dev, kv_scale=kv_scale)
+        return C
+
+    def decode_only(S=S0):
+        st = S.step
+        q_dec = st.q if w.with_projections else S.q_direct
         if sparse and fp8:
-            mla.decode_sparse_fp8(q_dec, kv, kv_scale, bt, sl, idx, kl, w.softmax_scale, w.causal, step.metadata,
-                                  parts, workspace=step.workspace, out=step.out, lse=step.lse)
+            mla.decode_sparse_fp8(q_dec, S.kv, kv_scale, S.bt, S.sl, S.idx, S.kl, w.softmax_scale, w.causal,
+                                  st.metadata, parts, workspace=st.workspace, out=st.out, lse=st.lse)
         elif sparse:
-            mla.decode_sparse(q_dec, kv, bt, sl, idx, kl, w.softmax_scale, w.causal, step.metadata, parts,
-                              workspace=step.workspace, out=step.out, lse=step.lse)
+            mla.decode_sparse(q_dec, S.kv, S.bt, S.sl, S.idx, S.kl, w.softmax_scale, w.causal, st.metadata, parts,
+                              workspace=st.workspace, out=st.out, lse=st.lse)
         elif fp8:
-            mla.decode_fp8(q_dec, kv, kv_scale, bt, sl, w.softmax_scale, w.causal, step.metadata, parts,
-                           workspace=step.workspace, out=step.out, lse=step.lse)
+            mla.decode_fp8(q_dec, S.kv, kv_scale, S.bt, S.sl, w.softmax_scale, w.causal, st.metadata, parts,
+                           workspace=st.workspace, out=st.out, lse=st.lse)
         else:
-            mla.decode(q_dec, kv, bt, sl, w.softmax_scale, w.causal, step.metadata, parts, workspace=step.workspace,
-                       out=step.out, lse=step.lse)
+            mla.decode(q_dec, S.kv, S.bt, S.sl, w.softmax_scale, w.causal, st.metadata, parts, workspace=st.workspace,
+                       out=st.out, lse=st.lse)
 
-    def absorb_call(qn, qp, pos_d):
+    def absorb_call(qn, qp, pos_d, S=S0):
         if proj_fp8:
-            mla.absorb_q_fp8(qn, w_uk_t, w.w_scale, step.q, q_pe=qp, positions=pos_d, workspace=fp8_ws)
+            mla.absorb_q_fp8(qn, S.w_uk_t, w.w_scale, S.step.q, q_pe=qp, positions=pos_d, workspace=S.fp8_ws)
         else:
-            mla.absorb_q(qn, w_uk, step.q, q_pe=qp, positions=pos_d)
+            mla.absorb_q(qn, S.w_uk, S.step.q, q_pe=qp, positions=pos_d)
 
-    def unabsorb_call():
+    def unabsorb_call(S=S0):
+        out = S.step.out.view(B * s_q, H, 512)
         if proj_fp8:
-            mla.unabsorb_o_fp8(step.out.view(B * s_q, H, 512), w_uv_t, w.w_scale, o=step.o, workspace=fp8_ws)
+            mla.unabsorb_o_fp8(out, S.w_uv_t, w.w_scale, o=S.step.o, workspace=S.fp8_ws)
         else:
-            mla.unabsorb_o(step.out.view(B * s_q, H, 512), w_uv, o=step.o)
+            mla.unabsorb_o(out, S.w_uv, o=S.step.o)
 
     # bf16 projections: the split schedule runs in the absorption's launch (one more CTA);
     # otherwise on a side stream beside the absorption
     fused_plan = w.with_projections and not proj_fp8 and B <= mla.absorb_plan_max_batch()
 
-    def absorb_and_plan(qn, qp, pos_d):
+    def absorb_and_plan(qn, qp, pos_d, S=S0):
         if fused_plan:
-            step.absorb_and_plan(qn, qp, w_uk, positions=pos_d)
+            S.step.absorb_and_plan(qn, qp, S.w_uk, positions=pos_d)
         else:
-            step.plan_beside(lambda: absorb_call(qn, qp, pos_d) if w.with_projections else None)
+            S.step.plan_beside(lambda: absorb_call(qn, qp, pos_d, S) if w.with_projections else None)
 
-    def one_step():
-        absorb_and_plan(q_nope, q_pe, positions)
-        decode_only()
+    def one_step(S=S0):
+        absorb_and_plan(S.q_nope, S.q_pe, S.positions, S)
+        decode_only(S)
         if w.with_projections:
-            unabsorb_call()
+            unabsorb_call(S)
 
     # schedule (alone or in the absorption's launch), decode + combine, the bmms
     launches_per_step = (0 if fused_plan else 1) + 2 + (2 if w.with_projections else 0)
+    # Each timed step runs `inner` passes back to back, so that the timed region lasts long
+    # enough for the clock samples to see the load.  The passes cycle through `copies` input
+    # sets, as many as it takes for the data touched between two uses of a set to exceed
+    # 512 MiB (four times the L2): no pass finds its cache, weights or queries in L2, as
+    # with the flush between steps.  ms_per_step is per pass.
+    inner = args.inner if args.inner > 0 else (1 if args.eager else 256)
+    set_bytes = sum(t.numel() * t.element_size() for t in vars(S0).values() if isinstance(t, torch.Tensor))
+    copies = 1 if inner == 1 else min(inner, max(2, 1 + -(-(512 << 20) // set_bytes)))
+    sets = [S0] + [copy_of(S0) for _ in range(copies - 1)]
     for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        one_step()
+        for S in sets:
+            flush.zero_()
+            one_step(S)
     torch.cuda.synchronize()
     status = mla.get_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} during warm-up")
+
+    def timed_step():
+        for j in range(inner):
+            one_step(sets[j % copies])
+
     # the step's library calls recorded once in a CUDA graph and replayed (one host call
-    # per step); --eager issues them one by one
-    step_fn = one_step if args.eager else _graphed(torch, one_step, dev)
+    # per timed step); --eager issues them one by one
+    step_fn = timed_step if args.eager else _graphed(torch, timed_step, dev)
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -610,7 +648,7 @@ def run_ours(args, w):
             comp["absorb_and_schedule"].append(ev[0].elapsed_time(ev[1]) * 1e3)
     components = {k: round(statistics.mean(v), 2) for k, v in comp.items()
                   if w.with_projections or k not in ("absorb", "unabsorb")}
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    step_ms = [s.elapsed_time(e) / inner for s, e in zip(starts, ends)]
     dec_ms = [a.elapsed_time(b) for a, b in zip(d0, d1)]
     t_step = statistics.mean(step_ms) / 1e3
     t_dec = statistics.mean(dec_ms) / 1e3
@@ -774,7 +812,10 @@ def run_ours(args, w):
                            "path": "mla_decode_sparse_fp8" if sparse else "mla_decode_fp8",
                            "mma": "kind::f8f6f4; q and P each as two E4M3 terms, fp32 accumulation"}
                           if fp8 else {}),
-                       "l2": "flushed between timed steps (256 MiB write, then 256 MiB read; outside the step events)",
+                       "l2": "flushed between timed steps (256 MiB write, then 256 MiB read; outside the step events)"
+                             + (f"; each timed step runs {inner} passes cycling over {copies} copies of the inputs, "
+                                f"weights and buffers ({(copies - 1) * set_bytes / 2**20:.0f} MiB touched between "
+                                "two uses of a copy); ms_per_step is per pass" if inner > 1 else ""),
                        "decode_timing": "K further decode calls inside the timed region, L2 flushed before each",
                        "launch": ("eager" if args.eager else "CUDA graph of the step's library calls")
                                  + ("; split schedule computed in the W_UK absorption's launch (one more CTA)"
@@ -786,7 +827,7 @@ def run_ours(args, w):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "components_us": components,
-            "gpu_launches": launches_per_step * args.steps + 2 * args.steps,
+            "gpu_launches": launches_per_step * args.steps * inner + 2 * args.steps,
             "clocks": clocks.summary(),
         }
         print(json.dumps(line))
@@ -807,6 +848,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch the step's calls one by one instead of a CUDA graph")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--inner", type=int, default=0,
+                    help="passes per timed step, cycling over input copies (default 256; 1 with --eager)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     from mla_absorbed_decode_gb300 import workloads as W
