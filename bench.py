@@ -584,9 +584,14 @@ def run_ours(args, w):
         for j in range(inner):
             one_step(sets[j % copies])
 
+    def timed_decodes():
+        for j in range(inner):
+            decode_only(sets[j % copies])
+
     # the step's library calls recorded once in a CUDA graph and replayed (one host call
     # per timed step); --eager issues them one by one
     step_fn = timed_step if args.eager else _graphed(torch, timed_step, dev)
+    dec_fn = timed_decodes if args.eager else _graphed(torch, timed_decodes, dev)
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -602,12 +607,13 @@ def run_ours(args, w):
             step_fn()
             ends[i].record()
         # the decode call (decode kernel + combine) on its own, with the step's metadata
-        # and q, L2 flushed before each launch: events between the kernels of a step
-        # would stop them from overlapping, so it is timed apart from the steps
+        # and q: events between the kernels of a step would stop them from overlapping,
+        # so it is timed apart from the steps, in the same way (L2 flushed before each
+        # timed step, `inner` calls back to back over the input copies)
         for i in range(args.steps):
             flush.zero_()
             d0[i].record()
-            decode_only()
+            dec_fn()
             d1[i].record()
         torch.cuda.synchronize()
     if dist:
@@ -649,7 +655,7 @@ def run_ours(args, w):
     components = {k: round(statistics.mean(v), 2) for k, v in comp.items()
                   if w.with_projections or k not in ("absorb", "unabsorb")}
     step_ms = [s.elapsed_time(e) / inner for s, e in zip(starts, ends)]
-    dec_ms = [a.elapsed_time(b) for a, b in zip(d0, d1)]
+    dec_ms = [a.elapsed_time(b) / inner for a, b in zip(d0, d1)]
     t_step = statistics.mean(step_ms) / 1e3
     t_dec = statistics.mean(dec_ms) / 1e3
     t_step, t_dec = max_over_ranks([t_step, t_dec], dist, dev)
@@ -816,7 +822,8 @@ def run_ours(args, w):
                              + (f"; each timed step runs {inner} passes cycling over {copies} copies of the inputs, "
                                 f"weights and buffers ({(copies - 1) * set_bytes / 2**20:.0f} MiB touched between "
                                 "two uses of a copy); ms_per_step is per pass" if inner > 1 else ""),
-                       "decode_timing": "K further decode calls inside the timed region, L2 flushed before each",
+                       "decode_timing": "K further timed steps of decode calls alone inside the timed region, timed like the "
+                                        "steps (ms_per_launch is per call)",
                        "launch": ("eager" if args.eager else "CUDA graph of the step's library calls")
                                  + ("; split schedule computed in the W_UK absorption's launch (one more CTA)"
                                     if fused_plan else "; split schedule on a side stream beside the W_UK absorption")},
@@ -827,7 +834,7 @@ def run_ours(args, w):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "components_us": components,
-            "gpu_launches": launches_per_step * args.steps * inner + 2 * args.steps,
+            "gpu_launches": (launches_per_step + 2) * args.steps * inner,
             "clocks": clocks.summary(),
         }
         print(json.dumps(line))
