@@ -59,9 +59,9 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 384;          // 12 warps; the sparse decode over an FP8 cache runs 16 (see SparseWarps)
+constexpr int kThreads = 384;          // 12 warps; the sparse decode runs 16 (see SparseWarps)
 template <bool kSparse, bool kF8>
-constexpr int threads_of() { return (kSparse && kF8) ? 512 : kThreads; }
+constexpr int threads_of() { return kSparse ? 512 : kThreads; }
 constexpr int kMaxStages = 4;                         // barrier slots: the deepest page ring
 constexpr int kSlots = 4;                             // O-CTA packet receive slots: a slot's credit
                                                       // round trip over DSMEM is hidden 4 pages deep
@@ -373,16 +373,16 @@ struct RowLookahead {
 
 // Gathering warps of the sparse decode.  Gathering warp slot ws owns rows
 // [gather_r0(ws), gather_r0(ws + 1)) of each page; lane l looks up row gather_r0(ws) + l.
-// bf16 cache (12 warps): the S-CTA gathers with warps 0, 2, 3 and 8..11, the O-CTA with
-// warps 0, 3 and 8..11 (one warp sustains only a few GB/s of 16-byte copies), and the
-// softmax and the epilogue run on warps 4..7 alone.  FP8 cache: the kernel runs 16 warps
-// (its registers fit 128 a thread); warps 12..15 gather as well, and the softmax and the
-// epilogue keep both warpgroups (4..11) as in the dense decode.  With one warpgroup the
-// FP8 softmax took ~2 us a page and set the period; with two but only warps 0, 2, 3 / 0, 3
-// gathering, the gather did.
+// The kernel runs 16 warps (its registers fit 128 a thread in both cache formats): the
+// S-CTA gathers with warps 0, 2, 3 and 12..15, the O-CTA with warps 0, 3 and 12..15 (one
+// warp sustains only a few GB/s of 16-byte copies), and the softmax and the epilogue keep
+// both warpgroups (4..11) as in the dense decode.  With 12 warps and one warpgroup for the
+// softmax (kOneWG, warps 8..11 gathering) the softmax took ~1.6 us (bf16) / ~2 us (FP8) of
+// each page and set the period; with two but only warps 0, 2, 3 / 0, 3 gathering, the
+// gather did.
 template <bool F8>
 struct SparseWarps {
-  static constexpr bool kOneWG = !F8;     // the softmax / epilogue on warps 4..7 only
+  static constexpr bool kOneWG = false;   // true: the softmax / epilogue on warps 4..7 only
   static constexpr int kS = 7, kO = 6;
   static constexpr int kFirstExtra = kOneWG ? 8 : 12;   // warps kFirstExtra..kFirstExtra+3 gather
   // gathering warp slot of warp `warp`, or -1
@@ -1406,13 +1406,14 @@ int decode_max_clusters(int cluster_ctas) {
 
 cudaError_t launch_decode(const KvMaps& maps, const DecodeParams& p, int cluster_ctas, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
-  if (p.indices && p.kv_fp8) {   // 16 warps (one CTA per SM either way: shared memory bounds it)
+  if (p.indices) {   // 16 warps (one CTA per SM either way: shared memory bounds it)
+    static_assert(threads_of<true, true>() == threads_of<true, false>(), "one sparse launch shape");
     cudaLaunchConfig_t cfg16 = decode_config(p.num_parts * cluster_ctas, cluster_ctas, stream, attr, true,
                                              threads_of<true, true>());
-    return cudaLaunchKernelEx(&cfg16, mla_decode_kernel<true, true>, maps, p);
+    if (p.kv_fp8) return cudaLaunchKernelEx(&cfg16, mla_decode_kernel<true, true>, maps, p);
+    return cudaLaunchKernelEx(&cfg16, mla_decode_kernel<true, false>, maps, p);
   }
   cudaLaunchConfig_t cfg = decode_config(p.num_parts * cluster_ctas, cluster_ctas, stream, attr, true);
-  if (p.indices) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true, false>, maps, p);
   if (p.kv_fp8) return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, true>, maps, p);
   return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false, false>, maps, p);
 }
