@@ -80,3 +80,14 @@ def test_graph_replay_equals_eager_and_follows_refilled_inputs():
     assert mla.get_device_status() == 0
     assert torch.equal(got2, ref2)
     assert not torch.equal(got1, got2)
+    # refill the lengths in place: the captured step recomputes its schedule (inside the
+    # absorption's launch) from them, as eager plan() does
+    sl.copy_(torch.tensor([700, 1, 333], dtype=torch.int32, device=dev))
+    eager.plan()
+    ref3 = eager.run(qn, qp, wuk, wuv, kv, bt).clone()
+    got3 = graphed.replay().clone()
+    torch.cuda.synchronize()
+    assert mla.get_device_status() == 0
+    assert torch.equal(graphed.metadata, eager.metadata)
+    assert torch.equal(got3, ref3)
+    assert not torch.equal(got3, got2)
