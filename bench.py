@@ -544,12 +544,16 @@ def run_ours(args, w):
         else:
             mla.unabsorb_o(out, S.w_uv, o=S.step.o)
 
-    # bf16 projections: the split schedule runs in the absorption's launch (one more CTA);
-    # otherwise on a side stream beside the absorption
-    fused_plan = w.with_projections and not proj_fp8 and B <= mla.absorb_plan_max_batch()
+    # with projections the split schedule runs in the absorption's launch (one more CTA: of the
+    # bf16 bmm, or of the FP8 path's amax pass); otherwise on a side stream
+    fused_plan = w.with_projections and B <= mla.absorb_plan_max_batch()
 
     def absorb_and_plan(qn, qp, pos_d, S=S0):
-        if fused_plan:
+        if fused_plan and proj_fp8:
+            st = S.step
+            mla.absorb_q_fp8_plan(qn, S.w_uk_t, w.w_scale, st.q, st.seqlens, st.parts, st.metadata, q_pe=qp,
+                                  positions=pos_d, workspace=S.fp8_ws)
+        elif fused_plan:
             S.step.absorb_and_plan(qn, qp, S.w_uk, positions=pos_d)
         else:
             S.step.plan_beside(lambda: absorb_call(qn, qp, pos_d, S) if w.with_projections else None)
@@ -561,7 +565,7 @@ def run_ours(args, w):
             unabsorb_call(S)
 
     # schedule (alone or in the absorption's launch), decode + combine, the bmms
-    launches_per_step = (0 if fused_plan else 1) + 2 + (2 if w.with_projections else 0)
+    launches_per_step = (0 if fused_plan else 1) + 2 + ((4 if proj_fp8 else 2) if w.with_projections else 0)
     # Each timed step runs `inner` passes back to back, so that the timed region lasts long
     # enough for the clock samples to see the load.  The passes cycle through `copies` input
     # sets, as many as it takes for the data touched between two uses of a set to exceed
@@ -732,7 +736,7 @@ def run_ours(args, w):
             dev_big.copy_(host_big, non_blocking=True)
             if fused_plan:   # the schedule in the absorption's launch, once both packs are in
                 cur.wait_stream(s_in)
-                step.absorb_and_plan(dv["q_nope"], dv["q_pe"], w_uk, positions=dv["pos"])
+                absorb_and_plan(dv["q_nope"], dv["q_pe"], dv["pos"])
             elif w.with_projections:
                 absorb_call(dv["q_nope"], dv["q_pe"], dv["pos"])
             cur.wait_stream(s_in)
@@ -825,8 +829,10 @@ def run_ours(args, w):
                        "decode_timing": "K further timed steps of decode calls alone inside the timed region, timed like the "
                                         "steps (ms_per_launch is per call)",
                        "launch": ("eager" if args.eager else "CUDA graph of the step's library calls")
-                                 + ("; split schedule computed in the W_UK absorption's launch (one more CTA)"
-                                    if fused_plan else "; split schedule on a side stream beside the W_UK absorption")},
+                                 + (("; split schedule computed by one more CTA of the FP8 absorption's amax pass"
+                                     if proj_fp8 else "; split schedule computed in the W_UK absorption's launch "
+                                     "(one more CTA)") if fused_plan else
+                                    "; split schedule on a side stream beside the W_UK absorption")},
             "hbm_gbs": gbs,
             "pct_of_roofline": 100.0 * rl_time / t_step,
             "roofline_spec": {"peak_tflops": SPEC_FLOPS / 1e12, "peak_gbs": SPEC_BW / 1e9},

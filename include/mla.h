@@ -255,6 +255,17 @@ mla_status_t mla_absorb_q_fp8(const mla_bf16_t* q_nope, int64_t q_nope_row_strid
                               const uint8_t* w_uk_t, float w_uk_scale, mla_bf16_t* q, int N, int H,
                               void* workspace, size_t workspace_bytes, mla_stream_t stream);
 
+/* mla_absorb_q_fp8 and mla_decode_metadata in one pass: one CTA beyond the activation's
+ * amax pass computes the split schedule, so that the decode issued next on the stream
+ * depends on a single chain of kernels.  Results are those of the two separate calls,
+ * bit for bit.  seqlens, B, num_sm_parts, metadata as for mla_absorb_q_plan (same limits);
+ * the rest as for mla_absorb_q_fp8.  Async on stream. */
+mla_status_t mla_absorb_q_fp8_plan(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                                   int64_t q_pe_row_stride, const int32_t* positions, float rope_theta,
+                                   const uint8_t* w_uk_t, float w_uk_scale, mla_bf16_t* q, int N, int H,
+                                   void* workspace, size_t workspace_bytes, const int32_t* seqlens, int B,
+                                   int num_sm_parts, void* metadata, mla_stream_t stream);
+
 /* mla_unabsorb_o with FP8 weights (see above), K = 512:
  *   o[n, h, 0:128] = bmm_fp8(input_to_float8(o_lat), W_UV)[n, h, :]
  *  o_lat [N, H, 512] bf16;  w_uv_t [H, 128, 512] E4M3 codes: W_UV[h] transposed;

@@ -17,7 +17,7 @@ __all__ = [
     "MLAError", "lib", "library_path", "num_sm_parts", "metadata_size", "decode_metadata",
     "decode_workspace_size", "decode", "decode_sparse", "decode_fp8", "decode_sparse_fp8", "absorb_q", "unabsorb_o",
     "absorb_plan_max_batch", "absorb_q_plan",
-    "bmm_fp8_workspace_size", "absorb_q_fp8", "unabsorb_o_fp8", "extend_workspace_size", "extend_chunked",
+    "bmm_fp8_workspace_size", "absorb_q_fp8", "absorb_q_fp8_plan", "unabsorb_o_fp8", "extend_workspace_size", "extend_chunked",
     "get_device_status",
     "schedule_params", "debug_withhold_first_load", "DecodeStep", "EXPORTED_SYMBOLS",
 ]
@@ -53,6 +53,8 @@ _SIGNATURES = {
     "mla_unabsorb_o": (_c_int, [_p, _p, _p, _c_int, _c_int, _p]),
     "mla_bmm_fp8_workspace_size": (_c_size, []),
     "mla_absorb_q_fp8": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _c_float, _p, _c_int, _c_int, _p, _c_size, _p]),
+    "mla_absorb_q_fp8_plan": (_c_int, [_p, _c_ll, _p, _c_ll, _p, _c_float, _p, _c_float, _p, _c_int, _c_int, _p,
+                                       _c_size, _p, _c_int, _c_int, _p, _p]),
     "mla_unabsorb_o_fp8": (_c_int, [_p, _p, _c_float, _p, _c_int, _c_int, _p, _c_size, _p]),
     "mla_extend_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
     "mla_extend_chunked": (_c_int, [_p, _p, _p, _p, _p, _c_ll, _p, _c_int, _c_int, _c_int, _c_float, _c_int, _p, _c_size,
@@ -288,6 +290,25 @@ def absorb_q_fp8(q_nope: torch.Tensor, w_uk_t: torch.Tensor, w_uk_scale: float, 
                                   None if positions is None else _ptr(positions), float(rope_theta), _ptr(w_uk_t),
                                   float(w_uk_scale), _ptr(q), N, H, _ptr(ws), ws.numel() * ws.element_size(),
                                   _stream(stream)), "mla_absorb_q_fp8")
+    return q
+
+
+def absorb_q_fp8_plan(q_nope: torch.Tensor, w_uk_t: torch.Tensor, w_uk_scale: float, q: torch.Tensor,
+                      seqlens: torch.Tensor, num_parts: int, metadata: torch.Tensor, q_pe: torch.Tensor | None = None,
+                      positions: torch.Tensor | None = None, rope_theta: float = 10000.0,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """absorb_q_fp8 and decode_metadata(seqlens, ..., num_parts, out=metadata) in one pass
+    (B = len(seqlens), s_q = N / B); returns q."""
+    N, H, _ = q_nope.shape
+    if w_uk_t.element_size() != 1:
+        raise TypeError("absorb_q_fp8_plan: w_uk_t must hold one E4M3 code per value")
+    ws = _fp8_workspace(q_nope.device, workspace)
+    pe_ptr, pe_stride = (0, 0) if q_pe is None else (_ptr(q_pe), q_pe.stride(0))
+    _check(lib().mla_absorb_q_fp8_plan(_ptr(q_nope), q_nope.stride(0), pe_ptr or None, pe_stride,
+                                       None if positions is None else _ptr(positions), float(rope_theta),
+                                       _ptr(w_uk_t), float(w_uk_scale), _ptr(q), N, H, _ptr(ws),
+                                       ws.numel() * ws.element_size(), _ptr(seqlens), seqlens.numel(),
+                                       int(num_parts), _ptr(metadata), _stream(stream)), "mla_absorb_q_fp8_plan")
     return q
 
 

@@ -465,11 +465,14 @@ size_t mla_bmm_fp8_workspace_size(void) { return static_cast<size_t>(kAmaxParts)
 namespace {
 
 // Shared body of mla_absorb_q_fp8 (absorb: x = q_nope, K = 128, 512 columns, optional q_pe
-// copy / RoPE) and mla_unabsorb_o_fp8 (x = o_lat, K = 512, 128 columns).
+// copy / RoPE) and mla_unabsorb_o_fp8 (x = o_lat, K = 512, 128 columns).  With sched_meta
+// set (absorb only), one more CTA of the amax launch writes the split schedule of
+// (sched_seqlens, sched_B, sched_parts) to sched_meta.
 mla_status_t bmm_fp8_impl(bool absorb, const mla_bf16_t* x, int64_t x_row_stride, const mla_bf16_t* q_pe,
                           int64_t q_pe_row_stride, const int32_t* positions, double rope_theta, const uint8_t* w_t,
                           float w_scale, mla_bf16_t* out, int N, int H, void* workspace, size_t workspace_bytes,
-                          mla_stream_t stream) {
+                          mla_stream_t stream, const int32_t* sched_seqlens = nullptr, int sched_B = 0,
+                          int sched_parts = 0, int32_t* sched_meta = nullptr) {
   const int K = absorb ? 128 : kDimV;
   const int J = absorb ? kDimV : 128;
   if (!x || !w_t || !out || N < 1 || H < 1) return MLA_ERR_INVALID_ARG;
@@ -518,6 +521,15 @@ mla_status_t bmm_fp8_impl(bool absorb, const mla_bf16_t* x, int64_t x_row_stride
     p.base.two_pi_hi = static_cast<float>(two_pi);
     p.base.two_pi_lo = static_cast<float>(two_pi - static_cast<double>(p.base.two_pi_hi));
   }
+  if (sched_meta) {
+    p.base.sched_seqlens = sched_seqlens;
+    p.base.sched_meta = sched_meta;
+    p.base.sched_B = sched_B;
+    p.base.sched_parts = sched_parts;
+    p.base.sched_fixed = kSegmentCostPages;
+    p.base.sched_hbm = kHbmParts;
+    p.base.sched_split = kSplitCostPages;
+  }
   p.partials = static_cast<const float*>(workspace);
   p.w = w_t;
   p.J = J;
@@ -542,6 +554,23 @@ mla_status_t mla_absorb_q_fp8(const mla_bf16_t* q_nope, int64_t q_nope_row_strid
   return bmm_fp8_impl(true, q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, positions,
                       static_cast<double>(rope_theta), w_uk_t, w_uk_scale, q, N, H, workspace, workspace_bytes,
                       stream);
+}
+
+mla_status_t mla_absorb_q_fp8_plan(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
+                                   int64_t q_pe_row_stride, const int32_t* positions, float rope_theta,
+                                   const uint8_t* w_uk_t, float w_uk_scale, mla_bf16_t* q, int N, int H,
+                                   void* workspace, size_t workspace_bytes, const int32_t* seqlens, int B,
+                                   int num_sm_parts, void* metadata, mla_stream_t stream) {
+  if (!seqlens || !metadata || B < 1 || num_sm_parts < 1 || N < 1 || H < 1 || N % B != 0) return MLA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(metadata) & 3u) != 0 || (reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0)
+    return MLA_ERR_INVALID_ARG;
+  if (B > kAbsorbPlanMaxB || pairs_for(N / B, H) > kMaxPairsPerCluster) return MLA_ERR_UNSUPPORTED;
+  if (positions && (!q_pe || (reinterpret_cast<uintptr_t>(positions) & 3u) || !std::isfinite(rope_theta) ||
+                    !(rope_theta > 1.f)))
+    return MLA_ERR_INVALID_ARG;
+  return bmm_fp8_impl(true, q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, positions,
+                      static_cast<double>(rope_theta), w_uk_t, w_uk_scale, q, N, H, workspace, workspace_bytes,
+                      stream, seqlens, B, num_sm_parts, static_cast<int32_t*>(metadata));
 }
 
 mla_status_t mla_unabsorb_o_fp8(const mla_bf16_t* o_lat, const uint8_t* w_uv_t, float w_uv_scale, mla_bf16_t* o, int N,

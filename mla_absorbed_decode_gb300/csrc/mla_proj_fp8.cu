@@ -25,6 +25,7 @@
 #include "mla_kernels.h"
 #include "mla_ptx.cuh"
 #include "mla_rope.cuh"
+#include "mla_schedule.cuh"
 
 namespace mla {
 
@@ -39,16 +40,30 @@ __device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity) {   // b
 }  // namespace
 
 // ---------------------------------------------------------- amax partials --
-// partials[blockIdx.x] = max |x| over this CTA's grid-stride share of x, viewed as `rows`
-// rows of `row_units` 16-byte units (8 bf16 values) at `row_stride` elements apart.
+// partials[blockIdx.x] = max |x| over the grid-stride share of x of CTA blockIdx.x <
+// kAmaxParts, x viewed as `rows` rows of `row_units` 16-byte units (8 bf16 values) at
+// `row_stride` elements apart.  With sched.sched_meta set, CTA kAmaxParts computes the
+// split schedule instead (mla_decode_metadata's output), its prefix sums in the launch's
+// dynamic shared memory.
 __global__ void __launch_bounds__(256) mla_amax_kernel(const __nv_bfloat16* x, int64_t rows, int64_t row_units,
-                                                       int64_t row_stride, float* partials) {
+                                                       int64_t row_stride, float* partials,
+                                                       const BmmParams sched) {
+  if (sched.sched_meta != nullptr && blockIdx.x == kAmaxParts) {
+    extern __shared__ int64_t amax_sched_c[];
+    __shared__ int64_t amax_scan[256 / 32 + 1];
+    griddep_wait();   // the lengths may come from the previous kernel
+    griddep_launch_dependents();
+    schedule_body<256>(sched.sched_seqlens, sched.sched_B, sched.sched_parts, sched.sched_fixed, sched.sched_hbm,
+                       sched.sched_split, sched.sched_meta, sched.sched_meta + kMetaInts * sched.sched_parts,
+                       amax_sched_c, reinterpret_cast<int32_t*>(amax_sched_c + sched.sched_B + 1), amax_scan);
+    return;
+  }
   griddep_wait();
   griddep_launch_dependents();
   const int64_t total = rows * row_units;
   float m = 0.f;
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
-       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+       u += static_cast<int64_t>(kAmaxParts) * blockDim.x) {
     const int64_t r = u / row_units, c = u - r * row_units;
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + r * row_stride) + c);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -294,8 +309,14 @@ mla_bmm_fp8_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_const
 #define MLA_FP8_ABSORB 128, 256
 #define MLA_FP8_UNABSORB 512, 128
 
+// dynamic shared memory of the amax launch when it also computes the schedule
+constexpr size_t kAmaxPlanSmem = sizeof(int64_t) * (kAbsorbPlanMaxB + 1) + sizeof(int32_t) * kAbsorbPlanMaxB;
+
 cudaError_t bmm_fp8_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(mla_bmm_fp8_kernel<MLA_FP8_ABSORB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(mla_amax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kAmaxPlanSmem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(mla_bmm_fp8_kernel<MLA_FP8_ABSORB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(Fp8BmmShape<MLA_FP8_ABSORB>::kSmem));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(mla_bmm_fp8_kernel<MLA_FP8_UNABSORB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -305,10 +326,15 @@ cudaError_t bmm_fp8_set_attributes() {
 cudaError_t launch_bmm_fp8(bool absorb, const __nv_bfloat16* x, int64_t x_row_stride, int K, const CUtensorMap& x_map,
                            const CUtensorMap& w_map, const BmmFp8Params& p, float* partials, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
-  {   // the partial maxima of |x| over the N rows of H * K values
-    const cudaLaunchConfig_t cfg = pdl_config(dim3(kAmaxParts), dim3(256), 0, stream, attr);
+  {   // the partial maxima of |x| over the N rows of H * K values (and the schedule, if asked)
+    const bool plan = p.base.sched_meta != nullptr;
+    if (plan && (!absorb || p.base.sched_B < 1 || p.base.sched_B > kAbsorbPlanMaxB || p.base.sched_parts < 1))
+      return cudaErrorInvalidValue;
+    const size_t smem = plan ? sizeof(int64_t) * (p.base.sched_B + 1) + sizeof(int32_t) * p.base.sched_B : 0;
+    const cudaLaunchConfig_t cfg = pdl_config(dim3(kAmaxParts + (plan ? 1 : 0)), dim3(256), smem, stream, attr);
     const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_amax_kernel, x, static_cast<int64_t>(p.base.N),
-                                             static_cast<int64_t>(p.base.H) * K / 8, x_row_stride, partials);
+                                             static_cast<int64_t>(p.base.H) * K / 8, x_row_stride, partials,
+                                             p.base);
     if (e != cudaSuccess) return e;
   }
   const unsigned mt = static_cast<unsigned>((p.base.N + 127) / 128);

@@ -160,3 +160,28 @@ def test_absorb_plan_argument_checks(mla):
     assert L.mla_absorb_q_plan(*bad) == 2                           # MLA_ERR_UNSUPPORTED
     bad = list(ok); bad[9] = 1024; bad[8] = 4                       # s_q * H beyond a cluster's pairs
     assert L.mla_absorb_q_plan(*bad) == 2
+
+
+def test_absorb_fp8_plan_argument_checks(mla):
+    L = mla.lib()
+    A = 0x10000  # 16-byte aligned, never dereferenced: every case returns before any launch
+    ws = mla.bmm_fp8_workspace_size()
+    # (q_nope, stride, q_pe, pe_stride, positions, theta, w_uk_t, w_scale, q, N, H, workspace, bytes,
+    #  seqlens, B, parts, metadata, stream)
+    ok = [A, 128, A, 64, A, 10000.0, A, 2.0 ** -9, A, 8, 1, A, ws, A, 4, 76, A, None]
+    for i in (13, 16):                                              # seqlens, metadata
+        bad = list(ok); bad[i] = None
+        assert L.mla_absorb_q_fp8_plan(*bad) == 1                   # MLA_ERR_INVALID_ARG
+    for i, v in ((14, 0), (14, 3), (15, 0)):                        # B < 1, N not a multiple of B, parts
+        bad = list(ok); bad[i] = v
+        assert L.mla_absorb_q_fp8_plan(*bad) == 1
+    bad = list(ok); bad[2] = None                                   # positions without q_pe
+    assert L.mla_absorb_q_fp8_plan(*bad) == 1
+    big = L.mla_absorb_plan_max_batch() + 1
+    bad = list(ok); bad[14] = big; bad[9] = big
+    assert L.mla_absorb_q_fp8_plan(*bad) == 2                       # MLA_ERR_UNSUPPORTED
+    for i in (0, 6, 8):                                             # q_nope, weights, q (checked by the FP8 bmm)
+        bad = list(ok); bad[i] = None
+        assert L.mla_absorb_q_fp8_plan(*bad) == 1
+    bad = list(ok); bad[12] = ws - 1
+    assert L.mla_absorb_q_fp8_plan(*bad) == 3                       # MLA_ERR_WORKSPACE

@@ -97,6 +97,18 @@ def test_more_query_rows_than_one_pair(s_q, H):
         compare(out, lse, ref_out, ref_lse, what=f"s_q={s_q} H={H} parts={P}")
 
 
+@pytest.mark.parametrize("s_q,H", [(1, 1), (1, 20), (1, 127), (2, 20), (2, 100), (3, 127)])
+def test_head_counts_off_the_tile(s_q, H):
+    # s_q * H rows that leave part of a 128-row block unused, and (causal) rows whose
+    # query position i = row // H changes inside a warp
+    seqlens = [3, 64, 190, 700]
+    inp = _case(len(seqlens), s_q, H, seqlens, causal=s_q > 1, seed=s_q * 7 + H)
+    ref_out, ref_lse, ref_abs = oracle_decode(inp)
+    for parts in (None, 1, 5):
+        out, lse, _, P = run_library(inp, parts=parts)
+        compare(out, lse, ref_out, ref_lse, what=f"s_q={s_q} H={H} parts={P}")
+
+
 def test_largest_batch():
     # the schedule's maximum batch (16384 requests), short contexts, sampled against the oracle
     B = 16384

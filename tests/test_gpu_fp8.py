@@ -57,7 +57,7 @@ def test_fp8_scale(kv_scale):
     compare(out, lse, ref_out, ref_lse, ref_abs=ref_abs, what=f"fp8 kv_scale={kv_scale}")
 
 
-@pytest.mark.parametrize("s_q,H", [(2, 128), (2, 16), (3, 128), (4, 128), (3, 40)])
+@pytest.mark.parametrize("s_q,H", [(2, 128), (2, 16), (3, 128), (4, 128), (3, 40), (2, 20), (3, 127)])
 def test_fp8_causal_query_rows(s_q, H):
     seqlens = [2, 65, 300, 1025]
     inp = _case(len(seqlens), s_q, H, seqlens, causal=True, seed=s_q * 100 + H)

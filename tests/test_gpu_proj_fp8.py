@@ -65,6 +65,34 @@ def test_absorb_q_fp8(N, H, rope):
         assert torch.equal(q[..., 512:].cpu(), q_pe)
 
 
+@pytest.mark.parametrize("B,s_q,H,parts,rope", [(1, 1, 16, 1, False), (64, 1, 128, 76, True), (37, 2, 128, 76, False),
+                                                (8000, 1, 1, 148, True)])
+def test_absorb_q_fp8_plan_matches_the_separate_calls(B, s_q, H, parts, rope):
+    """The FP8 absorption with the schedule in its amax pass gives the separate calls' q and
+    metadata bit for bit (a request of length 0 included)."""
+    import mla_absorbed_decode_gb300 as mla
+    g = torch.Generator().manual_seed(B * 5 + s_q + H)
+    N = B * s_q
+    q_nope = (torch.randn((N, H, 128), generator=g) * 1.7).to(torch.bfloat16).cuda()
+    q_pe = torch.randn((N, H, 64), generator=g).to(torch.bfloat16).cuda()
+    _, w_t = _weights_t(g, H, 128, 512)
+    w_t = w_t.cuda()
+    seqlens = torch.randint(0, 9000, (B,), generator=g, dtype=torch.int32)
+    if B > 1:
+        seqlens[0] = 0
+    seqlens = seqlens.cuda()
+    pos = torch.randint(0, 1 << 16, (N,), generator=g, dtype=torch.int32).cuda() if rope else None
+    q1 = torch.full((N, H, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mla.absorb_q_fp8(q_nope, w_t, W_SCALE, q1, q_pe=q_pe, positions=pos)
+    meta1 = mla.decode_metadata(seqlens, s_q, H, False, parts)
+    q2 = torch.full((N, H, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    meta2 = torch.full_like(meta1, -7)
+    mla.absorb_q_fp8_plan(q_nope, w_t, W_SCALE, q2, seqlens, parts, meta2, q_pe=q_pe, positions=pos)
+    assert mla.get_device_status() == 0
+    assert torch.equal(q1.view(torch.int16), q2.view(torch.int16))
+    assert torch.equal(meta1, meta2)
+
+
 @pytest.mark.parametrize("N,H", [(1, 1), (5, 16), (64, 128), (200, 4)])
 def test_unabsorb_o_fp8(N, H):
     import mla_absorbed_decode_gb300 as mla

@@ -54,7 +54,8 @@ def _ref(inp, idx, kl):
                                 causal=inp["causal"])
 
 
-@pytest.mark.parametrize("H,s_q,causal", [(16, 1, False), (128, 1, False), (128, 2, True), (64, 2, False)])
+@pytest.mark.parametrize("H,s_q,causal", [(16, 1, False), (128, 1, False), (128, 2, True), (64, 2, False),
+                                           (20, 2, True), (127, 1, False)])
 def test_sparse_small(H, s_q, causal):
     seqlens = [5000, 130, 64, 3000]
     ks = [2048, 130, 1, 777]   # top-k, everything, a single token, ragged
@@ -181,7 +182,8 @@ def _ref8(inp, idx, kl):
                                 causal=inp["causal"], kv_scale=inp["kv_scale"])
 
 
-@pytest.mark.parametrize("H,s_q,causal", [(16, 1, False), (128, 1, False), (128, 2, True), (64, 2, False)])
+@pytest.mark.parametrize("H,s_q,causal", [(16, 1, False), (128, 1, False), (128, 2, True), (64, 2, False),
+                                           (20, 2, True), (127, 1, False)])
 def test_sparse_fp8_small(H, s_q, causal):
     seqlens = [5000, 130, 64, 3000]
     ks = [2048, 130, 1, 777]
