@@ -173,8 +173,8 @@ mla_expand_kernel(const __grid_constant__ CUtensorMap c_map, const __grid_consta
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       pk[j] = in ? pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])) : 0u;
-    __nv_bfloat16* base = (c < 128 ? p.kx : p.vx) + (static_cast<int64_t>(rw0) * p.H + h) * 128;
-    store_rows32(stg, pk, base, static_cast<int64_t>(p.H) * 128, c & 127, lane,
+    __nv_bfloat16* base = (c < 128 ? p.kx : p.vx) + (static_cast<int64_t>(h) * p.cap + rw0) * 128;   // [H][cap][128]
+    store_rows32(stg, pk, base, 128, c & 127, lane,
                  [&](int x) { return ok_all && rw0 + x < p.cap; });
   }
   if (warp == 0 && lane == 0)   // loads in flight land before the CTA may exit
@@ -193,17 +193,22 @@ constexpr int kAttStages = 3;
 constexpr uint32_t kAttStage = 40960;        // Kx tile (2 x 8 KiB) + k^R tile (8 KiB) + Vx tile (2 x 8 KiB)
 constexpr uint32_t kAttOffQ = 0;             // Q tile: 3 chunks of 64 dims x 128 rows (48 KiB)
 constexpr uint32_t kAttOffStage = 49152;
-constexpr uint32_t kAttOffP = kAttOffStage + kAttStages * kAttStage;   // P: 128 rows x 64 keys bf16 (16 KiB)
-constexpr uint32_t kAttOffEpi = kAttOffP + 16384;                      // 4 x 2 KiB transpose buffers
-constexpr uint32_t kAttSmem = kAttOffEpi + 8192 + 1024;
+constexpr uint32_t kAttOffEpi = kAttOffStage + kAttStages * kAttStage;   // 8 x 2 KiB transpose buffers
+constexpr uint32_t kAttOffPm = kAttOffEpi + 16384;   // float [3][2][128]: row maxima by tile parity, then row sums
+constexpr uint32_t kAttSmem = kAttOffPm + 3072 + 1024;
+// TMEM columns: O [0, 128), S (two 64-key buffers) [128, 256), the query tile (A operand of
+// QK^T: 192 dims, two per column) [256, 352), P (A operand of PV: 64 keys, two buffers)
+// [352, 416).  With Q and P in TMEM both MMAs read only their B operand from shared memory.
+constexpr uint32_t kAttTmemS = 128, kAttTmemQ = 256, kAttTmemP = 352;
 constexpr float kAttRebase = 8.0f;           // rebase the row maximum when it grows by more than 2^8
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
 mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_constant__ CUtensorMap qp_map,
                   const __grid_constant__ CUtensorMap kx_map, const __grid_constant__ CUtensorMap vx_map,
                   const __grid_constant__ CUtensorMap kr_map, const ExtendParams p) {
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
-  __shared__ uint64_t full[kAttStages], empty[kAttStages], q_full, s_full[2], s_empty[2], p_full, pv_done, drain;
+  __shared__ uint64_t full[kAttStages], empty[kAttStages], q_full, q_tmem, s_full[2], s_empty[2], p_full[2],
+      pv_done[2], drain;
   __shared__ uint32_t tmem_base_s;
   const uint32_t smem = (smem_u32(dyn_smem) + 1023u) & ~1023u;
   const int qt = blockIdx.x, h = blockIdx.y;
@@ -218,12 +223,15 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
       mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(&q_full), 1);
+    mbar_init(smem_u32(&q_tmem), 8);   // the eight softmax warps, once the query tile is in TMEM
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_empty[i]), 4);   // the four softmax warps
+      mbar_init(smem_u32(&s_empty[i]), 8);   // the eight softmax warps
     }
-    mbar_init(smem_u32(&p_full), 4);
-    mbar_init(smem_u32(&pv_done), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&p_full[i]), 8);    // the eight softmax warps
+      mbar_init(smem_u32(&pv_done[i]), 1);
+    }
     mbar_init(smem_u32(&drain), 1);
     fence_mbar_init();
     prefetch_tensormap(&qn_map);
@@ -232,7 +240,7 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
     prefetch_tensormap(&vx_map);
     prefetch_tensormap(&kr_map);
   }
-  if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 256);   // O: columns [0, 128); S: [128, 256)
+  if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), 512);   // O, S, Q, P (kAttTmem*)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -264,11 +272,11 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
         const uint32_t st = smem + kAttOffStage + s * kAttStage;
         const uint32_t bar = smem_u32(&full[s]);
         mbar_arrive_expect_tx(bar, kAttStage);
-        tma_load_3d(st, &kx_map, bar, 0, h, 64 * k);
-        tma_load_3d(st + 8192, &kx_map, bar, 64, h, 64 * k);
+        tma_load_3d(st, &kx_map, bar, 0, 64 * k, h);
+        tma_load_3d(st + 8192, &kx_map, bar, 64, 64 * k, h);
         tma_load_3d(st + 16384, &kr_map, bar, 0, blk * kPageTokens, kDimV / 64);   // k^R: cache dims 512..575
-        tma_load_3d(st + 24576, &vx_map, bar, 0, h, 64 * k);
-        tma_load_3d(st + 32768, &vx_map, bar, 64, h, 64 * k);
+        tma_load_3d(st + 24576, &vx_map, bar, 0, 64 * k, h);
+        tma_load_3d(st + 32768, &vx_map, bar, 64, 64 * k, h);
         issued_phase[s] = (k / kAttStages) & 1;
       }
       ext_wait(qb, 0, p.status);   // loads in flight land before the CTA may exit
@@ -278,17 +286,18 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
   } else if (warp == 1) {   // MMA issue (one elected lane), QK^T of tile k ahead of PV of tile k - 1
     constexpr uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
     constexpr uint32_t id_o = idesc_bf16_f32(128, 128, 0, 1);
-    bool ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&q_full), 0, p.status));
-    auto pv = [&](int k) {   // O += P V for tile k
-      if (!__all_sync(0xffffffffu, ext_wait(smem_u32(&p_full), k & 1, p.status))) return false;
+    bool ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&q_tmem), 0, p.status));
+    tc_fence_after();
+    auto pv = [&](int k) {   // O += P V for tile k, P from TMEM buffer k % 2
+      if (!__all_sync(0xffffffffu, ext_wait(smem_u32(&p_full[k & 1]), (k >> 1) & 1, p.status))) return false;
       tc_fence_after();
       const uint32_t st = smem + kAttOffStage + (k % kAttStages) * kAttStage;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_bf16_ss_warp(tmem, smem_desc_sw128(smem + kAttOffP + kk * 32, 16, 1024),
+        mma_bf16_ts_warp(tmem, tmem + kAttTmemP + (k & 1) * 32 + kk * 8,
                          smem_desc_sw128(st + 24576 + kk * 2048, 8192, 1024), id_o, (k | kk) ? 1u : 0u);
       mma_commit_warp(smem_u32(&empty[k % kAttStages]));
-      mma_commit_warp(smem_u32(&pv_done));
+      mma_commit_warp(smem_u32(&pv_done[k & 1]));
       return true;
     };
     for (int k = 0; k < ntiles && ok; ++k) {
@@ -303,7 +312,7 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
       for (int c = 0; c < 3; ++c)   // q_nope . Kx (two 64-dim chunks), q_pe . k^R
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ss_warp(tmem + 128 + sb * 64, smem_desc_sw128(smem + kAttOffQ + c * 16384 + kk * 32, 16, 1024),
+          mma_bf16_ts_warp(tmem + kAttTmemS + sb * 64, tmem + kAttTmemQ + c * 32 + kk * 8,
                            smem_desc_sw128(st + c * 8192 + kk * 32, 16, 1024), id_s, (c | kk) ? 1u : 0u);
       mma_commit_warp(smem_u32(&s_full[sb]));
       if (k > 0 && !pv(k - 1)) ok = false;
@@ -312,47 +321,88 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
     // every MMA issued so far is done before the CTA may free TMEM (also after a failure)
     mma_commit_warp(smem_u32(&drain));
     ext_wait(smem_u32(&drain), 0, p.status);
-  } else if (warp >= 4) {   // softmax and epilogue: one thread per query row
-    const int r = threadIdx.x - 128, wq = r >> 5;
+  } else if (warp >= 4) {   // softmax and epilogue: two warpgroups, one thread per query row each
+    // warpgroup wg takes keys [32 wg, 32 wg + 32) of every tile and O columns [64 wg, 64 wg + 64);
+    // the two agree on the row maximum (and so on every rebase) through pm[][] and named
+    // barrier 1, and add their partial row sums at the end
+    const int t = threadIdx.x - 128, wg = t >> 7, r = t & 127, wq = r >> 5;
     const int q = 128 * qt + r;                      // query row within the request
     const int qpos = p.qpos0 + q;                    // its position
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    float m = -INFINITY, l = 0.f;                    // reference maximum (log2 units), row sum
-    bool ok = true;
+    // exchange slot j of this warpgroup / of the other one; j = tile parity in the loop, 2 after
+    // it (with one barrier per tile a warpgroup writes slot k % 2 again only after the other
+    // has passed the next barrier, i.e. after it read that slot)
+    const auto pm_mine = [&](int j) { return smem + kAttOffPm + ((j * 2 + wg) * 128 + r) * 4; };
+    const auto pm_other = [&](int j) { return smem + kAttOffPm + ((j * 2 + 1 - wg) * 128 + r) * 4; };
+    float m = -INFINITY, l = 0.f;                    // reference maximum (log2 units), this half's row sum
+    // the query tile into TMEM: row r's 192 dims (three 128-byte swizzled chunks) as 96
+    // columns of bf16 pairs (warpgroup 0: q_nope, warpgroup 1: q_pe)
+    bool ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&q_full), 0, p.status));
+    if (ok) {
+      for (int c = wg == 0 ? 0 : 2; c < (wg == 0 ? 2 : 3); ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = ld_shared_v4(smem + kAttOffQ + c * 16384 + r * 128 + ((u ^ (r & 7)) << 4));
+          v[4 * u] = x.x, v[4 * u + 1] = x.y, v[4 * u + 2] = x.z, v[4 * u + 3] = x.w;
+        }
+        tmem_st32(tl + kAttTmemQ + c * 32, v);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&q_tmem));   // arrives even after a failure: the MMA warp's wait ends
+    // Every exit from the loop is taken by all eight warps together, after a barrier that
+    // folds in each warp's wait results (a warp leaving alone would strand the others there).
     for (int k = 0; k < ntiles; ++k) {
       const uint32_t sb = k & 1;
-      if (!ext_wait(smem_u32(&s_full[sb]), (k >> 1) & 1, p.status)) { ok = false; }
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      float x[64];
-      tmem_ld32(tl + 128 + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(x));
-      tmem_ld32(tl + 128 + sb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s_empty[sb]));
-      // key j of the tile is visible if it lies in the chunk and at or before this query
-      const int t0 = p.c0 + 64 * k;
-      float rmax = -INFINITY;
+      const bool got = __all_sync(0xffffffffu, ok && ext_wait(smem_u32(&s_full[sb]), (k >> 1) & 1, p.status));
+      float x[32];
+      if (got) {
+        tc_fence_after();
+        tmem_ld32(tl + kAttTmemS + sb * 64 + wg * 32, *reinterpret_cast<uint32_t(*)[32]>(x));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s_empty[sb]));
+      } else {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const bool vis = (64 * k + j < p.n) && (t0 + j <= qpos) && (q < p.T);
-        x[j] = vis ? x[j] * p.scale_log2 : -INFINITY;
-        rmax = fmaxf(rmax, x[j]);
+        for (int j = 0; j < 32; ++j) x[j] = -INFINITY;
       }
-      // O and the P buffer are free once the previous tile's PV is done
-      if (k > 0 && !__all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done), (k - 1) & 1, p.status))) {
-        ok = false;
-        break;
+      // the keys a row sees form a prefix of the tile: inside the chunk and at or before
+      // this query's position
+      const int t0 = p.c0 + 64 * k;
+      const int nvis = q < p.T ? min(p.n - 64 * k, qpos - t0 + 1) : 0;
+      const int nvalid = nvis - 32 * wg;                // of this warpgroup's 32 keys
+      if (nvalid < 32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = j < nvalid ? x[j] : -INFINITY;
       }
-      const float m_new = fmaxf(m, rmax);
+      float rmax = x[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) rmax = fmaxf(rmax, x[j]);
+      asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine(k & 1)), "f"(rmax) : "memory");
+      // P buffer k % 2 is free once the PV of tile k - 2 (which read it) is done
+      bool go = got;
+      if (go && k > 1 && !ext_wait(smem_u32(&pv_done[k & 1]), ((k >> 1) & 1) ^ 1, p.status)) go = false;
+      // one barrier both exchanges the row maxima and makes the abort decision uniform
+      if (named_bar_or(1, 256, !go)) { ok = false; break; }
+      // softmax_scale > 0, so the scaled maximum is the scaled raw maximum
+      const float m_new = fmaxf(m, fmaxf(rmax, ld_shared_f32(pm_other(k & 1))) * p.scale_log2);
       if (m_new > m + kAttRebase) {   // rebase: O and l scale by 2^(m - m_new) (0 when m = -inf)
         const float alpha = fast_exp2(m - m_new);
         l *= alpha;
-        if (k > 0) {
+        // O holds every earlier tile once the PV of tile k - 1 is done (the MMAs complete in order);
+        // a failed wait is carried to the next barrier (or the one after the loop)
+        if (k > 0 && !__all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[(k - 1) & 1]), ((k - 1) >> 1) & 1,
+                                                        p.status))) {
+          ok = false;
+        }
+        if (k > 0 && ok) {
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 128; c += 32) {
+          for (int c = 64 * wg; c < 64 * wg + 64; c += 32) {
             uint32_t v[32];
             tmem_ld32(tl + c, v);
             tmem_wait_ld();
@@ -365,29 +415,31 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
         m = m_new;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      const uint32_t prow = smem + kAttOffP + r * 128;
-      float ps = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t w[16];   // P of this half's 32 keys as bf16 pairs (2^x of -inf is +0)
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {   // 8 keys -> one 16-byte unit of the P row (128-byte swizzle)
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a = (x[8 * u + 2 * e] == -INFINITY) ? 0.f : fast_exp2(x[8 * u + 2 * e] + neg_m);
-          const float b = (x[8 * u + 2 * e + 1] == -INFINITY) ? 0.f : fast_exp2(x[8 * u + 2 * e + 1] + neg_m);
-          ps += a + b;
-          w[e] = pack_bf16x2(a, b);
-        }
-        st_shared_v4(prow + ((u ^ (r & 7)) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+      for (int e = 0; e < 16; ++e) {
+        const float a = fast_exp2(fmaf(x[2 * e], p.scale_log2, neg_m));
+        const float b = fast_exp2(fmaf(x[2 * e + 1], p.scale_log2, neg_m));
+        ps[e & 3] += a + b;
+        w[e] = pack_bf16x2(a, b);
       }
-      l += ps;
-      fence_proxy_async_smem();
+      tmem_st16(tl + kAttTmemP + (k & 1) * 32 + wg * 16, w);
+      tmem_wait_st();
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_full));
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[k & 1]));
     }
-    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done), (ntiles - 1) & 1, p.status));
+    if (ok && ntiles > 0)
+      ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[(ntiles - 1) & 1]), ((ntiles - 1) >> 1) & 1, p.status));
+    // the row sum over both halves (the barrier also settles whether every warp finished)
+    asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine(2)), "f"(l) : "memory");
+    ok = !named_bar_or(1, 256, !ok);
+    l += ld_shared_f32(pm_other(2));
     tc_fence_after();
-    // epilogue: the chunk's o = O / l and lse, merged into the running accumulator by LSE
+    // epilogue: the chunk's o = O / l and lse, merged into the running accumulator by LSE;
+    // warpgroup wg writes O columns [64 wg, 64 wg + 64)
     const bool row_ok = ok && q < p.T;
     const float lse_c = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
@@ -400,9 +452,9 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
     const float z = wa + wc;
     const float ca = z > 0.f ? wa / z : 0.f, cc = z > 0.f ? wc * inv_l / z : 0.f;
     const float lse_new = z > 0.f ? M + logf(z) : -INFINITY;
-    const uint32_t stg = smem + kAttOffEpi + wq * 2048u;
+    const uint32_t stg = smem + kAttOffEpi + (wg * 4 + wq) * 2048u;
     const int qw0 = 128 * qt + wq * 32;
-    for (int c = 0; c < 128; c += 32) {
+    for (int c = 64 * wg; c < 64 * wg + 64; c += 32) {
       uint32_t v[32];
       if (ntiles > 0) {
         tmem_ld32(tl + c, v);
@@ -433,7 +485,7 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
         for (int j = 0; j < 8; ++j) d4[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
       }
     }
-    if (row_ok) {
+    if (row_ok && wg == 0) {
       if (p.last) p.lse[row] = lse_new;
       else p.acc_lse[row] = lse_new;
     }
@@ -442,7 +494,7 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -463,7 +515,7 @@ cudaError_t launch_extend_chunk(const ExtendMaps& maps, const ExtendParams& p, c
     if (e != cudaSuccess) return e;
   }
   const cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>((p.T + 127) / 128), static_cast<unsigned>(p.H)),
-                                            dim3(256), kAttSmem, stream, attr);
+                                            dim3(384), kAttSmem, stream, attr);
   return cudaLaunchKernelEx(&cfg, mla_attend_kernel, maps.qn, maps.qp, maps.kx, maps.vx, maps.kr, p);
 }
 

@@ -629,8 +629,10 @@ mla_status_t mla_extend_chunked(const mla_bf16_t* q_nope, const mla_bf16_t* q_pe
   __nv_bfloat16* vx = reinterpret_cast<__nv_bfloat16*>(ws + kv_bytes);
   float* acc_o = reinterpret_cast<float*>(ws + 2 * kv_bytes);
   float* acc_lse = reinterpret_cast<float*>(ws + 2 * kv_bytes + round256(static_cast<size_t>(T) * H * 128 * 4));
-  if (!maps_ok || !encode_3d(&m.kx, kx, 128, uH, static_cast<uint64_t>(cap), 256, uH * 256, 64, 1, 64) ||
-      !encode_3d(&m.vx, vx, 128, uH, static_cast<uint64_t>(cap), 256, uH * 256, 64, 1, 64))
+  // expanded keys and values head-major, [H][cap][128]: a 64-token tile of one head is 16 KiB in one run
+  const uint64_t ucap = static_cast<uint64_t>(cap);
+  if (!maps_ok || !encode_3d(&m.kx, kx, 128, ucap, uH, 256, ucap * 256, 64, 64, 1) ||
+      !encode_3d(&m.vx, vx, 128, ucap, uH, 256, ucap * 256, 64, 64, 1))
     return MLA_ERR_CUDA;
   m.kr = m.c;
 

@@ -168,8 +168,8 @@ struct ExtendParams {
   int c0, n, cap;               // chunk start (a multiple of 64), its tokens, Kx / Vx rows
   int T, H, qpos0;              // new tokens, heads, position of new token 0 (seqlen - T)
   float scale_log2;             // softmax_scale * log2(e)
-  __nv_bfloat16* kx;            // [cap, H, 128] expanded keys (no RoPE part)
-  __nv_bfloat16* vx;            // [cap, H, 128] expanded values
+  __nv_bfloat16* kx;            // [H, cap, 128] expanded keys (no RoPE part), head-major
+  __nv_bfloat16* vx;            // [H, cap, 128] expanded values, head-major
   float* acc_o;                 // [T, H, 128] running merged output (fp32)
   float* acc_lse;               // [T, H] running merged lse
   int first, last;              // the first / last chunk of the call
@@ -183,7 +183,7 @@ struct ExtendMaps {
   CUtensorMap wv;               // W_UV as [H * 512 rows][128], box 64 x 64
   CUtensorMap qn;               // q_nope [128, H, T], box 64 x 1 x 128
   CUtensorMap qp;               // q_pe [64, H, T], box 64 x 1 x 128
-  CUtensorMap kx, vx;           // [128, H, cap], box 64 x 1 x 64
+  CUtensorMap kx, vx;           // [128, cap, H], box 64 x 64 x 1
   CUtensorMap kr;               // the cache view of c, k^R = chunk 8
 };
 cudaError_t extend_set_attributes();
