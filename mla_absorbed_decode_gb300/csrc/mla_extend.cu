@@ -63,11 +63,11 @@ __device__ __forceinline__ void store_rows32(uint32_t stg, const uint32_t (&pk)[
 }  // namespace
 
 // ---------------------------------------------------------------- expand --
-constexpr int kExpStages = 4;
+constexpr int kExpStages = 2;
 constexpr uint32_t kExpStage = 3 * 16384;   // latent chunk (A) + W_UK chunk (B, K-major) + W_UV chunk (B, MN-major)
 constexpr uint32_t kExpSmem = kExpStages * kExpStage + 1024;
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128, 2)
 mla_expand_kernel(const __grid_constant__ CUtensorMap c_map, const __grid_constant__ CUtensorMap wk_map,
                   const __grid_constant__ CUtensorMap wv_map, const ExtendParams p) {
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
