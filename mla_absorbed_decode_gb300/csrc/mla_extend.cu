@@ -29,7 +29,7 @@ namespace {
 
 constexpr uint64_t kExtTimeoutNs = 500ull * 1000 * 1000;
 
-__device__ __forceinline__ bool ext_wait(uint32_t bar, uint32_t parity, int* status) {   // bounded
+__device__ __noinline__ bool ext_wait_slow(uint32_t bar, uint32_t parity, int* status) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_test(bar, parity)) {
     if (global_timer_ns() - t0 > kExtTimeoutNs) {
@@ -38,6 +38,12 @@ __device__ __forceinline__ bool ext_wait(uint32_t bar, uint32_t parity, int* sta
     }
   }
   return true;
+}
+// Bounded wait (0.5 s).  The phase is tested once before the clock is read: reading the
+// global timer costs hundreds of cycles, which a wait that is already satisfied should not pay.
+__device__ __forceinline__ bool ext_wait(uint32_t bar, uint32_t parity, int* status) {
+  if (mbar_test(bar, parity)) return true;
+  return ext_wait_slow(bar, parity, status);
 }
 
 // Stores 32 columns [c, c + 32) of the warp's 32 rows (one row per lane, values already
@@ -189,26 +195,40 @@ mla_expand_kernel(const __grid_constant__ CUtensorMap c_map, const __grid_consta
 }
 
 // ---------------------------------------------------------------- attend --
-constexpr int kAttStages = 3;
-constexpr uint32_t kAttStage = 40960;        // Kx tile (2 x 8 KiB) + k^R tile (8 KiB) + Vx tile (2 x 8 KiB)
+// Two rings: a key stage (Kx tile, 2 x 8 KiB, + k^R tile, 8 KiB) is refilled as soon as its QK^T
+// is done, a value stage (Vx tile, 2 x 8 KiB) after its PV, which comes a softmax later.  Key
+// stages 4 and 5 reuse the query tile's shared memory once the query tile is in TMEM.
+constexpr int kAttKStages = 6, kAttVStages = 4;
+constexpr uint32_t kAttKStage = 24576, kAttVStage = 16384;
 constexpr uint32_t kAttOffQ = 0;             // Q tile: 3 chunks of 64 dims x 128 rows (48 KiB)
-constexpr uint32_t kAttOffStage = 49152;
-constexpr uint32_t kAttOffEpi = kAttOffStage + kAttStages * kAttStage;   // 8 x 2 KiB transpose buffers
-constexpr uint32_t kAttOffPm = kAttOffEpi + 16384;   // float [3][2][128]: row maxima by tile parity, then row sums
-constexpr uint32_t kAttSmem = kAttOffPm + 3072 + 1024;
+constexpr uint32_t kAttOffStage = 49152;     // key stages 0..3, then the value stages
+constexpr uint32_t kAttOffV = kAttOffStage + 4 * kAttKStage;
+constexpr int kAttWG = 2;                      // softmax warpgroups: even and odd key tiles
+constexpr int kAttOCols = 128 / kAttWG;        // O columns per softmax thread in the epilogue
+constexpr int kAttThreads = 128 + 128 * kAttWG + 32;   // warps 0-3, the softmax warpgroups, the value producer
+// the epilogue's 2 KiB transpose buffer per softmax warp lies in the ring, idle once the last PV is done
+constexpr uint32_t kAttOffEpi = kAttOffStage;
+constexpr uint32_t kAttOffPm = kAttOffV + kAttVStages * kAttVStage;   // float [3][kAttWG][128]: exchange slots
+constexpr uint32_t kAttSmem = kAttOffPm + 3 * kAttWG * 512 + 1024;
+static_assert(kAttSmem <= 232448, "within one CTA's shared memory");
+static_assert(kAttWG * 4 * 2048 <= 4 * kAttKStage, "the transpose buffers fit in the ring");
+static_assert(kAttOffQ + (kAttKStages - 4) * kAttKStage <= kAttOffStage, "key stages 4.. fit in the query tile's memory");
+__device__ __forceinline__ uint32_t att_kstage(uint32_t smem, int s) {
+  return s < 4 ? smem + kAttOffStage + s * kAttKStage : smem + kAttOffQ + (s - 4) * kAttKStage;
+}
 // TMEM columns: O [0, 128), S (two 64-key buffers) [128, 256), the query tile (A operand of
 // QK^T: 192 dims, two per column) [256, 352), P (A operand of PV: 64 keys, two buffers)
 // [352, 416).  With Q and P in TMEM both MMAs read only their B operand from shared memory.
 constexpr uint32_t kAttTmemS = 128, kAttTmemQ = 256, kAttTmemP = 352;
 constexpr float kAttRebase = 8.0f;           // rebase the row maximum when it grows by more than 2^8
 
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kAttThreads, 1)
 mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_constant__ CUtensorMap qp_map,
                   const __grid_constant__ CUtensorMap kx_map, const __grid_constant__ CUtensorMap vx_map,
                   const __grid_constant__ CUtensorMap kr_map, const ExtendParams p) {
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
-  __shared__ uint64_t full[kAttStages], empty[kAttStages], q_full, q_tmem, s_full[2], s_empty[2], p_full[2],
-      pv_done[2], drain;
+  __shared__ uint64_t kfull[kAttKStages], kempty[kAttKStages], vfull[kAttVStages], vempty[kAttVStages], q_full,
+      q_tmem, s_full[2], s_empty[2], p_full[2], pv_done[2], drain;
   __shared__ uint32_t tmem_base_s;
   const uint32_t smem = (smem_u32(dyn_smem) + 1023u) & ~1023u;
   const int qt = blockIdx.x, h = blockIdx.y;
@@ -218,21 +238,25 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
   const int see_end = min(p.n, p.qpos0 + q_last + 1 - p.c0);          // keys [0, see_end) of the chunk
   const int ntiles = see_end > 0 ? (see_end + 63) / 64 : 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kAttStages; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+    for (int s = 0; s < kAttKStages; ++s) {
+      mbar_init(smem_u32(&kfull[s]), 1);
+      mbar_init(smem_u32(&kempty[s]), 1);
+    }
+    for (int s = 0; s < kAttVStages; ++s) {
+      mbar_init(smem_u32(&vfull[s]), 1);
+      mbar_init(smem_u32(&vempty[s]), 1);
     }
     mbar_init(smem_u32(&q_full), 1);
-    mbar_init(smem_u32(&q_tmem), 8);   // the eight softmax warps, once the query tile is in TMEM
+    mbar_init(smem_u32(&q_tmem), 4 * kAttWG);   // every softmax warp, once the query tile is in TMEM
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_empty[i]), 8);   // the eight softmax warps
+      mbar_init(smem_u32(&s_empty[i]), 4);   // the four warps of the warpgroup that owns buffer i
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&p_full[i]), 8);    // the eight softmax warps
+      mbar_init(smem_u32(&p_full[i]), 4);    // the four warps of the warpgroup that owns buffer i
       mbar_init(smem_u32(&pv_done[i]), 1);
     }
-    mbar_init(smem_u32(&drain), 1);
+    mbar_init(smem_u32(&drain), 3);   // one commit from each MMA-issuing warp
     fence_mbar_init();
     prefetch_tensormap(&qn_map);
     prefetch_tensormap(&qp_map);
@@ -249,97 +273,127 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
   griddep_launch_dependents();
 
   if (warp == 0) {
-    if (lane == 0) {   // producer: the query tile once, then the chunk's key tiles through the ring
+    if (lane == 0) {   // key producer: the query tile once, then the chunk's key tiles through the key ring
       const uint32_t qb = smem_u32(&q_full);
       mbar_arrive_expect_tx(qb, 3 * 16384);
       tma_load_3d(smem + kAttOffQ, &qn_map, qb, 0, h, 128 * qt);
       tma_load_3d(smem + kAttOffQ + 16384, &qn_map, qb, 64, h, 128 * qt);
       tma_load_3d(smem + kAttOffQ + 32768, &qp_map, qb, 0, h, 128 * qt);
-      int issued_phase[kAttStages];
-      for (int s = 0; s < kAttStages; ++s) issued_phase[s] = -1;
-      bool ok = true;
-      for (int k = 0; k < ntiles && ok; ++k) {
-        const int s = k % kAttStages;
-        if (k >= kAttStages && !ext_wait(smem_u32(&empty[s]), ((k / kAttStages) - 1) & 1, p.status)) {
-          ok = false;
-          break;
+      int kphase[kAttKStages];
+      for (int s = 0; s < kAttKStages; ++s) kphase[s] = -1;
+      for (int k = 0; k < ntiles; ++k) {
+        const int s = k % kAttKStages;
+        if (k >= kAttKStages && !ext_wait(smem_u32(&kempty[s]), ((k / kAttKStages) - 1) & 1, p.status)) break;
+        if (k == 4) {   // stages 4.. are the query tile's memory: free once the softmax warps copied it to TMEM
+          if (!ext_wait(smem_u32(&q_tmem), 0, p.status)) break;
+          fence_proxy_async_smem();   // their generic-proxy reads before these async-proxy writes
         }
         int blk = __ldg(p.block_row + (p.c0 / kPageTokens) + k);
         if (blk < 0 || blk >= p.num_blocks) {
           atomicCAS(p.status, 0, MLA_ERR_DEVICE_BOUNDS);
           blk = static_cast<int>(p.num_blocks);   // out of range: the TMA fills the tile with zeros
         }
-        const uint32_t st = smem + kAttOffStage + s * kAttStage;
-        const uint32_t bar = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(bar, kAttStage);
+        const uint32_t st = att_kstage(smem, s);
+        const uint32_t bar = smem_u32(&kfull[s]);
+        mbar_arrive_expect_tx(bar, kAttKStage);
         tma_load_3d(st, &kx_map, bar, 0, 64 * k, h);
         tma_load_3d(st + 8192, &kx_map, bar, 64, 64 * k, h);
         tma_load_3d(st + 16384, &kr_map, bar, 0, blk * kPageTokens, kDimV / 64);   // k^R: cache dims 512..575
-        tma_load_3d(st + 24576, &vx_map, bar, 0, 64 * k, h);
-        tma_load_3d(st + 32768, &vx_map, bar, 64, 64 * k, h);
-        issued_phase[s] = (k / kAttStages) & 1;
+        kphase[s] = (k / kAttKStages) & 1;
       }
       ext_wait(qb, 0, p.status);   // loads in flight land before the CTA may exit
-      for (int s = 0; s < kAttStages; ++s)
-        if (issued_phase[s] >= 0) ext_wait(smem_u32(&full[s]), static_cast<uint32_t>(issued_phase[s]), p.status);
+      for (int s = 0; s < kAttKStages; ++s)
+        if (kphase[s] >= 0) ext_wait(smem_u32(&kfull[s]), static_cast<uint32_t>(kphase[s]), p.status);
     }
-  } else if (warp == 1) {   // MMA issue (one elected lane), QK^T of tile k ahead of PV of tile k - 1
+  } else if (warp == 1 || warp == 2) {   // QK^T issue (one elected lane), warp 1 the even tiles, warp 2 the odd
+    // S = Q K^T of tile k into S buffer k % 2, once the tile is loaded and the softmax has read
+    // tile k - 2 out of that buffer.  QK^T (two warps, one per S buffer) and PV (a third) are
+    // issued apart: they share no accumulator, and each warp's waits and commits then overlap
+    // the others' MMAs.
     constexpr uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
-    constexpr uint32_t id_o = idesc_bf16_f32(128, 128, 0, 1);
     bool ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&q_tmem), 0, p.status));
     tc_fence_after();
-    auto pv = [&](int k) {   // O += P V for tile k, P from TMEM buffer k % 2
-      if (!__all_sync(0xffffffffu, ext_wait(smem_u32(&p_full[k & 1]), (k >> 1) & 1, p.status))) return false;
-      tc_fence_after();
-      const uint32_t st = smem + kAttOffStage + (k % kAttStages) * kAttStage;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_bf16_ts_warp(tmem, tmem + kAttTmemP + (k & 1) * 32 + kk * 8,
-                         smem_desc_sw128(st + 24576 + kk * 2048, 8192, 1024), id_o, (k | kk) ? 1u : 0u);
-      mma_commit_warp(smem_u32(&empty[k % kAttStages]));
-      mma_commit_warp(smem_u32(&pv_done[k & 1]));
-      return true;
-    };
-    for (int k = 0; k < ntiles && ok; ++k) {
-      const int s = k % kAttStages;
+    for (int k = warp - 1; k < ntiles && ok; k += 2) {
+      const int s = k % kAttKStages;
       const uint32_t sb = k & 1;
-      ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&full[s]), (k / kAttStages) & 1, p.status)) &&
+      ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&kfull[s]), (k / kAttKStages) & 1, p.status)) &&
            __all_sync(0xffffffffu, ext_wait(smem_u32(&s_empty[sb]), ((k >> 1) & 1) ^ 1, p.status));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t st = smem + kAttOffStage + s * kAttStage;
+      const uint64_t dk = smem_desc_sw128(att_kstage(smem, s), 16, 1024);
+      const uint32_t sd = tmem + kAttTmemS + sb * 64;
 #pragma unroll
       for (int c = 0; c < 3; ++c)   // q_nope . Kx (two 64-dim chunks), q_pe . k^R
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ts_warp(tmem + kAttTmemS + sb * 64, tmem + kAttTmemQ + c * 32 + kk * 8,
-                           smem_desc_sw128(st + c * 8192 + kk * 32, 16, 1024), id_s, (c | kk) ? 1u : 0u);
+          mma_bf16_ts_warp(sd, tmem + kAttTmemQ + c * 32 + kk * 8, dk + ((c * 8192 + kk * 32) >> 4), id_s,
+                           (c | kk) ? 1u : 0u);
+      mma_commit_warp(smem_u32(&kempty[s]));
       mma_commit_warp(smem_u32(&s_full[sb]));
-      if (k > 0 && !pv(k - 1)) ok = false;
     }
-    if (ok && ntiles > 0) pv(ntiles - 1);
-    // every MMA issued so far is done before the CTA may free TMEM (also after a failure)
+    // this warp's MMAs are done before the CTA may free TMEM (also after a failure)
     mma_commit_warp(smem_u32(&drain));
     ext_wait(smem_u32(&drain), 0, p.status);
-  } else if (warp >= 4) {   // softmax and epilogue: two warpgroups, one thread per query row each
-    // warpgroup wg takes keys [32 wg, 32 wg + 32) of every tile and O columns [64 wg, 64 wg + 64);
-    // the two agree on the row maximum (and so on every rebase) through pm[][] and named
-    // barrier 1, and add their partial row sums at the end
+  } else if (warp == 3) {   // PV issue (one elected lane): O += P V for tile k, P from TMEM buffer k % 2
+    constexpr uint32_t id_o = idesc_bf16_f32(128, 128, 0, 1);
+    bool ok = true;
+    for (int k = 0; k < ntiles && ok; ++k) {
+      const int s = k % kAttVStages;
+      ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&p_full[k & 1]), (k >> 1) & 1, p.status)) &&
+           __all_sync(0xffffffffu, ext_wait(smem_u32(&vfull[s]), (k / kAttVStages) & 1, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t dv = smem_desc_sw128(smem + kAttOffV + s * kAttVStage, 8192, 1024);
+      const uint32_t pa = tmem + kAttTmemP + (k & 1) * 32;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16_ts_warp(tmem, pa + kk * 8, dv + (kk * 2048 >> 4), id_o, (k | kk) ? 1u : 0u);
+      mma_commit_warp(smem_u32(&vempty[s]));
+      mma_commit_warp(smem_u32(&pv_done[k & 1]));
+    }
+    mma_commit_warp(smem_u32(&drain));
+    ext_wait(smem_u32(&drain), 0, p.status);
+  } else if (warp == 4 + 4 * kAttWG) {
+    if (lane == 0) {   // value producer: the chunk's value tiles through the value ring
+      int vphase[kAttVStages];
+      for (int s = 0; s < kAttVStages; ++s) vphase[s] = -1;
+      for (int k = 0; k < ntiles; ++k) {
+        const int s = k % kAttVStages;
+        if (k >= kAttVStages && !ext_wait(smem_u32(&vempty[s]), ((k / kAttVStages) - 1) & 1, p.status)) break;
+        const uint32_t st = smem + kAttOffV + s * kAttVStage;
+        const uint32_t bar = smem_u32(&vfull[s]);
+        mbar_arrive_expect_tx(bar, kAttVStage);
+        tma_load_3d(st, &vx_map, bar, 0, 64 * k, h);
+        tma_load_3d(st + 8192, &vx_map, bar, 64, 64 * k, h);
+        vphase[s] = (k / kAttVStages) & 1;
+      }
+      for (int s = 0; s < kAttVStages; ++s)   // loads in flight land before the CTA may exit
+        if (vphase[s] >= 0) ext_wait(smem_u32(&vfull[s]), static_cast<uint32_t>(vphase[s]), p.status);
+    }
+  } else if (warp >= 4 && warp < 4 + 4 * kAttWG) {   // softmax and epilogue: two warpgroups, one thread per query row each
+    // Warpgroup wg takes the key tiles k with k % 2 == wg whole (S buffer and P buffer wg), so
+    // that the two run their tiles' softmax side by side.  The online softmax's one serial
+    // dependency, the reference maximum, passes from tile k - 1 to tile k through a slot per
+    // warpgroup and a named barrier per direction (2 + g: "warpgroup g has published"), taken
+    // bar.arrive by the publisher and bar.sync by the other.  Every tile's barrier operations are
+    // executed whatever happened before (a failed wait only skips the work), so neither side
+    // can be left waiting.  The reference maximum only moves when a tile's maximum exceeds it
+    // by more than 2^kAttRebase; the warpgroup whose tile moves it rescales O (after the PV of
+    // tile k - 1), and each warpgroup rescales its own partial row sum when it sees it move.
+    constexpr uint32_t kST = 128 * kAttWG;           // softmax threads
     const int t = threadIdx.x - 128, wg = t >> 7, r = t & 127, wq = r >> 5;
     const int q = 128 * qt + r;                      // query row within the request
     const int qpos = p.qpos0 + q;                    // its position
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    // exchange slot j of this warpgroup / of the other one; j = tile parity in the loop, 2 after
-    // it (with one barrier per tile a warpgroup writes slot k % 2 again only after the other
-    // has passed the next barrier, i.e. after it read that slot)
-    const auto pm_mine = [&](int j) { return smem + kAttOffPm + ((j * 2 + wg) * 128 + r) * 4; };
-    const auto pm_other = [&](int j) { return smem + kAttOffPm + ((j * 2 + 1 - wg) * 128 + r) * 4; };
-    float m = -INFINITY, l = 0.f;                    // reference maximum (log2 units), this half's row sum
+    // slot j of warpgroup g: j = 0 the reference maximum it published last, j = 1 / 2 its
+    // reference and row sum after the loop
+    const auto pm = [&](int j, int g) { return smem + kAttOffPm + ((j * kAttWG + g) * 128 + r) * 4; };
+    float m = -INFINITY, l = 0.f;   // this warpgroup's reference maximum (log2 units) and row sum over its tiles
     // the query tile into TMEM: row r's 192 dims (three 128-byte swizzled chunks) as 96
-    // columns of bf16 pairs (warpgroup 0: q_nope, warpgroup 1: q_pe)
+    // columns of bf16 pairs, chunk c by warpgroup c % kAttWG
     bool ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&q_full), 0, p.status));
     if (ok) {
-      for (int c = wg == 0 ? 0 : 2; c < (wg == 0 ? 2 : 3); ++c) {
+      for (int c = wg; c < 3; c += kAttWG) {
         uint32_t v[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -353,56 +407,62 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&q_tmem));   // arrives even after a failure: the MMA warp's wait ends
-    // Every exit from the loop is taken by all eight warps together, after a barrier that
-    // folds in each warp's wait results (a warp leaving alone would strand the others there).
-    for (int k = 0; k < ntiles; ++k) {
-      const uint32_t sb = k & 1;
-      const bool got = __all_sync(0xffffffffu, ok && ext_wait(smem_u32(&s_full[sb]), (k >> 1) & 1, p.status));
-      float x[32];
-      if (got) {
+    const uint32_t sb = wg;                          // this warpgroup's S and P buffers
+    for (int k = wg; k < ntiles; k += 2) {
+      const uint32_t ph = (k >> 1) & 1;              // phase of this warpgroup's buffers for tile k
+      ok = __all_sync(0xffffffffu, ok && ext_wait(smem_u32(&s_full[sb]), ph, p.status));
+      float x[64];
+      if (ok) {
         tc_fence_after();
-        tmem_ld32(tl + kAttTmemS + sb * 64 + wg * 32, *reinterpret_cast<uint32_t(*)[32]>(x));
+        tmem_ld32(tl + kAttTmemS + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(x));
+        tmem_ld32(tl + kAttTmemS + sb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&s_empty[sb]));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = -INFINITY;
       }
       // the keys a row sees form a prefix of the tile: inside the chunk and at or before
       // this query's position
       const int t0 = p.c0 + 64 * k;
-      const int nvis = q < p.T ? min(p.n - 64 * k, qpos - t0 + 1) : 0;
-      const int nvalid = nvis - 32 * wg;                // of this warpgroup's 32 keys
-      if (nvalid < 32) {
+      const int nvis = (ok && q < p.T) ? min(p.n - 64 * k, qpos - t0 + 1) : 0;
+      if (nvis < 64) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = j < nvalid ? x[j] : -INFINITY;
+        for (int j = 0; j < 64; ++j) x[j] = j < nvis ? x[j] : -INFINITY;
       }
-      float rmax = x[0];
+      float mx[32];   // the row maximum by a tree
 #pragma unroll
-      for (int j = 1; j < 32; ++j) rmax = fmaxf(rmax, x[j]);
-      asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine(k & 1)), "f"(rmax) : "memory");
-      // P buffer k % 2 is free once the PV of tile k - 2 (which read it) is done
-      bool go = got;
-      if (go && k > 1 && !ext_wait(smem_u32(&pv_done[k & 1]), ((k >> 1) & 1) ^ 1, p.status)) go = false;
-      // one barrier both exchanges the row maxima and makes the abort decision uniform
-      if (named_bar_or(1, 256, !go)) { ok = false; break; }
+      for (int j = 0; j < 32; ++j) mx[j] = fmaxf(x[2 * j], x[2 * j + 1]);
+#pragma unroll
+      for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
+      // the reference maximum after tile k - 1, from the other warpgroup
+      float m_in = -INFINITY;
+      if (k > 0) {
+        named_bar_sync(2 + (wg ^ 1), kST);
+        m_in = ld_shared_f32(pm(0, wg ^ 1));
+      }
       // softmax_scale > 0, so the scaled maximum is the scaled raw maximum
-      const float m_new = fmaxf(m, fmaxf(rmax, ld_shared_f32(pm_other(k & 1))) * p.scale_log2);
-      if (m_new > m + kAttRebase) {   // rebase: O and l scale by 2^(m - m_new) (0 when m = -inf)
-        const float alpha = fast_exp2(m - m_new);
-        l *= alpha;
-        // O holds every earlier tile once the PV of tile k - 1 is done (the MMAs complete in order);
-        // a failed wait is carried to the next barrier (or the one after the loop)
-        if (k > 0 && !__all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[(k - 1) & 1]), ((k - 1) >> 1) & 1,
-                                                        p.status))) {
-          ok = false;
-        }
-        if (k > 0 && ok) {
+      const float cand = mx[0] * p.scale_log2;
+      const float m_k = cand > m_in + kAttRebase ? cand : m_in;   // the reference for tile k
+      if (k + 1 < ntiles) {
+        asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm(0, wg)), "f"(m_k) : "memory");
+        named_bar_arrive(2 + wg, kST);
+      }
+      if (m_k != m) {   // m_k > m: this warpgroup's row sum moves to the new reference (0 when m = -inf)
+        l *= fast_exp2(m - m_k);
+        m = m_k;
+      }
+      if (ok && m_k != m_in && k > 0 && m_in != -INFINITY) {
+        // this tile moves the reference: O (every earlier tile, once the PV of tile k - 1 is
+        // done; the MMAs complete in order) scales by 2^(m_in - m_k).  With m_in = -inf every
+        // earlier P was 0, and so is O.
+        const float alpha = fast_exp2(m_in - m_k);
+        ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[(k - 1) & 1]), ((k - 1) >> 1) & 1, p.status));
+        if (ok) {
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 64 * wg; c < 64 * wg + 64; c += 32) {
+          for (int c = 0; c < 128; c += 32) {
             uint32_t v[32];
             tmem_ld32(tl + c, v);
             tmem_wait_ld();
@@ -412,34 +472,44 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
           }
           tmem_wait_st();
         }
-        m = m_new;
       }
-      const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t w[16];   // P of this half's 32 keys as bf16 pairs (2^x of -inf is +0)
+      // P buffer sb is free once the PV of tile k - 2 (which read it) is done
+      if (ok && k > 1) ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[sb]), ph ^ 1, p.status));
+      if (ok) {
+        const float neg_m = (m_k == -INFINITY) ? 0.f : -m_k;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t w[32];   // P of the tile's 64 keys as bf16 pairs (2^x of -inf is +0)
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float a = fast_exp2(fmaf(x[2 * e], p.scale_log2, neg_m));
-        const float b = fast_exp2(fmaf(x[2 * e + 1], p.scale_log2, neg_m));
-        ps[e & 3] += a + b;
-        w[e] = pack_bf16x2(a, b);
+        for (int e = 0; e < 32; ++e) {
+          const float a = fast_exp2(fmaf(x[2 * e], p.scale_log2, neg_m));
+          const float b = fast_exp2(fmaf(x[2 * e + 1], p.scale_log2, neg_m));
+          ps[e & 3] += a + b;
+          w[e] = pack_bf16x2(a, b);
+        }
+        tmem_st32(tl + kAttTmemP + sb * 32, w);
+        tmem_wait_st();
+        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&p_full[sb]));
       }
-      tmem_st16(tl + kAttTmemP + (k & 1) * 32 + wg * 16, w);
-      tmem_wait_st();
-      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_full[k & 1]));
     }
     if (ok && ntiles > 0)
       ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[(ntiles - 1) & 1]), ((ntiles - 1) >> 1) & 1, p.status));
-    // the row sum over both halves (the barrier also settles whether every warp finished)
-    asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm_mine(2)), "f"(l) : "memory");
-    ok = !named_bar_or(1, 256, !ok);
-    l += ld_shared_f32(pm_other(2));
+    // the two row sums at the later (larger) reference, which is O's (the barrier also settles
+    // whether every warp finished)
+    asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm(1, wg)), "f"(m) : "memory");
+    asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm(2, wg)), "f"(l) : "memory");
+    ok = !named_bar_or(1, kST, !ok);
+    {
+      const float m_o = ld_shared_f32(pm(1, wg ^ 1)), l_o = ld_shared_f32(pm(2, wg ^ 1));
+      const float m_f = fmaxf(m, m_o);
+      if (m_f != -INFINITY) l = l * fast_exp2(m - m_f) + l_o * fast_exp2(m_o - m_f);
+      m = m_f;
+    }
     tc_fence_after();
     // epilogue: the chunk's o = O / l and lse, merged into the running accumulator by LSE;
-    // warpgroup wg writes O columns [64 wg, 64 wg + 64)
+    // warpgroup wg writes O columns [kAttOCols wg, kAttOCols (wg + 1))
     const bool row_ok = ok && q < p.T;
     const float lse_c = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
@@ -454,7 +524,7 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
     const float lse_new = z > 0.f ? M + logf(z) : -INFINITY;
     const uint32_t stg = smem + kAttOffEpi + (wg * 4 + wq) * 2048u;
     const int qw0 = 128 * qt + wq * 32;
-    for (int c = 64 * wg; c < 64 * wg + 64; c += 32) {
+    for (int c = kAttOCols * wg; c < kAttOCols * (wg + 1); c += 32) {
       uint32_t v[32];
       if (ntiles > 0) {
         tmem_ld32(tl + c, v);
@@ -515,7 +585,7 @@ cudaError_t launch_extend_chunk(const ExtendMaps& maps, const ExtendParams& p, c
     if (e != cudaSuccess) return e;
   }
   const cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>((p.T + 127) / 128), static_cast<unsigned>(p.H)),
-                                            dim3(384), kAttSmem, stream, attr);
+                                            dim3(kAttThreads), kAttSmem, stream, attr);
   return cudaLaunchKernelEx(&cfg, mla_attend_kernel, maps.qn, maps.qp, maps.kx, maps.vx, maps.kr, p);
 }
 
