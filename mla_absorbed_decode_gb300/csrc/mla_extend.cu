@@ -29,6 +29,11 @@ namespace {
 
 constexpr uint64_t kExtTimeoutNs = 500ull * 1000 * 1000;
 
+// Arrive on a named barrier without waiting (the producer side of a bar.arrive / bar.sync pair).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __noinline__ bool ext_wait_slow(uint32_t bar, uint32_t parity, int* status) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_test(bar, parity)) {
