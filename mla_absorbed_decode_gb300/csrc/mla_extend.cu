@@ -208,8 +208,7 @@ constexpr uint32_t kAttKStage = 24576, kAttVStage = 16384;
 constexpr uint32_t kAttOffQ = 0;             // Q tile: 3 chunks of 64 dims x 128 rows (48 KiB)
 constexpr uint32_t kAttOffStage = 49152;     // key stages 0..3, then the value stages
 constexpr uint32_t kAttOffV = kAttOffStage + 4 * kAttKStage;
-constexpr int kAttWG = 2;                      // softmax warpgroups: even and odd key tiles
-constexpr int kAttOCols = 128 / kAttWG;        // O columns per softmax thread in the epilogue
+constexpr int kAttWG = 2;                      // softmax warpgroups: warpgroup g takes the key tiles k = g mod kAttWG
 constexpr int kAttThreads = 128 + 128 * kAttWG + 32;   // warps 0-3, the softmax warpgroups, the value producer
 // the epilogue's 2 KiB transpose buffer per softmax warp lies in the ring, idle once the last PV is done
 constexpr uint32_t kAttOffEpi = kAttOffStage;
@@ -221,10 +220,12 @@ static_assert(kAttOffQ + (kAttKStages - 4) * kAttKStage <= kAttOffStage, "key st
 __device__ __forceinline__ uint32_t att_kstage(uint32_t smem, int s) {
   return s < 4 ? smem + kAttOffStage + s * kAttKStage : smem + kAttOffQ + (s - 4) * kAttKStage;
 }
-// TMEM columns: O [0, 128), S (two 64-key buffers) [128, 256), the query tile (A operand of
-// QK^T: 192 dims, two per column) [256, 352), P (A operand of PV: 64 keys, two buffers)
-// [352, 416).  With Q and P in TMEM both MMAs read only their B operand from shared memory.
-constexpr uint32_t kAttTmemS = 128, kAttTmemQ = 256, kAttTmemP = 352;
+// TMEM columns: O [0, 128), S (a 64-key buffer per softmax warpgroup), the query tile (A
+// operand of QK^T: 192 dims, two per column, 96 columns), P (A operand of PV: 64 keys, a
+// 32-column buffer per warpgroup).  With Q and P in TMEM both MMAs read only their B operand
+// from shared memory.
+constexpr uint32_t kAttTmemS = 128, kAttTmemQ = kAttTmemS + 64 * kAttWG, kAttTmemP = kAttTmemQ + 96;
+static_assert(kAttTmemP + 32 * kAttWG <= 512, "O, S, Q and P fit in TMEM");
 constexpr float kAttRebase = 8.0f;           // rebase the row maximum when it grows by more than 2^8
 
 __global__ void __launch_bounds__(kAttThreads, 1)
@@ -233,7 +234,7 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
                   const __grid_constant__ CUtensorMap kr_map, const ExtendParams p) {
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   __shared__ uint64_t kfull[kAttKStages], kempty[kAttKStages], vfull[kAttVStages], vempty[kAttVStages], q_full,
-      q_tmem, s_full[2], s_empty[2], p_full[2], pv_done[2], drain;
+      q_tmem, s_full[kAttWG], s_empty[kAttWG], p_full[kAttWG], pv_done[kAttWG], drain;
   __shared__ uint32_t tmem_base_s;
   const uint32_t smem = (smem_u32(dyn_smem) + 1023u) & ~1023u;
   const int qt = blockIdx.x, h = blockIdx.y;
@@ -253,11 +254,11 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
     }
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&q_tmem), 4 * kAttWG);   // every softmax warp, once the query tile is in TMEM
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kAttWG; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_empty[i]), 4);   // the four warps of the warpgroup that owns buffer i
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kAttWG; ++i) {
       mbar_init(smem_u32(&p_full[i]), 4);    // the four warps of the warpgroup that owns buffer i
       mbar_init(smem_u32(&pv_done[i]), 1);
     }
@@ -311,18 +312,18 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
         if (kphase[s] >= 0) ext_wait(smem_u32(&kfull[s]), static_cast<uint32_t>(kphase[s]), p.status);
     }
   } else if (warp == 1 || warp == 2) {   // QK^T issue (one elected lane), warp 1 the even tiles, warp 2 the odd
-    // S = Q K^T of tile k into S buffer k % 2, once the tile is loaded and the softmax has read
-    // tile k - 2 out of that buffer.  QK^T (two warps, one per S buffer) and PV (a third) are
-    // issued apart: they share no accumulator, and each warp's waits and commits then overlap
-    // the others' MMAs.
+    // S = Q K^T of tile k into S buffer k % kAttWG, once the tile is loaded and the softmax has
+    // read tile k - kAttWG out of that buffer.  QK^T (two warps) and PV (a third) are issued
+    // apart: they share no accumulator, and each warp's waits and commits then overlap the
+    // others' MMAs.
     constexpr uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
     bool ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&q_tmem), 0, p.status));
     tc_fence_after();
     for (int k = warp - 1; k < ntiles && ok; k += 2) {
       const int s = k % kAttKStages;
-      const uint32_t sb = k & 1;
+      const uint32_t sb = k % kAttWG;
       ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&kfull[s]), (k / kAttKStages) & 1, p.status)) &&
-           __all_sync(0xffffffffu, ext_wait(smem_u32(&s_empty[sb]), ((k >> 1) & 1) ^ 1, p.status));
+           __all_sync(0xffffffffu, ext_wait(smem_u32(&s_empty[sb]), ((k / kAttWG) & 1) ^ 1, p.status));
       if (!ok) break;
       tc_fence_after();
       const uint64_t dk = smem_desc_sw128(att_kstage(smem, s), 16, 1024);
@@ -339,22 +340,23 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
     // this warp's MMAs are done before the CTA may free TMEM (also after a failure)
     mma_commit_warp(smem_u32(&drain));
     ext_wait(smem_u32(&drain), 0, p.status);
-  } else if (warp == 3) {   // PV issue (one elected lane): O += P V for tile k, P from TMEM buffer k % 2
+  } else if (warp == 3) {   // PV issue (one elected lane): O += P V for tile k, P from TMEM buffer k % kAttWG
     constexpr uint32_t id_o = idesc_bf16_f32(128, 128, 0, 1);
     bool ok = true;
     for (int k = 0; k < ntiles && ok; ++k) {
       const int s = k % kAttVStages;
-      ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&p_full[k & 1]), (k >> 1) & 1, p.status)) &&
+      const int b = k % kAttWG;
+      ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&p_full[b]), (k / kAttWG) & 1, p.status)) &&
            __all_sync(0xffffffffu, ext_wait(smem_u32(&vfull[s]), (k / kAttVStages) & 1, p.status));
       if (!ok) break;
       tc_fence_after();
       const uint64_t dv = smem_desc_sw128(smem + kAttOffV + s * kAttVStage, 8192, 1024);
-      const uint32_t pa = tmem + kAttTmemP + (k & 1) * 32;
+      const uint32_t pa = tmem + kAttTmemP + b * 32;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         mma_bf16_ts_warp(tmem, pa + kk * 8, dv + (kk * 2048 >> 4), id_o, (k | kk) ? 1u : 0u);
       mma_commit_warp(smem_u32(&vempty[s]));
-      mma_commit_warp(smem_u32(&pv_done[k & 1]));
+      mma_commit_warp(smem_u32(&pv_done[b]));
     }
     mma_commit_warp(smem_u32(&drain));
     ext_wait(smem_u32(&drain), 0, p.status);
@@ -375,12 +377,12 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
       for (int s = 0; s < kAttVStages; ++s)   // loads in flight land before the CTA may exit
         if (vphase[s] >= 0) ext_wait(smem_u32(&vfull[s]), static_cast<uint32_t>(vphase[s]), p.status);
     }
-  } else if (warp >= 4 && warp < 4 + 4 * kAttWG) {   // softmax and epilogue: two warpgroups, one thread per query row each
-    // Warpgroup wg takes the key tiles k with k % 2 == wg whole (S buffer and P buffer wg), so
-    // that the two run their tiles' softmax side by side.  The online softmax's one serial
-    // dependency, the reference maximum, passes from tile k - 1 to tile k through a slot per
-    // warpgroup and a named barrier per direction (2 + g: "warpgroup g has published"), taken
-    // bar.arrive by the publisher and bar.sync by the other.  Every tile's barrier operations are
+  } else if (warp >= 4 && warp < 4 + 4 * kAttWG) {   // softmax and epilogue: kAttWG warpgroups, a thread per query row each
+    // Warpgroup wg takes the key tiles k with k % kAttWG == wg whole (S buffer and P buffer wg),
+    // so that the warpgroups run their tiles' softmax side by side.  The online softmax's one
+    // serial dependency, the reference maximum, passes from tile k - 1 to tile k through a slot
+    // per warpgroup and a named barrier per warpgroup (2 + g: "warpgroup g has published"),
+    // taken bar.arrive by the publisher and bar.sync by the next warpgroup.  Every tile's barrier operations are
     // executed whatever happened before (a failed wait only skips the work), so neither side
     // can be left waiting.  The reference maximum only moves when a tile's maximum exceeds it
     // by more than 2^kAttRebase; the warpgroup whose tile moves it rescales O (after the PV of
@@ -413,8 +415,9 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&q_tmem));   // arrives even after a failure: the MMA warp's wait ends
     const uint32_t sb = wg;                          // this warpgroup's S and P buffers
-    for (int k = wg; k < ntiles; k += 2) {
-      const uint32_t ph = (k >> 1) & 1;              // phase of this warpgroup's buffers for tile k
+    const int prev = (wg + kAttWG - 1) % kAttWG;     // the warpgroup of the tile before
+    for (int k = wg; k < ntiles; k += kAttWG) {
+      const uint32_t ph = (k / kAttWG) & 1;          // phase of this warpgroup's buffers for tile k
       ok = __all_sync(0xffffffffu, ok && ext_wait(smem_u32(&s_full[sb]), ph, p.status));
       float x[64];
       if (ok) {
@@ -441,18 +444,18 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
       for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
         for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
-      // the reference maximum after tile k - 1, from the other warpgroup
+      // the reference maximum after tile k - 1, from the warpgroup before
       float m_in = -INFINITY;
       if (k > 0) {
-        named_bar_sync(2 + (wg ^ 1), kST);
-        m_in = ld_shared_f32(pm(0, wg ^ 1));
+        named_bar_sync(2 + prev, 256);
+        m_in = ld_shared_f32(pm(0, prev));
       }
       // softmax_scale > 0, so the scaled maximum is the scaled raw maximum
       const float cand = mx[0] * p.scale_log2;
       const float m_k = cand > m_in + kAttRebase ? cand : m_in;   // the reference for tile k
       if (k + 1 < ntiles) {
         asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm(0, wg)), "f"(m_k) : "memory");
-        named_bar_arrive(2 + wg, kST);
+        named_bar_arrive(2 + wg, 256);
       }
       if (m_k != m) {   // m_k > m: this warpgroup's row sum moves to the new reference (0 when m = -inf)
         l *= fast_exp2(m - m_k);
@@ -463,7 +466,8 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
         // done; the MMAs complete in order) scales by 2^(m_in - m_k).  With m_in = -inf every
         // earlier P was 0, and so is O.
         const float alpha = fast_exp2(m_in - m_k);
-        ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[(k - 1) & 1]), ((k - 1) >> 1) & 1, p.status));
+        ok = __all_sync(0xffffffffu,
+                        ext_wait(smem_u32(&pv_done[(k - 1) % kAttWG]), ((k - 1) / kAttWG) & 1, p.status));
         if (ok) {
           tc_fence_after();
 #pragma unroll 1
@@ -478,20 +482,23 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
           tmem_wait_st();
         }
       }
-      // P buffer sb is free once the PV of tile k - 2 (which read it) is done
-      if (ok && k > 1) ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[sb]), ph ^ 1, p.status));
+      // P buffer sb is free once the PV of tile k - kAttWG (which read it) is done
+      if (ok && k >= kAttWG) ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[sb]), ph ^ 1, p.status));
       if (ok) {
         const float neg_m = (m_k == -INFINITY) ? 0.f : -m_k;
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t w[32];   // P of the tile's 64 keys as bf16 pairs (2^x of -inf is +0)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float a = fast_exp2(fmaf(x[2 * e], p.scale_log2, neg_m));
-          const float b = fast_exp2(fmaf(x[2 * e + 1], p.scale_log2, neg_m));
-          ps[e & 3] += a + b;
-          w[e] = pack_bf16x2(a, b);
+        for (int hf = 0; hf < 2; ++hf) {   // P of the tile's 64 keys as bf16 pairs, 32 keys at a time
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a = fast_exp2(fmaf(x[32 * hf + 2 * e], p.scale_log2, neg_m));   // 2^-inf = +0
+            const float b = fast_exp2(fmaf(x[32 * hf + 2 * e + 1], p.scale_log2, neg_m));
+            ps[e & 3] += a + b;
+            w[e] = pack_bf16x2(a, b);
+          }
+          tmem_st16(tl + kAttTmemP + sb * 32 + 16 * hf, w);
         }
-        tmem_st32(tl + kAttTmemP + sb * 32, w);
         tmem_wait_st();
         l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         tc_fence_before();
@@ -500,21 +507,28 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
       }
     }
     if (ok && ntiles > 0)
-      ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[(ntiles - 1) & 1]), ((ntiles - 1) >> 1) & 1, p.status));
-    // the two row sums at the later (larger) reference, which is O's (the barrier also settles
-    // whether every warp finished)
+      ok = __all_sync(0xffffffffu, ext_wait(smem_u32(&pv_done[(ntiles - 1) % kAttWG]), ((ntiles - 1) / kAttWG) & 1,
+                                            p.status));
+    // the row sums at the largest reference, which is O's (the barrier also settles whether
+    // every warp finished)
     asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm(1, wg)), "f"(m) : "memory");
     asm volatile("st.shared.f32 [%0], %1;" :: "r"(pm(2, wg)), "f"(l) : "memory");
     ok = !named_bar_or(1, kST, !ok);
     {
-      const float m_o = ld_shared_f32(pm(1, wg ^ 1)), l_o = ld_shared_f32(pm(2, wg ^ 1));
-      const float m_f = fmaxf(m, m_o);
-      if (m_f != -INFINITY) l = l * fast_exp2(m - m_f) + l_o * fast_exp2(m_o - m_f);
+      float m_f = m;
+#pragma unroll
+      for (int g = 0; g < kAttWG; ++g) m_f = fmaxf(m_f, ld_shared_f32(pm(1, g)));
+      if (m_f != -INFINITY) {
+        float l_f = 0.f;
+#pragma unroll
+        for (int g = 0; g < kAttWG; ++g) l_f += ld_shared_f32(pm(2, g)) * fast_exp2(ld_shared_f32(pm(1, g)) - m_f);
+        l = l_f;
+      }
       m = m_f;
     }
     tc_fence_after();
     // epilogue: the chunk's o = O / l and lse, merged into the running accumulator by LSE;
-    // warpgroup wg writes O columns [kAttOCols wg, kAttOCols (wg + 1))
+    // warpgroup wg writes the 32-column chunks c = wg mod kAttWG of O
     const bool row_ok = ok && q < p.T;
     const float lse_c = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
@@ -529,7 +543,7 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
     const float lse_new = z > 0.f ? M + logf(z) : -INFINITY;
     const uint32_t stg = smem + kAttOffEpi + (wg * 4 + wq) * 2048u;
     const int qw0 = 128 * qt + wq * 32;
-    for (int c = kAttOCols * wg; c < kAttOCols * (wg + 1); c += 32) {
+    for (int c = 32 * wg; c < 128; c += 32 * kAttWG) {
       uint32_t v[32];
       if (ntiles > 0) {
         tmem_ld32(tl + c, v);
