@@ -180,7 +180,11 @@ mla_status_t mla_decode_sparse_fp8(const mla_bf16_t* q, const uint8_t* kv_cache,
  *          (>= H*64, multiple of 8)
  *  w_uk    [H, 128, 512] bf16
  *  q       [N, H, 576] bf16 (the decode q, N = B*s_q)
- * Async on stream. */
+ * Async on stream.  The kernel is launched with programmatic stream serialization and
+ * starts loading the weights before the previous kernel on the stream has finished (the
+ * activations only after): the weights must not be written by the work queued just
+ * before the call on the same stream (put an event or a synchronization in between if
+ * they are).  The same holds for every absorption / un-absorption call below. */
 mla_status_t mla_absorb_q(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, const mla_bf16_t* q_pe,
                           int64_t q_pe_row_stride, const mla_bf16_t* w_uk, mla_bf16_t* q, int N, int H,
                           mla_stream_t stream);

@@ -151,12 +151,18 @@ uint32_t bmm_smem_bytes() {
   return STAGES * bmm_stage_bytes<K, NT, STAGES>() + 1024;
 }
 
-__device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity) {
+__device__ __noinline__ bool bmm_wait_slow(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_test(bar, parity)) {
     if (global_timer_ns() - t0 > 500000000ull) return false;
   }
   return true;
+}
+// Bounded wait (0.5 s).  The phase is tested once before the clock is read: reading the
+// global timer costs hundreds of cycles, which a wait that is already satisfied should not pay.
+__device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
+  return bmm_wait_slow(bar, parity);
 }
 
 template <int K, int NT, int STAGES>
@@ -200,8 +206,8 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
     prefetch_tensormap(&a_map);
     prefetch_tensormap(&w_map);
     // this head's weight matrix (K x 512 or 512 x 128 bf16, 128 KiB) into L2 while the
-    // previous kernel of the stream may still run: only a prefetch, the TMA loads that use
-    // it come after griddepcontrol.wait (one CTA per head issues it)
+    // previous kernel of the stream may still run, for the chunks past the ring (one CTA
+    // per head issues it)
     if (p.w != nullptr && n0 == 0 && m0 == 0)
       prefetch_l2(p.w + static_cast<int64_t>(h) * K * (K == 128 ? 512 : 128), static_cast<uint32_t>(K) * (K == 128 ? 512 : 128) * 2);
   }
@@ -210,26 +216,33 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  griddep_wait();
-  griddep_launch_dependents();
 
-  // producer (warp 0, lane 0): K chunks through the ring; the chunks that fit the
-  // ring at once are issued first, before anything else of the CTA
+  // producer (warp 0, lane 0): K chunks through the ring.  The weights are not written by
+  // the previous kernel of the stream, so the chunks that fit the ring at once have their
+  // weight parts issued before griddepcontrol.wait, overlapping that kernel's tail; the
+  // activations (A) follow once it is done.
   int last_phase[STAGES];
   for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
-  auto issue = [&](int c) {
+  auto issue_w = [&](int c) {   // expects the whole stage, loads its weight part
     const int s = c % STAGES;
     const uint32_t st = smem + s * kSB;
     const uint32_t bar = smem_u32(&full[s]);
     mbar_arrive_expect_tx(bar, kSB);
-    tma_load_3d(st, &a_map, bar, c * 64, h, m0);
 #pragma unroll
     for (int j = 0; j < NT / 64; ++j) tma_load_2d(st + 16384 + j * 8192, &w_map, bar, n0 + j * 64, h * K + c * 64);
     last_phase[s] = (c / STAGES) & 1;
   };
+  auto issue_a = [&](int c) {
+    const int s = c % STAGES;
+    tma_load_3d(smem + s * kSB, &a_map, smem_u32(&full[s]), c * 64, h, m0);
+  };
   constexpr int kFirst = KC < STAGES ? KC : STAGES;
   if (warp == 0 && lane == 0)
-    for (int c = 0; c < kFirst; ++c) issue(c);
+    for (int c = 0; c < kFirst; ++c) issue_w(c);
+  griddep_wait();
+  griddep_launch_dependents();
+  if (warp == 0 && lane == 0)
+    for (int c = 0; c < kFirst; ++c) issue_a(c);
 
   const int n = m0 + threadIdx.x;
   // the RoPE part of the decode query is copied by the first column tile; it is
@@ -250,7 +263,8 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
           fail_s = 1;
           break;
         }
-        issue(c);
+        issue_w(c);
+        issue_a(c);
       }
     }
   } else if (warp == 1) {   // MMA issue: the whole warp waits, one elected lane issues
@@ -339,7 +353,7 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
 
 // absorb: K = 128 -> two 256-column tiles of 512; un-absorb: K = 512 -> one 128-column tile
 #define MLA_BMM_ABSORB 128, 256, 2
-#define MLA_BMM_UNABSORB 512, 128, 3
+#define MLA_BMM_UNABSORB 512, 128, 6
 
 cudaError_t bmm_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(mla_bmm_kernel<MLA_BMM_ABSORB>, cudaFuncAttributeMaxDynamicSharedMemorySize,

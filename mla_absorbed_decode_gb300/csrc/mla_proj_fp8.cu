@@ -30,12 +30,18 @@
 namespace mla {
 
 namespace {
-__device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity) {   // bounded (0.5 s)
+__device__ __noinline__ bool bmm_wait_slow(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_test(bar, parity)) {
     if (global_timer_ns() - t0 > 500000000ull) return false;
   }
   return true;
+}
+// Bounded wait (0.5 s).  The phase is tested once before the clock is read: reading the
+// global timer costs hundreds of cycles, which a wait that is already satisfied should not pay.
+__device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
+  return bmm_wait_slow(bar, parity);
 }
 }  // namespace
 
