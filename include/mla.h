@@ -296,9 +296,13 @@ mla_status_t mla_unabsorb_o_fp8(const mla_bf16_t* o_lat, const uint8_t* w_uv_t, 
  *  MLA_ERR_DEVICE_BOUNDS and read as zeros);  seqlen (host) >= T >= 1;
  *  chunk_tokens: cached tokens expanded at a time, a positive multiple of 64;
  *  workspace >= mla_extend_workspace_size(T, H, chunk_tokens) bytes, 256-byte aligned
- *  (the expanded keys and values of one chunk, ~512 * H bytes a chunk token, and the
+ *  (two buffers of a chunk's expanded keys and values, ~512 * H bytes a chunk token each,
+ *  so that the expansion of one chunk overlaps the attention of the chunk before, and the
  *  running fp32 merge of the output);  out [T, H, 128] bf16;  lse [T, H] fp32.
- * Launches two kernels per chunk on `stream`, in order.  Async on stream. */
+ * Launches two kernels per chunk on `stream`, in order (programmatic launches: the first
+ * expansion waits for the work queued before the call, every later kernel for the one
+ * before it, except that an expansion reads only the cache and the weights before the
+ * previous chunk's attention has finished).  Async on stream. */
 size_t mla_extend_workspace_size(int T, int H, int chunk_tokens);
 mla_status_t mla_extend_chunked(const mla_bf16_t* q_nope, const mla_bf16_t* q_pe, const mla_bf16_t* w_uk,
                                 const mla_bf16_t* w_uv, const mla_bf16_t* kv_cache, int64_t num_blocks,

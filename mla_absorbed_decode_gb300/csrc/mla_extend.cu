@@ -106,7 +106,14 @@ mla_expand_kernel(const __grid_constant__ CUtensorMap c_map, const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  griddep_wait();
+  // The expansion of every chunk but the first reads only the cache and the weights, which
+  // the kernels before it in the call do not write, and writes the Kx / Vx buffer that the
+  // attention of the chunk before does not read (two buffers, alternating): it may run
+  // beside that attention's last CTAs.  Its last CTA waits for that attention at its end
+  // instead (the grid completes only after it), so that the attention after this kernel,
+  // which waits for it, also finds the merged accumulator of the chunk before complete; the
+  // other CTAs never wait, and leave their SMs as soon as they are done.
+  if (!p.defer_wait) griddep_wait();
   griddep_launch_dependents();
 
   // the tile's (up to) two cache pages; a page past the chunk is not loaded (its rows are
@@ -197,6 +204,7 @@ mla_expand_kernel(const __grid_constant__ CUtensorMap c_map, const __grid_consta
     tc_fence_after();
     tmem_dealloc(tmem, 256);
   }
+  if (p.defer_wait && blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1) griddep_wait();
 }
 
 // ---------------------------------------------------------------- attend --
@@ -595,7 +603,7 @@ cudaError_t extend_set_attributes() {
                               static_cast<int>(kAttSmem));
 }
 
-cudaError_t launch_extend_chunk(const ExtendMaps& maps, const ExtendParams& p, cudaStream_t stream) {
+cudaError_t launch_extend_chunk(const ExtendMaps& maps, const ExtendParams& p, int buf, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   {
     const cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>((p.n + 127) / 128), static_cast<unsigned>(p.H)),
@@ -605,7 +613,7 @@ cudaError_t launch_extend_chunk(const ExtendMaps& maps, const ExtendParams& p, c
   }
   const cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>((p.T + 127) / 128), static_cast<unsigned>(p.H)),
                                             dim3(kAttThreads), kAttSmem, stream, attr);
-  return cudaLaunchKernelEx(&cfg, mla_attend_kernel, maps.qn, maps.qp, maps.kx, maps.vx, maps.kr, p);
+  return cudaLaunchKernelEx(&cfg, mla_attend_kernel, maps.qn, maps.qp, maps.kx[buf], maps.vx[buf], maps.kr, p);
 }
 
 }  // namespace mla

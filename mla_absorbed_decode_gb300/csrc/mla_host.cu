@@ -589,7 +589,7 @@ size_t mla_extend_workspace_size(int T, int H, int chunk_tokens) {
   if (T < 1 || H < 1 || chunk_tokens < kPageTokens || chunk_tokens % kPageTokens) return 0;
   const size_t cap = static_cast<size_t>(extend_cap(chunk_tokens));
   const size_t kv = round256(cap * H * 128 * sizeof(uint16_t));
-  return 2 * kv + round256(static_cast<size_t>(T) * H * 128 * sizeof(float)) +
+  return 4 * kv + round256(static_cast<size_t>(T) * H * 128 * sizeof(float)) +
          round256(static_cast<size_t>(T) * H * sizeof(float));
 }
 
@@ -625,15 +625,20 @@ mla_status_t mla_extend_chunked(const mla_bf16_t* q_nope, const mla_bf16_t* q_pe
       encode_3d(&m.qp, q_pe, 64, uH, static_cast<uint64_t>(T), 128, uH * 128, 64, 1, 128);
   char* ws = static_cast<char*>(workspace);
   const size_t kv_bytes = round256(static_cast<size_t>(cap) * H * 128 * sizeof(uint16_t));
-  __nv_bfloat16* kx = reinterpret_cast<__nv_bfloat16*>(ws);
-  __nv_bfloat16* vx = reinterpret_cast<__nv_bfloat16*>(ws + kv_bytes);
-  float* acc_o = reinterpret_cast<float*>(ws + 2 * kv_bytes);
-  float* acc_lse = reinterpret_cast<float*>(ws + 2 * kv_bytes + round256(static_cast<size_t>(T) * H * 128 * 4));
+  // two Kx / Vx buffers: chunk j expands into buffer j % 2, so that the expansion of chunk j + 1
+  // may overlap the attention of chunk j
+  __nv_bfloat16* kx[2] = {reinterpret_cast<__nv_bfloat16*>(ws), reinterpret_cast<__nv_bfloat16*>(ws + 2 * kv_bytes)};
+  __nv_bfloat16* vx[2] = {reinterpret_cast<__nv_bfloat16*>(ws + kv_bytes),
+                          reinterpret_cast<__nv_bfloat16*>(ws + 3 * kv_bytes)};
+  float* acc_o = reinterpret_cast<float*>(ws + 4 * kv_bytes);
+  float* acc_lse = reinterpret_cast<float*>(ws + 4 * kv_bytes + round256(static_cast<size_t>(T) * H * 128 * 4));
   // expanded keys and values head-major, [H][cap][128]: a 64-token tile of one head is 16 KiB in one run
   const uint64_t ucap = static_cast<uint64_t>(cap);
-  if (!maps_ok || !encode_3d(&m.kx, kx, 128, ucap, uH, 256, ucap * 256, 64, 64, 1) ||
-      !encode_3d(&m.vx, vx, 128, ucap, uH, 256, ucap * 256, 64, 64, 1))
-    return MLA_ERR_CUDA;
+  if (!maps_ok) return MLA_ERR_CUDA;
+  for (int i = 0; i < 2; ++i)
+    if (!encode_3d(&m.kx[i], kx[i], 128, ucap, uH, 256, ucap * 256, 64, 64, 1) ||
+        !encode_3d(&m.vx[i], vx[i], 128, ucap, uH, 256, ucap * 256, 64, 64, 1))
+      return MLA_ERR_CUDA;
   m.kr = m.c;
 
   ExtendParams p;
@@ -644,8 +649,7 @@ mla_status_t mla_extend_chunked(const mla_bf16_t* q_nope, const mla_bf16_t* q_pe
   p.H = H;
   p.qpos0 = seqlen - T;
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634074);
-  p.kx = kx;
-  p.vx = vx;
+
   p.acc_o = acc_o;
   p.acc_lse = acc_lse;
   p.out = reinterpret_cast<__nv_bfloat16*>(out);
@@ -658,7 +662,10 @@ mla_status_t mla_extend_chunked(const mla_bf16_t* q_nope, const mla_bf16_t* q_pe
     p.n = seqlen - p.c0 < chunk_tokens ? seqlen - p.c0 : chunk_tokens;
     p.first = j == 0;
     p.last = j == n_chunks - 1;
-    if (launch_extend_chunk(m, p, cs) != cudaSuccess) return MLA_ERR_CUDA;
+    p.defer_wait = j > 0;   // the first expansion may read cache rows the caller has just written
+    p.kx = kx[j & 1];
+    p.vx = vx[j & 1];
+    if (launch_extend_chunk(m, p, j & 1, cs) != cudaSuccess) return MLA_ERR_CUDA;
   }
   return MLA_OK;
 }

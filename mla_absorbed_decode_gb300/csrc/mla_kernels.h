@@ -173,6 +173,7 @@ struct ExtendParams {
   float* acc_o;                 // [T, H, 128] running merged output (fp32)
   float* acc_lse;               // [T, H] running merged lse
   int first, last;              // the first / last chunk of the call
+  int defer_wait;               // expansion: griddepcontrol.wait at its end, not its start (below)
   __nv_bfloat16* out;           // [T, H, 128] bf16 (written by the last chunk)
   float* lse;                   // [T, H] (written by the last chunk)
   int* status;
@@ -183,10 +184,10 @@ struct ExtendMaps {
   CUtensorMap wv;               // W_UV as [H * 512 rows][128], box 64 x 64
   CUtensorMap qn;               // q_nope [128, H, T], box 64 x 1 x 128
   CUtensorMap qp;               // q_pe [64, H, T], box 64 x 1 x 128
-  CUtensorMap kx, vx;           // [128, cap, H], box 64 x 64 x 1
+  CUtensorMap kx[2], vx[2];     // the two Kx / Vx buffers as [128, cap, H], box 64 x 64 x 1
   CUtensorMap kr;               // the cache view of c, k^R = chunk 8
 };
 cudaError_t extend_set_attributes();
-cudaError_t launch_extend_chunk(const ExtendMaps& maps, const ExtendParams& p, cudaStream_t stream);
+cudaError_t launch_extend_chunk(const ExtendMaps& maps, const ExtendParams& p, int buf, cudaStream_t stream);
 
 }  // namespace mla
