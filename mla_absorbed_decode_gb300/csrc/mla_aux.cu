@@ -165,10 +165,16 @@ __device__ __forceinline__ bool bmm_wait(uint32_t bar, uint32_t parity) {
   return bmm_wait_slow(bar, parity);
 }
 
+// TMA store of a 3-D box from shared memory (completion tracked by the bulk-group helpers).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z) : "memory");
+}
+
 template <int K, int NT, int STAGES>
 __global__ void __launch_bounds__(128, 1)
 mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap w_map,
-               const BmmParams p) {
+               const __grid_constant__ CUtensorMap o_map, const BmmParams p) {
   static_assert(K % 64 == 0 && NT % 64 == 0 && NT >= 64 && NT <= 256 && STAGES >= 1, "tile shape");
   constexpr int KC = K / 64;
   constexpr uint32_t kSB = bmm_stage_bytes<K, NT, STAGES>();
@@ -294,47 +300,42 @@ mla_bmm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant_
   const bool store = got && !fail_s && n < p.N;
   __nv_bfloat16* dst = p.out + static_cast<int64_t>(n) * p.out_row_stride + static_cast<int64_t>(h) * p.out_head_stride + n0;
   const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  // The stores go through a 2 KiB transpose buffer per warp in the (now idle) first stage: a
-  // thread holds one token row, so direct stores would touch 32 rows per instruction; here
-  // each store instruction writes 64 contiguous bytes of 8 rows.  Buffer row x (64 B) holds
-  // 16-byte unit u at ((u ^ ((x >> 1) & 3)) * 16): the 8 rows a quarter-warp stores (or
-  // the 2 rows it loads) then touch 8 distinct 16-byte bank groups.
-  const uint32_t stg = smem + warp * 2048;
-  const int tq = lane & 3, nw0 = m0 + warp * 32;   // transposed: quad tq of rows 8j + (lane >> 2)
+  // The stores go out by TMA: warp w stages its 32 token rows as one 32-row x 64-column tile
+  // per 64 output columns (the 128-byte swizzle of the output map: row r's 16-byte unit u at
+  // r * 128 + ((u ^ (r & 7)) * 16), so that each store instruction of the warp covers all 32
+  // banks), in the idle ring, and one lane stores each tile; rows past N are clipped by the
+  // map.  A warp whose rows all lie past N does nothing.
+  const int nw0 = m0 + warp * 32;
   const bool ok_all = got && !fail_s;
-  __nv_bfloat16* const dst0 = p.out + static_cast<int64_t>(h) * p.out_head_stride + n0;
-  auto store32 = [&](int c, const uint32_t (&v)[32]) {   // columns [c, c + 32) of the warp's 32 rows
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint4 u;
-      u.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-      u.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-      u.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-      u.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-      st_shared_v4(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), u);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int x = 8 * j + (lane >> 2);
-      const uint4 u = ld_shared_v4(stg + x * 64 + ((tq ^ ((x >> 1) & 3)) << 4));
-      if (ok_all && nw0 + x < p.N)
-        *reinterpret_cast<uint4*>(dst0 + static_cast<int64_t>(nw0 + x) * p.out_row_stride + c + 8 * tq) = u;
-    }
-    __syncwarp();
-  };
-  uint32_t va[32], vb[32];
-  tmem_ld32(tl, va);
+  const uint32_t stg = smem + warp * (NT / 64) * 4096u;
+  if (ok_all && nw0 < p.N) {
 #pragma unroll 1
-  for (int c = 0; c < NT; c += 64) {
-    tmem_wait_ld();
-    tmem_ld32(tl + c + 32, vb);
-    store32(c, va);
-    tmem_wait_ld();
-    if (c + 64 < NT) tmem_ld32(tl + c + 64, va);
-    store32(c + 32, vb);
+    for (int g = 0; g < NT / 64; ++g) {
+      uint32_t va[32], vb[32];
+      tmem_ld32(tl + 64 * g, va);
+      tmem_ld32(tl + 64 * g + 32, vb);
+      tmem_wait_ld();
+      const uint32_t row = stg + g * 4096u + lane * 128u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t* v = u < 4 ? va + 8 * u : vb + 8 * (u - 4);
+        uint4 x;
+        x.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+        x.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+        x.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+        x.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+        st_shared_v4(row + ((u ^ (lane & 7)) << 4), x);
+      }
+    }
+    fence_proxy_async_smem();   // the staged tiles are visible to the TMA (async proxy)
+    __syncwarp();
+    if (lane == 0) {
+      for (int g = 0; g < NT / 64; ++g) tma_store_3d(&o_map, stg + g * 4096u, n0 + 64 * g, h, nw0);
+      bulk_commit_group();
+      bulk_wait_group_read<0>();   // the tiles are read before the CTA may exit
+    }
+    __syncwarp();
   }
-  tmem_wait_ld();
   if (store && copy_pe) {
     uint4* d4 = reinterpret_cast<uint4*>(dst + 512);
 #pragma unroll
@@ -363,8 +364,8 @@ cudaError_t bmm_set_attributes() {
                               static_cast<int>(bmm_smem_bytes<MLA_BMM_UNABSORB>()));
 }
 
-cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap& w_map, const BmmParams& p,
-                       cudaStream_t stream) {
+cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap& w_map, const CUtensorMap& o_map,
+                       const BmmParams& p, cudaStream_t stream) {
   const int64_t mt = (p.N + 127) / 128;
   cudaLaunchAttribute attr[1];
   if (absorb) {
@@ -376,14 +377,14 @@ cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap&
     if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
     const cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(ctas)), dim3(128),
                                               bmm_smem_bytes<MLA_BMM_ABSORB>(), stream, attr);
-    return cudaLaunchKernelEx(&cfg, mla_bmm_kernel<MLA_BMM_ABSORB>, a_map, w_map, p);
+    return cudaLaunchKernelEx(&cfg, mla_bmm_kernel<MLA_BMM_ABSORB>, a_map, w_map, o_map, p);
   }
   if (p.sched_meta != nullptr) return cudaErrorInvalidValue;
   const int64_t ctas = (128 / 128) * static_cast<int64_t>(p.H) * mt;
   if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
   const cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(ctas)), dim3(128),
                                             bmm_smem_bytes<MLA_BMM_UNABSORB>(), stream, attr);
-  return cudaLaunchKernelEx(&cfg, mla_bmm_kernel<MLA_BMM_UNABSORB>, a_map, w_map, p);
+  return cudaLaunchKernelEx(&cfg, mla_bmm_kernel<MLA_BMM_UNABSORB>, a_map, w_map, o_map, p);
 }
 
 

@@ -360,6 +360,10 @@ mla_status_t absorb_impl(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, co
                  static_cast<uint64_t>(q_nope_row_stride) * 2, 64, 1, 128))
     return MLA_ERR_CUDA;
   if (!encode_2d(&w_map, w_uk, 512, static_cast<uint64_t>(H) * 128, 1024, 64, 64)) return MLA_ERR_CUDA;
+  CUtensorMap o_map;   // q as [576, H, N], stored 64 columns x 32 rows at a time
+  if (!encode_3d(&o_map, q, kDimQK, static_cast<uint64_t>(H), static_cast<uint64_t>(N), kDimQK * 2,
+                 static_cast<uint64_t>(H) * kDimQK * 2, 64, 1, 32))
+    return MLA_ERR_CUDA;
   BmmParams p = {};
   p.out = reinterpret_cast<__nv_bfloat16*>(q);
   p.out_row_stride = static_cast<int64_t>(H) * kDimQK;
@@ -390,8 +394,9 @@ mla_status_t absorb_impl(const mla_bf16_t* q_nope, int64_t q_nope_row_stride, co
     p.two_pi_hi = static_cast<float>(two_pi);
     p.two_pi_lo = static_cast<float>(two_pi - static_cast<double>(p.two_pi_hi));
   }
-  return launch_bmm(true, a_map, w_map, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
-                                                                                               : MLA_ERR_CUDA;
+  return launch_bmm(true, a_map, w_map, o_map, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -443,6 +448,10 @@ mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla
                  static_cast<uint64_t>(H) * 1024, 64, 1, 128))
     return MLA_ERR_CUDA;
   if (!encode_2d(&w_map, w_uv, 128, static_cast<uint64_t>(H) * 512, 256, 64, 64)) return MLA_ERR_CUDA;
+  CUtensorMap o_map;   // o as [128, H, N], stored 64 columns x 32 rows at a time
+  if (!encode_3d(&o_map, o, 128, static_cast<uint64_t>(H), static_cast<uint64_t>(N), 256,
+                 static_cast<uint64_t>(H) * 256, 64, 1, 32))
+    return MLA_ERR_CUDA;
   BmmParams p;
   p.out = reinterpret_cast<__nv_bfloat16*>(o);
   p.out_row_stride = static_cast<int64_t>(H) * 128;
@@ -454,8 +463,9 @@ mla_status_t mla_unabsorb_o(const mla_bf16_t* o_lat, const mla_bf16_t* w_uv, mla
   p.pe_row_stride = 0;
   p.positions = nullptr;
   p.w = reinterpret_cast<const __nv_bfloat16*>(w_uv);
-  return launch_bmm(false, a_map, w_map, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK
-                                                                                                : MLA_ERR_CUDA;
+  return launch_bmm(false, a_map, w_map, o_map, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 size_t mla_bmm_fp8_workspace_size(void) { return static_cast<size_t>(kAmaxParts) * sizeof(float); }

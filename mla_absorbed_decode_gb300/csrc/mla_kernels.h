@@ -143,8 +143,8 @@ struct BmmParams {
 constexpr int kAbsorbPlanMaxB = 8000;   // (B + 1) * 8 + B * 4 bytes within the absorption's 97 KB
 cudaError_t bmm_set_attributes();
 // absorb: K = 128 -> 512 columns; unabsorb: K = 512 -> 128 columns
-cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap& w_map, const BmmParams& p,
-                       cudaStream_t stream);
+cudaError_t launch_bmm(bool absorb, const CUtensorMap& a_map, const CUtensorMap& w_map, const CUtensorMap& o_map,
+                       const BmmParams& p, cudaStream_t stream);
 
 // FP8 projections: x (bf16) quantized per tensor on the fly, E4M3 weights stored transposed
 // ([H, J, K], K contiguous) with one per-tensor scale.  `partials` (kAmaxParts floats of
