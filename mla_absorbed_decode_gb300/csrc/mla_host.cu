@@ -511,6 +511,13 @@ mla_status_t bmm_fp8_impl(bool absorb, const mla_bf16_t* x, int64_t x_row_stride
                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MLA_ERR_CUDA;
   }
+  CUtensorMap o_map;   // out as [W, H, N] (W = 576 for q, 128 for o), stored 64 columns x 32 rows at a time
+  {
+    const uint64_t width = absorb ? kDimQK : 128;
+    if (!encode_3d(&o_map, out, width, static_cast<uint64_t>(H), static_cast<uint64_t>(N), width * 2,
+                   static_cast<uint64_t>(H) * width * 2, 64, 1, 32))
+      return MLA_ERR_CUDA;
+  }
   BmmFp8Params p = {};
   p.base.out = reinterpret_cast<__nv_bfloat16*>(out);
   p.base.out_row_stride = static_cast<int64_t>(H) * (absorb ? kDimQK : 128);
@@ -544,7 +551,7 @@ mla_status_t bmm_fp8_impl(bool absorb, const mla_bf16_t* x, int64_t x_row_stride
   p.w = w_t;
   p.J = J;
   p.w_scale = w_scale;
-  return launch_bmm_fp8(absorb, reinterpret_cast<const __nv_bfloat16*>(x), x_row_stride, K, x_map, w_map, p,
+  return launch_bmm_fp8(absorb, reinterpret_cast<const __nv_bfloat16*>(x), x_row_stride, K, x_map, w_map, o_map, p,
                         static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;

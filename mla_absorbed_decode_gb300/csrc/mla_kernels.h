@@ -159,7 +159,8 @@ struct BmmFp8Params {
 };
 cudaError_t bmm_fp8_set_attributes();
 cudaError_t launch_bmm_fp8(bool absorb, const __nv_bfloat16* x, int64_t x_row_stride, int K, const CUtensorMap& x_map,
-                           const CUtensorMap& w_map, const BmmFp8Params& p, float* partials, cudaStream_t stream);
+                           const CUtensorMap& w_map, const CUtensorMap& o_map, const BmmFp8Params& p, float* partials,
+                           cudaStream_t stream);
 
 // Chunked extend on the expanded path: one chunk [c0, c0 + n) of a request's cache.
 struct ExtendParams {

@@ -14,8 +14,9 @@
 //      acc * x_scale * w_scale in bf16.
 // The quantization takes the same float32 steps as the oracle (inv = 448 / amax,
 // code = e4m3_rn_satfinite(x * inv)), so both reach the same codes.  The weight tile is
-// prefetched into L2 before griddepcontrol.wait (only a prefetch: its TMA loads come
-// after the wait), so its HBM read overlaps the tail of the previous kernel.
+// loaded before griddepcontrol.wait (the weights are not written by the previous kernel of
+// the stream), so its HBM read overlaps the tail of that kernel; x and the partial maxima
+// are read after it.  The bf16 result leaves by TMA stores of swizzled 32 x 64 tiles.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -109,10 +110,16 @@ struct Fp8BmmShape {
   static_assert(K % 128 == 0 && NT % 16 == 0 && NT >= 32 && NT <= 256, "tile shape");
 };
 
+// TMA store of a 3-D box from shared memory (completion tracked by the bulk-group helpers).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z) : "memory");
+}
+
 template <int K, int NT>
 __global__ void __launch_bounds__(128, 1)
 mla_bmm_fp8_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap w_map,
-                   const BmmFp8Params p) {
+                   const __grid_constant__ CUtensorMap o_map, const BmmFp8Params p) {
   using S = Fp8BmmShape<K, NT>;
   extern __shared__ __align__(1024) uint8_t dyn_smem[];
   __shared__ uint64_t w_full, x_full[S::kXStages], x_empty[S::kXStages], acc_full;
@@ -136,19 +143,27 @@ mla_bmm_fp8_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_const
     fence_mbar_init();
     prefetch_tensormap(&x_map);
     prefetch_tensormap(&w_map);
-    // the weight tile (NT rows of K codes, contiguous) into L2 while the previous kernel runs
-    prefetch_l2(p.w + (static_cast<int64_t>(h) * p.J + n0) * K, static_cast<uint32_t>(NT) * K);
+    prefetch_tensormap(&o_map);
   }
   if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), NT);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+
+  // producer: the whole weight tile (while the previous kernel may still run), then the
+  // first x chunks
+  bool issued_w = false;
+  if (threadIdx.x == 0) {
+    const uint32_t bar = smem_u32(&w_full);
+    mbar_arrive_expect_tx(bar, S::kWBytes);
+#pragma unroll
+    for (int cc = 0; cc < S::kCodeChunks; ++cc)
+      tma_load_2d(smem + S::kOffW + cc * (NT * 128u), &w_map, bar, cc * 128, h * p.J + n0);
+    issued_w = true;
+  }
   griddep_wait();
   griddep_launch_dependents();
-
-  // producer: the whole weight tile, then the first x chunks
-  bool issued_w = false;
   int x_issued = 0;
   auto issue_x = [&](int c) {
     const int s = c % S::kXStages;
@@ -157,12 +172,6 @@ mla_bmm_fp8_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_const
     tma_load_3d(smem + S::kOffX + s * 16384u, &x_map, bar, c * 64, h, m0);
   };
   if (threadIdx.x == 0) {
-    const uint32_t bar = smem_u32(&w_full);
-    mbar_arrive_expect_tx(bar, S::kWBytes);
-#pragma unroll
-    for (int cc = 0; cc < S::kCodeChunks; ++cc)
-      tma_load_2d(smem + S::kOffW + cc * (NT * 128u), &w_map, bar, cc * 128, h * p.J + n0);
-    issued_w = true;
     for (int c = 0; c < S::kXStages; ++c) issue_x(c);
     x_issued = S::kXStages;
   }
@@ -253,44 +262,42 @@ mla_bmm_fp8_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_const
     if (b.positions != nullptr) rope_row(pe, __ldg(b.positions + n), b);
   }
 
-  // epilogue: acc * x_scale * w_scale in bf16, through a 2 KiB transpose buffer per warp (in
-  // the idle x ring) so that every store instruction writes 64 contiguous bytes of 8 rows
+  // epilogue: acc * x_scale * w_scale in bf16.  Warp w stages its 32 rows as one 32-row x
+  // 64-column tile per 64 output columns (the output map's 128-byte swizzle: row r's 16-byte
+  // unit u at r * 128 + ((u ^ (r & 7)) * 16)) in the idle weight / code / x memory, and one
+  // lane stores each tile by TMA; rows past N are clipped by the map.
   const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  const uint32_t stg = smem + S::kOffX + warp * 2048u;
-  const int tq = lane & 3, nw0 = m0 + warp * 32;
-  __nv_bfloat16* const dst0 = b.out + static_cast<int64_t>(h) * b.out_head_stride + n0;
-  auto store32 = [&](int c, const uint32_t (&v)[32]) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint4 u;
-      u.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * out_scale, __uint_as_float(v[8 * j + 1]) * out_scale);
-      u.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * out_scale, __uint_as_float(v[8 * j + 3]) * out_scale);
-      u.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * out_scale, __uint_as_float(v[8 * j + 5]) * out_scale);
-      u.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * out_scale, __uint_as_float(v[8 * j + 7]) * out_scale);
-      st_shared_v4(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), u);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int x = 8 * j + (lane >> 2);
-      const uint4 u = ld_shared_v4(stg + x * 64 + ((tq ^ ((x >> 1) & 3)) << 4));
-      if (ok_all && nw0 + x < b.N)
-        *reinterpret_cast<uint4*>(dst0 + static_cast<int64_t>(nw0 + x) * b.out_row_stride + c + 8 * tq) = u;
-    }
-    __syncwarp();
-  };
-  uint32_t va[32], vb[32];
-  tmem_ld32(tl, va);
+  const int nw0 = m0 + warp * 32;
+  static_assert(4 * (NT / 64) * 4096u <= S::kOffX + S::kXStages * 16384u, "the staging tiles fit the idle operands");
+  const uint32_t stg = smem + warp * (NT / 64) * 4096u;
+  if (ok_all && nw0 < b.N) {
 #pragma unroll 1
-  for (int c = 0; c < NT; c += 64) {
-    tmem_wait_ld();
-    tmem_ld32(tl + c + 32, vb);
-    store32(c, va);
-    tmem_wait_ld();
-    if (c + 64 < NT) tmem_ld32(tl + c + 64, va);
-    store32(c + 32, vb);
+    for (int g = 0; g < NT / 64; ++g) {
+      uint32_t va[32], vb[32];
+      tmem_ld32(tl + 64 * g, va);
+      tmem_ld32(tl + 64 * g + 32, vb);
+      tmem_wait_ld();
+      const uint32_t row = stg + g * 4096u + lane * 128u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t* v = u < 4 ? va + 8 * u : vb + 8 * (u - 4);
+        uint4 x;
+        x.x = pack_bf16x2(__uint_as_float(v[0]) * out_scale, __uint_as_float(v[1]) * out_scale);
+        x.y = pack_bf16x2(__uint_as_float(v[2]) * out_scale, __uint_as_float(v[3]) * out_scale);
+        x.z = pack_bf16x2(__uint_as_float(v[4]) * out_scale, __uint_as_float(v[5]) * out_scale);
+        x.w = pack_bf16x2(__uint_as_float(v[6]) * out_scale, __uint_as_float(v[7]) * out_scale);
+        st_shared_v4(row + ((u ^ (lane & 7)) << 4), x);
+      }
+    }
+    fence_proxy_async_smem();   // the staged tiles are visible to the TMA (async proxy)
+    __syncwarp();
+    if (lane == 0) {
+      for (int g = 0; g < NT / 64; ++g) tma_store_3d(&o_map, stg + g * 4096u, n0 + 64 * g, h, nw0);
+      bulk_commit_group();
+      bulk_wait_group_read<0>();   // the tiles are read before the CTA may exit
+    }
+    __syncwarp();
   }
-  tmem_wait_ld();
   if (ok_all && copy_pe) {
     uint4* d4 = reinterpret_cast<uint4*>(b.out + static_cast<int64_t>(n) * b.out_row_stride +
                                          static_cast<int64_t>(h) * b.out_head_stride + 512);
@@ -330,7 +337,8 @@ cudaError_t bmm_fp8_set_attributes() {
 }
 
 cudaError_t launch_bmm_fp8(bool absorb, const __nv_bfloat16* x, int64_t x_row_stride, int K, const CUtensorMap& x_map,
-                           const CUtensorMap& w_map, const BmmFp8Params& p, float* partials, cudaStream_t stream) {
+                           const CUtensorMap& w_map, const CUtensorMap& o_map, const BmmFp8Params& p, float* partials,
+                           cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   {   // the partial maxima of |x| over the N rows of H * K values (and the schedule, if asked)
     const bool plan = p.base.sched_meta != nullptr;
@@ -347,11 +355,11 @@ cudaError_t launch_bmm_fp8(bool absorb, const __nv_bfloat16* x, int64_t x_row_st
   if (absorb) {
     const cudaLaunchConfig_t cfg = pdl_config(dim3(512 / 256, p.base.H, mt), dim3(128),
                                               Fp8BmmShape<MLA_FP8_ABSORB>::kSmem, stream, attr);
-    return cudaLaunchKernelEx(&cfg, mla_bmm_fp8_kernel<MLA_FP8_ABSORB>, x_map, w_map, p);
+    return cudaLaunchKernelEx(&cfg, mla_bmm_fp8_kernel<MLA_FP8_ABSORB>, x_map, w_map, o_map, p);
   }
   const cudaLaunchConfig_t cfg = pdl_config(dim3(128 / 128, p.base.H, mt), dim3(128),
                                             Fp8BmmShape<MLA_FP8_UNABSORB>::kSmem, stream, attr);
-  return cudaLaunchKernelEx(&cfg, mla_bmm_fp8_kernel<MLA_FP8_UNABSORB>, x_map, w_map, p);
+  return cudaLaunchKernelEx(&cfg, mla_bmm_fp8_kernel<MLA_FP8_UNABSORB>, x_map, w_map, o_map, p);
 }
 
 }  // namespace mla
