@@ -39,8 +39,9 @@
 // Roles (384 threads): warp 0 = TMA producer, warp 1 = MMA issuer (warp-uniform,
 // one elected lane issues), warp 2 = credit forwarder (O-CTA), warps 4..7 and
 // 8..11 = two softmax (S-CTA) or rescale/epilogue (O-CTA) warpgroups; a thread
-// of a warpgroup owns one query row (its TMEM lane).  The sparse decode gathers its
-// pages with warps (SparseWarps below); over an FP8 cache it runs 512 threads.
+// of a warpgroup owns one query row (its TMEM lane).  The sparse decode runs 512 threads:
+// over a bf16 cache warp 0 gathers its pages by TMA (tile::gather4, s_producer_gather);
+// over an FP8 cache gathering warps copy them with cp.async (SparseWarps below).
 // Every barrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT,
 // raises an abort flag in every CTA of its cluster, drains what it has in
 // flight and exits.
@@ -371,7 +372,8 @@ struct RowLookahead {
   }
 };
 
-// Gathering warps of the sparse decode.  Gathering warp slot ws owns rows
+// Gathering warps of the sparse decode over an FP8 cache (the bf16 cache is gathered by TMA,
+// see s_producer_gather).  Gathering warp slot ws owns rows
 // [gather_r0(ws), gather_r0(ws + 1)) of each page; lane l looks up row gather_r0(ws) + l.
 // The kernel runs 16 warps (its registers fit 128 a thread in both cache formats): the
 // S-CTA gathers with warps 0, 2, 3 and 12..15, the O-CTA with warps 0, 3 and 12..15 (one
@@ -513,6 +515,179 @@ __device__ void o_producer_sparse(const DecodeParams& p, Shared& sh, uint32_t sm
   __syncwarp();
 }
 
+// ------------------------------------------------ sparse gather by TMA (bf16) --
+// Over a bf16 cache the sparse decode gathers a page's 64 rows by TMA, four rows per
+// tile::gather4 load over a 2-D view of the cache ([cache row][576 dims], a 64-dim x 1-row
+// box).  The load writes its four 128-byte rows at 128-byte steps and swizzles each by its
+// own shared-memory address, so 16 loads per 64-dim chunk (destinations 512 bytes apart)
+// fill the chunk in the layout a 64-row box produces.  One warp per CTA: lane l looks up
+// rows l and l + 32 of every page (RowLookahead, the lookups running ahead of the loads), and
+// lanes 0..15 each load one group of four rows, chunk by chunk.  A row past the request's list,
+// or one whose lookup fails the bounds checks (reported as for the cp.async gather), loads
+// cache row 0, which is always in range: the softmax masks it by its list position.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                            const int (&r)[4]) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]),
+         "r"(bar)
+      : "memory");
+}
+// kGatherSlots warps gather a page: slot gs looks up rows [16 gs, 16 gs + 16) (lane l < 16 row
+// 16 gs + l, two pages ahead for the list entry and one for the block-table entry) and its lanes
+// 0..3 load the four groups of four rows.  Each slot arrives once on a stage's barrier with the
+// bytes of its own loads, and drains its own loads before the CTA exits.
+constexpr int kGatherSlots = 4;
+template <bool IsS>
+__device__ __forceinline__ int gather_slot(int warp) {   // S-CTA: warps 0, 2, 3, 12; O-CTA: 0, 3, 12, 13
+  if (warp == 0) return 0;
+  if (IsS) return warp == 2 ? 1 : warp == 3 ? 2 : warp == 12 ? 3 : -1;
+  return warp == 3 ? 1 : warp == 12 ? 2 : warp == 13 ? 3 : -1;
+}
+struct GatherRows {
+  RowLookahead<false> look;
+  int gs;
+  __device__ void init(const DecodeParams& p, int part, int slot, int lane) {
+    gs = slot;
+    look.init(p, part, 16 * slot + lane, lane < 16);
+  }
+  __device__ static int row_of(const DecodeParams& p, const __nv_bfloat16* row) {
+    return row ? static_cast<int>((reinterpret_cast<const uint8_t*>(row) - reinterpret_cast<const uint8_t*>(p.kv)) /
+                                  (2 * kDimQK))
+               : 0;
+  }
+  // The next page's group of four cache rows of lane `lane` (meaningful for lanes 0..3: rows
+  // 16 gs + 4 lane .. + 3); every lane of the warp takes part.
+  __device__ void step(const DecodeParams& p, int lane, int (&r)[4]) {
+    const int r0 = row_of(p, look.step(p));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r[j] = __shfl_sync(0xffffffffu, r0, 4 * (lane & 3) + j);
+  }
+};
+
+// Gathering slot gs of the S-CTA, sparse decode over a bf16 cache: the q blocks (slot 0, TMA
+// boxes; the other slots only arrive) and its rows of every page (tile::gather4), part A
+// (chunks 0..kKPartA-1) and part B as in the dense producer.
+__device__ void s_producer_gather(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
+                                  uint32_t cl, int rb, bool withhold, int gs) {
+  using C = Cfg<false>;
+  const int lane = threadIdx.x & 31;
+  SegmentWalker w;
+  w.init(p, part);
+  Segment s;
+  uint32_t i = 0;
+  int issued[C::kKStages], issued_b[C::kKStages];
+  uint32_t issued_phase[C::kKStages], issued_phase_b[C::kKStages];
+  for (int j = 0; j < C::kKStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
+  bool ok = true;
+  GatherRows g;
+  g.init(p, part, gs, lane);
+  while (ok && w.next(s)) {
+    const int qrow0 = s.b * p.rows + rb * 128;
+    for (int j = 0; j < C::kQItems && ok; ++j, ++i) {
+      const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;
+      if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl) ||
+          !warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sh.bar.full_b[st]));   // a q block lands whole; its second half needs no bytes
+        const uint32_t full = smem_u32(&sh.bar.full[st]);
+        if (gs != 0) {
+          mbar_arrive(full);
+        } else if (!(withhold && i == 0)) {   // test hook: this block never arrives
+          mbar_arrive_expect_tx(full, C::kQItemBytes);
+          tma_load_3d(smem + C::kOffStage + st * C::kKStageBytes, &maps->q, full, 0, qrow0 + C::kQRows * j, 0);
+          issued[st] = 1, issued_phase[st] = ph;
+        }
+      }
+    }
+    for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
+      const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;
+      const uint32_t stage = smem + C::kOffStage + st * C::kKStageBytes;
+      int r[4];
+      g.step(p, lane, r);   // page k of request s.b (the walks agree)
+      if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      const uint32_t full = smem_u32(&sh.bar.full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(full, 4u * 512u * C::kKPartA);
+      __syncwarp();
+      if (lane < 4)
+#pragma unroll
+        for (int c = 0; c < static_cast<int>(C::kKPartA); ++c)
+          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full, c * 64, r);
+      issued[st] = 1, issued_phase[st] = ph;
+      if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      const uint32_t full_b = smem_u32(&sh.bar.full_b[st]);
+      if (lane == 0) mbar_arrive_expect_tx(full_b, 4u * 512u * (9 - C::kKPartA));
+      __syncwarp();
+      if (lane < 4)
+#pragma unroll
+        for (int c = C::kKPartA; c < 9; ++c)
+          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full_b, c * 64, r);
+      issued_b[st] = 1, issued_phase_b[st] = ph;
+    }
+  }
+  if (lane == 0)   // this slot's loads still in flight land before the CTA may exit
+    for (int st = 0; st < C::kKStages; ++st) {
+      if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
+      if (issued_b[st]) drain_bar(smem_u32(&sh.bar.full_b[st]), issued_phase_b[st]);
+    }
+  __syncwarp();
+}
+
+// Gathering slot gs of the O-CTA, sparse decode over a bf16 cache: the 512 value dims of its
+// rows of every page (tile::gather4), as two halves of four chunks.
+__device__ void o_producer_gather(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
+                                  uint32_t cl, int gs) {
+  using C = Cfg<false>;
+  const int lane = threadIdx.x & 31;
+  SegmentWalker w;
+  w.init(p, part);
+  Segment s;
+  uint32_t T = 0;
+  int issued[C::kVStages], issued_b[C::kVStages];
+  uint32_t issued_phase[C::kVStages], issued_phase_b[C::kVStages];
+  for (int j = 0; j < C::kVStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
+  constexpr int kHalf = static_cast<int>(C::kVChunks / 2);
+  bool ok = true;
+  GatherRows g;
+  g.init(p, part, gs, lane);
+  while (ok && w.next(s)) {
+    for (int k = s.kb; k < s.ke && ok; ++k, ++T) {
+      const uint32_t st = T % C::kVStages, ph = (T / C::kVStages) & 1;
+      const uint32_t stage = smem + C::kOffStage + st * C::kVStageBytes;
+      int r[4];
+      g.step(p, lane, r);
+      if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      const uint32_t full = smem_u32(&sh.bar.full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(full, 4u * 512u * kHalf);
+      __syncwarp();
+      if (lane < 4)
+#pragma unroll
+        for (int c = 0; c < kHalf; ++c)
+          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full, c * 64, r);
+      issued[st] = 1, issued_phase[st] = ph;
+      if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
+      const uint32_t full_b = smem_u32(&sh.bar.full_b[st]);
+      if (lane == 0) mbar_arrive_expect_tx(full_b, 4u * 512u * kHalf);
+      __syncwarp();
+      if (lane < 4)
+#pragma unroll
+        for (int c = kHalf; c < 2 * kHalf; ++c)
+          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full_b, c * 64, r);
+      issued_b[st] = 1, issued_phase_b[st] = ph;
+    }
+  }
+  if (lane == 0)   // this slot's loads still in flight land before the CTA may exit
+    for (int st = 0; st < C::kVStages; ++st) {
+      if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
+      if (issued_b[st]) drain_bar(smem_u32(&sh.bar.full_b[st]), issued_phase_b[st]);
+    }
+  __syncwarp();
+}
+
 // Lane 0 of warp 0 of the O-CTA: the 512 value dims of every page, as two halves
 // (bf16: chunks 0..3 and 4..7, 32 KiB each; FP8: chunks 0..1 and 2..3, 16 KiB each);
 // each half is refilled as soon as the PV MMAs that read it are done.
@@ -644,7 +819,7 @@ __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       const uint32_t sb = T & 1, sph = (T >> 1) & 1;
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.s_empty[sb]), sph ^ 1, p.status, cl)) { ok = false; break; }
-      if constexpr (sparse) fence_proxy_async_smem();   // gathered by cp.async: generic-proxy writes
+      if constexpr (sparse && F8) fence_proxy_async_smem();   // gathered by cp.async: generic-proxy writes
       tc_fence_after();
       const uint32_t kstage = smem + C::kOffStage + st * C::kKStageBytes;
       const uint32_t d = tmem + kSCol0 + sb * 64;
@@ -657,7 +832,7 @@ __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
           for (int x = 0; x < kTerms; ++x) step(d, kstage, c, j, x, (c | j | x) ? 1u : 0u);
       mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // part A may be refilled
       if (!warp_wait(sh, smem_u32(&sh.bar.full_b[st]), ph, p.status, cl)) { ok = false; break; }
-      if constexpr (sparse) fence_proxy_async_smem();
+      if constexpr (sparse && F8) fence_proxy_async_smem();
       tc_fence_after();
       if constexpr (F8) {
 #pragma unroll
@@ -1007,7 +1182,7 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       __syncwarp();
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.p_full[ps]), pph, p.status, cl, true)) { ok = false; break; }
-      if constexpr (sparse) fence_proxy_async_smem();
+      if constexpr (sparse && F8) fence_proxy_async_smem();
       // tail page: zero the value rows past the sequence end up to the next MMA-step
       // boundary, so that P = 0 never meets a non-finite value in the MMA (per half)
       const int nvalid = min(64, L - k * 64);
@@ -1065,7 +1240,7 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
         pv(0, vstage);                                  // output columns 0..255
         mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // the first half may be refilled
         if (!warp_wait(sh, smem_u32(&sh.bar.full_b[st]), ph, p.status, cl)) { ok = false; break; }
-        if constexpr (sparse) fence_proxy_async_smem();
+        if constexpr (sparse && F8) fence_proxy_async_smem();
         zero_tail(vstage + C::kVStageBytes / 2);
         __syncwarp();
         tc_fence_after();
@@ -1286,10 +1461,13 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     prefetch_tensormap(&maps.c4);
     sh.abort = 0;
     sh.cmd = 0;
-    // sparse: one arrival per gathering lane
+    // sparse: one arrival per gathering lane (FP8 cache, cp.async) or per gathering slot (bf16
+    // cache, TMA gathers); dense: the producer's one arrival with the expected bytes
     using SW = SparseWarps<kF8>;
     constexpr uint32_t kGroupWarps = (kSparse && SW::kOneWG) ? 4 : 8;   // softmax / epilogue warps
-    const uint32_t fills = kSparse ? 32u * static_cast<uint32_t>(is_s ? SW::kS : SW::kO) : 1u;
+    const uint32_t fills = !kSparse ? 1u
+                           : kF8    ? 32u * static_cast<uint32_t>(is_s ? SW::kS : SW::kO)
+                                    : static_cast<uint32_t>(kGatherSlots);
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(smem_u32(&sh.bar.full[i]), fills);
       mbar_init(smem_u32(&sh.bar.empty[i]), 1);
@@ -1326,27 +1504,33 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     if (b0 >= 0) prefetch_request(p, b0);
   }
 
+  // sparse over a bf16 cache: warp 0 gathers by TMA; over an FP8 cache: cp.async gathering warps
+  constexpr bool kGather = kSparse && !kF8;
   if (is_s) {
-    if (kSparse && SparseWarps<kF8>::slot(true, warp) >= 0) {   // the gathering warps
+    if (kGather && gather_slot<true>(warp) >= 0) {
+      s_producer_gather(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0, gather_slot<true>(warp));
+    } else if (kSparse && !kGather && SparseWarps<kF8>::slot(true, warp) >= 0) {   // the gathering warps
       s_producer_sparse<kF8>(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0,
                              SparseWarps<kF8>::slot(true, warp));
-    } else if (warp == 0) {
+    } else if (!kSparse && warp == 0) {
       if ((threadIdx.x & 31) == 0) s_producer<kF8>(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
     } else if (warp == 1) {
       s_cta_mma<kSparse, kF8>(p, sh, smem, part, cl);
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 12) {
       s_cta_softmax<kSparse, kF8>(p, sh, smem, part, cl, rb, peer);
     }
   } else {
-    if (kSparse && SparseWarps<kF8>::slot(false, warp) >= 0) {   // the gathering warps
+    if (kGather && gather_slot<false>(warp) >= 0) {
+      o_producer_gather(p, &maps, sh, smem, part, cl, gather_slot<false>(warp));
+    } else if (kSparse && !kGather && SparseWarps<kF8>::slot(false, warp) >= 0) {   // the gathering warps
       o_producer_sparse<kF8>(p, sh, smem, part, cl, SparseWarps<kF8>::slot(false, warp));
-    } else if (warp == 0) {
+    } else if (!kSparse && warp == 0) {
       if ((threadIdx.x & 31) == 0) o_producer<kF8>(p, &maps, sh, smem, part, cl);
     } else if (warp == 1) {
       o_cta_mma<kSparse, kF8>(p, sh, smem, part, cl);
     } else if (warp == 2) {
       if ((threadIdx.x & 31) == 0) o_cta_forwarder(p, sh, part, cl, peer);
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 12) {
       o_cta_epilogue<kSparse, kF8>(p, sh, smem, part, cl, rb);
     }
   }

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
 #include "mla_kernels.h"
@@ -102,12 +103,21 @@ bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, cons
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
   const int64_t cache_rows = num_blocks * kPageTokens;
-  return enc(&maps->k_a, kv_cache, cache_rows, 5) && enc(&maps->c4, kv_cache, cache_rows, 4) &&
+  // the sparse decode's row gathers: the cache as [row][576 dims], one 64-dim x 1-row box (a
+  // tile::gather4 load reads four such rows)
+  const cuuint64_t gdims[2] = {kDimQK, static_cast<cuuint64_t>(cache_rows)};
+  const cuuint64_t gstrides[1] = {kDimQK * 2};
+  const cuuint32_t gbox[2] = {64, 1};
+  const bool g4_ok = encode(&maps->g4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache), gdims,
+                            gstrides, gbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return g4_ok && enc(&maps->k_a, kv_cache, cache_rows, 5) && enc(&maps->c4, kv_cache, cache_rows, 4) &&
          enc(&maps->q, q, q_rows, kDimQK / 64);
 }
 
 bool encode_kv_maps_fp8(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache,
                         int64_t num_blocks, const void* q, int64_t q_rows) {
+  std::memset(&maps->g4, 0, sizeof(maps->g4));   // bf16 cache only
   const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks * kPageTokens);
   const cuuint32_t es[3] = {1, 1, 1};
   auto enc3 = [&](CUtensorMap* m, uint32_t chunks) {   // [chunk][row][128 codes] of dims 0..511

@@ -73,6 +73,7 @@ struct KvMaps {
   CUtensorMap c4;
   CUtensorMap q;
   CUtensorMap rope;   // FP8 cache only
+  CUtensorMap g4;     // bf16 cache as [cache row][576 dims], box 64 dims x 1 row (tile::gather4 loads)
 };
 // Encodes the maps for a bf16 cache of num_blocks pages and q_rows rows of q; false on
 // failure.
