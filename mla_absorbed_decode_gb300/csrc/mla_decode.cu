@@ -592,17 +592,22 @@ __device__ void s_producer_gather(const DecodeParams& p, const KvMaps* maps, Sha
         ok = false;
         break;
       }
+      // Every arrival of this slot is recorded for the exit drain: the drain waits for the
+      // phase of the slot's latest arrival on a stage's barrier, which the barrier cannot have
+      // passed by more than one phase (an older phase's parity could alias the current one).
+      const bool arrives = gs != 0 || !(withhold && i == 0);   // test hook: q block 0 never arrives
       if (lane == 0) {
         mbar_arrive(smem_u32(&sh.bar.full_b[st]));   // a q block lands whole; its second half needs no bytes
         const uint32_t full = smem_u32(&sh.bar.full[st]);
         if (gs != 0) {
           mbar_arrive(full);
-        } else if (!(withhold && i == 0)) {   // test hook: this block never arrives
+        } else if (arrives) {
           mbar_arrive_expect_tx(full, C::kQItemBytes);
           tma_load_3d(smem + C::kOffStage + st * C::kKStageBytes, &maps->q, full, 0, qrow0 + C::kQRows * j, 0);
-          issued[st] = 1, issued_phase[st] = ph;
         }
       }
+      issued_b[st] = 1, issued_phase_b[st] = ph;
+      if (arrives) issued[st] = 1, issued_phase[st] = ph;
     }
     for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
       const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;

@@ -139,8 +139,9 @@ def test_sparse_calls_return_promptly():
     that waited for an aliased, older phase of a stage barrier once stalled 0.5-1 s at
     exit, with the result still correct)."""
     import mla_absorbed_decode_gb300 as mla
-    L, k = 4096, 640   # ten gathered pages per request
-    for B in (6, 7, 9, 12):
+    # ten gathered pages per request at four batch sizes, and the V3.2 shape at half batch
+    # (top 2048 of 16384), whose schedule ends parts on segments of one page
+    for B, L, k in ((6, 4096, 640), (7, 4096, 640), (9, 4096, 640), (12, 4096, 640), (32, 16384, 2048)):
         inp = _case(B, 1, 128, [L] * B, seed=B)
         idx, kl = _lists([L] * B, [k] * B, seed=B)
         q, kv, bt, sl = (inp[x].cuda() for x in ("q", "kv_cache", "block_table", "seqlens"))
