@@ -108,9 +108,10 @@ bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, cons
   const cuuint64_t gdims[2] = {kDimQK, static_cast<cuuint64_t>(cache_rows)};
   const cuuint64_t gstrides[1] = {kDimQK * 2};
   const cuuint32_t gbox[2] = {64, 1};
+  // (128-byte L2 fills: a gathered row is 1152 bytes, and 256-byte fills would overrun its end)
   const bool g4_ok = encode(&maps->g4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache), gdims,
                             gstrides, gbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   return g4_ok && enc(&maps->k_a, kv_cache, cache_rows, 5) && enc(&maps->c4, kv_cache, cache_rows, 4) &&
          enc(&maps->q, q, q_rows, kDimQK / 64);
 }
