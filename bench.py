@@ -21,7 +21,10 @@ extend on the expanded path (extend_t512_l32768_h128_chunk4096: mla_extend_chunk
 Each timed step replays --inner passes (default 256) back to back from one CUDA graph,
 cycling over enough copies of the inputs, weights and buffers that more than 512 MiB
 is touched between two uses of a copy (L2 holds 126 MB), so that the timed region
-lasts long enough for the clock samples; ms_per_step is per pass.
+lasts long enough for the clock samples; ms_per_step is per pass.  The decode call and
+(with projections) each projection call are timed the same way on their own
+(roofline.ms_per_launch, projections_back_to_back_us); components_us is an eager
+per-call breakdown (events between the calls, host work included).
 --impl reference times the CPU oracle (numpy float64) on a bounded sample of
 the same workload per step.  With N > 1 (torchrun) every rank runs its own
 replica of the workload (requests shard across GPUs with no exchange).
@@ -626,8 +629,64 @@ def run_ours(args, w):
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
 
+    # the projection calls on their own, timed like the decode call: `inner` calls back to back
+    # from one CUDA graph, L2 flushed before each timed step (outside the timed region).  Each
+    # call cycles through its own copies of what it reads and writes (activations, weights,
+    # output), as many as it takes for more than 512 MiB to be touched between two uses of a
+    # copy, so that no call finds its operands in L2.  Kernel time per call, launches
+    # overlapping as in a step; the absorption is timed without the schedule's CTA.
+    proj_b2b = None
+    if w.with_projections:
+        def cycled(tensors):
+            nbytes = sum(t.numel() * t.element_size() for t in tensors)
+            k = min(inner, max(2, 1 + -(-(512 << 20) // nbytes)))
+            return [tensors] + [[t.clone() for t in tensors] for _ in range(k - 1)]
+
+        w_uk_op = w_uk_t if proj_fp8 else w_uk
+        w_uv_op = w_uv_t if proj_fp8 else w_uv
+        a_sets = cycled([q_nope, q_pe, positions, w_uk_op, step.q])
+        u_sets = cycled([step.out.view(B * s_q, H, 512), w_uv_op, step.o])
+
+        def timed_absorbs():
+            for j in range(inner):
+                qn, qp, pos_d, wk, qo = a_sets[j % len(a_sets)]
+                if proj_fp8:
+                    mla.absorb_q_fp8(qn, wk, w.w_scale, qo, q_pe=qp, positions=pos_d, workspace=fp8_ws)
+                else:
+                    mla.absorb_q(qn, wk, qo, q_pe=qp, positions=pos_d)
+
+        def timed_unabsorbs():
+            for j in range(inner):
+                ol, wv, oo = u_sets[j % len(u_sets)]
+                if proj_fp8:
+                    mla.unabsorb_o_fp8(ol, wv, w.w_scale, o=oo, workspace=fp8_ws)
+                else:
+                    mla.unabsorb_o(ol, wv, o=oo)
+
+        proj_b2b = {}
+        for name, fn in (("absorb", timed_absorbs), ("unabsorb", timed_unabsorbs)):
+            fn()   # warm-up (and the graph's first capture sees every copy)
+            torch.cuda.synchronize()
+            g = fn if args.eager else _graphed(torch, fn, dev)
+            t = []
+            for i in range(args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g()
+                e1.record()
+                torch.cuda.synchronize()
+                t.append(e0.elapsed_time(e1) * 1e3 / inner)
+            proj_b2b[name] = round(statistics.mean(t), 2)
+        proj_b2b["copies"] = {"absorb": len(a_sets), "unabsorb": len(u_sets)}
+        del a_sets, u_sets
+        status = mla.get_device_status()
+        if status != 0:
+            raise RuntimeError(f"device status {status} timing the projections")
+
     # per-call breakdown of a step, outside the timed region: eager calls with events
-    # between them (so without launch overlap), L2 flushed before each step
+    # between them (so without launch overlap, and with each call's host work between its
+    # events), L2 flushed before each step
     comp = {"schedule": [], "absorb": [], "decode_and_combine": [], "unabsorb": []}
     for i in range(args.steps):
         flush.zero_()
@@ -840,6 +899,7 @@ def run_ours(args, w):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "components_us": components,
+            "projections_back_to_back_us": proj_b2b,
             "gpu_launches": (launches_per_step + 2) * args.steps * inner,
             "clocks": clocks.summary(),
         }
