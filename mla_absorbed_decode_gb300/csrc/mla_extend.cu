@@ -469,11 +469,14 @@ mla_attend_kernel(const __grid_constant__ CUtensorMap qn_map, const __grid_const
         l *= fast_exp2(m - m_k);
         m = m_k;
       }
-      if (ok && m_k != m_in && k > 0 && m_in != -INFINITY) {
-        // this tile moves the reference: O (every earlier tile, once the PV of tile k - 1 is
-        // done; the MMAs complete in order) scales by 2^(m_in - m_k).  With m_in = -inf every
-        // earlier P was 0, and so is O.
-        const float alpha = fast_exp2(m_in - m_k);
+      // A row whose reference this tile moves has O (every earlier tile, once the PV of tile
+      // k - 1 is done; the MMAs complete in order) scaled by 2^(m_in - m_k); with m_in = -inf
+      // every earlier P was 0, and so is O.  The decision is per row, but the wait and the
+      // TMEM loads and stores are warp-wide: if any row of the warp moves, the whole warp
+      // rescales, by 1 where its row does not.
+      const bool moves = m_k != m_in && k > 0 && m_in != -INFINITY;
+      if (ok && __any_sync(0xffffffffu, moves)) {
+        const float alpha = moves ? fast_exp2(m_in - m_k) : 1.f;
         ok = __all_sync(0xffffffffu,
                         ext_wait(smem_u32(&pv_done[(k - 1) % kAttWG]), ((k - 1) / kAttWG) & 1, p.status));
         if (ok) {

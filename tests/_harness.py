@@ -80,16 +80,21 @@ def oracle_decode(inp: dict, batches=None):
 
 
 def compare(out_gpu: torch.Tensor, lse_gpu: torch.Tensor, ref_out: np.ndarray, ref_lse: np.ndarray,
-            ref_abs: np.ndarray | None = None, what: str = "", lse_extra: np.ndarray | None = None):
+            ref_abs: np.ndarray | None = None, what: str = "", lse_extra: np.ndarray | None = None,
+            out_extra: np.ndarray | None = None):
     """ref_abs given (inputs with outliers): elementwise bound max(2e-2, 2^-7 * ref_abs).
     lse_extra (per row): an added allowance on lse for a path that rounds its keys to bf16
-    before the scores (the expanded path; see expanded_score_allowance)."""
+    before the scores (the expanded path; see expanded_score_allowance).  out_extra (per
+    element): an added allowance on the output for the same reason (see
+    expanded_output_allowance)."""
     o = to_np(out_gpu)
     lo = to_np(lse_gpu)
     assert o.shape == ref_out.shape, (o.shape, ref_out.shape)
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
     d = np.abs(o - ref_out)
     bound = np.maximum(OUT_ABS, OUT_REL_ULP * ref_abs) if ref_abs is not None else OUT_ABS
+    if out_extra is not None:
+        bound = bound + out_extra
     worst = np.unravel_index(np.argmax(d - bound), d.shape)
     assert np.all(d <= bound), f"{what}: max|dout|={d.max():.4g} at {worst} (ref {ref_out[worst]:.4g})"
     nrm = np.linalg.norm(ref_out)
@@ -109,6 +114,14 @@ def compare(out_gpu: torch.Tensor, lse_gpu: torch.Tensor, ref_out: np.ndarray, r
 
 def make(w: W.Workload, seed=0, **kw):
     return W.make_inputs(w, seed=seed, **kw)
+
+
+def expanded_output_allowance(score_allowance, ref_abs):
+    """If every score of a row moves by at most d (score_allowance, per (query, head)), each
+    softmax weight p_t moves by a factor within [e^-2d, e^2d] (numerator and normaliser each by
+    at most e^d), so an output element sum_t p_t v_t moves by at most (e^2d - 1) sum_t p_t |v_t|
+    = (e^2d - 1) * ref_abs.  Returns that bound per element (ref_abs [T, H, 128])."""
+    return np.expm1(2.0 * np.asarray(score_allowance))[..., None] * np.asarray(ref_abs)
 
 
 def expanded_score_allowance(q_nope, k_nope, softmax_scale, qpos):

@@ -8,7 +8,7 @@ import torch
 import oracle
 from mla_absorbed_decode_gb300 import workloads as W
 
-from _harness import compare, expanded_score_allowance, to_np
+from _harness import compare, expanded_output_allowance, expanded_score_allowance, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -96,3 +96,53 @@ def test_extend_reports_a_bad_block_table_entry():
                        inp["kv_cache"].cuda(), row.cuda(), seqlen, inp["softmax_scale"], chunk_tokens=64)
     assert mla.get_device_status() == 6      # MLA_ERR_DEVICE_BOUNDS
     assert mla.get_device_status() == 0
+
+
+def _rebases_by_warpgroup(s_log2, L, T, chunk):
+    """The attention kernel's rebase rule replayed on exact scores: per chunk, 64-key tiles
+    in order; a row's reference maximum moves when a tile's maximum exceeds it by more than
+    2^8; tile k of a chunk is processed by softmax warpgroup k % 2.  Counts the moves after
+    each chunk's first two tiles, per warpgroup."""
+    qpos = np.arange(L - T, L)
+    late = [0, 0]
+    for c0 in range(0, L, chunk):
+        c1 = min(L, c0 + chunk)
+        ref = np.full(s_log2.shape[:2], -np.inf)
+        for k, t0 in enumerate(range(c0, c1, 64)):
+            keys = np.arange(t0, min(c1, t0 + 64))
+            vis = keys[None, :] <= qpos[:, None]
+            m = np.where(vis[:, None, :], s_log2[:, :, keys], -np.inf).max(axis=2)
+            move = m > ref + 8
+            if k >= 2:
+                late[k % 2] += int(move.sum())
+            ref = np.where(move, m, ref)
+    return late
+
+
+def test_extend_rebases_the_reference_maximum_in_both_warpgroups():
+    # cache rows scaled x2 .. x8 at planted positions make the row maxima grow past the lazy
+    # rebase threshold late in a chunk, on tiles of both parities (both softmax warpgroups:
+    # the one whose tile moves the reference rescales O, each rescales its own row sum)
+    T, L, H, chunk = 37, 2100, 16, 1024
+    inp = _case(T, L, H, seed=11)
+    bt = inp["block_table"][0]
+    for t, f in {200: 2.0, 520: 4.0, 840: 8.0, 1400: 4.0, 1800: 8.0}.items():
+        inp["kv_cache"][bt[t // 64], t % 64] = (inp["kv_cache"][bt[t // 64], t % 64].float() * f).to(torch.bfloat16)
+    rows = oracle.gather_request(inp["kv_cache"].float().numpy(), bt.numpy(), L)
+    k_nope, k_pe, v = oracle.expand_chunk(rows, to_np(inp["w_uk"]), to_np(inp["w_uv"]))
+    qn, qp = to_np(inp["q_nope"]), to_np(inp["q_pe"])
+    s = (np.einsum("thd,hnd->thn", qn, k_nope) + np.einsum("thd,nd->thn", qp, k_pe)) * inp["softmax_scale"]
+    late = _rebases_by_warpgroup(s * np.log2(np.e), L, T, chunk)
+    assert min(late) > 0, late   # the case exercises what it is meant to
+    out, lse = _run(inp, L, chunk)
+    ref_o, ref_l = _ref(inp, L, chunk)
+    # magnitude of each output element (outlier rows are not unit-scale): attention to |v|
+    qpos = np.arange(L - T, L)
+    ref_abs, _ = oracle.attend_chunk(qn, qp, k_nope, k_pe, np.abs(v), np.arange(L), qpos, inp["softmax_scale"])
+    # With x8 rows the scores are large, and rounding the expanded keys to bf16 (the path's
+    # definition) moves P by a few percent on rows that a few outlier tokens dominate: the
+    # output gets the allowance that follows from the score allowance (a mistake in the
+    # rescales would be off by up to a factor of 2^8).
+    extra = _allowance(inp, L)
+    compare(out, lse, ref_o, ref_l, ref_abs=ref_abs, what="extend with planted outlier rows", lse_extra=extra,
+            out_extra=expanded_output_allowance(extra, ref_abs))

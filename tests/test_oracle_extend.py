@@ -79,3 +79,25 @@ def test_pins_catch_planted_mistakes(monkeypatch):
             plant(m)
             assert not _pins_hold(), f"planted mistake not caught: {name}"
     assert _pins_hold()
+
+
+def test_output_allowance_covers_score_moves():
+    # the parity harness's expanded-path output allowance: if every score of a row moves by at
+    # most d, an attention output moves by at most (e^2d - 1) * sum_t p_t |v_t|; checked on
+    # random rows and values with random moves inside d, including moves of +d / -d on
+    # different keys (the worst case)
+    import sys, os
+    sys.path.insert(0, os.path.dirname(__file__))
+    from _harness import expanded_output_allowance
+    rng = np.random.default_rng(3)
+    for trial in range(200):
+        n = int(rng.integers(1, 50))
+        s = rng.normal(0, 3, n)
+        v = rng.normal(0, 2, (n, 4))
+        d = float(rng.uniform(0, 0.3))
+        ds = rng.choice([-d, d], n) if trial % 2 else rng.uniform(-d, d, n)
+        p = np.exp(s - s.max()); p /= p.sum()
+        p2 = np.exp(s + ds - (s + ds).max()); p2 /= p2.sum()
+        moved = np.abs(p2 @ v - p @ v)
+        bound = expanded_output_allowance(np.array([[d]]), (p @ np.abs(v))[None, None, :])[0, 0]
+        assert np.all(moved <= bound * (1 + 1e-12) + 1e-15), (trial, moved, bound)
