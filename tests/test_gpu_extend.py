@@ -56,6 +56,7 @@ def _allowance(inp, seqlen):
     (64, 64, 8, (64,)),                # a prefill without a prefix (T = seqlen)
     (3, 256, 128, (128,)),             # all 128 heads
     (37, 2100, 16, (1024, 2048)),      # a longer prefix, a chunk boundary inside a query tile's view
+    (300, 300, 2, (64, 128)),          # a prefill of three query tiles: the first sees none of the later chunks
 ])
 def test_extend_chunked_matches_the_oracle(T, seqlen, H, chunks):
     inp = _case(T, seqlen, H, seed=T + seqlen + H)
