@@ -40,8 +40,8 @@
 // one elected lane issues), warp 2 = credit forwarder (O-CTA), warps 4..7 and
 // 8..11 = two softmax (S-CTA) or rescale/epilogue (O-CTA) warpgroups; a thread
 // of a warpgroup owns one query row (its TMEM lane).  The sparse decode runs 512 threads:
-// over a bf16 cache warp 0 gathers its pages by TMA (tile::gather4, s_producer_gather);
-// over an FP8 cache gathering warps copy them with cp.async (SparseWarps below).
+// four gathering warps per CTA load its pages' rows by TMA (tile::gather4,
+// s_producer_gather / o_producer_gather).
 // Every barrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT,
 // raises an abort flag in every CTA of its cluster, drains what it has in
 // flight and exits.
@@ -60,7 +60,7 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 384;          // 12 warps; the sparse decode runs 16 (see SparseWarps)
+constexpr int kThreads = 384;          // 12 warps; the sparse decode runs 16 (see gather_slot)
 template <bool kSparse, bool kF8>
 constexpr int threads_of() { return kSparse ? 512 : kThreads; }
 constexpr int kMaxStages = 4;                         // barrier slots: the deepest page ring
@@ -278,9 +278,8 @@ __device__ __forceinline__ int request_block(const DecodeParams& p, int b, int k
 // Sparse decode ("为什么 MLA + MTP 容易吃亏？" section 6: the selected latents are
 // gathered by index): page k of request b is entries [64k, 64k + 64) of its list, and
 // entry e is the token at position t = indices[b][e], read through the block table
-// like a dense token.  A whole warp gathers a page with 16-byte cp.async copies into
-// the same swizzled layout a TMA box would produce; the stage's barrier expects one
-// arrival per lane (cp.async.mbarrier.arrive.noinc when the lane's copies land).
+// like a dense token.  The rows are loaded by TMA row gathers (below) into the same
+// swizzled layout a 64-row TMA box produces.
 
 // The row lookups run ahead of the copies: a lane loads the list entry of its row two
 // pages ahead and that token's block-table entry one page ahead, so that the two
@@ -372,159 +371,17 @@ struct RowLookahead {
   }
 };
 
-// Gathering warps of the sparse decode over an FP8 cache (the bf16 cache is gathered by TMA,
-// see s_producer_gather).  Gathering warp slot ws owns rows
-// [gather_r0(ws), gather_r0(ws + 1)) of each page; lane l looks up row gather_r0(ws) + l.
-// The kernel runs 16 warps (its registers fit 128 a thread in both cache formats): the
-// S-CTA gathers with warps 0, 2, 3 and 12..15, the O-CTA with warps 0, 3 and 12..15 (one
-// warp sustains only a few GB/s of 16-byte copies), and the softmax and the epilogue keep
-// both warpgroups (4..11) as in the dense decode.  With 12 warps and one warpgroup for the
-// softmax (kOneWG, warps 8..11 gathering) the softmax took ~1.6 us (bf16) / ~2 us (FP8) of
-// each page and set the period; with two but only warps 0, 2, 3 / 0, 3 gathering, the
-// gather did.
-template <bool F8>
-struct SparseWarps {
-  static constexpr bool kOneWG = false;   // true: the softmax / epilogue on warps 4..7 only
-  static constexpr int kS = 7, kO = 6;
-  static constexpr int kFirstExtra = kOneWG ? 8 : 12;   // warps kFirstExtra..kFirstExtra+3 gather
-  // gathering warp slot of warp `warp`, or -1
-  __device__ static int slot(bool is_s, int warp) {
-    if (warp == 0) return 0;
-    if (warp >= kFirstExtra) return warp - kFirstExtra + (is_s ? 3 : 2);
-    if (is_s) return (warp == 2 || warp == 3) ? warp - 1 : -1;
-    return warp == 3 ? 1 : -1;
-  }
-};
-__device__ __forceinline__ int gather_r0(int ws, int nwarps) { return ws * 64 / nwarps; }
-
-// The warp copies units [u0, u0 + kPerRow) (unit u = bytes 16u..16u+15 of a row: bf16 dims
-// 8u..8u+7 or FP8 dims 16u..16u+15; chunk u / 8) of rows
-// [r0, r0 + nrows) of the page into `stage` (chunk c at c * 8192, row r at r * 128,
-// 128-byte swizzle), the (row, unit) pairs spread evenly over the lanes; `mine` is the
-// address of row r0 + lane (nullptr: not gathered).
-template <int kPerRow>
-__device__ __forceinline__ void gather_rows(uint32_t stage, const __nv_bfloat16* mine, int r0, int nrows, int u0,
-                                            int lane) {
-  const int total = nrows * kPerRow;
-  for (int j0 = 0; j0 < total; j0 += 32) {
-    const int j = j0 + lane;
-    const int rr = j < total ? j / kPerRow : 0;
-    const uint64_t src = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(mine), rr);
-    if (j < total && src != 0) {
-      const int u = u0 + j % kPerRow, r = r0 + rr, c = u >> 3, v = u & 7;
-      cp_async16(stage + c * 8192 + r * 128 + ((v ^ (r & 7)) << 4), reinterpret_cast<const __nv_bfloat16*>(src) + u * 8);
-    }
-  }
-}
-
-// Gathering warp ws of the S-CTA, sparse decode: the q blocks by TMA (lane 0 of warp
-// 0) and its rows of every page by cp.async, through the same stages as the dense
-// producer; a stage's barriers expect one arrival per gathering lane.  The row
-// addresses of the next page are looked up while the current page's copies fly.
-// Part A of a page is its first kKPartA chunks (bf16: dims 0..319; FP8: 0..511), part B
-// the rest of the row (FP8: the 64 RoPE codes, the first half of the fifth chunk).
-template <bool F8>
-__device__ void s_producer_sparse(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
-                                  uint32_t cl, int rb, bool withhold, int ws) {
-  using C = Cfg<F8>;
-  constexpr int kRowUnits = F8 ? kDimQK / 16 : kDimQK / 8;   // 16-byte units of a cached row
-  constexpr int kUnitsA = static_cast<int>(C::kKPartA) * 8;
-  const int lane = threadIdx.x & 31;
-  const bool issuer = (ws == 0 && lane == 0);
-  const int r0 = gather_r0(ws, SparseWarps<F8>::kS), nrows = gather_r0(ws + 1, SparseWarps<F8>::kS) - r0;
-  SegmentWalker w;
-  w.init(p, part);
-  Segment s;
-  uint32_t i = 0;
-  int issued[C::kKStages];
-  uint32_t issued_phase[C::kKStages];
-  for (int j = 0; j < C::kKStages; ++j) issued[j] = 0, issued_phase[j] = 0;
-  bool ok = true;
-  RowLookahead<F8> look;
-  look.init(p, part, r0 + lane, lane < nrows);
-  while (ok && w.next(s)) {
-    const int qrow0 = s.b * p.rows + rb * 128;
-    for (int j = 0; j < C::kQItems && ok; ++j, ++i) {
-      const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;
-      if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl) ||
-          !warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive(smem_u32(&sh.bar.full_b[st]));   // a q block lands whole; its second half needs no bytes
-      const uint32_t full = smem_u32(&sh.bar.full[st]);
-      if (!issuer) {
-        mbar_arrive(full);
-      } else if (!(withhold && i == 0)) {   // test hook: this block never arrives
-        mbar_arrive_expect_tx(full, C::kQItemBytes);
-        tma_load_3d(smem + C::kOffStage + st * C::kKStageBytes, &maps->q, full, 0, qrow0 + C::kQRows * j, 0);
-        issued[st] = 1, issued_phase[st] = ph;
-      }
-    }
-    for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
-      const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;
-      const uint32_t stage = smem + C::kOffStage + st * C::kKStageBytes;
-      const __nv_bfloat16* mine = look.step(p);   // page k of request s.b (the walks agree)
-      if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      // the stage's latest use is now a gathered page (waited for by cp.async.wait_all): the
-      // drain below must not wait for an older phase of its barrier, whose parity can alias
-      issued[st] = 0;
-      gather_rows<kUnitsA>(stage, mine, r0, nrows, 0, lane);
-      cp_async_arrive_noinc(smem_u32(&sh.bar.full[st]));
-      if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      gather_rows<kRowUnits - kUnitsA>(stage, mine, r0, nrows, kUnitsA, lane);
-      cp_async_arrive_noinc(smem_u32(&sh.bar.full_b[st]));
-    }
-  }
-  cp_async_wait_all();   // this lane's copies land before the CTA may exit
-  if (issuer)   // a q block whose stage saw no later page may still be in flight (after an abort)
-    for (int st = 0; st < C::kKStages; ++st)
-      if (issued[st]) drain_bar(smem_u32(&sh.bar.full[st]), issued_phase[st]);
-  __syncwarp();
-}
-
-// Gathering warp ws of the O-CTA, sparse decode: its rows' 512 value dims of every page,
-// as two halves of kVChunks / 2 chunks.
-template <bool F8>
-__device__ void o_producer_sparse(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int ws) {
-  using C = Cfg<F8>;
-  constexpr int kHalfUnits = static_cast<int>(C::kVChunks / 2) * 8;
-  const int lane = threadIdx.x & 31;
-  const int r0 = gather_r0(ws, SparseWarps<F8>::kO), nrows = gather_r0(ws + 1, SparseWarps<F8>::kO) - r0;
-  SegmentWalker w;
-  w.init(p, part);
-  Segment s;
-  uint32_t T = 0;
-  bool ok = true;
-  RowLookahead<F8> look;
-  look.init(p, part, r0 + lane, lane < nrows);
-  while (ok && w.next(s)) {
-    for (int k = s.kb; k < s.ke && ok; ++k, ++T) {
-      const uint32_t st = T % C::kVStages, ph = (T / C::kVStages) & 1;
-      const uint32_t stage = smem + C::kOffStage + st * C::kVStageBytes;
-      const __nv_bfloat16* mine = look.step(p);   // page k of request s.b
-      if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      gather_rows<kHalfUnits>(stage, mine, r0, nrows, 0, lane);
-      cp_async_arrive_noinc(smem_u32(&sh.bar.full[st]));
-      if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
-      gather_rows<kHalfUnits>(stage, mine, r0, nrows, kHalfUnits, lane);
-      cp_async_arrive_noinc(smem_u32(&sh.bar.full_b[st]));
-    }
-  }
-  cp_async_wait_all();
-  __syncwarp();
-}
-
-// ------------------------------------------------ sparse gather by TMA (bf16) --
-// Over a bf16 cache the sparse decode gathers a page's 64 rows by TMA, four rows per
-// tile::gather4 load over a 2-D view of the cache ([cache row][576 dims], a 64-dim x 1-row
-// box).  The load writes its four 128-byte rows at 128-byte steps and swizzles each by its
-// own shared-memory address, so 16 loads per 64-dim chunk (destinations 512 bytes apart)
-// fill the chunk in the layout a 64-row box produces.  One warp per CTA: lane l looks up
-// rows l and l + 32 of every page (RowLookahead, the lookups running ahead of the loads), and
-// lanes 0..15 each load one group of four rows, chunk by chunk.  A row past the request's list,
-// or one whose lookup fails the bounds checks (reported as for the cp.async gather), loads
-// cache row 0, which is always in range: the softmax masks it by its list position.
+// ------------------------------------------------------ sparse gather by TMA --
+// The sparse decode gathers a page's 64 rows by TMA, four rows per tile::gather4 load over a
+// 2-D view of the cache ([cache row][576 values], a box one chunk wide and one row high: 64
+// bf16 values, or 128 E4M3 codes).  The load writes its four 128-byte rows at 128-byte steps
+// and swizzles each by its own shared-memory address, so 16 loads per chunk (destinations 512
+// bytes apart) fill the chunk in the layout a 64-row box produces.  Four warps per CTA
+// (gather_slot): each looks up 16 rows of every page (RowLookahead, the lookups running ahead
+// of the loads) and four of its lanes load its four groups of four rows, chunk by chunk.  A row
+// past the request's list, or one whose lookup fails the bounds checks (reported as a bounds
+// error), loads cache row 0, which is always in range: the softmax masks it by its list
+// position.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
                                             const int (&r)[4]) {
   asm volatile(
@@ -545,8 +402,9 @@ __device__ __forceinline__ int gather_slot(int warp) {   // S-CTA: warps 0, 2, 3
   if (IsS) return warp == 2 ? 1 : warp == 3 ? 2 : warp == 12 ? 3 : -1;
   return warp == 3 ? 1 : warp == 12 ? 2 : warp == 13 ? 3 : -1;
 }
+template <bool F8>
 struct GatherRows {
-  RowLookahead<false> look;
+  RowLookahead<F8> look;
   int gs;
   __device__ void init(const DecodeParams& p, int part, int slot, int lane) {
     gs = slot;
@@ -554,7 +412,7 @@ struct GatherRows {
   }
   __device__ static int row_of(const DecodeParams& p, const __nv_bfloat16* row) {
     return row ? static_cast<int>((reinterpret_cast<const uint8_t*>(row) - reinterpret_cast<const uint8_t*>(p.kv)) /
-                                  (2 * kDimQK))
+                                  (F8 ? kDimQK : 2 * kDimQK))
                : 0;
   }
   // The next page's group of four cache rows of lane `lane` (meaningful for lanes 0..3: rows
@@ -566,12 +424,14 @@ struct GatherRows {
   }
 };
 
-// Gathering slot gs of the S-CTA, sparse decode over a bf16 cache: the q blocks (slot 0, TMA
+// Gathering slot gs of the S-CTA, sparse decode: the q blocks (slot 0, TMA
 // boxes; the other slots only arrive) and its rows of every page (tile::gather4), part A
 // (chunks 0..kKPartA-1) and part B as in the dense producer.
+template <bool F8>
 __device__ void s_producer_gather(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
                                   uint32_t cl, int rb, bool withhold, int gs) {
-  using C = Cfg<false>;
+  using C = Cfg<F8>;
+  constexpr int kX = F8 ? 128 : 64;   // elements of a chunk's row
   const int lane = threadIdx.x & 31;
   SegmentWalker w;
   w.init(p, part);
@@ -581,7 +441,7 @@ __device__ void s_producer_gather(const DecodeParams& p, const KvMaps* maps, Sha
   uint32_t issued_phase[C::kKStages], issued_phase_b[C::kKStages];
   for (int j = 0; j < C::kKStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
   bool ok = true;
-  GatherRows g;
+  GatherRows<F8> g;
   g.init(p, part, gs, lane);
   while (ok && w.next(s)) {
     const int qrow0 = s.b * p.rows + rb * 128;
@@ -621,16 +481,18 @@ __device__ void s_producer_gather(const DecodeParams& p, const KvMaps* maps, Sha
       if (lane < 4)
 #pragma unroll
         for (int c = 0; c < static_cast<int>(C::kKPartA); ++c)
-          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full, c * 64, r);
+          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full, c * kX, r);
       issued[st] = 1, issued_phase[st] = ph;
       if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
       const uint32_t full_b = smem_u32(&sh.bar.full_b[st]);
-      if (lane == 0) mbar_arrive_expect_tx(full_b, 4u * 512u * (9 - C::kKPartA));
+      if (lane == 0) mbar_arrive_expect_tx(full_b, 4u * 512u * (C::kKChunks - C::kKPartA));
       __syncwarp();
+      // (FP8: the RoPE chunk is bytes 512..639 of a row, 576..639 filled with zeros, as in the
+      // dense loads: the MMAs never read that half)
       if (lane < 4)
 #pragma unroll
-        for (int c = C::kKPartA; c < 9; ++c)
-          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full_b, c * 64, r);
+        for (int c = C::kKPartA; c < static_cast<int>(C::kKChunks); ++c)
+          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full_b, c * kX, r);
       issued_b[st] = 1, issued_phase_b[st] = ph;
     }
   }
@@ -642,11 +504,13 @@ __device__ void s_producer_gather(const DecodeParams& p, const KvMaps* maps, Sha
   __syncwarp();
 }
 
-// Gathering slot gs of the O-CTA, sparse decode over a bf16 cache: the 512 value dims of its
+// Gathering slot gs of the O-CTA, sparse decode: the 512 value dims of its
 // rows of every page (tile::gather4), as two halves of four chunks.
+template <bool F8>
 __device__ void o_producer_gather(const DecodeParams& p, const KvMaps* maps, Shared& sh, uint32_t smem, int part,
                                   uint32_t cl, int gs) {
-  using C = Cfg<false>;
+  using C = Cfg<F8>;
+  constexpr int kX = F8 ? 128 : 64;   // elements of a chunk's row
   const int lane = threadIdx.x & 31;
   SegmentWalker w;
   w.init(p, part);
@@ -657,7 +521,7 @@ __device__ void o_producer_gather(const DecodeParams& p, const KvMaps* maps, Sha
   for (int j = 0; j < C::kVStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
   constexpr int kHalf = static_cast<int>(C::kVChunks / 2);
   bool ok = true;
-  GatherRows g;
+  GatherRows<F8> g;
   g.init(p, part, gs, lane);
   while (ok && w.next(s)) {
     for (int k = s.kb; k < s.ke && ok; ++k, ++T) {
@@ -672,7 +536,7 @@ __device__ void o_producer_gather(const DecodeParams& p, const KvMaps* maps, Sha
       if (lane < 4)
 #pragma unroll
         for (int c = 0; c < kHalf; ++c)
-          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full, c * 64, r);
+          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full, c * kX, r);
       issued[st] = 1, issued_phase[st] = ph;
       if (!warp_wait(sh, smem_u32(&sh.bar.empty_b[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
       const uint32_t full_b = smem_u32(&sh.bar.full_b[st]);
@@ -681,7 +545,7 @@ __device__ void o_producer_gather(const DecodeParams& p, const KvMaps* maps, Sha
       if (lane < 4)
 #pragma unroll
         for (int c = kHalf; c < 2 * kHalf; ++c)
-          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full_b, c * 64, r);
+          tma_gather4(stage + c * kChunk + (4 * gs + lane) * 512, &maps->g4, full_b, c * kX, r);
       issued_b[st] = 1, issued_phase_b[st] = ph;
     }
   }
@@ -824,7 +688,6 @@ __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       const uint32_t sb = T & 1, sph = (T >> 1) & 1;
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.s_empty[sb]), sph ^ 1, p.status, cl)) { ok = false; break; }
-      if constexpr (sparse && F8) fence_proxy_async_smem();   // gathered by cp.async: generic-proxy writes
       tc_fence_after();
       const uint32_t kstage = smem + C::kOffStage + st * C::kKStageBytes;
       const uint32_t d = tmem + kSCol0 + sb * 64;
@@ -837,7 +700,6 @@ __device__ void s_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
           for (int x = 0; x < kTerms; ++x) step(d, kstage, c, j, x, (c | j | x) ? 1u : 0u);
       mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // part A may be refilled
       if (!warp_wait(sh, smem_u32(&sh.bar.full_b[st]), ph, p.status, cl)) { ok = false; break; }
-      if constexpr (sparse && F8) fence_proxy_async_smem();
       tc_fence_after();
       if constexpr (F8) {
 #pragma unroll
@@ -951,9 +813,8 @@ template <bool sparse, bool F8>
 __device__ void s_cta_softmax(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb,
                               uint32_t peer) {
   using C = Cfg<F8>;
-  // Two warpgroups, each covering 32 of a page's 64 columns; sparse over a bf16 cache:
-  // one warpgroup covering all 64 in two passes (the other four warps gather).
-  constexpr int kWG = (sparse && SparseWarps<F8>::kOneWG) ? 1 : 2;
+  // Two warpgroups, each covering 32 of a page's 64 columns.
+  constexpr int kWG = 2;
   constexpr uint32_t kST = kWG * 128;      // softmax threads
   constexpr int kPieces = 2 / kWG;         // 32-column pieces per thread and page
   const int t = threadIdx.x - 128;
@@ -1187,7 +1048,6 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
       __syncwarp();
       if (!warp_wait(sh, smem_u32(&sh.bar.full[st]), ph, p.status, cl)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.p_full[ps]), pph, p.status, cl, true)) { ok = false; break; }
-      if constexpr (sparse && F8) fence_proxy_async_smem();
       // tail page: zero the value rows past the sequence end up to the next MMA-step
       // boundary, so that P = 0 never meets a non-finite value in the MMA (per half)
       const int nvalid = min(64, L - k * 64);
@@ -1245,8 +1105,7 @@ __device__ void o_cta_mma(const DecodeParams& p, Shared& sh, uint32_t smem, int 
         pv(0, vstage);                                  // output columns 0..255
         mma_commit_warp(smem_u32(&sh.bar.empty[st]));   // the first half may be refilled
         if (!warp_wait(sh, smem_u32(&sh.bar.full_b[st]), ph, p.status, cl)) { ok = false; break; }
-        if constexpr (sparse && F8) fence_proxy_async_smem();
-        zero_tail(vstage + C::kVStageBytes / 2);
+          zero_tail(vstage + C::kVStageBytes / 2);
         __syncwarp();
         tc_fence_after();
         pv(1, vstage + C::kVStageBytes / 2);            // output columns 256..511
@@ -1298,12 +1157,11 @@ __device__ void o_cta_forwarder(const DecodeParams& p, Shared& sh, int part, uin
 
 // Warps 4..11 of the O-CTA: rescale O rows, or normalise and store a finished
 // segment.  Warpgroup wg owns O columns [256 wg, 256 wg + 256).
-// Two warpgroups, one per 256-column half of O; sparse over a bf16 cache: warps 4..7 alone
-// cover both halves (warps 8..11 gather).
+// Two warpgroups, one per 256-column half of O.
 template <bool sparse, bool F8>
 __device__ void o_cta_epilogue(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int rb) {
   using C = Cfg<F8>;
-  constexpr int kHalves = (sparse && SparseWarps<F8>::kOneWG) ? 2 : 1;   // 256-column halves of O per thread
+  constexpr int kHalves = 1;   // 256-column halves of O per thread
   const int t = threadIdx.x - 128;
   const int wg = t >> 7;
   const int r = t & 127;
@@ -1466,13 +1324,10 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     prefetch_tensormap(&maps.c4);
     sh.abort = 0;
     sh.cmd = 0;
-    // sparse: one arrival per gathering lane (FP8 cache, cp.async) or per gathering slot (bf16
-    // cache, TMA gathers); dense: the producer's one arrival with the expected bytes
-    using SW = SparseWarps<kF8>;
-    constexpr uint32_t kGroupWarps = (kSparse && SW::kOneWG) ? 4 : 8;   // softmax / epilogue warps
-    const uint32_t fills = !kSparse ? 1u
-                           : kF8    ? 32u * static_cast<uint32_t>(is_s ? SW::kS : SW::kO)
-                                    : static_cast<uint32_t>(kGatherSlots);
+    // sparse: one arrival per gathering warp, each with its own bytes; dense: the producer's one
+    // arrival with the expected bytes
+    constexpr uint32_t kGroupWarps = 8;   // softmax / epilogue warps
+    const uint32_t fills = kSparse ? static_cast<uint32_t>(kGatherSlots) : 1u;
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(smem_u32(&sh.bar.full[i]), fills);
       mbar_init(smem_u32(&sh.bar.empty[i]), 1);
@@ -1509,14 +1364,10 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     if (b0 >= 0) prefetch_request(p, b0);
   }
 
-  // sparse over a bf16 cache: warp 0 gathers by TMA; over an FP8 cache: cp.async gathering warps
-  constexpr bool kGather = kSparse && !kF8;
+  // sparse: four gathering warps load the listed rows by TMA (s_producer_gather / o_producer_gather)
   if (is_s) {
-    if (kGather && gather_slot<true>(warp) >= 0) {
-      s_producer_gather(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0, gather_slot<true>(warp));
-    } else if (kSparse && !kGather && SparseWarps<kF8>::slot(true, warp) >= 0) {   // the gathering warps
-      s_producer_sparse<kF8>(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0,
-                             SparseWarps<kF8>::slot(true, warp));
+    if (kSparse && gather_slot<true>(warp) >= 0) {
+      s_producer_gather<kF8>(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0, gather_slot<true>(warp));
     } else if (!kSparse && warp == 0) {
       if ((threadIdx.x & 31) == 0) s_producer<kF8>(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0);
     } else if (warp == 1) {
@@ -1525,10 +1376,8 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
       s_cta_softmax<kSparse, kF8>(p, sh, smem, part, cl, rb, peer);
     }
   } else {
-    if (kGather && gather_slot<false>(warp) >= 0) {
-      o_producer_gather(p, &maps, sh, smem, part, cl, gather_slot<false>(warp));
-    } else if (kSparse && !kGather && SparseWarps<kF8>::slot(false, warp) >= 0) {   // the gathering warps
-      o_producer_sparse<kF8>(p, sh, smem, part, cl, SparseWarps<kF8>::slot(false, warp));
+    if (kSparse && gather_slot<false>(warp) >= 0) {
+      o_producer_gather<kF8>(p, &maps, sh, smem, part, cl, gather_slot<false>(warp));
     } else if (!kSparse && warp == 0) {
       if ((threadIdx.x & 31) == 0) o_producer<kF8>(p, &maps, sh, smem, part, cl);
     } else if (warp == 1) {

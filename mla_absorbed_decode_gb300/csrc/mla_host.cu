@@ -7,7 +7,6 @@
 #include <stdint.h>
 
 #include <cmath>
-#include <cstring>
 #include <mutex>
 
 #include "mla_kernels.h"
@@ -118,9 +117,16 @@ bool encode_kv_maps(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, cons
 
 bool encode_kv_maps_fp8(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, const void* kv_cache,
                         int64_t num_blocks, const void* q, int64_t q_rows) {
-  std::memset(&maps->g4, 0, sizeof(maps->g4));   // bf16 cache only
   const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks * kPageTokens);
   const cuuint32_t es[3] = {1, 1, 1};
+  // the sparse decode's row gathers: the cache as [row][576 codes], one 128-code x 1-row box
+  // (the RoPE chunk's box, at code 512, reads zeros past the row's end as the dense loads do)
+  const cuuint64_t gdims[2] = {kDimQK, rows};
+  const cuuint64_t gstrides[1] = {kDimQK};
+  const cuuint32_t gbox[2] = {128, 1};
+  const bool g4_ok = encode(&maps->g4, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv_cache), gdims,
+                            gstrides, gbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   auto enc3 = [&](CUtensorMap* m, uint32_t chunks) {   // [chunk][row][128 codes] of dims 0..511
     const cuuint64_t dims[3] = {128, rows, kDimV / 128};
     const cuuint64_t strides[2] = {kDimQK, 128};
@@ -142,7 +148,7 @@ bool encode_kv_maps_fp8(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, 
   const bool q_ok = encode(&maps->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qdims, qstrides, qbox,
                            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-  return enc3(&maps->k_a, 4) && enc3(&maps->c4, 2) && rope_ok && q_ok;
+  return g4_ok && enc3(&maps->k_a, 4) && enc3(&maps->c4, 2) && rope_ok && q_ok;
 }
 
 namespace {
