@@ -47,7 +47,10 @@ METRIC = "MLA decode TFLOP/s and HBM GB/s, % of GB300 roofline (1 GPU)"
 SPEC_FLOPS = 2.25e15
 SPEC_FLOPS_FP8 = 4.5e15   # nominal dense FP8 tensor rate (twice bf16)
 SPEC_BW = 8.0e12
-DECODE_KERNEL_SOURCES = ("mla_absorbed_decode_gb300/csrc/mla_decode.cu", "mla_absorbed_decode_gb300/csrc/mla_ptx.cuh")
+# the decode kernel and the host code that encodes its tensor maps (their L2 fill units set part
+# of the traffic)
+DECODE_KERNEL_SOURCES = ("mla_absorbed_decode_gb300/csrc/mla_decode.cu", "mla_absorbed_decode_gb300/csrc/mla_ptx.cuh",
+                         "mla_absorbed_decode_gb300/csrc/mla_host.cu")
 
 
 def _peaks():

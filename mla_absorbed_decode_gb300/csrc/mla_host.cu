@@ -120,13 +120,15 @@ bool encode_kv_maps_fp8(PFN_cuTensorMapEncodeTiled_v12000 encode, KvMaps* maps, 
   const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks * kPageTokens);
   const cuuint32_t es[3] = {1, 1, 1};
   // the sparse decode's row gathers: the cache as [row][576 codes], one 128-code x 1-row box
-  // (the RoPE chunk's box, at code 512, reads zeros past the row's end as the dense loads do)
+  // (the RoPE chunk's box, at code 512, reads zeros past the row's end as the dense loads do).
+  // 64-byte L2 fills: a 576-byte row starts 0 or 64 bytes into a 128-byte line, so 128-byte fills
+  // would read 640 bytes a row.
   const cuuint64_t gdims[2] = {kDimQK, rows};
   const cuuint64_t gstrides[1] = {kDimQK};
   const cuuint32_t gbox[2] = {128, 1};
   const bool g4_ok = encode(&maps->g4, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv_cache), gdims,
                             gstrides, gbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_64B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   auto enc3 = [&](CUtensorMap* m, uint32_t chunks) {   // [chunk][row][128 codes] of dims 0..511
     const cuuint64_t dims[3] = {128, rows, kDimV / 128};
     const cuuint64_t strides[2] = {kDimQK, 128};
