@@ -40,8 +40,8 @@
 // one elected lane issues), warp 2 = credit forwarder (O-CTA), warps 4..7 and
 // 8..11 = two softmax (S-CTA) or rescale/epilogue (O-CTA) warpgroups; a thread
 // of a warpgroup owns one query row (its TMEM lane).  The sparse decode runs 512 threads:
-// four gathering warps per CTA load its pages' rows by TMA (tile::gather4,
-// s_producer_gather / o_producer_gather).
+// two lookup warps per CTA find its pages' cache rows (row_lookup) and four gathering warps
+// load them by TMA (tile::gather4, s_producer_gather / o_producer_gather).
 // Every barrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT,
 // raises an abort flag in every CTA of its cluster, drains what it has in
 // flight and exits.
@@ -66,6 +66,7 @@ constexpr int threads_of() { return kSparse ? 512 : kThreads; }
 constexpr int kMaxStages = 4;                         // barrier slots: the deepest page ring
 constexpr int kSlots = 4;                             // O-CTA packet receive slots: a slot's credit
                                                       // round trip over DSMEM is hidden 4 pages deep
+constexpr int kRowSlots = 4;                          // sparse: pages of looked-up cache rows in flight
 constexpr uint32_t kChunk = 8192;                     // one swizzled chunk of a page: 64 rows x 128 B
 constexpr uint32_t kPBytes = 128 * 128;               // P: 128 rows x 128 B in the MMA A layout (bf16: 64
                                                       // tokens; FP8: hi and lo codes of 64 tokens)
@@ -115,7 +116,8 @@ struct Cfg {
   static constexpr uint32_t kOffSharedO = kOffInvL + 512;
   static constexpr uint32_t kOffShared = kOffSharedO > kOffLpart + 512 ? kOffSharedO : kOffLpart + 512;  // both roles
   static constexpr uint32_t kOffEpi = kOffShared + 640;                    // O-CTA: 2 KiB transpose buffer per epilogue warp
-  static constexpr uint32_t kSmemBytes = kOffEpi + 8 * 2048;
+  static constexpr uint32_t kOffRows = kOffEpi + 8 * 2048;                 // sparse: cache rows of kRowSlots pages
+  static constexpr uint32_t kSmemBytes = kOffRows + kRowSlots * 64 * 4;
   static_assert(kKStages <= kMaxStages && kVStages <= kMaxStages, "barrier slots");
   static_assert(kQItemBytes <= kKStageBytes, "a q block fits a page stage");
   static_assert(kQItems <= kKStages, "the q blocks of a segment are resident together");
@@ -139,6 +141,8 @@ struct Bars {
   uint64_t corr_go;         // O-CTA: command for the rescale/epilogue warpgroups
   uint64_t corr_done;       // O-CTA: rescale finished (8 arrivals)
   uint64_t drain;           // both: final MMA completion
+  uint64_t rows_full[kRowSlots];    // sparse: a page's 64 cache rows looked up (64 arrivals)
+  uint64_t rows_empty[kRowSlots];   // sparse: every gathering warp has read them (one arrival each)
 };
 
 struct Shared {
@@ -376,9 +380,10 @@ struct RowLookahead {
 // 2-D view of the cache ([cache row][576 values], a box one chunk wide and one row high: 64
 // bf16 values, or 128 E4M3 codes).  The load writes its four 128-byte rows at 128-byte steps
 // and swizzles each by its own shared-memory address, so 16 loads per chunk (destinations 512
-// bytes apart) fill the chunk in the layout a 64-row box produces.  Four warps per CTA
-// (gather_slot): each looks up 16 rows of every page (RowLookahead, the lookups running ahead
-// of the loads) and four of its lanes load its four groups of four rows, chunk by chunk.  A row
+// bytes apart) fill the chunk in the layout a 64-row box produces.  Two lookup warps per CTA
+// find every page's rows ahead of the loads (row_lookup), and four gathering warps
+// (gather_slot) take them from a ring in shared memory; four lanes of each load its four groups
+// of four rows, chunk by chunk.  A row
 // past the request's list, or one whose lookup fails the bounds checks (reported as a bounds
 // error), loads cache row 0, which is always in range: the softmax masks it by its list
 // position.
@@ -391,10 +396,9 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
          "r"(bar)
       : "memory");
 }
-// kGatherSlots warps gather a page: slot gs looks up rows [16 gs, 16 gs + 16) (lane l < 16 row
-// 16 gs + l, two pages ahead for the list entry and one for the block-table entry) and its lanes
-// 0..3 load the four groups of four rows.  Each slot arrives once on a stage's barrier with the
-// bytes of its own loads, and drains its own loads before the CTA exits.
+// kGatherSlots warps gather a page: slot gs loads rows [16 gs, 16 gs + 16), its lanes 0..3 one
+// group of four rows each.  Each slot arrives once on a stage's barrier with the bytes of its own
+// loads, and drains its own loads before the CTA exits.
 constexpr int kGatherSlots = 4;
 template <bool IsS>
 __device__ __forceinline__ int gather_slot(int warp) {   // S-CTA: warps 0, 2, 3, 12; O-CTA: 0, 3, 12, 13
@@ -402,27 +406,65 @@ __device__ __forceinline__ int gather_slot(int warp) {   // S-CTA: warps 0, 2, 3
   if (IsS) return warp == 2 ? 1 : warp == 3 ? 2 : warp == 12 ? 3 : -1;
   return warp == 3 ? 1 : warp == 12 ? 2 : warp == 13 ? 3 : -1;
 }
+// Two lookup warps per CTA find the cache rows of every page ahead of the gathers: warp h looks
+// up rows [32 h, 32 h + 32) (RowLookahead, one row per lane) and stores their row numbers in a
+// ring of kRowSlots pages in shared memory.  The gathering warps only read them, so the lookups'
+// dependent loads never stall the warps that issue the TMA loads.
+template <bool IsS>
+__device__ __forceinline__ int lookup_half(int warp) {   // S-CTA: warps 13, 14; O-CTA: 14, 15
+  return IsS ? (warp == 13 ? 0 : warp == 14 ? 1 : -1) : (warp == 14 ? 0 : warp == 15 ? 1 : -1);
+}
+// Cache row of a looked-up address (row 0 for none: always in range, and masked by the softmax).
 template <bool F8>
-struct GatherRows {
+__device__ __forceinline__ int cache_row(const DecodeParams& p, const __nv_bfloat16* row) {
+  return row ? static_cast<int>((reinterpret_cast<const uint8_t*>(row) - reinterpret_cast<const uint8_t*>(p.kv)) /
+                                (F8 ? kDimQK : 2 * kDimQK))
+             : 0;
+}
+__device__ __forceinline__ void st_shared_s32(uint32_t a, int v) {
+  asm volatile("st.shared.b32 [%0], %1;" :: "r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_shared_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+template <bool F8>
+__device__ void row_lookup(const DecodeParams& p, Shared& sh, uint32_t smem, int part, uint32_t cl, int half) {
+  using C = Cfg<F8>;
+  const int lane = threadIdx.x & 31;
   RowLookahead<F8> look;
-  int gs;
-  __device__ void init(const DecodeParams& p, int part, int slot, int lane) {
-    gs = slot;
-    look.init(p, part, 16 * slot + lane, lane < 16);
+  look.init(p, part, 32 * half + lane, true);
+  SegmentWalker w;
+  w.init(p, part);
+  Segment s;
+  uint32_t T = 0;
+  while (w.next(s)) {
+    for (int k = s.kb; k < s.ke; ++k, ++T) {
+      const int row = cache_row<F8>(p, look.step(p));   // page k of request s.b (the walks agree)
+      const uint32_t slot = T % kRowSlots, ph = (T / kRowSlots) & 1;
+      if (!warp_wait(sh, smem_u32(&sh.bar.rows_empty[slot]), ph ^ 1, p.status, cl)) return;
+      st_shared_s32(smem + C::kOffRows + (slot * 64 + 32 * half + lane) * 4, row);
+      mbar_arrive(smem_u32(&sh.bar.rows_full[slot]));
+    }
   }
-  __device__ static int row_of(const DecodeParams& p, const __nv_bfloat16* row) {
-    return row ? static_cast<int>((reinterpret_cast<const uint8_t*>(row) - reinterpret_cast<const uint8_t*>(p.kv)) /
-                                  (F8 ? kDimQK : 2 * kDimQK))
-               : 0;
-  }
-  // The next page's group of four cache rows of lane `lane` (meaningful for lanes 0..3: rows
-  // 16 gs + 4 lane .. + 3); every lane of the warp takes part.
-  __device__ void step(const DecodeParams& p, int lane, int (&r)[4]) {
-    const int r0 = row_of(p, look.step(p));
+}
+// Page T's group of four cache rows of lane `lane` of gathering slot gs (meaningful for lanes
+// 0..3: rows 16 gs + 4 lane .. + 3).  Waits for the lookups, reads the rows and hands the ring
+// slot back.  False on abort or timeout.
+template <bool F8>
+__device__ __forceinline__ bool take_rows(const DecodeParams& p, Shared& sh, uint32_t smem, uint32_t cl, uint32_t T,
+                                          int gs, int lane, int (&r)[4]) {
+  using C = Cfg<F8>;
+  const uint32_t slot = T % kRowSlots, ph = (T / kRowSlots) & 1;
+  if (!warp_wait(sh, smem_u32(&sh.bar.rows_full[slot]), ph, p.status, cl)) return false;
+  const uint32_t src = smem + C::kOffRows + (slot * 64 + 16 * gs + 4 * (lane & 3)) * 4;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) r[j] = __shfl_sync(0xffffffffu, r0, 4 * (lane & 3) + j);
-  }
-};
+  for (int j = 0; j < 4; ++j) r[j] = ld_shared_s32(src + j * 4);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&sh.bar.rows_empty[slot]));
+  return true;
+}
 
 // Gathering slot gs of the S-CTA, sparse decode: the q blocks (slot 0, TMA
 // boxes; the other slots only arrive) and its rows of every page (tile::gather4), part A
@@ -441,8 +483,7 @@ __device__ void s_producer_gather(const DecodeParams& p, const KvMaps* maps, Sha
   uint32_t issued_phase[C::kKStages], issued_phase_b[C::kKStages];
   for (int j = 0; j < C::kKStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
   bool ok = true;
-  GatherRows<F8> g;
-  g.init(p, part, gs, lane);
+  uint32_t T = 0;   // pages
   while (ok && w.next(s)) {
     const int qrow0 = s.b * p.rows + rb * 128;
     for (int j = 0; j < C::kQItems && ok; ++j, ++i) {
@@ -469,11 +510,11 @@ __device__ void s_producer_gather(const DecodeParams& p, const KvMaps* maps, Sha
       issued_b[st] = 1, issued_phase_b[st] = ph;
       if (arrives) issued[st] = 1, issued_phase[st] = ph;
     }
-    for (int k = s.kb; k < s.ke && ok; ++k, ++i) {
+    for (int k = s.kb; k < s.ke && ok; ++k, ++i, ++T) {
       const uint32_t st = i % C::kKStages, ph = (i / C::kKStages) & 1;
       const uint32_t stage = smem + C::kOffStage + st * C::kKStageBytes;
       int r[4];
-      g.step(p, lane, r);   // page k of request s.b (the walks agree)
+      if (!take_rows<F8>(p, sh, smem, cl, T, gs, lane, r)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
       const uint32_t full = smem_u32(&sh.bar.full[st]);
       if (lane == 0) mbar_arrive_expect_tx(full, 4u * 512u * C::kKPartA);
@@ -521,14 +562,12 @@ __device__ void o_producer_gather(const DecodeParams& p, const KvMaps* maps, Sha
   for (int j = 0; j < C::kVStages; ++j) issued[j] = 0, issued_phase[j] = 0, issued_b[j] = 0, issued_phase_b[j] = 0;
   constexpr int kHalf = static_cast<int>(C::kVChunks / 2);
   bool ok = true;
-  GatherRows<F8> g;
-  g.init(p, part, gs, lane);
   while (ok && w.next(s)) {
     for (int k = s.kb; k < s.ke && ok; ++k, ++T) {
       const uint32_t st = T % C::kVStages, ph = (T / C::kVStages) & 1;
       const uint32_t stage = smem + C::kOffStage + st * C::kVStageBytes;
       int r[4];
-      g.step(p, lane, r);
+      if (!take_rows<F8>(p, sh, smem, cl, T, gs, lane, r)) { ok = false; break; }
       if (!warp_wait(sh, smem_u32(&sh.bar.empty[st]), ph ^ 1, p.status, cl)) { ok = false; break; }
       const uint32_t full = smem_u32(&sh.bar.full[st]);
       if (lane == 0) mbar_arrive_expect_tx(full, 4u * 512u * kHalf);
@@ -1350,6 +1389,10 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     mbar_init(smem_u32(&sh.bar.corr_go), 1);
     mbar_init(smem_u32(&sh.bar.corr_done), kGroupWarps);
     mbar_init(smem_u32(&sh.bar.drain), 1);
+    for (int i = 0; i < kRowSlots; ++i) {
+      mbar_init(smem_u32(&sh.bar.rows_full[i]), 64);              // one arrival per looked-up row
+      mbar_init(smem_u32(&sh.bar.rows_empty[i]), kGatherSlots);   // one arrival per gathering warp
+    }
     fence_mbar_init();
   }
   __syncwarp();
@@ -1364,7 +1407,8 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
     if (b0 >= 0) prefetch_request(p, b0);
   }
 
-  // sparse: four gathering warps load the listed rows by TMA (s_producer_gather / o_producer_gather)
+  // sparse: two warps look up the listed rows (row_lookup) and four load them by TMA
+  // (s_producer_gather / o_producer_gather)
   if (is_s) {
     if (kSparse && gather_slot<true>(warp) >= 0) {
       s_producer_gather<kF8>(p, &maps, sh, smem, part, cl, rb, p.withhold_first_load != 0, gather_slot<true>(warp));
@@ -1374,6 +1418,8 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
       s_cta_mma<kSparse, kF8>(p, sh, smem, part, cl);
     } else if (warp >= 4 && warp < 12) {
       s_cta_softmax<kSparse, kF8>(p, sh, smem, part, cl, rb, peer);
+    } else if (kSparse && lookup_half<true>(warp) >= 0) {
+      row_lookup<kF8>(p, sh, smem, part, cl, lookup_half<true>(warp));
     }
   } else {
     if (kSparse && gather_slot<false>(warp) >= 0) {
@@ -1386,6 +1432,8 @@ mla_decode_kernel(const __grid_constant__ KvMaps maps, const DecodeParams p) {
       if ((threadIdx.x & 31) == 0) o_cta_forwarder(p, sh, part, cl, peer);
     } else if (warp >= 4 && warp < 12) {
       o_cta_epilogue<kSparse, kF8>(p, sh, smem, part, cl, rb);
+    } else if (kSparse && lookup_half<false>(warp) >= 0) {
+      row_lookup<kF8>(p, sh, smem, part, cl, lookup_half<false>(warp));
     }
   }
 
