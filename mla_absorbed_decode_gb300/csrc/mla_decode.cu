@@ -60,7 +60,7 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 384;          // 12 warps; the sparse decode runs 16 (see gather_slot)
+constexpr int kThreads = 384;          // 12 warps; the sparse decode runs 16 (see gather_slot, lookup_half)
 template <bool kSparse, bool kF8>
 constexpr int threads_of() { return kSparse ? 512 : kThreads; }
 constexpr int kMaxStages = 4;                         // barrier slots: the deepest page ring
@@ -285,10 +285,10 @@ __device__ __forceinline__ int request_block(const DecodeParams& p, int b, int k
 // like a dense token.  The rows are loaded by TMA row gathers (below) into the same
 // swizzled layout a 64-row TMA box produces.
 
-// The row lookups run ahead of the copies: a lane loads the list entry of its row two
-// pages ahead and that token's block-table entry one page ahead, so that the two
-// dependent loads of a page are spread over the two previous pages' gathers instead of
-// stalling the warp between pages.
+// The row lookups run in their own warps, ahead of the copies: a lane loads the list entry
+// of its row two pages ahead and that token's block-table entry one page ahead, so that the
+// two dependent loads of a page overlap instead of stalling the lookup warp between pages,
+// and the ring of looked-up rows (row_lookup) keeps the lookups off the gathers' path.
 constexpr int kNoEntry = INT_MIN;   // a row past the request's list: nothing to gather
 
 // Walks the (request, page) pairs of one part in the order the kernel processes them.
@@ -343,7 +343,7 @@ __device__ __forceinline__ const __nv_bfloat16* sparse_address(const DecodeParam
                                                 row * (F8 ? kDimQK : 2 * kDimQK));
 }
 
-// One gathering lane's lookups: (b0, t0, blk0) for the page being gathered, (b1, t1)
+// One lookup lane's lookups: (b0, t0, blk0) for the page being looked up, (b1, t1)
 // for the next one; `ahead` walks two pages ahead.
 template <bool F8>
 struct RowLookahead {
